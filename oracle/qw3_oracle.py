@@ -1,0 +1,492 @@
+"""CPU oracle for the Qwen3-style dense decoder over GGUF Q8_0 weights.
+
+TEST INFRASTRUCTURE. This module is the slow, plain statement of what the
+model computes, written from the source pages, and nothing else. Only the test
+suite, the smoke check and the benchmark's CPU-baseline leg may import it; the
+product path (the CUDA library and its Python binding) never does. It shares no
+code, tables or constants with the CUDA path: the only common module is the
+seeded input generator, which holds none of the model's arithmetic.
+
+Numerics. Weights are Q8_0 blocks dequantised exactly (d*q has at most 18
+significant bits, so it is exact in f32 and f64). Every tensor handed from one
+step to the next -- the residual stream, normalised activations, projections,
+the KV cache, logits -- is stored in f32, as the pages store activations and
+as the f32 KV cache of the workloads fixes. Inside each step the arithmetic is
+f64: dot products (a library matmul on f64 operands), norms, RoPE angles,
+softmax. The Q8_0 encoder itself is specified in f32 by the pages and is done
+in f32 here.
+
+Sources (page title, section):
+  * "A transformer from scratch" (Fucina course ch. 12): sections 12.1 (config),
+    12.3 (forward pass), 12.3.2 (RMSNorm), 12.3.3 (QKV), 12.3.4 (RoPE),
+    12.3.5 (GQA, causal attention, scale), 12.3.6 (SwiGLU), 12.3.7 (residual,
+    final norm, last-row lm_head), 12.4 (KV cache and its contracts),
+    12.6 (greedy loop).
+  * "Model files and quantization" (Fucina course ch. 11): section 11.7
+    (Q8_0 block, encoder, decoder, round-trip bound), 11.10 (finite-input
+    guard).
+  * "The LLM stack (fucina_llm)" (Fucina reference section 13): 13.4 (KV cache
+    contract and its worked test), 13.6 (greedy argmax example).
+  * minfer "Qwen3 Support Plan (dense)": section 1 (tensor inventory),
+    section 2.1 (head_dim 128, scale 1/sqrt(128), full-head NeoX RoPE,
+    theta 1e6), section 2.2 (per-head Q/K RMSNorm before RoPE).
+
+Parity status: every function here is pinned by tests/test_oracle.py against
+closed forms, invariants, the pages' worked examples and an independent f64
+cacheless brute force; nothing here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import Sequence
+
+import numpy as np
+
+QK8_0 = 32          # values per Q8_0 block
+Q8_0_BYTES = 34     # f16 scale + 32 int8 quants
+
+
+class OracleError(ValueError):
+    """Base of the oracle's typed errors (the pages' error names)."""
+
+
+class NonFiniteValue(OracleError):
+    """Encoder input held NaN or +-inf (course 11.10, the allFinite guard)."""
+
+
+class InvalidShape(OracleError):
+    """A length or shape the format or model cannot take."""
+
+
+class InvalidSequenceLength(OracleError):
+    """forward called with pos0 != cache length (course 12.4, contract 2)."""
+
+
+class KvCacheOverflow(OracleError):
+    """The cache has no room for the new rows (course 12.4, contract 2)."""
+
+
+# ---------------------------------------------------------------------------
+# Q8_0 codec -- "Model files and quantization", section 11.7
+# ---------------------------------------------------------------------------
+
+def _round_half_away(v32: np.ndarray) -> np.ndarray:
+    """Round f32 values to integers, halves away from zero.
+
+    Reading of the pages: the course encoder rounds with Zig's @round, which
+    the text says rounds halves away from zero (section 11.10 contrasts it with
+    ggml's round-to-nearest-even). Done in f64, where |v| + 0.5 is exact for
+    every f32 v below 2**29, so no double rounding can occur.
+    """
+    v = v32.astype(np.float64)
+    return np.sign(v) * np.floor(np.abs(v) + 0.5)
+
+
+def q8_0_quantize_parts(x: np.ndarray):
+    """Encode f32 values in blocks of 32; return (d32, q, d16).
+
+    Per block (section 11.7): amax = max|v|; d = amax / 127 in f32;
+    inv_d = 0 if d == 0 else 1 / d in f32; q = clamp(round(v * inv_d), -127, 127)
+    with the product v * inv_d rounded once to f32; the stored scale is d as
+    an IEEE f16 (round to nearest even). d32 is the f32 scale used to encode,
+    d16 the stored one.
+
+    Edge readings (not covered by the pages): when d is so small that 1/d
+    overflows to +inf, a nonzero v saturates to +-127 and a zero v (0 * inf is
+    NaN) encodes as 0.
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    if x.size % QK8_0:
+        raise InvalidShape(f"length {x.size} is not a multiple of {QK8_0}")
+    if not np.all(np.isfinite(x)):
+        raise NonFiniteValue("Q8_0 encoder input holds NaN or inf")
+    v = x.reshape(-1, QK8_0)
+    amax = np.max(np.abs(v), axis=1)
+    d = (amax / np.float32(127.0)).astype(np.float32)
+    with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
+        inv_d = np.where(d == 0, np.float32(0.0), np.float32(1.0) / d).astype(np.float32)
+        prod = (v * inv_d[:, None]).astype(np.float32)
+    nan = np.isnan(prod)
+    prod = np.where(nan, np.float32(0.0), prod)
+    r = np.clip(_round_half_away(prod), -127.0, 127.0)
+    q = r.astype(np.int8)
+    d16 = d.astype(np.float16)
+    return d, q, d16
+
+
+def q8_0_quantize(x: np.ndarray) -> np.ndarray:
+    """Encode to the GGUF wire format: per block 2 bytes f16 d (little endian)
+    then 32 int8 quants, 34 bytes in all (section 11.7, BlockQ8_0)."""
+    _, q, d16 = q8_0_quantize_parts(x)
+    nb = q.shape[0]
+    out = np.empty((nb, Q8_0_BYTES), dtype=np.uint8)
+    out[:, 0:2] = d16.astype("<f2").view(np.uint8).reshape(nb, 2)
+    out[:, 2:] = q.view(np.uint8)
+    return out.reshape(-1)
+
+
+def q8_0_unpack(blocks: np.ndarray, n: int):
+    """Split wire bytes into (d16 [nb] float16, q [nb, 32] int8)."""
+    if n % QK8_0:
+        raise InvalidShape(f"length {n} is not a multiple of {QK8_0}")
+    nb = n // QK8_0
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1)
+    if b.size != nb * Q8_0_BYTES:
+        raise InvalidShape(f"{b.size} bytes do not hold {nb} Q8_0 blocks")
+    b = b.reshape(nb, Q8_0_BYTES)
+    d16 = np.ascontiguousarray(b[:, 0:2]).view("<f2").reshape(nb)
+    q = np.ascontiguousarray(b[:, 2:]).view(np.int8)
+    return d16, q
+
+
+def q8_0_dequantize(blocks: np.ndarray, n: int) -> np.ndarray:
+    """Decode: x = f32(d) * q per element (section 11.7). Exact in f32."""
+    d16, q = q8_0_unpack(blocks, n)
+    d = d16.astype(np.float32)
+    return (d[:, None] * q.astype(np.float32)).astype(np.float32).reshape(-1)
+
+
+def matrix_from_blocks(blocks: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """Dequantise a Q8_0 matrix stored [rows][cols/32 blocks] to f32 [rows, cols]."""
+    return q8_0_dequantize(blocks, rows * cols).reshape(rows, cols)
+
+
+# ---------------------------------------------------------------------------
+# Elementwise and reduction steps -- "A transformer from scratch", 12.3
+# ---------------------------------------------------------------------------
+
+def rms_norm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+    """y_i = x_i / sqrt(mean(x^2) + eps) * w_i over the last axis (12.3.2).
+
+    The same function serves the per-head Q/K norm (minfer section 2.2): the
+    last axis is then the head's head_dim values and w has length head_dim.
+    """
+    x64 = np.asarray(x, dtype=np.float32).astype(np.float64)
+    ms = np.mean(x64 * x64, axis=-1, keepdims=True)
+    y = x64 / np.sqrt(ms + float(eps)) * np.asarray(w, np.float32).astype(np.float64)
+    return y.astype(np.float32)
+
+
+def rope_inv_freq(head_dim: int, theta: float) -> np.ndarray:
+    """f_i = theta^(-2i/d) for i < d/2 (12.3.4): pair i turns p*f_i radians."""
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    return np.power(float(theta), -2.0 * i / float(head_dim))
+
+
+def rope_neox(x: np.ndarray, positions: Sequence[int], theta: float) -> np.ndarray:
+    """NeoX "half" RoPE on x [M, heads, d] at positions [M] (12.3.4).
+
+    Channel i pairs with channel i + d/2; the pair (a, b) at position p turns
+    by angle p * f_i to (a cos - b sin, a sin + b cos), the course's rotate().
+    Angles and rotation in f64, the result rounded to f32.
+    """
+    x64 = np.asarray(x, dtype=np.float32).astype(np.float64)
+    d = x64.shape[-1]
+    half = d // 2
+    pos = np.asarray(positions, dtype=np.float64)
+    ang = pos[:, None] * rope_inv_freq(d, theta)[None, :]          # [M, d/2]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    a = x64[..., :half]
+    b = x64[..., half:]
+    out = np.concatenate([a * c - b * s, a * s + b * c], axis=-1)
+    return out.astype(np.float32)
+
+
+def kv_head_map(n_heads: int, n_kv_heads: int) -> list[int]:
+    """Query head h reads KV head h / (n_heads / n_kv_heads) (12.3.5)."""
+    if n_kv_heads <= 0 or n_heads % n_kv_heads:
+        raise InvalidShape("n_heads must be a positive multiple of n_kv_heads")
+    per = n_heads // n_kv_heads
+    return [h // per for h in range(n_heads)]
+
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_positions: Sequence[int],
+              scale: float, kv_head_for_head: Sequence[int]) -> np.ndarray:
+    """Causal grouped-query attention (12.3.5).
+
+    q [M, nh, d] at absolute positions q_positions; k, v [T, nkv, d] hold cache
+    rows 0..T-1. The query at position p attends keys 0..p with weights
+    softmax_j(q . k_j * scale) (max subtracted before exp) and returns the
+    weighted sum of v_j. Returns [M, nh, d] f32.
+    """
+    q64 = np.asarray(q, np.float32).astype(np.float64)
+    k64 = np.asarray(k, np.float32).astype(np.float64)
+    v64 = np.asarray(v, np.float32).astype(np.float64)
+    M, nh, d = q64.shape
+    T = k64.shape[0]
+    pos = np.asarray(q_positions, dtype=np.int64)
+    masked = np.arange(T)[None, :] > pos[:, None]                   # [M, T]
+    out = np.empty((M, nh, d), dtype=np.float64)
+    for h in range(nh):
+        g = kv_head_for_head[h]
+        s = (q64[:, h, :] @ k64[:, g, :].T) * float(scale)
+        s[masked] = -np.inf
+        s -= np.max(s, axis=1, keepdims=True)
+        p = np.exp(s)
+        p /= np.sum(p, axis=1, keepdims=True)
+        out[:, h, :] = p @ v64[:, g, :]
+    return out.astype(np.float32)
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """silu(z) = z * sigmoid(z) = z / (1 + e^-z), f64 (12.3.6)."""
+    z64 = np.asarray(z, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return z64 / (1.0 + np.exp(-z64))
+
+
+def swiglu(gate: np.ndarray, up: np.ndarray) -> np.ndarray:
+    """silu(gate) * up, elementwise, rounded to f32 (12.3.6)."""
+    return (silu(gate) * np.asarray(up, np.float32).astype(np.float64)).astype(np.float32)
+
+
+def add_f32(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Residual add of two f32 tensors (12.3.7)."""
+    return (np.asarray(a, np.float32).astype(np.float64)
+            + np.asarray(b, np.float32).astype(np.float64)).astype(np.float32)
+
+
+def argmax_lowest(logits: np.ndarray) -> int:
+    """Greedy pick: the largest logit, the lowest index among equals (12.6).
+
+    NaN logits are an error.
+    """
+    lg = np.asarray(logits)
+    if np.isnan(lg).any():
+        raise NonFiniteValue("NaN logit")
+    return int(np.argmax(lg))
+
+
+# ---------------------------------------------------------------------------
+# Linear layers over dequantised Q8_0 weights
+# ---------------------------------------------------------------------------
+
+class QLinear:
+    """A Q8_0 weight [out][in], kept dequantised (exactly) for f64 matmuls."""
+
+    def __init__(self, blocks: np.ndarray, rows: int, cols: int, keep_f64: bool):
+        if cols % QK8_0:
+            raise InvalidShape(f"in-dimension {cols} is not a multiple of {QK8_0}")
+        self.rows, self.cols = rows, cols
+        w32 = matrix_from_blocks(blocks, rows, cols)
+        self.w = w32.astype(np.float64) if keep_f64 else w32
+
+    def __call__(self, x: np.ndarray) -> np.ndarray:
+        """y[m, n] = sum_k W[n, k] x[m, k] in f64 (a library matmul), f32 out."""
+        x64 = np.asarray(x, np.float32).astype(np.float64)
+        if self.w.dtype == np.float64:
+            return (x64 @ self.w.T).astype(np.float32)
+        out = np.empty((x64.shape[0], self.rows), dtype=np.float32)
+        step = 8192
+        for r0 in range(0, self.rows, step):
+            wc = self.w[r0:r0 + step].astype(np.float64)
+            out[:, r0:r0 + step] = (x64 @ wc.T).astype(np.float32)
+        return out
+
+    def row(self, r: np.ndarray) -> np.ndarray:
+        """Rows of the dequantised matrix as f32 (the embedding gather)."""
+        return np.asarray(self.w[r], dtype=np.float32)
+
+
+# ---------------------------------------------------------------------------
+# KV cache -- course 12.4 and reference 13.4
+# ---------------------------------------------------------------------------
+
+class KvCache:
+    """Per-layer f32 K and V, each [capacity, kv_heads, head_dim].
+
+    K is stored after the Q/K norm and RoPE, V as projected. append_layer
+    writes at rows len.. without moving len; advance(m) moves it once per
+    forward; truncate(keep) rewinds by a single store.
+    """
+
+    def __init__(self, n_layers: int, n_kv_heads: int, head_dim: int, capacity: int):
+        self.capacity = capacity
+        self.k = np.zeros((n_layers, capacity, n_kv_heads, head_dim), np.float32)
+        self.v = np.zeros((n_layers, capacity, n_kv_heads, head_dim), np.float32)
+        self.len = 0
+
+    def append_layer(self, layer: int, k_rows: np.ndarray, v_rows: np.ndarray) -> None:
+        m = k_rows.shape[0]
+        if self.len + m > self.capacity:
+            raise KvCacheOverflow(f"len {self.len} + {m} > capacity {self.capacity}")
+        self.k[layer, self.len:self.len + m] = k_rows
+        self.v[layer, self.len:self.len + m] = v_rows
+
+    def advance(self, m: int) -> None:
+        if self.len + m > self.capacity:
+            raise KvCacheOverflow(f"len {self.len} + {m} > capacity {self.capacity}")
+        self.len += m
+
+    def truncate(self, keep_len: int) -> None:
+        if keep_len < self.len:
+            self.len = keep_len
+
+    def reset(self) -> None:
+        self.len = 0
+
+    def layer_rows(self, layer: int, n: int):
+        return self.k[layer, :n], self.v[layer, :n]
+
+
+# ---------------------------------------------------------------------------
+# The model
+# ---------------------------------------------------------------------------
+
+@dataclass
+class _Layer:
+    attn_norm: np.ndarray
+    wq: QLinear
+    wk: QLinear
+    wv: QLinear
+    q_norm: np.ndarray
+    k_norm: np.ndarray
+    wo: QLinear
+    ffn_norm: np.ndarray
+    wg: QLinear
+    wu: QLinear
+    wd: QLinear
+
+
+class OracleModel:
+    """The dense Qwen3 decoder over Q8_0 weights (course 12.3, minfer 1-2).
+
+    `shape` carries vocab, hidden, n_layers, n_heads, n_kv_heads, head_dim,
+    intermediate, rms_eps, rope_theta and tied. `tensors` maps GGUF names to
+    Q8_0 wire bytes (linear weights) or f32 arrays (norm weights).
+    """
+
+    F64_BUDGET_BYTES = 12 << 30
+
+    def __init__(self, shape, tensors: dict, keep_f64: bool | None = None):
+        s = shape
+        self.shape = s
+        if s.head_dim % 2:
+            raise InvalidShape("head_dim must be even for the half-layout RoPE")
+        self.kv_head_for_head = kv_head_map(s.n_heads, s.n_kv_heads)
+        n_params = s.vocab * s.hidden * (1 if s.tied else 2) + s.n_layers * (
+            s.hidden * (2 * s.q_width + 2 * s.kv_width) + 3 * s.hidden * s.intermediate)
+        if keep_f64 is None:
+            keep_f64 = n_params * 8 <= self.F64_BUDGET_BYTES
+
+        def lin(name, rows, cols):
+            return QLinear(tensors[name], rows, cols, keep_f64)
+
+        def norm(name, n):
+            w = np.asarray(tensors[name], np.float32)
+            if w.shape != (n,):
+                raise InvalidShape(f"{name}: expected [{n}], got {list(w.shape)}")
+            return w
+
+        self.tok_embd = lin("token_embd", s.vocab, s.hidden)
+        self.layers = []
+        for i in range(s.n_layers):
+            p = f"blk.{i}."
+            self.layers.append(_Layer(
+                attn_norm=norm(p + "attn_norm", s.hidden),
+                wq=lin(p + "attn_q", s.q_width, s.hidden),
+                wk=lin(p + "attn_k", s.kv_width, s.hidden),
+                wv=lin(p + "attn_v", s.kv_width, s.hidden),
+                q_norm=norm(p + "attn_q_norm", s.head_dim),
+                k_norm=norm(p + "attn_k_norm", s.head_dim),
+                wo=lin(p + "attn_output", s.hidden, s.q_width),
+                ffn_norm=norm(p + "ffn_norm", s.hidden),
+                wg=lin(p + "ffn_gate", s.intermediate, s.hidden),
+                wu=lin(p + "ffn_up", s.intermediate, s.hidden),
+                wd=lin(p + "ffn_down", s.hidden, s.intermediate),
+            ))
+        self.output_norm = norm("output_norm", s.hidden)
+        # tied lm_head: no output.weight means the embedding table is reused
+        self.output = self.tok_embd if s.tied else lin("output", s.vocab, s.hidden)
+
+    @classmethod
+    def from_f32(cls, shape, weights: dict, keep_f64: bool | None = None) -> "OracleModel":
+        """Quantise f32 linear weights with this module's Q8_0 encoder."""
+        from quantized_transformer_decode_gb300.inputs import tensor_specs
+        tensors = {}
+        for name, kind, _ in tensor_specs(shape):
+            w = weights[name]
+            tensors[name] = q8_0_quantize(w) if kind == "linear" else np.asarray(w, np.float32)
+        return cls(shape, tensors, keep_f64)
+
+    def new_cache(self, capacity: int) -> KvCache:
+        s = self.shape
+        return KvCache(s.n_layers, s.n_kv_heads, s.head_dim, capacity)
+
+    # -- blocks -------------------------------------------------------------
+
+    def _attention_block(self, li: int, lw: _Layer, x, positions, cache: KvCache):
+        s = self.shape
+        M = x.shape[0]
+        h = rms_norm(x, lw.attn_norm, s.rms_eps)
+        q = lw.wq(h).reshape(M, s.n_heads, s.head_dim)
+        k = lw.wk(h).reshape(M, s.n_kv_heads, s.head_dim)
+        v = lw.wv(h).reshape(M, s.n_kv_heads, s.head_dim)
+        q = rope_neox(rms_norm(q, lw.q_norm, s.rms_eps), positions, s.rope_theta)
+        k = rope_neox(rms_norm(k, lw.k_norm, s.rms_eps), positions, s.rope_theta)
+        cache.append_layer(li, k, v)
+        kk, vv = cache.layer_rows(li, cache.len + M)
+        o = attention(q, kk, vv, positions, 1.0 / math.sqrt(s.head_dim), self.kv_head_for_head)
+        return add_f32(x, lw.wo(o.reshape(M, s.q_width)))
+
+    def _ffn_block(self, lw: _Layer, x):
+        s = self.shape
+        h2 = rms_norm(x, lw.ffn_norm, s.rms_eps)
+        return add_f32(x, lw.wd(swiglu(lw.wg(h2), lw.wu(h2))))
+
+    # -- entry points -------------------------------------------------------
+
+    def forward(self, cache: KvCache, tokens, pos0: int, all_logits: bool = False):
+        """Append len(tokens) rows at pos0 and return logits (12.3, 12.4).
+
+        pos0 must equal cache.len (else InvalidSequenceLength) and the rows
+        must fit (else KvCacheOverflow). Returns the last row's logits [vocab]
+        unless all_logits, then [M, vocab]. The cache length moves once, after
+        the layer loop.
+        """
+        s = self.shape
+        tok = np.asarray(tokens, dtype=np.int64).reshape(-1)
+        M = tok.size
+        if M == 0:
+            raise InvalidShape("empty token list")
+        if pos0 != cache.len:
+            raise InvalidSequenceLength(f"pos0 {pos0} != cache length {cache.len}")
+        if cache.len + M > cache.capacity:
+            raise KvCacheOverflow(f"len {cache.len} + {M} > capacity {cache.capacity}")
+        if tok.min() < 0 or tok.max() >= s.vocab:
+            raise InvalidShape("token id out of range")
+        positions = np.arange(pos0, pos0 + M)
+        x = self.tok_embd.row(tok)
+        for li, lw in enumerate(self.layers):
+            x = self._attention_block(li, lw, x, positions, cache)
+            x = self._ffn_block(lw, x)
+        cache.advance(M)
+        xf = rms_norm(x, self.output_norm, s.rms_eps)
+        if all_logits:
+            return self.output(xf)
+        return self.output(xf[-1:])[0]
+
+    def generate_greedy(self, cache: KvCache, prompt, n_steps: int):
+        """Prefill the prompt, then n_steps greedy decode steps (12.6).
+
+        Returns (ids, logits): ids[0] is the prefill's argmax and ids[s] the
+        argmax of decode step s, which was fed ids[s-1] at position
+        len(prompt) + s - 1; logits[s] is the row each id was taken from.
+        """
+        lg = self.forward(cache, prompt, cache.len)
+        ids = [argmax_lowest(lg)]
+        logits = [lg]
+        for _ in range(n_steps):
+            lg = self.forward(cache, [ids[-1]], cache.len)
+            ids.append(argmax_lowest(lg))
+            logits.append(lg)
+        return ids, logits
+
+    def teacher_forced(self, cache: KvCache, prompt, fed_ids: Sequence[int]):
+        """Prefill, then decode the given ids one by one; return every logits row."""
+        out = [self.forward(cache, prompt, cache.len)]
+        for t in fed_ids:
+            out.append(self.forward(cache, [int(t)], cache.len))
+        return out

@@ -1,0 +1,428 @@
+"""Pins for the CPU oracle: closed forms, invariants, the pages' worked examples,
+library routines for special cases and an f64 cacheless brute force.
+
+None of these re-types an oracle formula and compares it with itself; each
+check would fail on a plausible slip (a dropped term, a wrong sign, pairing or
+index, a transposed operand, the other tie rule).
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle as orc
+from conftest import golden
+from quantized_transformer_decode_gb300 import inputs
+
+
+# ----------------------------------------------------------------- Q8_0 codec
+
+def test_q8_0_wire_layout_and_integer_block():
+    # amax 127 gives d = 1.0 exactly (f16 bits 0x3C00, little endian) and the
+    # integers encode as themselves: 34 bytes, scale first (section 11.7).
+    spec = golden("q8_0_roundtrip.json")
+    vals = np.arange(-16, 16, dtype=np.float32)
+    vals[0] = -127.0
+    b = orc.q8_0_quantize(vals)
+    assert b.size == spec["block_bytes"]
+    assert b[0] == 0x00 and b[1] == 0x3C
+    assert np.array_equal(b[2:].view(np.int8).astype(np.float32), vals)
+
+
+def test_q8_0_roundtrip_course_bounds():
+    spec = golden("q8_0_roundtrip.json")
+    for seed in range(20):
+        x = inputs.uniform_block_values(seed, 32 * 64)
+        d32, q, d16 = orc.q8_0_quantize_parts(x)
+        xb = x.reshape(-1, 32).astype(np.float64)
+        # course test: within half a step of the f32 scale
+        err32 = np.abs(xb - d32[:, None].astype(np.float64) * q)
+        assert np.all(err32 <= d32[:, None] / 2 + 1e-6)
+        # public seam with the stored f16 scale
+        y = orc.q8_0_dequantize(orc.q8_0_quantize(x), x.size).reshape(-1, 32)
+        assert np.max(np.abs(y - xb)) <= spec["f16_scale_seam_bound"]
+        bound = d32.astype(np.float64) / 2 + 127 * np.abs(d32.astype(np.float64) - d16.astype(np.float64))
+        assert np.all(np.abs(y - xb) <= bound[:, None] + 1e-6)
+
+
+def test_q8_0_zero_block_is_all_zero_bytes():
+    b = orc.q8_0_quantize(np.zeros(64, np.float32))
+    assert not b.any()
+
+
+def test_q8_0_ramp_closed_form():
+    # v_k = k/31: amax 1, so q_k = round(127 k / 31); 127k/31 is never within
+    # 1/62 of a half-integer, far beyond f32 rounding, so exact rationals decide.
+    x = (np.arange(32, dtype=np.float32) / np.float32(31)).astype(np.float32)
+    _, q, _ = orc.q8_0_quantize_parts(x)
+    want = [int(Fraction(127 * k, 31) + Fraction(1, 2)) for k in range(32)]
+    assert q[0].tolist() == want
+    assert want[-1] == 127 and want[0] == 0
+
+
+def test_q8_0_single_spike():
+    rng = np.random.default_rng(5)
+    x = (rng.random(32, dtype=np.float32) * 0.02 - 0.01).astype(np.float32)
+    x[7] = -3.0
+    _, q, _ = orc.q8_0_quantize_parts(x)
+    assert q[0, 7] == -127
+    assert np.all(np.delete(q[0], 7) == 0)      # |v| * 127/3 < 0.43
+
+
+def test_q8_0_exact_ties_round_half_away_from_zero():
+    # d = 1 (amax 127), so v * inv_d = v exactly: halves must go away from 0.
+    x = np.zeros(32, np.float32)
+    x[:8] = [127.0, 2.5, -2.5, 0.5, -0.5, 126.5, 1.5, -1.5]
+    _, q, _ = orc.q8_0_quantize_parts(x)
+    assert q[0, :8].tolist() == [127, 3, -3, 1, -1, 127, 2, -2]
+
+
+@pytest.mark.parametrize("amax,bits", [
+    (127.0, 0x3C00),                       # d = 1
+    (254.0, 0x4000),                       # d = 2
+    (127.0 * 2.0 ** -24, 0x0001),          # d = smallest f16 subnormal
+    (127.0 * 2.0 ** -25, 0x0000),          # exact tie between 0 and 2^-24 -> even
+    (127.0 * 3 * 2.0 ** -25, 0x0002),      # tie between 1 and 2 (x 2^-24) -> even
+    (127.0 * 65504.0, 0x7BFF),             # largest finite f16
+])
+def test_q8_0_f16_scale_is_ieee_round_to_nearest_even(amax, bits):
+    x = np.zeros(32, np.float32)
+    x[3] = np.float32(amax)
+    assert float(np.float32(amax)) == amax
+    b = orc.q8_0_quantize(x)
+    assert int(b[0]) | (int(b[1]) << 8) == bits
+
+
+def test_q8_0_tiny_scale_saturates():
+    # d subnormal enough that 1/d overflows: nonzero v saturate, zeros stay 0
+    x = np.zeros(32, np.float32)
+    x[0] = np.float32(1e-38)
+    x[1] = np.float32(-5e-39)
+    _, q, d16 = orc.q8_0_quantize_parts(x)
+    assert q[0, 0] == 127 and q[0, 1] == -127 and np.all(q[0, 2:] == 0)
+    assert float(d16[0]) == 0.0
+
+
+def test_q8_0_errors():
+    with pytest.raises(orc.InvalidShape):
+        orc.q8_0_quantize(np.zeros(33, np.float32))
+    for bad in (np.nan, np.inf, -np.inf):
+        x = np.zeros(64, np.float32)
+        x[40] = bad
+        with pytest.raises(orc.NonFiniteValue):
+            orc.q8_0_quantize(x)
+
+
+def test_q8_0_dequantize_is_scale_times_code():
+    x = inputs.uniform_block_values(7, 96)
+    b = orc.q8_0_quantize(x).reshape(3, 34)
+    y = orc.q8_0_dequantize(b.reshape(-1), 96).reshape(3, 32)
+    for i in range(3):
+        d = float(np.frombuffer(b[i, :2].tobytes(), "<f2")[0])
+        qs = np.frombuffer(b[i, 2:].tobytes(), np.int8)
+        assert np.array_equal(y[i], np.array([d * int(c) for c in qs], np.float32))
+
+
+# ------------------------------------------------------------------- linear
+
+def test_linear_one_hot_selects_a_column_and_brute_force_sum():
+    rng = np.random.default_rng(3)
+    W = (rng.standard_normal((5, 64)) * 0.02).astype(np.float32)
+    lin = orc.QLinear(orc.q8_0_quantize(W), 5, 64, keep_f64=True)
+    Wd = orc.matrix_from_blocks(orc.q8_0_quantize(W), 5, 64)
+    for j in (0, 31, 32, 63):
+        e = np.zeros((1, 64), np.float32)
+        e[0, j] = 1.0
+        assert np.array_equal(lin(e)[0], Wd[:, j])
+    x = rng.standard_normal((2, 64)).astype(np.float32)
+    y = lin(x)
+    for m in range(2):
+        for n in range(5):
+            exact = sum(Fraction(float(Wd[n, k])) * Fraction(float(x[m, k])) for k in range(64))
+            assert abs(float(y[m, n]) - float(exact)) <= 1e-7 * max(1.0, abs(float(exact)))
+
+
+def test_linear_f32_storage_matches_f64_storage():
+    rng = np.random.default_rng(4)
+    W = (rng.standard_normal((9000, 32)) * 0.02).astype(np.float32)
+    b = orc.q8_0_quantize(W)
+    x = rng.standard_normal((3, 32)).astype(np.float32)
+    assert np.array_equal(orc.QLinear(b, 9000, 32, True)(x), orc.QLinear(b, 9000, 32, False)(x))
+
+
+# ------------------------------------------------------------------ RMSNorm
+
+def test_rms_norm_constant_vector_closed_form():
+    rng = np.random.default_rng(1)
+    w = (1 + 0.1 * rng.standard_normal(64)).astype(np.float32)
+    c = 0.37
+    y = orc.rms_norm(np.full(64, c, np.float32), w, 1e-6)
+    cc = float(np.float32(c))
+    want = cc / math.sqrt(cc * cc + 1e-6) * w.astype(np.float64)
+    assert np.allclose(y, want, rtol=1e-7, atol=0)
+
+
+def test_rms_norm_unit_rms_scale_invariance_and_zero():
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((4, 128)).astype(np.float32) * 3
+    y = orc.rms_norm(x, np.ones(128, np.float32), 1e-6).astype(np.float64)
+    assert np.allclose(np.sqrt(np.mean(y * y, axis=1)), 1.0, atol=1e-6)
+    y2 = orc.rms_norm(x * 1000, np.ones(128, np.float32), 1e-6)
+    assert np.allclose(y, y2, rtol=1e-6, atol=1e-7)
+    assert not orc.rms_norm(np.zeros(8, np.float32), np.ones(8, np.float32), 1e-6).any()
+
+
+def test_rms_norm_per_head_groups_last_axis():
+    # per-head Q/K norm (minfer 2.2): each head normalised on its own
+    x = np.ones((1, 3, 4), np.float32) * np.array([1.0, 10.0, 100.0], np.float32)[None, :, None]
+    y = orc.rms_norm(x, np.ones(4, np.float32), 0.0)
+    assert np.allclose(y, 1.0)
+
+
+# --------------------------------------------------------------------- RoPE
+
+def test_rope_position_zero_is_identity():
+    x = np.random.default_rng(0).standard_normal((1, 3, 128)).astype(np.float32)
+    assert np.array_equal(orc.rope_neox(x, [0], 1e6), x)
+
+
+def test_rope_pair_zero_turns_one_radian_per_position():
+    x = np.zeros((1, 1, 128), np.float32)
+    x[0, 0, 0] = 1.0
+    y = orc.rope_neox(x, [1], 1e6)[0, 0]
+    assert y[0] == np.float32(math.cos(1.0)) and y[64] == np.float32(math.sin(1.0))
+    assert np.count_nonzero(y) == 2          # half layout: channel 0 pairs with 64
+
+
+@pytest.mark.parametrize("i", [1, 5, 63])
+def test_rope_pair_frequency(i):
+    # theta = 1e6, d = 128: f_i = 1e6^(-2i/128) = 10^(-12 i / 128)
+    p = 37
+    x = np.zeros((1, 1, 128), np.float32)
+    x[0, 0, i + 64] = 1.0
+    y = orc.rope_neox(x, [p], 1e6)[0, 0]
+    ang = p * 10.0 ** (-12.0 * i / 128.0)
+    # (a, b) = (0, 1) -> (-sin, cos)
+    assert abs(y[i] + math.sin(ang)) < 1e-7 and abs(y[i + 64] - math.cos(ang)) < 1e-7
+
+
+def test_rope_preserves_norm():
+    x = np.random.default_rng(8).standard_normal((6, 4, 128)).astype(np.float32)
+    y = orc.rope_neox(x, np.arange(100, 106), 1e6)
+    assert np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-6)
+
+
+def test_rope_relative_position_course_numbers():
+    g = golden("rope_relative_position.json")
+    q = np.array(g["q"], np.float32).reshape(1, 1, 2)
+    k = np.array(g["k"], np.float32).reshape(1, 1, 2)
+
+    def score(pq, pk):
+        a = orc.rope_neox(q, [pq], 1e6).astype(np.float64)
+        b = orc.rope_neox(k, [pk], 1e6).astype(np.float64)
+        return float(np.sum(a * b))
+
+    s = [score(*pp) for pp in g["equal_pairs"]]
+    assert abs(s[0] - s[1]) <= g["equal_tolerance"] and abs(s[0] - s[2]) <= g["equal_tolerance"]
+    assert abs(s[0] - score(*g["different_pair"])) > g["different_min_gap"]
+
+
+# ---------------------------------------------------------------- attention
+
+def test_gqa_map_pages_example():
+    g = golden("gqa_map.json")
+    m = orc.kv_head_map(g["n_heads"], g["n_kv_heads"])
+    for h, kv in g["head_to_kv"].items():
+        assert m[int(h)] == kv
+    assert orc.kv_head_map(32, 8)[:8] == [0, 0, 0, 0, 1, 1, 1, 1]
+
+
+def test_attention_single_position_returns_v():
+    rng = np.random.default_rng(9)
+    q = rng.standard_normal((1, 4, 16)).astype(np.float32)
+    k = rng.standard_normal((1, 2, 16)).astype(np.float32)
+    v = rng.standard_normal((1, 2, 16)).astype(np.float32)
+    o = orc.attention(q, k, v, [0], 0.25, orc.kv_head_map(4, 2))
+    assert np.array_equal(o[0, 0], v[0, 0]) and np.array_equal(o[0, 3], v[0, 1])
+
+
+def test_attention_zero_query_is_mean_of_visible_values():
+    rng = np.random.default_rng(10)
+    T = 7
+    k = rng.standard_normal((T, 1, 8)).astype(np.float32)
+    v = rng.standard_normal((T, 1, 8)).astype(np.float32)
+    q = np.zeros((2, 1, 8), np.float32)
+    o = orc.attention(q, k, v, [2, 6], 1.0, [0])
+    assert np.allclose(o[0, 0], v[:3, 0].astype(np.float64).mean(0), atol=1e-7)
+    assert np.allclose(o[1, 0], v[:, 0].astype(np.float64).mean(0), atol=1e-7)
+
+
+def test_attention_two_keys_sigmoid_with_scale():
+    hd = 128
+    q = np.zeros((1, 1, hd), np.float32)
+    k = np.zeros((2, 1, hd), np.float32)
+    v = np.zeros((2, 1, hd), np.float32)
+    q[0, 0, 0] = 2.0
+    k[0, 0, 0], k[1, 0, 0] = 3.0, -1.0
+    v[0, 0, 1], v[1, 0, 2] = 1.0, 1.0
+    o = orc.attention(q, k, v, [1], 1.0 / math.sqrt(hd), [0])
+    s0, s1 = 6.0 / math.sqrt(hd), -2.0 / math.sqrt(hd)
+    w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    assert abs(o[0, 0, 1] - w0) < 1e-7 and abs(o[0, 0, 2] - (1 - w0)) < 1e-7
+
+
+def test_attention_is_causal():
+    rng = np.random.default_rng(11)
+    k = rng.standard_normal((5, 1, 8)).astype(np.float32)
+    v = rng.standard_normal((5, 1, 8)).astype(np.float32)
+    q = rng.standard_normal((1, 1, 8)).astype(np.float32)
+    o1 = orc.attention(q, k, v, [0], 0.3, [0])
+    k[1:] *= 50
+    v[1:] = 7
+    assert np.array_equal(o1, orc.attention(q, k, v, [0], 0.3, [0]))
+    assert np.array_equal(o1[0, 0], v[0, 0])
+
+
+# ----------------------------------------------------------- SwiGLU, argmax
+
+def test_silu_matches_library_logistic():
+    z = np.linspace(-40, 40, 1001)
+    assert np.allclose(orc.silu(z), z * scipy.special.expit(z), rtol=1e-14, atol=1e-300)
+    assert orc.silu(np.array([0.0]))[0] == 0.0
+    g = np.array([1.0, -2.0], np.float32)
+    u = np.array([3.0, 0.5], np.float32)
+    assert np.allclose(orc.swiglu(g, u), g * scipy.special.expit(g.astype(np.float64)) * u, rtol=1e-7)
+
+
+def test_argmax_pages_example_ties_and_nan():
+    g = golden("greedy_argmax.json")
+    assert orc.argmax_lowest(np.array(g["logits"], np.float32)) == g["argmax"]
+    assert orc.argmax_lowest(np.array([1.0, 3.0, 3.0, 2.0])) == 1
+    with pytest.raises(orc.NonFiniteValue):
+        orc.argmax_lowest(np.array([0.0, np.nan]))
+
+
+# ----------------------------------------------------------------- KV cache
+
+def test_kv_cache_contract_pages_example():
+    g = golden("kv_cache_contract.json")
+    c = orc.KvCache(g["n_layers"], g["kv_heads"], g["head_dim"], g["capacity"])
+    k = np.full((g["append_rows"], g["kv_heads"], g["head_dim"]), g["k_fill"], np.float32)
+    v = np.full_like(k, g["v_fill"])
+    c.append_layer(0, k, v)
+    assert c.len == g["len_after_append_before_advance"]
+    c.advance(g["append_rows"])
+    assert c.len == g["len_after_advance"]
+    assert c.layer_rows(0, c.len)[0].size == g["k_slice_elements"]
+    c.truncate(g["truncate_to"])
+    assert c.len == g["len_after_truncate"]
+    c.truncate(5)                      # at or above len: no-op
+    assert c.len == 1
+    with pytest.raises(orc.KvCacheOverflow):
+        c.append_layer(0, np.zeros((8, 2, 4), np.float32), np.zeros((8, 2, 4), np.float32))
+
+
+# -------------------------------------------------------------- whole model
+
+def test_qwen3_0_6b_projection_widths():
+    g = golden("qwen3_widths.json")
+    s = inputs.QWEN3_0_6B
+    cfg = g["config"]
+    assert (s.vocab, s.hidden, s.intermediate, s.n_layers, s.n_heads, s.n_kv_heads, s.head_dim) == (
+        cfg["vocab"], cfg["hidden"], cfg["intermediate"], cfg["n_layers"], cfg["n_heads"],
+        cfg["n_kv_heads"], cfg["head_dim"])
+    small = inputs.Qwen3Shape(vocab=64, hidden=1024, n_layers=1, n_heads=16, n_kv_heads=8,
+                              head_dim=128, intermediate=3072)
+    m = orc.OracleModel.from_f32(small, inputs.generate_weights(small, 0))
+    lw = m.layers[0]
+    assert lw.wq.rows == g["q_width"] and lw.wk.rows == g["kv_width"] and lw.wv.rows == g["kv_width"]
+    assert (lw.wo.rows, lw.wo.cols) == (1024, g["q_width"])
+    for name, ne in g["gguf_ne"].items():
+        obj = getattr(lw, {"attn_q": "wq", "attn_k": "wk", "attn_v": "wv", "attn_output": "wo",
+                           "ffn_gate": "wg", "ffn_up": "wu", "ffn_down": "wd"}.get(name, "x"), None)
+        if obj is not None:                       # GGUF ne order is [in, out]
+            assert [obj.cols, obj.rows] == ne
+    kv_f16 = s.n_layers * 2 * s.n_kv_heads * s.head_dim * 2
+    assert kv_f16 == g["kv_bytes_per_position_f16"]
+    c = m.new_cache(4)
+    assert m.forward(c, [1, 2], 0).shape == (64,)
+
+
+def _rel_l2(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+SMALL_SHAPES = [
+    inputs.Qwen3Shape(vocab=96, hidden=64, n_layers=1, n_heads=4, n_kv_heads=1, head_dim=32,
+                      intermediate=96, tied=True),
+    inputs.Qwen3Shape(vocab=80, hidden=96, n_layers=2, n_heads=2, n_kv_heads=2, head_dim=32,
+                      intermediate=64, tied=False, rope_theta=10000.0),
+    inputs.Qwen3Shape(vocab=64, hidden=128, n_layers=1, n_heads=6, n_kv_heads=3, head_dim=64,
+                      intermediate=160, tied=False, rms_eps=1e-5),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL_SHAPES)
+def test_oracle_matches_f64_cacheless_brute_force_small(shape):
+    from bruteforce_f64 import BruteForceModel
+    w = inputs.generate_weights(shape, 11)
+    m = orc.OracleModel.from_f32(shape, w)
+    tensors = {n: (orc.q8_0_quantize(a) if k == "linear" else a)
+               for n, k, _ in inputs.tensor_specs(shape) for a in [w[n]]}
+    bf = BruteForceModel(shape, tensors)
+    toks = inputs.prompt_tokens(shape, 11, 9)
+    c = m.new_cache(12)
+    got = [m.forward(c, toks[:5], 0)]
+    for t in toks[5:]:
+        got.append(m.forward(c, [t], c.len))
+    for j, lg in enumerate(got):
+        want = bf.last_logits(toks[:5 + j])
+        assert _rel_l2(lg, want) < 2e-6, j
+        assert np.max(np.abs(lg - want)) < 1e-5
+
+
+def test_oracle_matches_f64_cacheless_brute_force_tiny_config():
+    from bruteforce_f64 import BruteForceModel
+    wl = inputs.WORKLOADS["tiny"]
+    s = wl.shape
+    w = inputs.generate_weights(s, wl.seed)
+    m = orc.OracleModel.from_f32(s, w)
+    tensors = {n: (orc.q8_0_quantize(w[n]) if k == "linear" else w[n]) for n, k, _ in inputs.tensor_specs(s)}
+    bf = BruteForceModel(s, tensors)
+    prompt = inputs.prompt_tokens(s, wl.seed, wl.prompt_len)
+    n_steps = 4
+    ids, logits = m.generate_greedy(m.new_cache(64), prompt, n_steps)
+    seq = list(prompt)
+    for j in range(n_steps + 1):
+        want = bf.last_logits(seq)
+        assert _rel_l2(logits[j], want) < 2e-6
+        assert np.max(np.abs(logits[j] - want)) < 1e-5
+        assert ids[j] == int(np.argmax(want))
+        seq.append(ids[j])
+
+
+def test_cached_equals_uncached_and_contract_errors():
+    s = SMALL_SHAPES[0]
+    m = orc.OracleModel.from_f32(s, inputs.generate_weights(s, 3))
+    toks = inputs.prompt_tokens(s, 3, 10)
+    c1 = m.new_cache(10)
+    full = m.forward(c1, toks, 0, all_logits=True)
+    c2 = m.new_cache(10)
+    rows = [m.forward(c2, toks[:4], 0, all_logits=True)]
+    for t in toks[4:]:
+        rows.append(m.forward(c2, [t], c2.len, all_logits=True))
+    inc = np.concatenate(rows, axis=0)
+    assert np.max(np.abs(inc - full)) < 1e-6
+    # K cache rows are identical either way (per-token projections and RoPE)
+    assert np.max(np.abs(c1.k - c2.k)) < 1e-6
+    with pytest.raises(orc.InvalidSequenceLength):
+        m.forward(c2, [1], 3)
+    with pytest.raises(orc.KvCacheOverflow):
+        m.forward(c2, [1], c2.len)
+    c2.truncate(6)
+    lg = m.forward(c2, toks[6:7], 6)
+    assert np.max(np.abs(lg - full[6])) < 1e-6
