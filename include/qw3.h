@@ -1,0 +1,220 @@
+/*
+ * qw3.h -- C ABI of libqw3: the forward pass of a Qwen3-style dense decoder
+ * whose linear weights are GGUF Q8_0 blocks, on one NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (page titles and sections):
+ *   "A transformer from scratch" (Fucina course ch. 12)
+ *     12.3    forward pass: embedding gather, L x (attention block + FFN
+ *             block), final RMSNorm, lm_head on the last row only
+ *     12.3.1  embedding rows dequantised on the fly; tied lm_head reuses the
+ *             embedding table when there is no output weight
+ *     12.3.2  RMSNorm y = x / sqrt(mean(x^2) + eps) * w
+ *     12.3.3  Q/K/V projections; q is n_heads*head_dim wide, k and v
+ *             n_kv_heads*head_dim wide
+ *     12.3.4  NeoX ("half") RoPE, angle p / theta^(2i/d) for pair (i, i+d/2)
+ *     12.3.5  grouped-query causal attention, kv head = h / (n_heads/n_kv),
+ *             scale 1/sqrt(head_dim)
+ *     12.3.6  SwiGLU FFN down(silu(gate x) * up x)
+ *     12.3.7  residual adds
+ *     12.4    KV cache: K stored after norm and RoPE, V as projected; the new
+ *             rows are written at the current length, which moves once per
+ *             call; pos must equal the length, and rows must fit
+ *     12.6    greedy decoding (argmax, lowest index on ties)
+ *   minfer "Qwen3 Support Plan (dense)"
+ *     1       tensor inventory; 2.1 head_dim decoupled from hidden/n_heads;
+ *     2.2     per-head Q/K RMSNorm (length head_dim) before RoPE
+ *   "Model files and quantization" (Fucina course ch. 11)
+ *     11.7    Q8_0: blocks of 32, f16 scale d then 32 int8 q (34 bytes),
+ *             value = d * q; encoder d = max|x| / 127, q = round(x * (1/d))
+ *     11.10   non-finite encoder input is an error
+ *
+ * Conventions
+ *   - Every function returns an int status (enum qw3_status); 0 is success.
+ *   - "_dev" pointers are CUDA device pointers; "_host" pointers are host
+ *     memory read during the call. The caller owns every buffer it passes.
+ *     Buffers are accessed with plain loads and stores of their element
+ *     type: f32/int32 buffers must be 4-byte aligned, Q8_0 blocks 2-byte
+ *     aligned (QW3_ERR_INVALID_ARG otherwise).
+ *   - Q8_0 matrices are [rows][cols/32] blocks in GGUF order (row-major,
+ *     blocks along the input dimension), 34 bytes per block, so a matrix of
+ *     rows x cols takes rows*cols/32*34 bytes. cols must be a multiple of 32.
+ *   - Activations, norm weights, logits and the KV cache are float32.
+ *   - Model calls run asynchronously on the model's stream; host-side
+ *     validation happens before anything is enqueued, and an error leaves
+ *     every sequence length unchanged. Device-side conditions (NaN logits, a
+ *     bounded wait that timed out) are recorded in a status word that
+ *     qw3_sync() returns and clears.
+ *   - Not thread-safe per model: calls on one qw3_model must not overlap.
+ */
+#ifndef QW3_H
+#define QW3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QW3_API __attribute__((visibility("default")))
+#else
+#define QW3_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum qw3_status {
+    QW3_OK = 0,
+    QW3_ERR_INVALID_ARG = 1,  /* null or misaligned pointer, bad count or id */
+    QW3_ERR_SHAPE = 2,        /* a size the format or model cannot take     */
+    QW3_ERR_SEQ_POS = 3,      /* pos != current sequence length (12.4)      */
+    QW3_ERR_KV_OVERFLOW = 4,  /* rows would not fit in the KV cache (12.4)  */
+    QW3_ERR_NONFINITE = 5,    /* NaN/inf encoder input, or NaN logits       */
+    QW3_ERR_OOM = 6,          /* a device or host allocation failed         */
+    QW3_ERR_CUDA = 7,         /* a CUDA runtime call failed                 */
+    QW3_ERR_TIMEOUT = 8       /* a bounded device-side wait expired         */
+};
+
+/* Model geometry and capacities (course 12.1: the nine integers of Config). */
+typedef struct qw3_config {
+    int32_t vocab;          /* V                                            */
+    int32_t hidden;         /* H, multiple of 32                            */
+    int32_t n_layers;       /* L                                            */
+    int32_t n_heads;        /* query heads                                  */
+    int32_t n_kv_heads;     /* key/value heads; n_heads % n_kv_heads == 0   */
+    int32_t head_dim;       /* 64 or 128                                    */
+    int32_t intermediate;   /* FFN width, multiple of 32                    */
+    float rms_eps;          /* 1e-6 for Qwen3                               */
+    float rope_theta;       /* 1e6 for Qwen3                                */
+    int32_t tied_lm_head;   /* 1: lm_head is token_embd                     */
+    int32_t max_seqs;       /* number of sequence slots (KV caches)         */
+    int32_t max_seq_len;    /* KV capacity per sequence, in positions       */
+    int32_t max_prefill;    /* largest chunk one prefill pass processes;
+                               longer prompts run in chunks of this size   */
+    int32_t flags;          /* QW3_FLAG_* bits                              */
+} qw3_config;
+
+#define QW3_FLAG_NO_GRAPH 0x1  /* launch decode kernels directly, no CUDA graph */
+#define QW3_FLAG_NO_PDL   0x2  /* no programmatic dependent launch               */
+#define QW3_FLAG_TRACE    0x4  /* record per-kernel timestamps of decode steps   */
+
+/* One decoder layer (minfer section 1). Q8_0 matrices [out][in]:
+ *   attn_q [n_heads*head_dim][H], attn_k and attn_v [n_kv_heads*head_dim][H],
+ *   attn_output [H][n_heads*head_dim], ffn_gate and ffn_up [I][H],
+ *   ffn_down [H][I]. Norm weights f32: attn_norm [H], attn_q_norm and
+ *   attn_k_norm [head_dim], ffn_norm [H]. */
+typedef struct qw3_layer_weights {
+    const void *attn_q, *attn_k, *attn_v, *attn_output;
+    const void *ffn_gate, *ffn_up, *ffn_down;
+    const float *attn_norm, *attn_q_norm, *attn_k_norm, *ffn_norm;
+} qw3_layer_weights;
+
+/* token_embd and output are Q8_0 [V][H]; output is ignored (may be NULL)
+ * when tied_lm_head. output_norm is f32 [H]. layers is a host array of
+ * n_layers entries. on_device: 1 if every weight pointer is device memory,
+ * 0 if host memory. */
+typedef struct qw3_weights {
+    const void *token_embd;
+    const void *output;
+    const float *output_norm;
+    const qw3_layer_weights *layers;
+    int32_t on_device;
+} qw3_weights;
+
+typedef struct qw3_model qw3_model;
+
+/* Validate cfg (shapes as above, plus the head_dim checks of minfer 2.1),
+ * copy and repack every weight into device storage owned by the model (the
+ * caller may free its buffers when this returns), allocate the KV caches
+ * (max_seqs x max_seq_len positions, f32) and the RoPE table. cuda_stream is
+ * a cudaStream_t the model will run on; NULL makes the model create its own.
+ * On error *out is NULL and nothing is leaked. */
+QW3_API int qw3_create(const qw3_config *cfg, const qw3_weights *weights,
+               void *cuda_stream, qw3_model **out);
+
+/* Wait for outstanding work and free everything the model owns. NULL is ok. */
+QW3_API int qw3_destroy(qw3_model *m);
+
+/* Prefill (course 12.3 with seq = n): append n tokens to sequence `seq` at
+ * positions len..len+n-1 and, when requested, return the last row's logits
+ * (last_logits_dev, f32 [V]) and its argmax (argmax_dev, int32 [1]); both are
+ * nullable. tokens_dev: int32 [n], each in [0, V). n >= 1 and len + n must
+ * not exceed max_seq_len (QW3_ERR_KV_OVERFLOW). */
+QW3_API int qw3_prefill(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n,
+                float *last_logits_dev, int32_t *argmax_dev);
+
+/* One decode step for B sequences at once (course 12.5, batch decode: one
+ * pass over the weights, RoPE positions, KV appends and attention per
+ * sequence). seqs_host: int32 [B] distinct slot ids, NULL means 0..B-1.
+ * tokens_dev: int32 [B]. pos_host: int32 [B], pos_host[b] must equal the
+ * current length of sequence seqs[b] (QW3_ERR_SEQ_POS). logits_dev: nullable
+ * f32 [B][V]. argmax_dev: nullable int32 [B]. Each sequence grows by one. */
+QW3_API int qw3_decode(qw3_model *m, int32_t B, const int32_t *seqs_host,
+               const int32_t *tokens_dev, const int32_t *pos_host,
+               float *logits_dev, int32_t *argmax_dev);
+
+/* n_steps greedy decode steps for B sequences without host round trips
+ * (course 12.6). Step 0 feeds first_tokens_dev[b] (int32 [B]) at the current
+ * length of seqs[b]; step s feeds the argmax of step s-1. out_tokens_dev
+ * receives int32 [n_steps][B] argmax ids. Each sequence grows by n_steps. */
+QW3_API int qw3_generate_greedy(qw3_model *m, int32_t B, const int32_t *seqs_host,
+                        int32_t n_steps, const int32_t *first_tokens_dev,
+                        int32_t *out_tokens_dev);
+
+/* Sequence bookkeeping (course 12.4): reset sets the length to 0, truncate
+ * to min(len, keep_len); neither touches device memory. */
+QW3_API int qw3_reset(qw3_model *m, int32_t seq);
+QW3_API int qw3_truncate(qw3_model *m, int32_t seq, int32_t keep_len);
+QW3_API int qw3_seq_len(const qw3_model *m, int32_t seq, int32_t *len_out);
+
+/* Copy positions [pos0, pos0+n) of one layer's cache for `seq` into
+ * k_out_dev and v_out_dev, each f32 [n][n_kv_heads][head_dim] (the pages'
+ * [seq, kv_head, d] layout). Enqueued on the model's stream. */
+QW3_API int qw3_debug_read_kv(qw3_model *m, int32_t layer, int32_t seq, int32_t pos0,
+                      int32_t n, float *k_out_dev, float *v_out_dev);
+
+/* Timestamps of the most recent decode step, recorded when the model was
+ * created with QW3_FLAG_TRACE: for each kernel of the step, in launch order,
+ * two records (its first and its last CTA) of 8 u64 each: %globaltimer (ns)
+ * at entry, after the wait for the previous kernel, after the prologue, after
+ * the weight/KV stream, at exit; then two kernel-specific words, then the SM
+ * id. out_host receives min(max_records, available) records; *n_out is the
+ * number written. Synchronises the model's stream. */
+QW3_API int qw3_debug_read_trace(qw3_model *m, uint64_t *out_host, int32_t max_records, int32_t *n_out);
+
+/* Block until the model's stream is idle; return and clear the first
+ * device-side status recorded since the last call (QW3_ERR_NONFINITE for NaN
+ * logits, QW3_ERR_TIMEOUT for an expired bounded wait), else QW3_OK. */
+QW3_API int qw3_sync(qw3_model *m);
+
+/* The model's stream as a cudaStream_t. */
+QW3_API void *qw3_stream(const qw3_model *m);
+
+QW3_API const char *qw3_status_string(int status);
+/* Detail of the last error on this model (never NULL). */
+QW3_API const char *qw3_last_error(const qw3_model *m);
+
+/* ---- standalone Q8_0 entries on caller device buffers ----------------- */
+
+/* Encode n f32 values (n % 32 == 0, else QW3_ERR_SHAPE) into n/32 Q8_0
+ * blocks at blocks_dev (n/32*34 bytes), course 11.7: per block amax, d =
+ * amax/127 (f32), inv_d = d ? 1/d : 0, q = clamp(round(x*inv_d), +-127) with
+ * halves rounded away from zero, d stored as IEEE f16 (nearest even). A block
+ * holding NaN or inf is written as all-zero bytes and, if status_dev is not
+ * NULL, *status_dev is set to QW3_ERR_NONFINITE (the caller zeroes it first).
+ * Asynchronous on `stream`. */
+QW3_API int qw3_q8_0_quantize(const float *x_dev, int64_t n, void *blocks_dev,
+                      int32_t *status_dev, void *stream);
+
+/* Decode n values (n % 32 == 0) of Q8_0 blocks to f32: y = f32(d) * q. */
+QW3_API int qw3_q8_0_dequantize(const void *blocks_dev, int64_t n, float *y_dev, void *stream);
+
+/* y[b][r] = sum_k W[r][k] * x[b][k] for a raw Q8_0 matrix W [rows][cols/32]
+ * (GGUF layout), x f32 [B][cols], y f32 [B][rows]; f32 accumulation.
+ * 1 <= B <= 8, cols % 32 == 0. */
+QW3_API int qw3_q8_0_gemv(const void *W_dev, int32_t rows, int32_t cols,
+                  const float *x_dev, int32_t B, float *y_dev, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QW3_H */

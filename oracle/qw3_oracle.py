@@ -111,7 +111,8 @@ def q8_0_quantize_parts(x: np.ndarray):
     prod = np.where(nan, np.float32(0.0), prod)
     r = np.clip(_round_half_away(prod), -127.0, 127.0)
     q = r.astype(np.int8)
-    d16 = d.astype(np.float16)
+    with np.errstate(over="ignore"):
+        d16 = d.astype(np.float16)   # |d| above the f16 range stores as inf
     return d, q, d16
 
 

@@ -1,0 +1,575 @@
+// Grouped-query causal attention ("A transformer from scratch", 12.3.5):
+// query head h reads KV head h / (n_heads / n_kv_heads); scores q.k * scale,
+// scale = 1/sqrt(head_dim) (minfer 2.1); softmax with the running maximum
+// subtracted; output = softmax-weighted sum of V. The cache holds K after the
+// per-head norm and RoPE and V as projected (12.4).
+//
+// KV cache layout (device, f32): [layer][seq][K|V][kv_head][capacity][head_dim]
+// so one head's positions are contiguous and stream as single bulk copies.
+//
+// Decode kernel (one new token per sequence): split-K over the context.
+// CTA (g, s, b) covers positions [s*chunk, min((s+1)*chunk, ctx)) of kv head g
+// for sequence b, for all n_heads/n_kv query heads of the group at once, so
+// each K/V byte is read once. Cached rows are staged by 1-D bulk copies
+// (TMA) issued before griddepcontrol.wait: they were written by earlier
+// steps. After the wait the CTA applies the per-head Q/K RMSNorm and RoPE to
+// the new q/k (minfer 2.2, course 12.3.4); the CTA whose range holds the new
+// position also appends k, v to the cache. Partial (max, sum, acc) per head
+// and split go to global memory; the last CTA of (b, g) to arrive merges
+// them (flash-decoding combine) and writes o.
+#include "qw3_internal.cuh"
+
+namespace qw3 {
+
+namespace {
+
+constexpr int kAttnThreads = 128;
+constexpr int kTileP = 32;   // positions per staged tile
+constexpr int kStages = 2;
+
+// A partial row holds acc[HD], then m and l; padded to HD + 4 floats so every
+// row starts on a 16-byte boundary for the vector stores.
+template <int HD>
+__host__ __device__ constexpr int part_stride() { return HD + 4; }
+
+template <int HD>
+__device__ __forceinline__ void load_lane(const float *src, float (&v)[HD / 32], int lane) {
+    constexpr int E = HD / 32;
+    if constexpr (E == 4) {
+        const float4 t = *reinterpret_cast<const float4 *>(src + lane * 4);
+        v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+        const float2 t = *reinterpret_cast<const float2 *>(src + lane * 2);
+        v[0] = t.x; v[1] = t.y;
+    }
+}
+
+template <int HD>
+__device__ __forceinline__ void store_lane(float *dst, const float (&v)[HD / 32], int lane) {
+    constexpr int E = HD / 32;
+    if constexpr (E == 4) {
+        *reinterpret_cast<float4 *>(dst + lane * 4) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+        *reinterpret_cast<float2 *>(dst + lane * 2) = make_float2(v[0], v[1]);
+    }
+}
+
+// Per-head RMSNorm over head_dim then NeoX rotation at position p; the lane
+// holds dims [lane*E, lane*E+E), its rotation partner sits in lane ^ 16.
+template <int HD>
+__device__ __forceinline__ void norm_rope_lane(float (&v)[HD / 32], const float *w, float eps,
+                                               const float2 *rope_row, int lane) {
+    constexpr int E = HD / 32;
+    float ss = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
+    ss = warp_sum(ss);
+    const float r = 1.0f / sqrtf(ss / static_cast<float>(HD) + eps);
+    float wl[E];
+    load_lane<HD>(w, wl, lane);
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = v[e] * r * wl[e];
+    const bool first_half = lane < 16;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const float other = __shfl_xor_sync(0xffffffffu, v[e], 16);
+        const float2 cs = rope_row[(lane & 15) * E + e];
+        v[e] = first_half ? (v[e] * cs.x - other * cs.y) : (other * cs.y + v[e] * cs.x);
+    }
+}
+
+template <int HD, int G>
+__global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, int nsplit) {
+    constexpr int E = HD / 32;
+    constexpr int PS = part_stride<HD>();
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    float *ktile = reinterpret_cast<float *>(smem + 128);               // [kStages][kTileP][HD]
+    float *vtile = ktile + kStages * kTileP * HD;                         // [kStages][kTileP][HD]
+    float *qn = vtile + kStages * kTileP * HD;                            // [G][HD]
+    float *knew = qn + G * HD;                                            // [HD]
+    float *vnew = knew + HD;                                              // [HD]
+    float *mrg = vnew + HD;                                               // [4][G][PS]
+    int *flags = reinterpret_cast<int *>(mrg + 4 * G * PS);
+
+    const int g = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    unsigned long long *tr = (tid == 0) ? trace_slot(a.trace) : nullptr;
+    if (tr) {
+        tr[0] = globaltimer_ns();
+        tr[5] = clock64();
+        tr[7] = smid();
+    }
+    const int seq = a.seq_ids[b];
+    const int p = a.pos[b];
+    const int ctx = p + 1;
+    const int chunk = (ctx + nsplit - 1) / nsplit;
+    const int start = s * chunk;
+    const int end = min(ctx, start + chunk);
+    const bool has_new = (start <= p) && (p < end);
+    const int n_cached = max(0, min(end, p) - start);
+    const int ntiles = (n_cached + kTileP - 1) / kTileP;
+
+    const float *kbase = a.kv + static_cast<size_t>(seq) * a.seq_stride + static_cast<size_t>(g) * a.head_stride;
+    const float *vbase = kbase + a.kvsel_stride;
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        flags[0] = 0;
+        flags[1] = 0;
+    }
+    __syncthreads();
+    const uint64_t pol = policy_evict_first();
+    if (tid == 0) {
+        for (int t = 0; t < ntiles && t < kStages; ++t) {
+            const int rows = min(kTileP, n_cached - t * kTileP);
+            const uint32_t bytes = static_cast<uint32_t>(rows * HD * 4);
+            const size_t off = static_cast<size_t>(start + t * kTileP) * HD;
+            mbar_arrive_expect_tx(&bars[t], 2 * bytes);
+            bulk_g2s(ktile + t * kTileP * HD, kbase + off, bytes, &bars[t], pol);
+            bulk_g2s(vtile + t * kTileP * HD, vbase + off, bytes, &bars[t], pol);
+        }
+    }
+    pdl_wait();
+    if (tr) tr[1] = globaltimer_ns();
+
+    // ---- new token: per-head norm + RoPE of q (and k), append k and v
+    const float2 *rope_row = a.rope + static_cast<size_t>(p) * (HD / 2);
+    const float *qkv_b = a.qkv + static_cast<size_t>(b) * a.qkv_stride;
+    for (int t = warp; t < G + 2; t += kAttnThreads / 32) {
+        float v[E];
+        if (t < G) {
+            load_lane<HD>(qkv_b + (g * G + t) * HD, v, lane);
+            norm_rope_lane<HD>(v, a.q_norm, a.eps, rope_row, lane);
+            store_lane<HD>(qn + t * HD, v, lane);
+        } else if (has_new && t == G) {
+            load_lane<HD>(qkv_b + a.nh * HD + g * HD, v, lane);
+            norm_rope_lane<HD>(v, a.k_norm, a.eps, rope_row, lane);
+            store_lane<HD>(knew, v, lane);
+            store_lane<HD>(const_cast<float *>(kbase) + static_cast<size_t>(p) * HD, v, lane);
+        } else if (has_new && t == G + 1) {
+            load_lane<HD>(qkv_b + (a.nh + a.nkv) * HD + g * HD, v, lane);
+            store_lane<HD>(vnew, v, lane);
+            store_lane<HD>(const_cast<float *>(vbase) + static_cast<size_t>(p) * HD, v, lane);
+        }
+    }
+    __syncthreads();
+    pdl_trigger();
+    if (tr) tr[2] = globaltimer_ns();
+
+    float qv[G][E];
+#pragma unroll
+    for (int t = 0; t < G; ++t) load_lane<HD>(qn + t * HD, qv[t], lane);
+    float m[G], l[G], acc[G][E];
+#pragma unroll
+    for (int t = 0; t < G; ++t) {
+        m[t] = -INFINITY;
+        l[t] = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[t][e] = 0.0f;
+    }
+
+    // Score NP positions at once: NP * G independent butterfly reductions
+    // keep the shuffle pipe busy; one online-softmax update per batch.
+    constexpr int NP = 4;
+    auto consume = [&](const float *krows, const float *vrows, int n) {
+        float kv_[NP][E];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            if (j < n) {
+                load_lane<HD>(krows + j * HD, kv_[j], lane);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) kv_[j][e] = 0.0f;
+            }
+        }
+        float sc[G][NP];
+#pragma unroll
+        for (int t = 0; t < G; ++t)
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                float d = 0.0f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) d = fmaf(qv[t][e], kv_[j][e], d);
+                sc[t][j] = d;
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int t = 0; t < G; ++t)
+#pragma unroll
+                for (int j = 0; j < NP; ++j) sc[t][j] += __shfl_xor_sync(0xffffffffu, sc[t][j], o);
+        float vv[NP][E];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            if (j < n) load_lane<HD>(vrows + j * HD, vv[j], lane);
+        }
+#pragma unroll
+        for (int t = 0; t < G; ++t) {
+            float mx = m[t];
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                sc[t][j] = (j < n) ? sc[t][j] * a.scale : -INFINITY;
+                mx = fmaxf(mx, sc[t][j]);
+            }
+            const float corr = expf(m[t] - mx);
+            l[t] *= corr;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[t][e] *= corr;
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                if (j < n) {
+                    const float pr = expf(sc[t][j] - mx);
+                    l[t] += pr;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[t][e] = fmaf(pr, vv[j][e], acc[t][e]);
+                }
+            }
+            m[t] = mx;
+        }
+    };
+
+    for (int t = 0; t < ntiles; ++t) {
+        const int si = t % kStages;
+        const bool ok = mbar_wait_bounded(&bars[si], static_cast<uint32_t>((t / kStages) & 1));
+        if (!ok) flags[0] = 1, flags[1] = t;
+        if (ok) {
+            const int rows = min(kTileP, n_cached - t * kTileP);
+            // warp w takes positions [w*NP, w*NP+NP), then every 4th batch
+            for (int j0 = warp * NP; j0 < rows; j0 += (kAttnThreads / 32) * NP)
+                consume(ktile + (si * kTileP + j0) * HD, vtile + (si * kTileP + j0) * HD, min(NP, rows - j0));
+        }
+        __syncthreads();
+        if (flags[0]) break;
+        if (tid == 0 && t + kStages < ntiles) {
+            const int tt = t + kStages;
+            const int rows = min(kTileP, n_cached - tt * kTileP);
+            const uint32_t bytes = static_cast<uint32_t>(rows * HD * 4);
+            const size_t off = static_cast<size_t>(start + tt * kTileP) * HD;
+            mbar_arrive_expect_tx(&bars[si], 2 * bytes);
+            bulk_g2s(ktile + si * kTileP * HD, kbase + off, bytes, &bars[si], pol);
+            bulk_g2s(vtile + si * kTileP * HD, vbase + off, bytes, &bars[si], pol);
+        }
+        __syncthreads();
+    }
+    if (flags[0]) {
+        if (tid == 0) {
+            record_status(a.status, QW3_ERR_TIMEOUT);
+            const int first = flags[1];
+            for (int t = first; t < ntiles && t < first + kStages; ++t)
+                (void)mbar_wait_bounded(&bars[t % kStages], static_cast<uint32_t>((t / kStages) & 1));
+        }
+        return;
+    }
+    if (has_new && warp == (kAttnThreads / 32) - 1) consume(knew, vnew, 1);
+    if (tr) tr[3] = globaltimer_ns();
+
+    // ---- merge the four warps, write this split's partial
+#pragma unroll
+    for (int t = 0; t < G; ++t) {
+        float *mw = mrg + (warp * G + t) * PS;
+        store_lane<HD>(mw, acc[t], lane);
+        if (lane == 0) {
+            mw[HD] = m[t];
+            mw[HD + 1] = l[t];
+        }
+    }
+    __syncthreads();
+    for (int t = warp; t < G; t += kAttnThreads / 32) {
+        float M = -INFINITY;
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, mrg[(w * G + t) * PS + HD]);
+        float L = 0.0f, o[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = 0.0f;
+        if (M != -INFINITY) {
+            for (int w = 0; w < 4; ++w) {
+                const float *mw = mrg + (w * G + t) * PS;
+                const float f = expf(mw[HD] - M);
+                L = fmaf(mw[HD + 1], f, L);
+                float aw[E];
+                load_lane<HD>(mw, aw, lane);
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[e] = fmaf(aw[e], f, o[e]);
+            }
+        }
+        const int h = g * G + t;
+        float *pp = a.partial + ((static_cast<size_t>(b) * a.nh + h) * nsplit + s) * PS;
+        store_lane<HD>(pp, o, lane);
+        if (lane == 0) {
+            pp[HD] = M;
+            pp[HD + 1] = L;
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(&a.counters[b * a.nkv + g], 1u);
+        flags[2] = (prev == static_cast<unsigned>(nsplit - 1)) ? 1 : 0;
+    }
+    __syncthreads();
+    if (tr) {
+        tr[4] = globaltimer_ns();
+        tr[6] = clock64();
+    }
+    if (!flags[2]) return;
+    __threadfence();
+    // ---- last CTA of (b, g): merge the splits. The G heads' partials are
+    // contiguous ([h][split][PS]); pull them into the (now free) K/V tile
+    // buffer with one coalesced pass, then reduce from shared memory.
+    {
+        const float *src = a.partial + (static_cast<size_t>(b) * a.nh + g * G) * nsplit * PS;
+        const int nf = G * nsplit * PS;
+        float *stage = ktile;   // 2 * kStages * kTileP * HD floats available
+        for (int i = tid * 4; i < nf; i += kAttnThreads * 4)
+            *reinterpret_cast<float4 *>(stage + i) = __ldcg(reinterpret_cast<const float4 *>(src + i));
+        __syncthreads();
+        for (int t = warp; t < G; t += kAttnThreads / 32) {
+            const float *base = stage + t * nsplit * PS;
+            float M = -INFINITY;
+            for (int j = lane; j < nsplit; j += 32) M = fmaxf(M, base[j * PS + HD]);
+            M = warp_max(M);
+            float L = 0.0f, o[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[e] = 0.0f;
+            for (int j = 0; j < nsplit; ++j) {
+                const float mj = base[j * PS + HD];
+                if (mj == -INFINITY) continue;
+                const float f = expf(mj - M);
+                L = fmaf(base[j * PS + HD + 1], f, L);
+                float aw[E];
+                load_lane<HD>(base + j * PS, aw, lane);
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[e] = fmaf(aw[e], f, o[e]);
+            }
+            const float inv = 1.0f / L;
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[e] *= inv;
+            store_lane<HD>(a.out + static_cast<size_t>(b) * a.nh * HD + (g * G + t) * HD, o, lane);
+        }
+    }
+    if (tid == 0) a.counters[b * a.nkv + g] = 0u;
+}
+
+size_t attn_decode_smem(int HD, int G) {
+    return 128 + static_cast<size_t>(2 * kStages * kTileP * HD + G * HD + 2 * HD + 4 * G * (HD + 4)) * 4 + 16;
+}
+
+template <int HD, int G>
+cudaError_t configure_attn_t() {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_decode<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(attn_decode_smem(HD, G)));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_attn_decode<HD, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+}
+
+template <int HD, int G>
+cudaError_t launch_attn_t(const AttnDecodeArgs &a, int B, int nsplit, bool pdl, cudaStream_t s) {
+    const size_t smem = attn_decode_smem(HD, G);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(a.nkv, nsplit, B);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_attn_decode<HD, G>, a, nsplit);
+}
+
+// ------------------------------------------------------------- prefill
+// Causal flash attention over a chunk of M query rows at positions
+// pos0..pos0+M-1, keys 0..pos0+M-1 from the cache (this chunk's rows were
+// appended just before). CTA = (64-query tile, query head); warp w owns 8
+// query rows; for each 32-key tile lane j scores key j, then lanes own
+// head_dim slices for the P.V product. f32 throughout.
+template <int HD>
+__global__ void __launch_bounds__(256) k_attn_prefill(const float *__restrict__ qkv, int M, int qkv_stride,
+                                                      const float *__restrict__ kv_k, const float *__restrict__ kv_v,
+                                                      size_t head_stride, int pos0, int nh, int group, float scale,
+                                                      float *__restrict__ out) {
+    constexpr int E = HD / 32;
+    constexpr int KP = HD + 4;   // padded K row
+    extern __shared__ __align__(16) float sm[];
+    float *Qs = sm;                       // [64][HD]
+    float *Ks = Qs + 64 * HD;             // [32][KP]
+    float *Vs = Ks + 32 * KP;             // [32][HD]
+    float *Ps = Vs + 32 * HD;             // [8 warps][8][32]
+    const int tile = gridDim.x - 1 - blockIdx.x;   // heavy (late) tiles first
+    const int h = blockIdx.y;
+    const int g = h / group;
+    const int q0 = tile * 64;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const float *kb = kv_k + static_cast<size_t>(g) * head_stride;
+    const float *vb = kv_v + static_cast<size_t>(g) * head_stride;
+
+    for (int i = tid; i < 64 * HD / 4; i += 256) {
+        const int r = (i * 4) / HD, c = (i * 4) % HD;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (q0 + r < M) v = *reinterpret_cast<const float4 *>(qkv + static_cast<size_t>(q0 + r) * qkv_stride + h * HD + c);
+        *reinterpret_cast<float4 *>(Qs + r * HD + c) = v;
+    }
+    float m[8], l[8], acc[8][E];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        m[r] = -INFINITY;
+        l[r] = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[r][e] = 0.0f;
+    }
+    const int last_q = min(M, q0 + 64) - 1;
+    const int nkeys = pos0 + last_q + 1;
+    for (int t0 = 0; t0 < nkeys; t0 += 32) {
+        __syncthreads();
+        for (int i = tid; i < 32 * HD / 4; i += 256) {
+            const int r = (i * 4) / HD, c = (i * 4) % HD;
+            float4 kv4 = make_float4(0.f, 0.f, 0.f, 0.f), vv4 = kv4;
+            if (t0 + r < nkeys) {
+                kv4 = *reinterpret_cast<const float4 *>(kb + static_cast<size_t>(t0 + r) * HD + c);
+                vv4 = *reinterpret_cast<const float4 *>(vb + static_cast<size_t>(t0 + r) * HD + c);
+            }
+            *reinterpret_cast<float4 *>(Ks + r * KP + c) = kv4;
+            *reinterpret_cast<float4 *>(Vs + r * HD + c) = vv4;
+        }
+        __syncthreads();
+        float s[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) s[r] = 0.0f;
+        for (int d = 0; d < HD; d += 4) {
+            const float4 k4 = *reinterpret_cast<const float4 *>(Ks + lane * KP + d);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const float4 q4 = *reinterpret_cast<const float4 *>(Qs + (warp * 8 + r) * HD + d);
+                s[r] = fmaf(q4.x, k4.x, s[r]);
+                s[r] = fmaf(q4.y, k4.y, s[r]);
+                s[r] = fmaf(q4.z, k4.z, s[r]);
+                s[r] = fmaf(q4.w, k4.w, s[r]);
+            }
+        }
+        const int kpos = t0 + lane;
+        float corr[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int qpos = pos0 + q0 + warp * 8 + r;
+            const float sc = (kpos <= qpos && kpos < nkeys) ? s[r] * scale : -INFINITY;
+            const float mx = warp_max(sc);
+            const float mn = fmaxf(m[r], mx);
+            // rows beyond M, or with nothing visible yet, keep m = -inf
+            const float pr = (mn == -INFINITY) ? 0.0f : expf(sc - mn);
+            corr[r] = (mn == -INFINITY) ? 1.0f : expf(m[r] - mn);
+            l[r] = l[r] * corr[r] + warp_sum(pr);
+            m[r] = mn;
+            Ps[(warp * 8 + r) * 32 + lane] = pr;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[r][e] *= corr[r];
+        for (int j = 0; j < 32; ++j) {
+            float vv[E];
+            load_lane<HD>(Vs + j * HD, vv, lane);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const float pj = Ps[(warp * 8 + r) * 32 + j];
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[r][e] = fmaf(pj, vv[e], acc[r][e]);
+            }
+        }
+        __syncwarp();
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int row = q0 + warp * 8 + r;
+        if (row < M) {
+            const float inv = 1.0f / l[r];
+            float o[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[e] = acc[r][e] * inv;
+            store_lane<HD>(out + static_cast<size_t>(row) * nh * HD + h * HD, o, lane);
+        }
+    }
+}
+
+template <int HD>
+size_t prefill_smem() {
+    return static_cast<size_t>(64 * HD + 32 * (HD + 4) + 32 * HD + 8 * 8 * 32) * 4;
+}
+
+template <int HD>
+cudaError_t launch_prefill_t(const float *qkv, int M, int qkv_stride, const float *kv_k, const float *kv_v,
+                             size_t head_stride, int pos0, int nh, int group, float scale, float *out,
+                             cudaStream_t s) {
+    const size_t smem = prefill_smem<HD>();
+    dim3 grid((M + 63) / 64, nh);
+    k_attn_prefill<HD><<<grid, 256, smem, s>>>(qkv, M, qkv_stride, kv_k, kv_v, head_stride, pos0, nh, group,
+                                               scale, out);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int attn_decode_max_nsplit(int hd, int G) {
+    // the last CTA stages G * nsplit partial rows in its K/V tile buffer
+    const int cap = 2 * kStages * kTileP * hd;
+    const int n = cap / (G * (hd + 4));
+    return n < 1 ? 1 : (n > 64 ? 64 : n);
+}
+
+cudaError_t configure_attention() {
+    cudaError_t e;
+#define QW3_CFG(x) if ((e = (x)) != cudaSuccess) return e
+    QW3_CFG((configure_attn_t<128, 1>()));
+    QW3_CFG((configure_attn_t<128, 2>()));
+    QW3_CFG((configure_attn_t<128, 4>()));
+    QW3_CFG((configure_attn_t<128, 8>()));
+    QW3_CFG((configure_attn_t<64, 1>()));
+    QW3_CFG((configure_attn_t<64, 2>()));
+    QW3_CFG((configure_attn_t<64, 4>()));
+    QW3_CFG((configure_attn_t<64, 8>()));
+    QW3_CFG(cudaFuncSetAttribute(k_attn_prefill<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(prefill_smem<128>())));
+    QW3_CFG(cudaFuncSetAttribute(k_attn_prefill<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(prefill_smem<64>())));
+#undef QW3_CFG
+    return cudaSuccess;
+}
+
+cudaError_t launch_attn_decode(const AttnDecodeArgs &a, int B, int nsplit, bool pdl, cudaStream_t s) {
+    const int G = a.nh / a.nkv;
+    if (nsplit < 1 || nsplit > attn_decode_max_nsplit(a.hd, G)) return cudaErrorInvalidValue;
+    if (a.hd == 128) {
+        switch (G) {
+            case 1: return launch_attn_t<128, 1>(a, B, nsplit, pdl, s);
+            case 2: return launch_attn_t<128, 2>(a, B, nsplit, pdl, s);
+            case 4: return launch_attn_t<128, 4>(a, B, nsplit, pdl, s);
+            case 8: return launch_attn_t<128, 8>(a, B, nsplit, pdl, s);
+            default: break;
+        }
+    } else if (a.hd == 64) {
+        switch (G) {
+            case 1: return launch_attn_t<64, 1>(a, B, nsplit, pdl, s);
+            case 2: return launch_attn_t<64, 2>(a, B, nsplit, pdl, s);
+            case 4: return launch_attn_t<64, 4>(a, B, nsplit, pdl, s);
+            case 8: return launch_attn_t<64, 8>(a, B, nsplit, pdl, s);
+            default: break;
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_prefill(const float *qkv, int M, int qkv_stride, const float *kv, size_t layer_off,
+                                size_t seq_off, size_t kvsel_stride, size_t head_stride, int pos0, int nh,
+                                int nkv, int hd, float scale, float *out, cudaStream_t s) {
+    const float *kk = kv + layer_off + seq_off;
+    const float *vv = kk + kvsel_stride;
+    const int group = nh / nkv;
+    if (hd == 128) return launch_prefill_t<128>(qkv, M, qkv_stride, kk, vv, head_stride, pos0, nh, group, scale, out, s);
+    if (hd == 64) return launch_prefill_t<64>(qkv, M, qkv_stride, kk, vv, head_stride, pos0, nh, group, scale, out, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace qw3

@@ -1,0 +1,789 @@
+// Host side of libqw3: the C ABI declared in include/qw3.h.
+//
+// The forward pass follows "A transformer from scratch" (Fucina course
+// ch. 12), sections 12.3-12.6, with the Qwen3 deltas of minfer's "Qwen3
+// Support Plan (dense)", section 2: embedding gather, per layer
+// [RMSNorm -> QKV -> per-head Q/K RMSNorm -> NeoX RoPE -> KV append -> causal
+// GQA -> o_proj + residual -> RMSNorm -> gate/up -> SwiGLU -> down + residual],
+// final RMSNorm, lm_head on the last row, greedy argmax.
+//
+// Decode (B <= 4 rows): one GEMV kernel per projection with fused norm
+// prologues and residual/SwiGLU/argmax epilogues, one split-K attention kernel
+// per layer; the step is captured once per B as a CUDA graph whose kernels
+// are chained with programmatic dependent launch. Larger batches and prefill
+// use the tiled GEMM path.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "qw3_internal.cuh"
+
+namespace qw3 {
+
+namespace {
+thread_local std::string g_err;
+}
+
+void set_thread_error(const std::string &msg) { g_err = msg; }
+const std::string &thread_error() { return g_err; }
+
+int cuda_fail(cudaError_t e, const char *what, const char *file, int line) {
+    char buf[512];
+    snprintf(buf, sizeof buf, "%s failed: %s (%s:%d)", what, cudaGetErrorString(e), file, line);
+    set_thread_error(buf);
+    if (e == cudaErrorMemoryAllocation) return QW3_ERR_OOM;
+    return QW3_ERR_CUDA;
+}
+
+int num_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 1;
+    }
+    return cached[dev];
+}
+
+namespace {
+
+std::once_flag g_cfg_once;
+cudaError_t g_cfg_err = cudaSuccess;
+
+cudaError_t configure_all() {
+    std::call_once(g_cfg_once, [] {
+        cudaError_t e = configure_gemv();
+        if (e == cudaSuccess) e = configure_attention();
+        if (e == cudaSuccess) e = configure_misc();
+        g_cfg_err = e;
+    });
+    return g_cfg_err;
+}
+
+// Device allocations go through here so that tests can make the n-th one
+// fail (QW3_FAULT_ALLOC_AT=n) and check that create cleans up.
+int g_alloc_count = 0;
+int g_alloc_fail_at = -1;
+
+cudaError_t dev_alloc(void **p, size_t bytes) {
+    ++g_alloc_count;
+    if (g_alloc_fail_at > 0 && g_alloc_count == g_alloc_fail_at) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMalloc(p, bytes);
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+}  // namespace qw3
+
+using namespace qw3;
+
+struct qw3_model {
+    qw3_config cfg{};
+    cudaStream_t stream = nullptr;
+    bool own_stream = false;
+    cudaStream_t cap_stream = nullptr;
+    std::string err;
+
+    std::vector<void *> allocs;
+
+    std::vector<LayerDev> layers;
+    QMat embd, out;
+    float *out_norm = nullptr;
+    float2 *rope = nullptr;
+
+    float *kv = nullptr;
+    size_t head_stride = 0, kvsel_stride = 0, seq_stride = 0, layer_stride = 0;
+    std::vector<int32_t> seq_len;
+
+    // decode scratch
+    int qkv_w = 0;
+    float *x = nullptr, *h = nullptr, *qkv = nullptr, *o = nullptr, *act = nullptr, *partial = nullptr;
+    unsigned int *counters = nullptr, *done_counter = nullptr;
+    unsigned long long *argmax_key = nullptr;
+    int32_t *d_tok = nullptr, *d_pos = nullptr, *d_seq = nullptr, *d_step = nullptr, *d_status = nullptr;
+    DecodeIO *d_io = nullptr;
+    int max_nsplit = 0;
+
+    // prefill scratch
+    float *px = nullptr, *ph = nullptr, *pqkv = nullptr, *po = nullptr, *pact = nullptr;
+
+    std::map<int, cudaGraphExec_t> graphs;
+
+    // QW3_FLAG_TRACE: per-kernel timestamp records of the latest decode step
+    unsigned long long *trace = nullptr;
+    int trace_kernels = 0;
+};
+
+namespace {
+
+int fail(qw3_model *m, int code, const std::string &msg) {
+    if (m) m->err = msg;
+    set_thread_error(msg);
+    return code;
+}
+
+int cuda_err(qw3_model *m, cudaError_t e, const char *what) {
+    const int code = (e == cudaErrorMemoryAllocation) ? QW3_ERR_OOM : QW3_ERR_CUDA;
+    return fail(m, code, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define M_TRY(m, expr)                                        \
+    do {                                                      \
+        cudaError_t _e = (expr);                              \
+        if (_e != cudaSuccess) return cuda_err((m), _e, #expr); \
+    } while (0)
+
+cudaError_t model_alloc(qw3_model *m, void **p, size_t bytes) {
+    cudaError_t e = dev_alloc(p, bytes < 256 ? 256 : bytes);
+    if (e == cudaSuccess) m->allocs.push_back(*p);
+    return e;
+}
+
+void free_all(qw3_model *m) {
+    for (auto &kv : m->graphs) cudaGraphExecDestroy(kv.second);
+    m->graphs.clear();
+    for (void *p : m->allocs) cudaFree(p);
+    m->allocs.clear();
+    if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
+    m->cap_stream = nullptr;
+    if (m->own_stream && m->stream) cudaStreamDestroy(m->stream);
+    m->stream = nullptr;
+}
+
+// Tile width of the repacked layout: the whole row up to 4096 columns.
+int tile_width(int cols) {
+    int kt = cols;
+    while (kt > 4096 && kt % 2 == 0 && (kt / 2) % 32 == 0) kt /= 2;
+    return kt;
+}
+
+QMat qmat_shape(int rows, int cols, int kt = 0, int ktile_major = 0) {
+    QMat q;
+    q.rows = rows;
+    q.cols = cols;
+    q.rows_pad = static_cast<int>(align_up(static_cast<size_t>(rows), kRowAlign));
+    q.kt = kt ? kt : tile_width(cols);
+    q.ktile_major = ktile_major;
+    return q;
+}
+
+size_t qmat_bytes(int rows, int cols) { return align_up(qm_bytes(qmat_shape(rows, cols)), 256); }
+
+void qmat_place(QMat &q, uint8_t *&cursor, int rows, int cols) {
+    q = qmat_shape(rows, cols);
+    q.base = cursor;
+    cursor += align_up(qm_bytes(q), 256);
+}
+
+// Copy (if on the host) and repack one raw Q8_0 matrix into rows
+// dst_row0 + r * dst_stride of q.
+int repack_into(qw3_model *m, const QMat &q, const void *raw, int rows, int cols, int dst_row0, int dst_stride,
+                bool on_device, uint8_t *staging) {
+    if (!raw) return fail(m, QW3_ERR_INVALID_ARG, "null weight pointer");
+    if (on_device && (reinterpret_cast<uintptr_t>(raw) & 1u))
+        return fail(m, QW3_ERR_INVALID_ARG, "Q8_0 blocks must be 2-byte aligned");
+    const size_t bytes = static_cast<size_t>(rows) * (cols / 32) * 34;
+    const uint8_t *src = static_cast<const uint8_t *>(raw);
+    if (!on_device) {
+        M_TRY(m, cudaMemcpyAsync(staging, raw, bytes, cudaMemcpyHostToDevice, m->stream));
+        src = staging;
+    }
+    M_TRY(m, launch_repack(src, rows, cols, q, dst_row0, dst_stride, m->stream));
+    if (!on_device) M_TRY(m, cudaStreamSynchronize(m->stream));
+    return QW3_OK;
+}
+
+int copy_f32(qw3_model *m, float *dst, const float *src, size_t n, bool on_device) {
+    if (!src) return fail(m, QW3_ERR_INVALID_ARG, "null norm weight pointer");
+    M_TRY(m, cudaMemcpyAsync(dst, src, n * 4, on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
+                             m->stream));
+    if (!on_device) M_TRY(m, cudaStreamSynchronize(m->stream));
+    return QW3_OK;
+}
+
+int validate_config(const qw3_config *c, std::string &why) {
+    auto bad = [&](const char *w) { why = w; return QW3_ERR_SHAPE; };
+    if (c->vocab <= 0 || c->hidden <= 0 || c->n_layers <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 ||
+        c->head_dim <= 0 || c->intermediate <= 0)
+        return bad("every config size must be positive");
+    if (c->hidden % 32) return bad("hidden must be a multiple of 32");
+    if (c->intermediate % 32) return bad("intermediate must be a multiple of 32");
+    if ((c->n_heads * c->head_dim) % 32) return bad("n_heads*head_dim must be a multiple of 32");
+    if (c->n_heads % c->n_kv_heads) return bad("n_heads must be a multiple of n_kv_heads");
+    if (c->head_dim % 2) return bad("head_dim must be even");
+    if (c->head_dim != 64 && c->head_dim != 128) return bad("head_dim must be 64 or 128");
+    const int group = c->n_heads / c->n_kv_heads;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return bad("n_heads/n_kv_heads must be 1, 2, 4 or 8");
+    if (c->max_seqs <= 0 || c->max_seq_len <= 0 || c->max_prefill <= 0)
+        return bad("max_seqs, max_seq_len and max_prefill must be positive");
+    if (!(c->rms_eps >= 0.0f) || !(c->rope_theta > 0.0f)) return bad("rms_eps must be >= 0 and rope_theta > 0");
+    if (c->hidden > 16384 || c->intermediate > 65536) return bad("hidden or intermediate too large");
+    return QW3_OK;
+}
+
+int pick_nsplit(int B, int nkv, int hd, int G) {
+    const int sms = num_sms();
+    const int units = B * nkv;
+    int ns = units >= sms ? (4 * sms + units - 1) / units : (sms + units - 1) / units;
+    const int cap = attn_decode_max_nsplit(hd, G);
+    if (ns > cap) ns = cap;
+    if (ns < 1) ns = 1;
+    return ns;
+}
+
+// The decode GEMV path stages B activation rows of up to max(H, I, n_heads*hd)
+// floats in shared memory; larger batches use the tiled GEMM path.
+bool use_gemv(const qw3_config &c, int B) {
+    const int kmax = std::max(c.hidden, std::max(c.intermediate, c.n_heads * c.head_dim));
+    return B <= 4 && B * kmax <= kGemvMaxBK;
+}
+
+// Enqueue one decode step for B rows on stream s: inputs d_tok/d_seq/d_pos,
+// outputs through d_io; afterwards d_tok holds the argmax and d_pos moved by 1.
+int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
+    const qw3_config &c = m->cfg;
+    const bool pdl = !(c.flags & QW3_FLAG_NO_PDL);
+    const int H = c.hidden, hd = c.head_dim, nh = c.n_heads, nkv = c.n_kv_heads, I = c.intermediate;
+    const int qw = nh * hd;
+    const int nsplit = pick_nsplit(B, nkv, hd, nh / nkv);
+    const bool gv = use_gemv(c, B);
+    int kidx = 0;
+    auto tr = [&]() -> unsigned long long * {
+        if (!m->trace) return nullptr;
+        const int i = kidx++;
+        return i < m->trace_kernels ? m->trace + static_cast<size_t>(i) * 2 * kTraceWords : nullptr;
+    };
+    M_TRY(m, launch_embed(m->d_tok, B, m->embd, m->x, pdl && gv, s, tr()));
+    for (int l = 0; l < c.n_layers; ++l) {
+        const LayerDev &L = m->layers[l];
+        if (gv) {
+            GemvArgs a{};
+            a.W = L.qkv; a.N = L.qkv.rows; a.K = H; a.B = B;
+            a.x = m->x; a.norm_w = L.attn_norm; a.eps = c.rms_eps; a.y = m->qkv; a.status = m->d_status;
+            a.trace = tr();
+            M_TRY(m, launch_gemv(a, GEMV_STORE, pdl, s));
+        } else {
+            M_TRY(m, launch_rmsnorm_rows(m->x, B, H, L.attn_norm, c.rms_eps, m->h, s));
+            M_TRY(m, launch_gemm(m->h, B, H, L.qkv, m->qkv, GEMV_STORE, nullptr, nullptr, s));
+        }
+        AttnDecodeArgs at{};
+        at.qkv = m->qkv; at.qkv_stride = m->qkv_w; at.q_norm = L.q_norm; at.k_norm = L.k_norm; at.eps = c.rms_eps;
+        at.rope = m->rope; at.kv = m->kv + static_cast<size_t>(l) * m->layer_stride;
+        at.seq_stride = m->seq_stride; at.kvsel_stride = m->kvsel_stride; at.head_stride = m->head_stride;
+        at.seq_ids = m->d_seq; at.pos = m->d_pos; at.nh = nh; at.nkv = nkv; at.hd = hd;
+        at.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(hd)));
+        at.partial = m->partial; at.counters = m->counters; at.out = m->o; at.status = m->d_status;
+        at.trace = tr();
+        M_TRY(m, launch_attn_decode(at, B, nsplit, pdl && gv, s));
+        if (gv) {
+            GemvArgs a{};
+            a.W = L.o; a.N = H; a.K = qw; a.B = B; a.x = m->o; a.norm_w = nullptr;
+            a.eps = c.rms_eps; a.y = m->x; a.status = m->d_status;
+            a.trace = tr();
+            M_TRY(m, launch_gemv(a, GEMV_RESID, pdl, s));
+            GemvArgs g{};
+            g.W = L.gu; g.N = 2 * I; g.K = H; g.B = B; g.x = m->x; g.norm_w = L.ffn_norm;
+            g.eps = c.rms_eps; g.y = m->act; g.status = m->d_status;
+            g.trace = tr();
+            M_TRY(m, launch_gemv(g, GEMV_SWIGLU, pdl, s));
+            GemvArgs dn{};
+            dn.W = L.down; dn.N = H; dn.K = I; dn.B = B; dn.x = m->act; dn.norm_w = nullptr;
+            dn.eps = c.rms_eps; dn.y = m->x; dn.status = m->d_status;
+            dn.trace = tr();
+            M_TRY(m, launch_gemv(dn, GEMV_RESID, pdl, s));
+        } else {
+            M_TRY(m, launch_gemm(m->o, B, qw, L.o, m->x, GEMV_RESID, nullptr, nullptr, s));
+            M_TRY(m, launch_rmsnorm_rows(m->x, B, H, L.ffn_norm, c.rms_eps, m->h, s));
+            M_TRY(m, launch_gemm(m->h, B, H, L.gu, m->act, GEMV_SWIGLU, nullptr, nullptr, s));
+            M_TRY(m, launch_gemm(m->act, B, I, L.down, m->x, GEMV_RESID, nullptr, nullptr, s));
+        }
+    }
+    if (gv) {
+        GemvArgs a{};
+        a.W = m->out; a.N = c.vocab; a.K = H; a.B = B; a.x = m->x; a.norm_w = m->out_norm;
+        a.eps = c.rms_eps; a.y = nullptr; a.argmax_key = m->argmax_key; a.done_counter = m->done_counter;
+        a.io = m->d_io; a.next_token = m->d_tok; a.step_ctr = m->d_step; a.pos_inc = m->d_pos;
+        a.status = m->d_status;
+        a.trace = tr();
+        M_TRY(m, launch_gemv(a, GEMV_ARGMAX, pdl, s));
+    } else {
+        M_TRY(m, launch_rmsnorm_rows(m->x, B, H, m->out_norm, c.rms_eps, m->h, s));
+        M_TRY(m, launch_gemm(m->h, B, H, m->out, nullptr, GEMV_ARGMAX, m->argmax_key, m->d_io, s));
+        M_TRY(m, launch_argmax_finalize(m->argmax_key, B, m->d_io, m->d_tok, m->d_step, m->d_pos, m->d_status, s));
+    }
+    return QW3_OK;
+}
+
+// Launch one decode step: replay the captured graph for B, capturing it on
+// first use, or enqueue the kernels directly when graphs are disabled.
+int run_decode_step(qw3_model *m, int B) {
+    if (m->cfg.flags & QW3_FLAG_NO_GRAPH) return enqueue_decode(m, B, m->stream);
+    auto it = m->graphs.find(B);
+    if (it == m->graphs.end()) {
+        M_TRY(m, cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+        const int rc = enqueue_decode(m, B, m->cap_stream);
+        cudaGraph_t g = nullptr;
+        const cudaError_t e = cudaStreamEndCapture(m->cap_stream, &g);
+        if (rc != QW3_OK) {
+            if (g) cudaGraphDestroy(g);
+            return rc;
+        }
+        if (e != cudaSuccess) return cuda_err(m, e, "cudaStreamEndCapture");
+        cudaGraphExec_t ex = nullptr;
+        const cudaError_t e2 = cudaGraphInstantiate(&ex, g, 0);
+        cudaGraphDestroy(g);
+        if (e2 != cudaSuccess) return cuda_err(m, e2, "cudaGraphInstantiate");
+        it = m->graphs.emplace(B, ex).first;
+    }
+    M_TRY(m, cudaGraphLaunch(it->second, m->stream));
+    return QW3_OK;
+}
+
+int check_model(const qw3_model *m) { return m ? QW3_OK : QW3_ERR_INVALID_ARG; }
+
+// Caller buffers are read and written with plain scalar accesses of their
+// element type; a pointer off that alignment is rejected here instead of
+// faulting on the device.
+bool misaligned(const void *p, size_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+int check_seq(qw3_model *m, int32_t seq) {
+    if (seq < 0 || seq >= m->cfg.max_seqs) return fail(m, QW3_ERR_INVALID_ARG, "sequence id out of range");
+    return QW3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *qw3_status_string(int status) {
+    switch (status) {
+        case QW3_OK: return "ok";
+        case QW3_ERR_INVALID_ARG: return "invalid argument";
+        case QW3_ERR_SHAPE: return "invalid shape";
+        case QW3_ERR_SEQ_POS: return "position does not match the sequence length";
+        case QW3_ERR_KV_OVERFLOW: return "KV cache overflow";
+        case QW3_ERR_NONFINITE: return "non-finite value";
+        case QW3_ERR_OOM: return "out of memory";
+        case QW3_ERR_CUDA: return "CUDA error";
+        case QW3_ERR_TIMEOUT: return "device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+const char *qw3_last_error(const qw3_model *m) {
+    if (m) return m->err.c_str();
+    return thread_error().c_str();
+}
+
+void *qw3_stream(const qw3_model *m) { return m ? static_cast<void *>(m->stream) : nullptr; }
+
+int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, qw3_model **out) {
+    if (!out) return fail(nullptr, QW3_ERR_INVALID_ARG, "out is null");
+    *out = nullptr;
+    if (!cfg || !w || !w->layers || !w->token_embd || !w->output_norm)
+        return fail(nullptr, QW3_ERR_INVALID_ARG, "null config or weights");
+    std::string why;
+    if (int rc = validate_config(cfg, why)) return fail(nullptr, rc, why);
+    if (!cfg->tied_lm_head && !w->output) return fail(nullptr, QW3_ERR_INVALID_ARG, "untied lm_head needs output");
+    {
+        const char *fa = getenv("QW3_FAULT_ALLOC_AT");
+        g_alloc_fail_at = fa ? atoi(fa) : -1;
+        g_alloc_count = 0;
+    }
+    if (cudaError_t e = configure_all(); e != cudaSuccess) return cuda_err(nullptr, e, "configure kernels");
+
+    qw3_model *m = new qw3_model();
+    m->cfg = *cfg;
+    auto bail = [&](int rc) {
+        if (m->stream) cudaStreamSynchronize(m->stream);
+        const std::string msg = m->err;
+        free_all(m);
+        delete m;
+        set_thread_error(msg);
+        return rc;
+    };
+    if (cuda_stream) {
+        m->stream = static_cast<cudaStream_t>(cuda_stream);
+    } else {
+        if (cudaError_t e = cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking); e != cudaSuccess)
+            return bail(cuda_err(m, e, "cudaStreamCreate"));
+        m->own_stream = true;
+    }
+    if (cudaError_t e = cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking); e != cudaSuccess)
+        return bail(cuda_err(m, e, "cudaStreamCreate"));
+
+    const qw3_config &c = m->cfg;
+    const int H = c.hidden, hd = c.head_dim, nh = c.n_heads, nkv = c.n_kv_heads, I = c.intermediate, V = c.vocab;
+    m->qkv_w = (nh + 2 * nkv) * hd;
+    const int qw = nh * hd;
+
+    // ---- weights: one arena, zero-filled so padding rows are zero
+    size_t wbytes = qmat_bytes(V, H) + (c.tied_lm_head ? 0 : qmat_bytes(V, H));
+    wbytes += static_cast<size_t>(c.n_layers) *
+              (qmat_bytes(m->qkv_w, H) + qmat_bytes(H, qw) + qmat_bytes(2 * I, H) + qmat_bytes(H, I) +
+               align_up(static_cast<size_t>(2 * H + 2 * hd) * 4, 256) + 4 * 256);
+    wbytes += align_up(static_cast<size_t>(H) * 4, 256);
+    uint8_t *arena = nullptr;
+    if (cudaError_t e = model_alloc(m, reinterpret_cast<void **>(&arena), wbytes); e != cudaSuccess)
+        return bail(cuda_err(m, e, "weight arena"));
+    if (cudaError_t e = cudaMemsetAsync(arena, 0, wbytes, m->stream); e != cudaSuccess)
+        return bail(cuda_err(m, e, "memset"));
+    uint8_t *cur = arena;
+    const bool on_dev = w->on_device != 0;
+    uint8_t *staging = nullptr;
+    if (!on_dev) {
+        size_t biggest = static_cast<size_t>(V) * H;
+        biggest = std::max(biggest, static_cast<size_t>(qw) * H);
+        biggest = std::max(biggest, static_cast<size_t>(I) * H);
+        biggest = biggest / 32 * 34;
+        if (cudaError_t e = model_alloc(m, reinterpret_cast<void **>(&staging), biggest); e != cudaSuccess)
+            return bail(cuda_err(m, e, "staging"));
+    }
+    qmat_place(m->embd, cur, V, H);
+    if (int rc = repack_into(m, m->embd, w->token_embd, V, H, 0, 1, on_dev, staging)) return bail(rc);
+    if (c.tied_lm_head) {
+        m->out = m->embd;
+    } else {
+        qmat_place(m->out, cur, V, H);
+        if (int rc = repack_into(m, m->out, w->output, V, H, 0, 1, on_dev, staging)) return bail(rc);
+    }
+    m->layers.resize(c.n_layers);
+    for (int l = 0; l < c.n_layers; ++l) {
+        const qw3_layer_weights &lw = w->layers[l];
+        LayerDev &L = m->layers[l];
+        qmat_place(L.qkv, cur, m->qkv_w, H);
+        qmat_place(L.o, cur, H, qw);
+        qmat_place(L.gu, cur, 2 * I, H);
+        qmat_place(L.down, cur, H, I);
+        int rc = repack_into(m, L.qkv, lw.attn_q, qw, H, 0, 1, on_dev, staging);
+        if (!rc) rc = repack_into(m, L.qkv, lw.attn_k, nkv * hd, H, qw, 1, on_dev, staging);
+        if (!rc) rc = repack_into(m, L.qkv, lw.attn_v, nkv * hd, H, qw + nkv * hd, 1, on_dev, staging);
+        if (!rc) rc = repack_into(m, L.o, lw.attn_output, H, qw, 0, 1, on_dev, staging);
+        if (!rc) rc = repack_into(m, L.gu, lw.ffn_gate, I, H, 0, 2, on_dev, staging);
+        if (!rc) rc = repack_into(m, L.gu, lw.ffn_up, I, H, 1, 2, on_dev, staging);
+        if (!rc) rc = repack_into(m, L.down, lw.ffn_down, H, I, 0, 1, on_dev, staging);
+        if (rc) return bail(rc);
+        float *nb = reinterpret_cast<float *>(cur);
+        L.attn_norm = nb;
+        L.ffn_norm = nb + align_up(H, 64);
+        L.q_norm = L.ffn_norm + align_up(H, 64);
+        L.k_norm = L.q_norm + align_up(hd, 64);
+        cur += align_up(static_cast<size_t>(2 * align_up(H, 64) + 2 * align_up(hd, 64)) * 4, 256);
+        if ((rc = copy_f32(m, L.attn_norm, lw.attn_norm, H, on_dev))) return bail(rc);
+        if ((rc = copy_f32(m, L.ffn_norm, lw.ffn_norm, H, on_dev))) return bail(rc);
+        if ((rc = copy_f32(m, L.q_norm, lw.attn_q_norm, hd, on_dev))) return bail(rc);
+        if ((rc = copy_f32(m, L.k_norm, lw.attn_k_norm, hd, on_dev))) return bail(rc);
+    }
+    m->out_norm = reinterpret_cast<float *>(cur);
+    cur += align_up(static_cast<size_t>(H) * 4, 256);
+    if (int rc = copy_f32(m, m->out_norm, w->output_norm, H, on_dev)) return bail(rc);
+    if (static_cast<size_t>(cur - arena) > wbytes) return bail(fail(m, QW3_ERR_CUDA, "internal: arena overflow"));
+
+    // ---- RoPE table (course 12.3.4): angle p * theta^(-2i/d), f64 -> f32
+    {
+        const size_t n = static_cast<size_t>(c.max_seq_len) * (hd / 2);
+        std::vector<float2> tab(n);
+        for (int p = 0; p < c.max_seq_len; ++p)
+            for (int i = 0; i < hd / 2; ++i) {
+                const double inv = std::pow(static_cast<double>(c.rope_theta), -2.0 * i / hd);
+                const double ang = static_cast<double>(p) * inv;
+                tab[static_cast<size_t>(p) * (hd / 2) + i] =
+                    make_float2(static_cast<float>(std::cos(ang)), static_cast<float>(std::sin(ang)));
+            }
+        if (cudaError_t e = model_alloc(m, reinterpret_cast<void **>(&m->rope), n * sizeof(float2)); e != cudaSuccess)
+            return bail(cuda_err(m, e, "rope table"));
+        if (cudaError_t e = cudaMemcpyAsync(m->rope, tab.data(), n * sizeof(float2), cudaMemcpyHostToDevice, m->stream);
+            e != cudaSuccess)
+            return bail(cuda_err(m, e, "rope upload"));
+        if (cudaError_t e = cudaStreamSynchronize(m->stream); e != cudaSuccess) return bail(cuda_err(m, e, "sync"));
+    }
+
+    // ---- KV cache: [layer][seq][K|V][kv_head][capacity][head_dim] f32
+    m->head_stride = static_cast<size_t>(c.max_seq_len) * hd;
+    m->kvsel_stride = m->head_stride * nkv;
+    m->seq_stride = 2 * m->kvsel_stride;
+    m->layer_stride = m->seq_stride * c.max_seqs;
+    {
+        const size_t bytes = m->layer_stride * c.n_layers * sizeof(float);
+        if (cudaError_t e = model_alloc(m, reinterpret_cast<void **>(&m->kv), bytes); e != cudaSuccess)
+            return bail(cuda_err(m, e, "KV cache"));
+    }
+    m->seq_len.assign(c.max_seqs, 0);
+
+    // ---- decode scratch
+    const int Bm = c.max_seqs;
+    m->max_nsplit = 64;
+    auto A = [&](void **p, size_t bytes) { return model_alloc(m, p, bytes); };
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->x), static_cast<size_t>(Bm) * H * 4);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->h), static_cast<size_t>(Bm) * H * 4);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->qkv), static_cast<size_t>(Bm) * m->qkv_w * 4);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->o), static_cast<size_t>(Bm) * qw * 4);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->act), static_cast<size_t>(Bm) * I * 4);
+    if (e == cudaSuccess)
+        e = A(reinterpret_cast<void **>(&m->partial), static_cast<size_t>(Bm) * nh * m->max_nsplit * (hd + 4) * 4);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->counters), static_cast<size_t>(Bm) * nkv * 4);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->done_counter), 64);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->argmax_key), static_cast<size_t>(Bm) * 8);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->d_tok), static_cast<size_t>(Bm) * 4);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->d_pos), static_cast<size_t>(Bm) * 4);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->d_seq), static_cast<size_t>(Bm) * 4);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->d_step), 64);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->d_status), 64);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->d_io), sizeof(DecodeIO));
+    if (e == cudaSuccess && (c.flags & QW3_FLAG_TRACE)) {
+        m->trace_kernels = 2 + 5 * c.n_layers + 4;
+        const size_t tb = static_cast<size_t>(m->trace_kernels) * 2 * kTraceWords * 8;
+        e = A(reinterpret_cast<void **>(&m->trace), tb);
+        if (e == cudaSuccess) e = cudaMemsetAsync(m->trace, 0, tb, m->stream);
+    }
+    // ---- prefill scratch
+    const size_t P = static_cast<size_t>(c.max_prefill);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->px), P * H * 4);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->ph), P * H * 4);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->pqkv), P * m->qkv_w * 4);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->po), P * qw * 4);
+    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->pact), P * I * 4);
+    if (e != cudaSuccess) return bail(cuda_err(m, e, "scratch allocation"));
+    e = cudaMemsetAsync(m->counters, 0, static_cast<size_t>(Bm) * nkv * 4, m->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(m->done_counter, 0, 64, m->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(m->argmax_key, 0, static_cast<size_t>(Bm) * 8, m->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(m->d_step, 0, 64, m->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(m->d_status, 0, 64, m->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(m->d_io, 0, sizeof(DecodeIO), m->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
+    if (e != cudaSuccess) return bail(cuda_err(m, e, "scratch init"));
+    *out = m;
+    return QW3_OK;
+}
+
+int qw3_destroy(qw3_model *m) {
+    if (!m) return QW3_OK;
+    if (m->stream) cudaStreamSynchronize(m->stream);
+    free_all(m);
+    delete m;
+    return QW3_OK;
+}
+
+int qw3_prefill(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n, float *last_logits_dev,
+                int32_t *argmax_dev) {
+    if (check_model(m)) return QW3_ERR_INVALID_ARG;
+    if (int rc = check_seq(m, seq)) return rc;
+    if (!tokens_dev || n < 1) return fail(m, QW3_ERR_INVALID_ARG, "prefill needs n >= 1 tokens");
+    if (misaligned(tokens_dev, 4) || misaligned(last_logits_dev, 4) || misaligned(argmax_dev, 4))
+        return fail(m, QW3_ERR_INVALID_ARG, "device buffers must be 4-byte aligned");
+    const qw3_config &c = m->cfg;
+    const int len = m->seq_len[seq];
+    if (static_cast<int64_t>(len) + n > c.max_seq_len)
+        return fail(m, QW3_ERR_KV_OVERFLOW, "prefill would overflow the KV cache");
+    const int H = c.hidden, hd = c.head_dim, nh = c.n_heads, nkv = c.n_kv_heads, I = c.intermediate;
+    const int qw = nh * hd;
+    const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(hd)));
+    cudaStream_t s = m->stream;
+    for (int off = 0; off < n; off += c.max_prefill) {
+        const int M = std::min(c.max_prefill, n - off);
+        const int pos0 = len + off;
+        M_TRY(m, launch_embed(tokens_dev + off, M, m->embd, m->px, false, s));
+        for (int l = 0; l < c.n_layers; ++l) {
+            const LayerDev &L = m->layers[l];
+            float *kvl = m->kv + static_cast<size_t>(l) * m->layer_stride;
+            M_TRY(m, launch_rmsnorm_rows(m->px, M, H, L.attn_norm, c.rms_eps, m->ph, s));
+            M_TRY(m, launch_gemm(m->ph, M, H, L.qkv, m->pqkv, GEMV_STORE, nullptr, nullptr, s));
+            M_TRY(m, launch_qk_rope_append(m->pqkv, M, m->qkv_w, L.q_norm, L.k_norm, c.rms_eps, m->rope, nullptr, seq,
+                                           nullptr, pos0, kvl, m->seq_stride, m->kvsel_stride, m->head_stride, nh,
+                                           nkv, hd, s));
+            M_TRY(m, launch_attn_prefill(m->pqkv, M, m->qkv_w, kvl, 0, static_cast<size_t>(seq) * m->seq_stride,
+                                         m->kvsel_stride, m->head_stride, pos0, nh, nkv, hd, scale, m->po, s));
+            M_TRY(m, launch_gemm(m->po, M, qw, L.o, m->px, GEMV_RESID, nullptr, nullptr, s));
+            M_TRY(m, launch_rmsnorm_rows(m->px, M, H, L.ffn_norm, c.rms_eps, m->ph, s));
+            M_TRY(m, launch_gemm(m->ph, M, H, L.gu, m->pact, GEMV_SWIGLU, nullptr, nullptr, s));
+            M_TRY(m, launch_gemm(m->pact, M, I, L.down, m->px, GEMV_RESID, nullptr, nullptr, s));
+        }
+        if (off + M == n && (last_logits_dev || argmax_dev)) {
+            GemvArgs a{};
+            a.W = m->out; a.N = c.vocab; a.K = H; a.B = 1;
+            a.x = m->px + static_cast<size_t>(M - 1) * H; a.norm_w = m->out_norm; a.eps = c.rms_eps;
+            a.y = last_logits_dev; a.argmax_key = m->argmax_key; a.done_counter = m->done_counter; a.io = nullptr;
+            a.argmax_out = argmax_dev; a.status = m->d_status;
+            M_TRY(m, launch_gemv(a, GEMV_ARGMAX, false, s));
+        }
+    }
+    m->seq_len[seq] = len + n;
+    return QW3_OK;
+}
+
+int qw3_decode(qw3_model *m, int32_t B, const int32_t *seqs_host, const int32_t *tokens_dev, const int32_t *pos_host,
+               float *logits_dev, int32_t *argmax_dev) {
+    if (check_model(m)) return QW3_ERR_INVALID_ARG;
+    const qw3_config &c = m->cfg;
+    if (B < 1 || B > c.max_seqs) return fail(m, QW3_ERR_INVALID_ARG, "batch must be in [1, max_seqs]");
+    if (!tokens_dev || !pos_host) return fail(m, QW3_ERR_INVALID_ARG, "null tokens or positions");
+    if (misaligned(tokens_dev, 4) || misaligned(logits_dev, 4) || misaligned(argmax_dev, 4))
+        return fail(m, QW3_ERR_INVALID_ARG, "device buffers must be 4-byte aligned");
+    std::vector<int32_t> seqs(B), pos(B);
+    std::vector<char> seen(c.max_seqs, 0);
+    for (int b = 0; b < B; ++b) {
+        const int sq = seqs_host ? seqs_host[b] : b;
+        if (sq < 0 || sq >= c.max_seqs) return fail(m, QW3_ERR_INVALID_ARG, "sequence id out of range");
+        if (seen[sq]) return fail(m, QW3_ERR_INVALID_ARG, "duplicate sequence id in batch");
+        seen[sq] = 1;
+        if (pos_host[b] != m->seq_len[sq]) return fail(m, QW3_ERR_SEQ_POS, "pos != current sequence length");
+        if (m->seq_len[sq] + 1 > c.max_seq_len) return fail(m, QW3_ERR_KV_OVERFLOW, "decode would overflow the KV cache");
+        seqs[b] = sq;
+        pos[b] = pos_host[b];
+    }
+    DecodeIO io{logits_dev, argmax_dev, nullptr, nullptr};
+    M_TRY(m, cudaMemcpyAsync(m->d_seq, seqs.data(), B * 4, cudaMemcpyHostToDevice, m->stream));
+    M_TRY(m, cudaMemcpyAsync(m->d_pos, pos.data(), B * 4, cudaMemcpyHostToDevice, m->stream));
+    M_TRY(m, cudaMemcpyAsync(m->d_io, &io, sizeof io, cudaMemcpyHostToDevice, m->stream));
+    M_TRY(m, cudaMemcpyAsync(m->d_tok, tokens_dev, B * 4, cudaMemcpyDeviceToDevice, m->stream));
+    if (int rc = run_decode_step(m, B)) return rc;
+    for (int b = 0; b < B; ++b) m->seq_len[seqs[b]] += 1;
+    return QW3_OK;
+}
+
+int qw3_generate_greedy(qw3_model *m, int32_t B, const int32_t *seqs_host, int32_t n_steps,
+                        const int32_t *first_tokens_dev, int32_t *out_tokens_dev) {
+    if (check_model(m)) return QW3_ERR_INVALID_ARG;
+    const qw3_config &c = m->cfg;
+    if (B < 1 || B > c.max_seqs) return fail(m, QW3_ERR_INVALID_ARG, "batch must be in [1, max_seqs]");
+    if (n_steps < 0 || !first_tokens_dev || (n_steps > 0 && !out_tokens_dev))
+        return fail(m, QW3_ERR_INVALID_ARG, "bad generate arguments");
+    if (misaligned(first_tokens_dev, 4) || misaligned(out_tokens_dev, 4))
+        return fail(m, QW3_ERR_INVALID_ARG, "device buffers must be 4-byte aligned");
+    if (n_steps == 0) return QW3_OK;
+    std::vector<int32_t> seqs(B), pos(B);
+    std::vector<char> seen(c.max_seqs, 0);
+    for (int b = 0; b < B; ++b) {
+        const int sq = seqs_host ? seqs_host[b] : b;
+        if (sq < 0 || sq >= c.max_seqs) return fail(m, QW3_ERR_INVALID_ARG, "sequence id out of range");
+        if (seen[sq]) return fail(m, QW3_ERR_INVALID_ARG, "duplicate sequence id in batch");
+        seen[sq] = 1;
+        if (static_cast<int64_t>(m->seq_len[sq]) + n_steps > c.max_seq_len)
+            return fail(m, QW3_ERR_KV_OVERFLOW, "generation would overflow the KV cache");
+        seqs[b] = sq;
+        pos[b] = m->seq_len[sq];
+    }
+    DecodeIO io{nullptr, nullptr, out_tokens_dev, nullptr};
+    const int32_t zero = 0;
+    M_TRY(m, cudaMemcpyAsync(m->d_seq, seqs.data(), B * 4, cudaMemcpyHostToDevice, m->stream));
+    M_TRY(m, cudaMemcpyAsync(m->d_pos, pos.data(), B * 4, cudaMemcpyHostToDevice, m->stream));
+    M_TRY(m, cudaMemcpyAsync(m->d_io, &io, sizeof io, cudaMemcpyHostToDevice, m->stream));
+    M_TRY(m, cudaMemcpyAsync(m->d_step, &zero, 4, cudaMemcpyHostToDevice, m->stream));
+    M_TRY(m, cudaMemcpyAsync(m->d_tok, first_tokens_dev, B * 4, cudaMemcpyDeviceToDevice, m->stream));
+    for (int sidx = 0; sidx < n_steps; ++sidx) {
+        if (int rc = run_decode_step(m, B)) return rc;
+    }
+    for (int b = 0; b < B; ++b) m->seq_len[seqs[b]] += n_steps;
+    return QW3_OK;
+}
+
+int qw3_reset(qw3_model *m, int32_t seq) {
+    if (check_model(m)) return QW3_ERR_INVALID_ARG;
+    if (int rc = check_seq(m, seq)) return rc;
+    m->seq_len[seq] = 0;
+    return QW3_OK;
+}
+
+int qw3_truncate(qw3_model *m, int32_t seq, int32_t keep_len) {
+    if (check_model(m)) return QW3_ERR_INVALID_ARG;
+    if (int rc = check_seq(m, seq)) return rc;
+    if (keep_len < 0) return fail(m, QW3_ERR_INVALID_ARG, "keep_len must be >= 0");
+    if (keep_len < m->seq_len[seq]) m->seq_len[seq] = keep_len;
+    return QW3_OK;
+}
+
+int qw3_seq_len(const qw3_model *m, int32_t seq, int32_t *len_out) {
+    if (!m || !len_out) return QW3_ERR_INVALID_ARG;
+    if (seq < 0 || seq >= m->cfg.max_seqs) return QW3_ERR_INVALID_ARG;
+    *len_out = m->seq_len[seq];
+    return QW3_OK;
+}
+
+int qw3_debug_read_kv(qw3_model *m, int32_t layer, int32_t seq, int32_t pos0, int32_t n, float *k_out_dev,
+                      float *v_out_dev) {
+    if (check_model(m)) return QW3_ERR_INVALID_ARG;
+    if (int rc = check_seq(m, seq)) return rc;
+    const qw3_config &c = m->cfg;
+    if (layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 || static_cast<int64_t>(pos0) + n > c.max_seq_len ||
+        !k_out_dev || !v_out_dev || misaligned(k_out_dev, 4) || misaligned(v_out_dev, 4))
+        return fail(m, QW3_ERR_INVALID_ARG, "bad KV read range");
+    const float *base = m->kv + static_cast<size_t>(layer) * m->layer_stride + static_cast<size_t>(seq) * m->seq_stride;
+    M_TRY(m, launch_copy_kv_rows(base, m->kvsel_stride, m->head_stride, pos0, n, c.n_kv_heads, c.head_dim, k_out_dev,
+                                 v_out_dev, m->stream));
+    return QW3_OK;
+}
+
+int qw3_debug_read_trace(qw3_model *m, uint64_t *out_host, int32_t max_records, int32_t *n_out) {
+    if (check_model(m)) return QW3_ERR_INVALID_ARG;
+    if (!n_out || max_records < 0 || (max_records > 0 && !out_host))
+        return fail(m, QW3_ERR_INVALID_ARG, "bad trace arguments");
+    *n_out = 0;
+    if (!m->trace) return fail(m, QW3_ERR_INVALID_ARG, "model was created without QW3_FLAG_TRACE");
+    const int n = std::min(max_records, 2 * m->trace_kernels);
+    M_TRY(m, cudaStreamSynchronize(m->stream));
+    M_TRY(m, cudaMemcpy(out_host, m->trace, static_cast<size_t>(n) * kTraceWords * 8, cudaMemcpyDeviceToHost));
+    *n_out = n;
+    return QW3_OK;
+}
+
+int qw3_sync(qw3_model *m) {
+    if (check_model(m)) return QW3_ERR_INVALID_ARG;
+    M_TRY(m, cudaStreamSynchronize(m->stream));
+    int32_t st = 0;
+    M_TRY(m, cudaMemcpy(&st, m->d_status, 4, cudaMemcpyDeviceToHost));
+    if (st != 0) {
+        M_TRY(m, cudaMemset(m->d_status, 0, 4));
+        return fail(m, st, std::string("device reported: ") + qw3_status_string(st));
+    }
+    return QW3_OK;
+}
+
+int qw3_q8_0_quantize(const float *x_dev, int64_t n, void *blocks_dev, int32_t *status_dev, void *stream) {
+    if (n < 0 || (n > 0 && (!x_dev || !blocks_dev))) return fail(nullptr, QW3_ERR_INVALID_ARG, "bad quantize arguments");
+    if (n % 32) return fail(nullptr, QW3_ERR_SHAPE, "n must be a multiple of 32");
+    if (misaligned(x_dev, 4) || misaligned(blocks_dev, 2) || misaligned(status_dev, 4))
+        return fail(nullptr, QW3_ERR_INVALID_ARG, "x must be 4-byte, blocks 2-byte aligned");
+    QW3_CUDA_TRY(launch_quantize(x_dev, n / 32, static_cast<uint8_t *>(blocks_dev), status_dev,
+                                 static_cast<cudaStream_t>(stream)));
+    return QW3_OK;
+}
+
+int qw3_q8_0_dequantize(const void *blocks_dev, int64_t n, float *y_dev, void *stream) {
+    if (n < 0 || (n > 0 && (!y_dev || !blocks_dev))) return fail(nullptr, QW3_ERR_INVALID_ARG, "bad dequantize arguments");
+    if (n % 32) return fail(nullptr, QW3_ERR_SHAPE, "n must be a multiple of 32");
+    if (misaligned(blocks_dev, 2) || misaligned(y_dev, 4))
+        return fail(nullptr, QW3_ERR_INVALID_ARG, "blocks must be 2-byte, y 4-byte aligned");
+    QW3_CUDA_TRY(launch_dequantize(static_cast<const uint8_t *>(blocks_dev), n / 32, y_dev,
+                                   static_cast<cudaStream_t>(stream)));
+    return QW3_OK;
+}
+
+int qw3_q8_0_gemv(const void *W_dev, int32_t rows, int32_t cols, const float *x_dev, int32_t B, float *y_dev,
+                  void *stream) {
+    if (!W_dev || !x_dev || !y_dev || rows < 0 || cols < 0 || B < 1 || B > 8)
+        return fail(nullptr, QW3_ERR_INVALID_ARG, "bad gemv arguments");
+    if (cols % 32) return fail(nullptr, QW3_ERR_SHAPE, "cols must be a multiple of 32");
+    if (misaligned(W_dev, 2) || misaligned(x_dev, 4) || misaligned(y_dev, 4))
+        return fail(nullptr, QW3_ERR_INVALID_ARG, "W must be 2-byte, x and y 4-byte aligned");
+    if (rows == 0) return QW3_OK;
+    QW3_CUDA_TRY(launch_gemv_raw(static_cast<const uint8_t *>(W_dev), rows, cols, x_dev, B, y_dev,
+                                 static_cast<cudaStream_t>(stream)));
+    return QW3_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,307 @@
+// Internal declarations of libqw3 (not part of the C ABI).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/qw3.h"
+
+namespace qw3 {
+
+// ---------------------------------------------------------------- weights
+
+// A Q8_0 matrix repacked at create time into tiles of 8 rows x kt columns.
+// A tile holds the 8 rows' int8 codes ([8][kt]) followed by their f16 scales
+// ([8][kt/32]): 8.5 * kt bytes, the same 34 bytes per 32 weights as the GGUF
+// blocks. Tiles are stored row-group-major (every k-tile of rows 0..7, then
+// rows 8..15, ...) or k-tile-major (k-tile 0 of every row group, then k-tile
+// 1, ...), so the slice a kernel needs is one contiguous 16-byte-aligned
+// range and streams with a single bulk copy. Rows are padded to a multiple of
+// 16 with zero rows.
+struct QMat {
+    uint8_t *base = nullptr;
+    int rows = 0;         // logical rows
+    int rows_pad = 0;     // allocated rows (multiple of 16)
+    int cols = 0;
+    int kt = 0;           // tile width: divides cols, multiple of 32
+    int ktile_major = 0;  // 0: row-group-major, 1: k-tile-major
+};
+
+constexpr int kRowAlign = 16;
+
+__host__ __device__ inline size_t qm_tile_bytes(int kt) { return static_cast<size_t>(kt) * 17 / 2; }
+
+__host__ __device__ inline size_t qm_bytes(const QMat &m) {
+    return static_cast<size_t>(m.rows_pad / 8) * (m.cols / m.kt) * qm_tile_bytes(m.kt);
+}
+
+__host__ __device__ inline size_t qm_tile_offset(const QMat &m, int group, int t) {
+    const size_t ngroups = static_cast<size_t>(m.rows_pad / 8), ntiles = static_cast<size_t>(m.cols / m.kt);
+    const size_t idx = m.ktile_major ? static_cast<size_t>(t) * ngroups + group : static_cast<size_t>(group) * ntiles + t;
+    return idx * qm_tile_bytes(m.kt);
+}
+
+// Codes of row r from column k (k and the run read must stay inside one tile).
+__host__ __device__ inline const int8_t *qm_codes(const QMat &m, int r, int k) {
+    const int t = k / m.kt, kk = k - t * m.kt;
+    return reinterpret_cast<const int8_t *>(m.base + qm_tile_offset(m, r >> 3, t)) + (r & 7) * m.kt + kk;
+}
+
+// Scale of the 32-column block of row r that holds column k.
+__host__ __device__ inline const __half *qm_scale(const QMat &m, int r, int k) {
+    const int t = k / m.kt, kk = k - t * m.kt;
+    return reinterpret_cast<const __half *>(m.base + qm_tile_offset(m, r >> 3, t) + 8 * static_cast<size_t>(m.kt)) +
+           (r & 7) * (m.kt / 32) + kk / 32;
+}
+
+struct LayerDev {
+    QMat qkv;   // rows: q (n_heads*hd), k (n_kv*hd), v (n_kv*hd); cols H
+    QMat o;     // [H][n_heads*hd]
+    QMat gu;    // rows interleaved: 2i = gate_i, 2i+1 = up_i; cols H
+    QMat down;  // [H][I]
+    float *attn_norm, *q_norm, *k_norm, *ffn_norm;
+};
+
+// ------------------------------------------------------------ GEMV params
+
+// Output pointers of a decode step, kept in device memory so that one
+// captured CUDA graph serves calls with different caller buffers.
+struct DecodeIO {
+    float *logits;     // nullable [B][V]
+    int32_t *argmax;   // nullable [B]
+    int32_t *hist;     // nullable [step][B] token history
+    int32_t *unused;
+};
+
+enum GemvMode : int { GEMV_STORE = 0, GEMV_RESID = 1, GEMV_SWIGLU = 2, GEMV_ARGMAX = 3 };
+
+struct GemvArgs {
+    QMat W;                   // row-group-major tiles
+    int N, K;                 // logical rows, cols
+    int B;                    // activation rows (1..4)
+    const float *x;           // [B][K] input
+    const float *norm_w;      // [K] RMSNorm weight, nullptr = no norm prologue
+    float eps;
+    float *y;                 // STORE: [B][N]; RESID: [B][N] += ; SWIGLU: [B][N/2]
+    // ARGMAX mode
+    unsigned long long *argmax_key;  // [B] packed (value, index) keys, reset to 0
+    unsigned int *done_counter;      // CTA arrival counter, reset by the last CTA
+    const DecodeIO *io;              // nullable: output pointers read on the device
+    int32_t *argmax_out;             // used when io == nullptr (nullable) [B]
+    int32_t *next_token;             // nullable [B]: written with the argmax
+    int32_t *step_ctr;               // nullable: incremented by the last CTA
+    int32_t *pos_inc;                // nullable [B]: +1 by the last CTA
+    int32_t *status;                 // device status word
+    unsigned long long *trace;       // nullable: 2 records of 8 u64 (first, last CTA)
+};
+
+struct AttnDecodeArgs {
+    const float *qkv;     // [B][(nh+2nkv)*hd] raw projections
+    int qkv_stride;
+    const float *q_norm, *k_norm;
+    float eps;
+    const float2 *rope;   // [max_seq_len][hd/2] (cos, sin)
+    float *kv;            // this layer's cache: [seq][K|V][kv_head][capacity][head_dim]
+    size_t seq_stride, kvsel_stride, head_stride;  // floats
+    const int32_t *seq_ids;  // [B]
+    const int32_t *pos;      // [B] position of the new token
+    int nh, nkv, hd;
+    float scale;
+    float *partial;          // [B][nh][nsplit][hd+4]: acc[hd], m, l, pad
+    unsigned int *counters;  // [B][nkv]
+    float *out;              // [B][nh*hd]
+    int32_t *status;
+    unsigned long long *trace;  // nullable: 2 records of 8 u64 (first, last CTA)
+};
+
+// ---------------------------------------------------------------- helpers
+
+#define QW3_CUDA_TRY(expr)                                   \
+    do {                                                     \
+        cudaError_t _e = (expr);                             \
+        if (_e != cudaSuccess) return ::qw3::cuda_fail(_e, #expr, __FILE__, __LINE__); \
+    } while (0)
+
+int cuda_fail(cudaError_t e, const char *what, const char *file, int line);
+void set_thread_error(const std::string &msg);
+const std::string &thread_error();
+
+int num_sms();
+
+// Set the dynamic shared-memory limits of every kernel instantiation; called
+// once per process before any launch or graph capture.
+cudaError_t configure_gemv();
+cudaError_t configure_attention();
+cudaError_t configure_misc();
+
+// launchers (return cudaError_t of the launch)
+cudaError_t launch_quantize(const float *x, int64_t nblocks, uint8_t *out, int32_t *status, cudaStream_t s);
+cudaError_t launch_dequantize(const uint8_t *blocks, int64_t nblocks, float *y, cudaStream_t s);
+cudaError_t launch_repack(const uint8_t *raw, int rows, int cols, const QMat &dst,
+                          int dst_row0, int dst_row_stride, cudaStream_t s);
+cudaError_t launch_gemv_raw(const uint8_t *W, int rows, int cols, const float *x, int B, float *y,
+                            cudaStream_t s);
+
+cudaError_t launch_gemv(const GemvArgs &a, int mode, bool pdl, cudaStream_t s);
+// largest B * K the decode GEMV stages (activations live in shared memory)
+constexpr int kGemvMaxBK = 16384;
+cudaError_t launch_attn_decode(const AttnDecodeArgs &a, int B, int nsplit, bool pdl, cudaStream_t s);
+// largest split count the decode attention kernel accepts for (head_dim, group)
+int attn_decode_max_nsplit(int hd, int G);
+cudaError_t launch_embed(const int32_t *tokens, int n, const QMat &E, float *x, bool pdl, cudaStream_t s,
+                         unsigned long long *trace = nullptr);
+
+// prefill / batched path
+cudaError_t launch_rmsnorm_rows(const float *x, int M, int K, const float *w, float eps, float *y,
+                                cudaStream_t s);
+cudaError_t launch_gemm(const float *A, int M, int K, const QMat &W, float *C, int mode,
+                        unsigned long long *argmax_key, const DecodeIO *io, cudaStream_t s);
+cudaError_t launch_qk_rope_append(float *qkv, int M, int qkv_stride, const float *q_norm,
+                                  const float *k_norm, float eps, const float2 *rope,
+                                  const int32_t *row_seq, int seq0, const int32_t *row_pos, int pos0,
+                                  float *kv_layer, size_t seq_stride, size_t kvsel_stride,
+                                  size_t head_stride, int nh, int nkv, int hd, cudaStream_t s);
+cudaError_t launch_attn_prefill(const float *qkv, int M, int qkv_stride, const float *kv,
+                                size_t layer_off, size_t seq_off, size_t kvsel_stride,
+                                size_t head_stride, int pos0, int nh, int nkv, int hd,
+                                float scale, float *out, cudaStream_t s);
+cudaError_t launch_argmax_finalize(unsigned long long *key, int B, const DecodeIO *io,
+                                   int32_t *next_token, int32_t *step_ctr, int32_t *pos_inc,
+                                   int32_t *status, cudaStream_t s);
+cudaError_t launch_copy_kv_rows(const float *kv_layer_seq, size_t kvsel_stride, size_t head_stride,
+                                int pos0, int n, int nkv, int hd, float *k_out, float *v_out,
+                                cudaStream_t s);
+
+}  // namespace qw3
+
+// ------------------------------------------------------------ device PTX
+
+#ifdef __CUDACC__
+namespace qw3 {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on an mbarrier phase: gives up after ~1 s and returns false.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// 1-D bulk copy global -> shared (TMA), completion counted on `bar` in bytes.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy) : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Programmatic dependent launch controls (no-ops without the launch attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Order-preserving map of f32 to u32 (larger float -> larger unsigned).
+__device__ __forceinline__ uint32_t float_order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float float_from_order_key(uint32_t k) {
+    uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+    return __uint_as_float(u);
+}
+
+// (value, index) packed so that u64 max picks the largest value and, among
+// equal values, the lowest index.
+__device__ __forceinline__ unsigned long long argmax_pack(float v, int idx) {
+    return (static_cast<unsigned long long>(float_order_key(v)) << 32) |
+           static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(idx));
+}
+
+// Trace record of one CTA: 8 u64 words, see qw3_debug_read_trace.
+constexpr int kTraceWords = 8;
+
+__device__ __forceinline__ unsigned long long *trace_slot(unsigned long long *trace) {
+    if (!trace) return nullptr;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) return trace;
+    if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 && blockIdx.z == gridDim.z - 1)
+        return trace + kTraceWords;
+    return nullptr;
+}
+
+__device__ __forceinline__ uint32_t smid() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void record_status(int32_t *status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+}  // namespace qw3
+#endif

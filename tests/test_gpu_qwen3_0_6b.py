@@ -1,0 +1,77 @@
+"""GPU parity at the Qwen3-0.6B geometry (seed 1, tied lm_head): prefill of
+512 seeded tokens, then greedy decode at batch 1 in the launch configuration
+the benchmark times (captured graph, qw3_generate_greedy).
+
+Free-running greedy ids must equal the oracle's for 64 steps; logits are
+checked under teacher forcing on the prefill row and every step.
+"""
+import os
+
+import numpy as np
+import pytest
+
+from oracle import qw3_oracle as orc
+from quantized_transformer_decode_gb300 import inputs
+from parity import assert_logits_close, cuda_ints
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+STEPS = int(os.environ.get("QW3_PARITY_STEPS", "64"))
+
+
+@pytest.fixture(scope="module")
+def pair():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_transformer_decode_gb300 import build
+    from quantized_transformer_decode_gb300.qw3 import Qw3Model
+    build.build()
+    w = inputs.WORKLOADS["qwen3-0.6b-decode"]
+    om = orc.OracleModel.from_f32(w.shape, inputs.generate_weights(w.shape, w.seed))
+    gm = Qw3Model.from_f32(w.shape, inputs.iter_weights(w.shape, w.seed), max_seqs=1,
+                           max_seq_len=w.prompt_len + w.decode_steps + 1, max_prefill=512)
+    prompt = inputs.prompt_tokens(w.shape, w.seed, w.prompt_len)
+    ids, logits = om.generate_greedy(om.new_cache(w.prompt_len + STEPS + 1), prompt, STEPS)
+    yield w, om, gm, prompt, ids, logits
+    gm.close()
+
+
+def test_greedy_ids_bit_exact(pair):
+    w, _, gm, prompt, ids, _ = pair
+    gm.reset(0)
+    _, am = gm.prefill(0, cuda_ints(prompt), want_logits=False)
+    out = gm.generate_greedy(am, w.decode_steps)   # the full 256-step run the benchmark times
+    gm.sync()
+    got = [int(am.cpu()[0])] + [int(v) for v in out.cpu().numpy()[:, 0]]
+    first_bad = next((i for i in range(len(ids)) if got[i] != ids[i]), None)
+    assert first_bad is None, f"first divergence at id {first_bad}: {got[first_bad]} vs {ids[first_bad]}"
+    assert gm.seq_len(0) == w.prompt_len + w.decode_steps
+
+
+def test_teacher_forced_logits(pair):
+    w, _, gm, prompt, ids, logits = pair
+    gm.reset(0)
+    lg, _ = gm.prefill(0, cuda_ints(prompt))
+    worst = [assert_logits_close(lg.cpu().numpy(), logits[0], "prefill last row")]
+    for s in range(STEPS):
+        lg, am = gm.decode(cuda_ints([ids[s]]), [w.prompt_len + s])
+        worst.append(assert_logits_close(lg.cpu().numpy()[0], logits[s + 1], f"step {s + 1}"))
+        assert int(am.cpu()[0]) == ids[s + 1]
+    gm.sync()
+    ma = max(x[0] for x in worst)
+    rel = max(x[1] for x in worst)
+    print(f"0.6B teacher-forced: worst max-abs {ma:.3e}, worst rel-L2 {rel:.3e} over {STEPS + 1} rows")
+
+
+def test_kv_rows_sampled(pair):
+    """Sampled cache rows after the prefill: layers 0, 13, 27."""
+    w, om, gm, prompt, _, _ = pair
+    gm.reset(0)
+    gm.prefill(0, cuda_ints(prompt), want_logits=False)
+    c = om.new_cache(w.prompt_len)
+    om.forward(c, prompt, 0)
+    for layer in (0, 13, 27):
+        k, v = gm.read_kv(layer, 0, 0, w.prompt_len)
+        assert_logits_close(k.cpu().numpy(), c.k[layer], f"K layer {layer}", max_abs=2e-3, rel_l2=1e-4)
+        assert_logits_close(v.cpu().numpy(), c.v[layer], f"V layer {layer}", max_abs=2e-3, rel_l2=1e-4)

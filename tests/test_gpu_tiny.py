@@ -1,0 +1,250 @@
+"""GPU parity of the whole model on small configurations, through the C ABI.
+
+The tiny Qwen3-shaped decoder (2 layers, hidden 256, 4/2 heads, head_dim
+64, seed 0, prompt 32, 16 greedy steps) and a mid-sized one with the 0.6B
+layer geometry (hidden 1024, 16/8 heads, head_dim 128, intermediate 3072)
+but 2 layers and a ragged vocabulary, so that every kernel instantiation of
+the decode and prefill paths runs against the oracle in seconds.
+"""
+import numpy as np
+import pytest
+
+from oracle import qw3_oracle as orc
+from quantized_transformer_decode_gb300 import inputs
+from parity import assert_logits_close, build_pair, cuda_ints
+
+pytestmark = pytest.mark.gpu
+
+MID = inputs.Qwen3Shape(vocab=5003, hidden=1024, n_layers=2, n_heads=16, n_kv_heads=8, head_dim=128,
+                        intermediate=3072, tied=True)
+MID_UNTIED = inputs.Qwen3Shape(vocab=3001, hidden=512, n_layers=2, n_heads=8, n_kv_heads=2, head_dim=128,
+                               intermediate=1536, tied=False)
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_transformer_decode_gb300 import build
+    build.build()
+    return t
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def run_greedy_case(torch, shape, seed, prompt_len, steps, flags=0, max_prefill=64):
+    """Prefill + free-running greedy (ids bit-exact) + teacher-forced logits."""
+    om, gm = build_pair(shape, seed, max_seq_len=prompt_len + steps + 8, max_prefill=max_prefill, flags=flags)
+    prompt = inputs.prompt_tokens(shape, seed, prompt_len)
+    try:
+        ids, ologits = om.generate_greedy(om.new_cache(prompt_len + steps + 1), prompt, steps)
+        # teacher-forced: feed the oracle's ids, compare every row
+        lg, am = gm.prefill(0, cuda_ints(prompt))
+        assert_logits_close(_np(lg), ologits[0], "prefill last row")
+        assert int(_np(am)[0]) == ids[0]
+        for s in range(steps):
+            lg, am = gm.decode(cuda_ints([ids[s]]), [prompt_len + s])
+            assert_logits_close(_np(lg)[0], ologits[s + 1], f"decode step {s + 1}")
+            assert int(_np(am)[0]) == ids[s + 1], f"argmax at step {s + 1}"
+        gm.sync()
+        # free-running on a fresh sequence state: ids bit-exact
+        gm.reset(0)
+        _, am = gm.prefill(0, cuda_ints(prompt), want_logits=False)
+        out = gm.generate_greedy(am, steps)
+        gm.sync()
+        got = [int(_np(am)[0])] + [int(v) for v in _np(out)[:, 0]]
+        assert got == ids
+        assert gm.seq_len(0) == prompt_len + steps
+        return om, gm, ids
+    except Exception:
+        gm.close()
+        raise
+
+
+def test_tiny_greedy_and_logits(torch):
+    w = inputs.WORKLOADS["tiny"]
+    _, gm, _ = run_greedy_case(torch, w.shape, w.seed, w.prompt_len, w.decode_steps)
+    gm.close()
+
+
+@pytest.mark.parametrize("flags", [0x1, 0x2, 0x3])
+def test_tiny_launch_modes_agree(torch, flags):
+    """Direct launches and launches without programmatic dependent launch
+    compute the same numbers as the captured graph."""
+    w = inputs.WORKLOADS["tiny"]
+    _, gm, _ = run_greedy_case(torch, w.shape, w.seed, w.prompt_len, 6, flags=flags)
+    gm.close()
+
+
+def test_mid_greedy_and_logits(torch):
+    _, gm, _ = run_greedy_case(torch, MID, 4, prompt_len=70, steps=12, max_prefill=32)
+    gm.close()
+
+
+def test_untied_lm_head(torch):
+    _, gm, _ = run_greedy_case(torch, MID_UNTIED, 5, prompt_len=40, steps=6)
+    gm.close()
+
+
+def test_kv_cache_contents(torch):
+    """K after Q/K-norm and RoPE, V as projected, at the right positions."""
+    shape = inputs.TINY
+    om, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=16)
+    prompt = inputs.prompt_tokens(shape, 0, 21)
+    cache = om.new_cache(64)
+    om.forward(cache, prompt, 0)
+    nxt = 17
+    om.forward(cache, [nxt], 21)
+    gm.prefill(0, cuda_ints(prompt), want_logits=False)
+    gm.decode(cuda_ints([nxt]), [21], want_logits=False)
+    for layer in range(shape.n_layers):
+        k, v = gm.read_kv(layer, 0, 0, 22)
+        assert_logits_close(_np(k), cache.k[layer, :22], f"K layer {layer}", max_abs=1e-4, rel_l2=1e-5)
+        assert_logits_close(_np(v), cache.v[layer, :22], f"V layer {layer}", max_abs=1e-4, rel_l2=1e-5)
+    gm.close()
+
+
+@pytest.mark.parametrize("B", [2, 3, 4, 8])
+def test_batched_decode_matches_per_sequence_oracle(torch, B):
+    """B sequences of different lengths in one decode call (B <= 4: GEMV path,
+    B = 8: the tiled GEMM path), against the oracle run per sequence."""
+    shape = inputs.TINY
+    om, gm = build_pair(shape, 0, max_seqs=B, max_seq_len=96, max_prefill=32)
+    lens = [5 + 11 * b for b in range(B)]
+    seqs = list(range(B))[::-1]            # slot order differs from batch order
+    caches = []
+    try:
+        for b in range(B):
+            pre = inputs.batch_prefix_tokens(shape, 0, b, lens[b])
+            c = om.new_cache(96)
+            lg = om.forward(c, pre, 0)
+            caches.append((c, orc.argmax_lowest(lg)))
+            gm.prefill(seqs[b], cuda_ints(pre), want_logits=False)
+        toks = [t for _, t in caches]
+        pos = list(lens)
+        for step in range(3):
+            lg, am = gm.decode(cuda_ints(toks), pos, seqs=seqs)
+            lg, am = _np(lg), _np(am)
+            for b in range(B):
+                o = om.forward(caches[b][0], [toks[b]], pos[b])
+                assert_logits_close(lg[b], o, f"B={B} seq {b} step {step}")
+                assert int(am[b]) == orc.argmax_lowest(o)
+                toks[b] = int(am[b])
+                pos[b] += 1
+        gm.sync()
+        for b in range(B):
+            assert gm.seq_len(seqs[b]) == lens[b] + 3
+    finally:
+        gm.close()
+
+
+def test_batched_generate_greedy(torch):
+    shape = inputs.TINY
+    B, steps = 3, 8
+    om, gm = build_pair(shape, 0, max_seqs=B, max_seq_len=64, max_prefill=32)
+    try:
+        firsts, want = [], []
+        for b in range(B):
+            pre = inputs.batch_prefix_tokens(shape, 0, b, 9 + b)
+            ids, _ = om.generate_greedy(om.new_cache(64), pre, steps)
+            want.append(ids)
+            _, am = gm.prefill(b, cuda_ints(pre), want_logits=False)
+            firsts.append(int(_np(am)[0]))
+        assert firsts == [w[0] for w in want]
+        out = _np(gm.generate_greedy(cuda_ints(firsts), steps))
+        gm.sync()
+        for b in range(B):
+            assert [int(v) for v in out[:, b]] == want[b][1:]
+    finally:
+        gm.close()
+
+
+def test_chunked_prefill_equals_single_pass(torch):
+    """A prompt longer than max_prefill runs in chunks; the result is the
+    oracle's single forward over the whole prompt."""
+    shape = inputs.TINY
+    om, gm = build_pair(shape, 0, max_seq_len=128, max_prefill=16)
+    prompt = inputs.prompt_tokens(shape, 0, 53)
+    lg, am = gm.prefill(0, cuda_ints(prompt))
+    o = om.forward(om.new_cache(128), prompt, 0)
+    assert_logits_close(_np(lg), o, "chunked prefill")
+    assert int(_np(am)[0]) == orc.argmax_lowest(o)
+    gm.close()
+
+
+def test_prefill_in_two_calls(torch):
+    shape = inputs.TINY
+    om, gm = build_pair(shape, 0, max_seq_len=128, max_prefill=64)
+    prompt = inputs.prompt_tokens(shape, 0, 40)
+    gm.prefill(0, cuda_ints(prompt[:23]), want_logits=False)
+    lg, _ = gm.prefill(0, cuda_ints(prompt[23:]))
+    c = om.new_cache(128)
+    om.forward(c, prompt[:23], 0)
+    o = om.forward(c, prompt[23:], 23)
+    assert_logits_close(_np(lg), o, "second prefill call")
+    gm.close()
+
+
+def test_contract_errors_leave_state_unchanged(torch):
+    """Course 12.4: pos must equal the length; rows must fit. An error leaves
+    every sequence length as it was."""
+    from quantized_transformer_decode_gb300.qw3 import Qw3Error
+    shape = inputs.TINY
+    _, gm = build_pair(shape, 0, max_seqs=2, max_seq_len=40, max_prefill=16)
+    prompt = inputs.prompt_tokens(shape, 0, 36)
+    gm.prefill(0, cuda_ints(prompt), want_logits=False)
+    with pytest.raises(Qw3Error) as e:
+        gm.decode(cuda_ints([1]), [35])
+    assert e.value.status == 3
+    with pytest.raises(Qw3Error) as e:
+        gm.prefill(0, cuda_ints(prompt[:5]))
+    assert e.value.status == 4
+    with pytest.raises(Qw3Error) as e:
+        gm.generate_greedy(cuda_ints([1]), 5)
+    assert e.value.status == 4
+    with pytest.raises(Qw3Error) as e:
+        gm.decode(cuda_ints([1, 2]), [36, 36], seqs=[0, 0])
+    assert e.value.status == 1
+    with pytest.raises(Qw3Error) as e:
+        gm.decode(cuda_ints([1]), [0], seqs=[2])
+    assert e.value.status == 1
+    assert gm.seq_len(0) == 36 and gm.seq_len(1) == 0
+    gm.generate_greedy(cuda_ints([1]), 4)
+    gm.sync()
+    assert gm.seq_len(0) == 40
+    gm.close()
+
+
+def test_truncate_then_redecode_is_reproducible(torch):
+    shape = inputs.TINY
+    _, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=32)
+    prompt = inputs.prompt_tokens(shape, 0, 20)
+    gm.prefill(0, cuda_ints(prompt), want_logits=False)
+    a, _ = gm.decode(cuda_ints([7]), [20])
+    b, _ = gm.decode(cuda_ints([9]), [21])
+    gm.truncate(0, 20)
+    assert gm.seq_len(0) == 20
+    a2, _ = gm.decode(cuda_ints([7]), [20])
+    b2, _ = gm.decode(cuda_ints([9]), [21])
+    np.testing.assert_array_equal(_np(a), _np(a2))
+    np.testing.assert_array_equal(_np(b), _np(b2))
+    gm.truncate(0, 99)
+    assert gm.seq_len(0) == 22
+    gm.close()
+
+
+def test_trace_records_every_kernel(torch):
+    shape = inputs.TINY
+    _, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=32, flags=0x4)
+    gm.prefill(0, cuda_ints(inputs.prompt_tokens(shape, 0, 8)), want_logits=False)
+    gm.decode(cuda_ints([3]), [8])
+    tr = gm.read_trace()
+    n_kernels = 2 + 5 * shape.n_layers
+    assert tr.shape[0] >= 2 * n_kernels
+    entry = tr[0:2 * n_kernels:2, 0].astype(np.int64)
+    exits = tr[0:2 * n_kernels:2, 4].astype(np.int64)
+    assert np.all(entry > 0) and np.all(exits >= entry)
+    gm.close()
