@@ -214,6 +214,32 @@ QW3_API int qw3_q8_0_dequantize(const void *blocks_dev, int64_t n, float *y_dev,
 QW3_API int qw3_q8_0_gemv(const void *W_dev, int32_t rows, int32_t cols,
                   const float *x_dev, int32_t B, float *y_dev, void *stream);
 
+/* ---- no-allocation variant ------------------------------------------- */
+
+/* The same product as qw3_q8_0_gemv (y[b][r] = sum_k W[r][k] x[b][k], raw
+ * Q8_0 blocks, f32 accumulation), computed split-K: the K range of each
+ * 8-row group is spread over several CTAs whose partial sums the last CTA of
+ * the group adds in a fixed order. The pages have no counterpart of this
+ * call; it serves callers that must not allocate device memory during a
+ * call (a serving loop whose memory a caching allocator has fully reserved,
+ * or one that cannot take cudaFree's device-wide synchronisation).
+ *
+ * No allocation: the scratch (65536 row-group arrival counters and 1048576
+ * f32 partial sums, 4.25 MiB) is a static device array of the library,
+ * limiting rows to 524288 and B*rows to 1048576 (QW3_ERR_SHAPE beyond).
+ * The counters must be zero when a call starts: static storage starts at
+ * zero and every call leaves them at zero.
+ * The first call on each device looks up the scratch address
+ * (cudaGetSymbolAddress, which can load the module); make that first call
+ * before any stream capture.
+ * Calls that overlap on one device (two streams, or two threads without
+ * ordering) share the scratch and race: order them on one stream.
+ * Arguments as qw3_q8_0_gemv, except that x_dev must be 8-byte aligned.
+ * rows == 0 is a no-op; cols == 0 writes zeros. Asynchronous on `stream`. */
+QW3_API int qw3_q8_0_gemv_splitk_noalloc(const void *W_dev, int32_t rows, int32_t cols,
+                                         const float *x_dev, int32_t B, float *y_dev,
+                                         void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -37,7 +37,7 @@ EXPORTS = (
     "qw3_create", "qw3_destroy", "qw3_prefill", "qw3_decode", "qw3_generate_greedy",
     "qw3_reset", "qw3_truncate", "qw3_seq_len", "qw3_debug_read_kv", "qw3_debug_read_trace",
     "qw3_sync", "qw3_stream", "qw3_status_string", "qw3_last_error",
-    "qw3_q8_0_quantize", "qw3_q8_0_dequantize", "qw3_q8_0_gemv",
+    "qw3_q8_0_quantize", "qw3_q8_0_dequantize", "qw3_q8_0_gemv", "qw3_q8_0_gemv_splitk_noalloc",
 )
 
 
@@ -106,6 +106,7 @@ def lib() -> ctypes.CDLL:
         "qw3_q8_0_quantize": (ctypes.c_int, [_P, _I64, _P, _P, _P]),
         "qw3_q8_0_dequantize": (ctypes.c_int, [_P, _I64, _P, _P]),
         "qw3_q8_0_gemv": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P]),
+        "qw3_q8_0_gemv_splitk_noalloc": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -208,6 +209,11 @@ def qw3_q8_0_dequantize(blocks_ptr: int, n: int, y_ptr: int, stream: int = 0) ->
 
 def qw3_q8_0_gemv(W_ptr: int, rows: int, cols: int, x_ptr: int, B: int, y_ptr: int, stream: int = 0) -> None:
     _check(lib().qw3_q8_0_gemv(W_ptr, rows, cols, x_ptr, B, y_ptr, stream or None))
+
+
+def qw3_q8_0_gemv_splitk_noalloc(W_ptr: int, rows: int, cols: int, x_ptr: int, B: int, y_ptr: int,
+                                 stream: int = 0) -> None:
+    _check(lib().qw3_q8_0_gemv_splitk_noalloc(W_ptr, rows, cols, x_ptr, B, y_ptr, stream or None))
 
 
 # ---------------------------------------------------------- torch wrapper
