@@ -284,8 +284,10 @@ def run_decode(a, w: inputs.Workload):
     s, B, P = w.shape, w.batch, w.prompt_len
     K, W = a.steps, a.warmup
     cap = P + max(K, 1) + W + 2
+    flags = (qw3.QW3_FLAG_NO_MEGA | qw3.QW3_FLAG_TRACE) if a.per_kernel else 0
     model = qw3.Qw3Model.from_f32(s, inputs.iter_weights(s, w.seed), max_seqs=B, max_seq_len=cap,
-                                  max_prefill=min(P, 4096), flags=qw3.QW3_FLAG_TRACE if B == 1 else 0)
+                                  max_prefill=min(P, 4096), flags=flags)
+    persistent, launches_per_step = model.decode_plan(B)
     stream = model.stream
     firsts = []
     for b in range(B):
@@ -326,7 +328,7 @@ def run_decode(a, w: inputs.Workload):
 
     # per-kernel durations of the last timed step from the device trace
     kernel_stats = None
-    if B == 1:
+    if a.per_kernel and B == 1:
         tr = model.read_trace(4096).astype(np.int64)
         n_k = decode_launches_per_step(s, B)
         if tr.shape[0] >= 2 * n_k:
@@ -369,7 +371,10 @@ def run_decode(a, w: inputs.Workload):
     del h_tok, h_out
     torch.cuda.synchronize()
 
-    gpu_launches = decode_launches_per_step(s, B) * K
+    gpu_launches = 1 if persistent else launches_per_step * K
+    kernel_desc = ("k_decode_mega: one persistent launch runs all K timed steps (every layer, attention, lm_head "
+                   "and argmax); its duration is the timed region" if persistent else
+                   "decode step (per-kernel path: Q8_0 GEMVs, attention, embedding, lm_head + argmax)")
     line = {
         "metric": METRIC if w.name == "qwen3-0.6b-decode" else f"{w.name} decode tok/s",
         "value": value, "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
@@ -377,13 +382,12 @@ def run_decode(a, w: inputs.Workload):
         "dtype": "f32", "data": "synthetic (seeded random-init weights quantised to Q8_0, seeded prompt)",
         "config": dict(workload_config(w, K), parallelism="replicas" if world > 1 else "single GPU",
                        timing="CUDA events on the model stream around one qw3_generate_greedy call of K steps"),
-        "roofline": {"bound": "hbm", "kernel": "decode step (all launches of one token: Q8_0 GEMVs, attention, "
-                                               "embedding, lm_head + argmax)",
+        "roofline": {"bound": "hbm", "kernel": kernel_desc,
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_step": alg_bytes / K,
-                     "traffic": profiled_traffic("decode_step_0.6b")},
+                     "traffic": profiled_traffic("k_decode_mega" if persistent else "decode_step")},
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "e2e": {"value": e2e_val, "unit": "tok/s", "h2d_bytes_per_step": 4 * B, "d2h_bytes_per_step": 4 * B,
                 "how": "per step: pinned host token -> device, qw3_decode, argmax -> pinned host, stream sync",
@@ -499,6 +503,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="qwen3-0.6b-decode", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--cpu-steps", type=int, default=8, help="oracle decode steps timed for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--per-kernel", action="store_true",
+                    help="batch-1 decode through per-kernel launches (with a device trace) instead of the "
+                         "persistent kernel")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -95,7 +95,9 @@ typedef struct qw3_config {
 
 #define QW3_FLAG_NO_GRAPH 0x1  /* launch decode kernels directly, no CUDA graph */
 #define QW3_FLAG_NO_PDL   0x2  /* no programmatic dependent launch               */
-#define QW3_FLAG_TRACE    0x4  /* record per-kernel timestamps of decode steps   */
+#define QW3_FLAG_TRACE    0x4  /* record timestamps of decode steps          */
+#define QW3_FLAG_NO_MEGA  0x8  /* batch-1 decode through per-kernel launches
+                                  instead of the persistent decode kernel       */
 
 /* One decoder layer (minfer section 1). Q8_0 matrices [out][in]:
  *   attn_q [n_heads*head_dim][H], attn_k and attn_v [n_kv_heads*head_dim][H],
@@ -172,14 +174,31 @@ QW3_API int qw3_seq_len(const qw3_model *m, int32_t seq, int32_t *len_out);
 QW3_API int qw3_debug_read_kv(qw3_model *m, int32_t layer, int32_t seq, int32_t pos0,
                       int32_t n, float *k_out_dev, float *v_out_dev);
 
-/* Timestamps of the most recent decode step, recorded when the model was
- * created with QW3_FLAG_TRACE: for each kernel of the step, in launch order,
- * two records (its first and its last CTA) of 8 u64 each: %globaltimer (ns)
- * at entry, after the wait for the previous kernel, after the prologue, after
- * the weight/KV stream, at exit; then two kernel-specific words, then the SM
- * id. out_host receives min(max_records, available) records; *n_out is the
+/* Timestamps recorded when the model was created with QW3_FLAG_TRACE, in
+ * records of 8 u64 (%globaltimer ns unless stated).
+ * Per-kernel decode path (B > 1, or QW3_FLAG_NO_MEGA): the most recent step;
+ * for each kernel, in launch order, two records (its first and its last CTA):
+ * entry, after the wait for the previous kernel, after the prologue, after the
+ * weight/KV stream, exit, two kernel-specific words, SM id.
+ * Persistent batch-1 kernel: the last step of the most recent call, for two
+ * CTAs (slot 0: the first CTA of KV head group 0; slot 1: the last CTA), each
+ * 2L+1 records: per layer an attention record (block start, QKV done, q/k/v
+ * gathered, scores done, values done, partials combined, o_proj done) and an
+ * FFN record (block start, normed, gate/up done, channels gathered, down
+ * done), then an lm_head record (start, normed, lm_head done, token known);
+ * then one record per CTA of wait totals over the whole call (ring waits,
+ * grid-sync waits, cluster-sync waits, producer waits for free slots), entry,
+ * exit, cluster id, SM id.
+ * out_host receives min(max_records, available) records; *n_out is the
  * number written. Synchronises the model's stream. */
 QW3_API int qw3_debug_read_trace(qw3_model *m, uint64_t *out_host, int32_t max_records, int32_t *n_out);
+
+/* How decode calls of batch B run: *persistent = 1 when they use the
+ * persistent decode kernel (one kernel launch per qw3_decode or
+ * qw3_generate_greedy call, whatever the step count), else 0 and
+ * *launches_per_step kernels per decode step. */
+QW3_API int qw3_decode_plan(const qw3_model *m, int32_t B, int32_t *persistent,
+                            int32_t *launches_per_step);
 
 /* Block until the model's stream is idle; return and clear the first
  * device-side status recorded since the last call (QW3_ERR_NONFINITE for NaN

@@ -23,6 +23,7 @@
 #include <vector>
 
 #include "qw3_internal.cuh"
+#include "decode_mega.cuh"
 
 namespace qw3 {
 
@@ -64,6 +65,7 @@ cudaError_t configure_all() {
         cudaError_t e = configure_gemv();
         if (e == cudaSuccess) e = configure_attention();
         if (e == cudaSuccess) e = configure_misc();
+        if (e == cudaSuccess) e = configure_mega();
         g_cfg_err = e;
     });
     return g_cfg_err;
@@ -126,6 +128,13 @@ struct qw3_model {
     // QW3_FLAG_TRACE: per-kernel timestamp records of the latest decode step
     unsigned long long *trace = nullptr;
     int trace_kernels = 0;
+
+    // persistent batch-1 decode kernel (decode_mega.cu)
+    bool mega = false;
+    MegaParams mp{};
+    MegaLayer *d_mega_layers = nullptr;
+    int mega_trace_records = 0;
+    int32_t *d_first = nullptr;
 };
 
 namespace {
@@ -204,6 +213,23 @@ int repack_into(qw3_model *m, const QMat &q, const void *raw, int rows, int cols
     }
     M_TRY(m, launch_repack(src, rows, cols, q, dst_row0, dst_stride, m->stream));
     if (!on_device) M_TRY(m, cudaStreamSynchronize(m->stream));
+    return QW3_OK;
+}
+
+// Device address of a raw Q8_0 matrix: the caller's buffer, or a copy in the
+// staging buffer (synchronous) when the weights are in host memory.
+int raw_on_device(qw3_model *m, const void *raw, int rows, int cols, bool on_device, uint8_t *staging,
+                  const uint8_t **out) {
+    if (!raw) return fail(m, QW3_ERR_INVALID_ARG, "null weight pointer");
+    if (on_device) {
+        if (reinterpret_cast<uintptr_t>(raw) & 1u) return fail(m, QW3_ERR_INVALID_ARG, "Q8_0 blocks must be 2-byte aligned");
+        *out = static_cast<const uint8_t *>(raw);
+        return QW3_OK;
+    }
+    const size_t bytes = static_cast<size_t>(rows) * (cols / 32) * 34;
+    M_TRY(m, cudaStreamSynchronize(m->stream));
+    M_TRY(m, cudaMemcpyAsync(staging, raw, bytes, cudaMemcpyHostToDevice, m->stream));
+    *out = staging;
     return QW3_OK;
 }
 
@@ -350,6 +376,172 @@ int run_decode_step(qw3_model *m, int B) {
         it = m->graphs.emplace(B, ex).first;
     }
     M_TRY(m, cudaGraphLaunch(it->second, m->stream));
+    return QW3_OK;
+}
+
+// ---- persistent batch-1 decode kernel: plan, weight copies, launch
+
+size_t align128h(size_t v) { return (v + 127) / 128 * 128; }
+
+// Shared-memory layout of the persistent kernel for NC clusters; false if it
+// does not fit.
+bool mega_layout(MegaParams &P, int max_seq_len) {
+    const int H = P.H, G = P.G, hd = P.hd;
+    int kt_max = 0;
+    for (int c = 0; c < P.NC; ++c) {
+        const int a = (c * P.act_units / P.NC) * 32, b = ((c + 1) * P.act_units / P.NC) * 32;
+        kt_max = std::max(kt_max, b - a);
+    }
+    const int apc_max = kt_max / P.CS;
+    P.maxpos = (max_seq_len + P.CS - 1) / P.CS + 2;
+    size_t off = 0;
+    auto take = [&](uint32_t &o, size_t bytes) {
+        o = static_cast<uint32_t>(off);
+        off = align128h(off + bytes);
+    };
+    take(P.o_bar, 512);
+    take(P.o_x, static_cast<size_t>(H) * 4);
+    take(P.o_xn, static_cast<size_t>(H) * 4);
+    take(P.o_qkvpub, static_cast<size_t>(P.RPC) * 4);
+    take(P.o_qkv, static_cast<size_t>(P.RG) * 4);
+    take(P.o_scores, static_cast<size_t>(G) * P.maxpos * 4);
+    take(P.o_apub, static_cast<size_t>(G) * (hd + 4) * 4);
+    take(P.o_vred, static_cast<size_t>(8) * G * hd * 4);
+    take(P.o_oall, static_cast<size_t>(G) * hd * 4);
+    take(P.o_guout, static_cast<size_t>(2) * apc_max * 4);
+    take(P.o_actpub, static_cast<size_t>(apc_max) * 4);
+    take(P.o_act, static_cast<size_t>(kt_max) * 4);
+    take(P.o_red, 1024);
+    P.o_ring = static_cast<uint32_t>(off);
+    const size_t tbH = static_cast<size_t>(H) * 17 / 2;
+    size_t sb = tbH * std::max<size_t>(1, 28672 / tbH);
+    sb = align128h(sb);
+    P.SB = static_cast<uint32_t>(sb);
+    if (static_cast<size_t>(kMegaMaxSmem) < off + 2 * sb) return false;
+    P.NS = static_cast<int>(std::min<size_t>(16, (kMegaMaxSmem - off) / sb));
+    return P.NS >= 2;
+}
+
+int setup_mega(qw3_model *m, const qw3_weights *w, bool on_dev, uint8_t *staging) {
+    const qw3_config &c = m->cfg;
+    if (c.flags & QW3_FLAG_NO_MEGA) return QW3_OK;
+    const int H = c.hidden, hd = c.head_dim, nh = c.n_heads, nkv = c.n_kv_heads, I = c.intermediate;
+    const int G = nh / nkv, CS = kMegaCS;
+    const int RG = (G + 2) * hd;
+    if (G > 7 || H > 4096 || H % (8 * CS) || RG % (8 * CS) || I % 32 || I / 32 < nkv) return QW3_OK;
+    MegaParams P{};
+    P.L = c.n_layers; P.H = H; P.I = I; P.V = c.vocab; P.hd = hd; P.G = G;
+    P.NA = nkv; P.CS = CS; P.RG = RG; P.RPC = RG / CS; P.ORPC = H / CS; P.o_groups = H / 8;
+    P.act_units = I / 32;
+    P.eps = c.rms_eps;
+    P.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(hd)));
+    int nc = std::min(16, P.act_units);
+    for (int iter = 0; iter < 4; ++iter) {
+        P.NC = nc;
+        P.NCTA = nc * CS;
+        if (!mega_layout(P, c.max_seq_len)) return QW3_OK;
+        int maxc = 0;
+        if (mega_max_clusters(P, &maxc) != cudaSuccess) {
+            cudaGetLastError();
+            return QW3_OK;
+        }
+        if (maxc >= nc) break;
+        nc = maxc;
+        if (nc < nkv) return QW3_OK;
+    }
+    if (P.NC < nkv) return QW3_OK;
+    int maxc = 0;
+    if (mega_max_clusters(P, &maxc) != cudaSuccess || maxc < P.NC) {
+        cudaGetLastError();
+        return QW3_OK;
+    }
+
+    // weight copies in the streamed layouts
+    const int qw = nh * hd;
+    QMat qkv_m = qmat_shape(nkv * RG, H, H, 0);
+    QMat o_m = qmat_shape(H, qw, G * hd, 1);
+    const size_t b_qkv = align_up(qm_bytes(qkv_m), 256), b_o = align_up(qm_bytes(o_m), 256);
+    const size_t b_down = align_up(static_cast<size_t>(H) * I / 32 * 34, 256);
+    const size_t per_layer = b_qkv + b_o + b_down;
+    uint8_t *arena = nullptr;
+    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&arena), per_layer * c.n_layers));
+    M_TRY(m, cudaMemsetAsync(arena, 0, per_layer * c.n_layers, m->stream));
+    std::vector<MegaLayer> hl(c.n_layers);
+    const size_t qrow = static_cast<size_t>(H / 32) * 34;
+    for (int l = 0; l < c.n_layers; ++l) {
+        const qw3_layer_weights &lw = w->layers[l];
+        const LayerDev &L = m->layers[l];
+        uint8_t *base = arena + per_layer * l;
+        qkv_m.base = base;
+        o_m.base = base + b_qkv;
+        uint8_t *down = base + b_qkv + b_o;
+        const uint8_t *raw = nullptr;
+        if (int rc = raw_on_device(m, lw.attn_q, qw, H, on_dev, staging, &raw)) return rc;
+        for (int g = 0; g < nkv; ++g)
+            M_TRY(m, launch_repack(raw + static_cast<size_t>(g) * G * hd * qrow, G * hd, H, qkv_m, g * RG, 1, m->stream));
+        if (int rc = raw_on_device(m, lw.attn_k, nkv * hd, H, on_dev, staging, &raw)) return rc;
+        for (int g = 0; g < nkv; ++g)
+            M_TRY(m, launch_repack(raw + static_cast<size_t>(g) * hd * qrow, hd, H, qkv_m, g * RG + G * hd, 1, m->stream));
+        if (int rc = raw_on_device(m, lw.attn_v, nkv * hd, H, on_dev, staging, &raw)) return rc;
+        for (int g = 0; g < nkv; ++g)
+            M_TRY(m, launch_repack(raw + static_cast<size_t>(g) * hd * qrow, hd, H, qkv_m, g * RG + (G + 1) * hd, 1,
+                                   m->stream));
+        if (int rc = raw_on_device(m, lw.attn_output, H, qw, on_dev, staging, &raw)) return rc;
+        M_TRY(m, launch_repack(raw, H, qw, o_m, 0, 1, m->stream));
+        if (int rc = raw_on_device(m, lw.ffn_down, H, I, on_dev, staging, &raw)) return rc;
+        M_TRY(m, launch_repack_colpart(raw, H, I, P.NC, down, m->stream));
+        M_TRY(m, cudaStreamSynchronize(m->stream));
+        hl[l].qkv = qkv_m.base;
+        hl[l].o = o_m.base;
+        hl[l].gu = L.gu.base;
+        hl[l].down = down;
+        hl[l].attn_norm = L.attn_norm;
+        hl[l].q_norm = L.q_norm;
+        hl[l].k_norm = L.k_norm;
+        hl[l].ffn_norm = L.ffn_norm;
+    }
+    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&m->d_mega_layers), sizeof(MegaLayer) * c.n_layers));
+    M_TRY(m, cudaMemcpy(m->d_mega_layers, hl.data(), sizeof(MegaLayer) * c.n_layers, cudaMemcpyHostToDevice));
+    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&P.opart), static_cast<size_t>(P.NA) * H * 4));
+    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&P.dpart), static_cast<size_t>(P.NC) * H * 4));
+    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&P.gctr), 256));
+    P.key = reinterpret_cast<unsigned long long *>(reinterpret_cast<uint8_t *>(P.gctr) + 64);
+    if (c.flags & QW3_FLAG_TRACE) {
+        m->mega_trace_records = 2 * (2 * P.L + 1) + P.NCTA;
+        const size_t tb = static_cast<size_t>(m->mega_trace_records) * 64;
+        M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&P.trace), tb));
+        M_TRY(m, cudaMemsetAsync(P.trace, 0, tb, m->stream));
+    }
+    P.layers = m->d_mega_layers;
+    P.embd = m->embd;
+    P.out = m->out;
+    P.out_norm = m->out_norm;
+    P.rope = m->rope;
+    P.kv = m->kv;
+    P.seq_stride = m->seq_stride;
+    P.kvsel_stride = m->kvsel_stride;
+    P.head_stride = m->head_stride;
+    P.layer_stride = m->layer_stride;
+    P.status = m->d_status;
+    m->mp = P;
+    m->mega = true;
+    return QW3_OK;
+}
+
+// One launch of the persistent kernel: n_steps greedy steps of sequence seq
+// from position pos0, first input token at first_tok (device).
+int run_mega(qw3_model *m, int seq, int pos0, int n_steps, const int32_t *first_tok, int32_t *hist, float *logits,
+             int32_t *argmax_out) {
+    MegaParams P = m->mp;
+    P.seq = seq;
+    P.pos0 = pos0;
+    P.n_steps = n_steps;
+    P.first_token = first_tok;
+    P.hist = hist;
+    P.logits = logits;
+    P.argmax_out = argmax_out;
+    M_TRY(m, cudaMemsetAsync(P.gctr, 0, 256, m->stream));
+    M_TRY(m, launch_mega(P, m->stream));
     return QW3_OK;
 }
 
@@ -559,6 +751,7 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->po), P * qw * 4);
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->pact), P * I * 4);
     if (e != cudaSuccess) return bail(cuda_err(m, e, "scratch allocation"));
+    if (int rc = setup_mega(m, w, on_dev, staging)) return bail(rc);
     e = cudaMemsetAsync(m->counters, 0, static_cast<size_t>(Bm) * nkv * 4, m->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->done_counter, 0, 64, m->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->argmax_key, 0, static_cast<size_t>(Bm) * 8, m->stream);
@@ -646,6 +839,11 @@ int qw3_decode(qw3_model *m, int32_t B, const int32_t *seqs_host, const int32_t 
         seqs[b] = sq;
         pos[b] = pos_host[b];
     }
+    if (m->mega && B == 1) {
+        if (int rc = run_mega(m, seqs[0], pos[0], 1, tokens_dev, nullptr, logits_dev, argmax_dev)) return rc;
+        m->seq_len[seqs[0]] += 1;
+        return QW3_OK;
+    }
     DecodeIO io{logits_dev, argmax_dev, nullptr, nullptr};
     M_TRY(m, cudaMemcpyAsync(m->d_seq, seqs.data(), B * 4, cudaMemcpyHostToDevice, m->stream));
     M_TRY(m, cudaMemcpyAsync(m->d_pos, pos.data(), B * 4, cudaMemcpyHostToDevice, m->stream));
@@ -677,6 +875,11 @@ int qw3_generate_greedy(qw3_model *m, int32_t B, const int32_t *seqs_host, int32
             return fail(m, QW3_ERR_KV_OVERFLOW, "generation would overflow the KV cache");
         seqs[b] = sq;
         pos[b] = m->seq_len[sq];
+    }
+    if (m->mega && B == 1) {
+        if (int rc = run_mega(m, seqs[0], pos[0], n_steps, first_tokens_dev, out_tokens_dev, nullptr, nullptr)) return rc;
+        m->seq_len[seqs[0]] += n_steps;
+        return QW3_OK;
     }
     DecodeIO io{nullptr, nullptr, out_tokens_dev, nullptr};
     const int32_t zero = 0;
@@ -734,10 +937,26 @@ int qw3_debug_read_trace(qw3_model *m, uint64_t *out_host, int32_t max_records, 
         return fail(m, QW3_ERR_INVALID_ARG, "bad trace arguments");
     *n_out = 0;
     if (!m->trace) return fail(m, QW3_ERR_INVALID_ARG, "model was created without QW3_FLAG_TRACE");
-    const int n = std::min(max_records, 2 * m->trace_kernels);
+    const bool mega = m->mega && m->mp.trace;
+    const int avail = mega ? m->mega_trace_records : 2 * m->trace_kernels;
+    const int n = std::min(max_records, avail);
     M_TRY(m, cudaStreamSynchronize(m->stream));
-    M_TRY(m, cudaMemcpy(out_host, m->trace, static_cast<size_t>(n) * kTraceWords * 8, cudaMemcpyDeviceToHost));
+    M_TRY(m, cudaMemcpy(out_host, mega ? m->mp.trace : m->trace, static_cast<size_t>(n) * kTraceWords * 8,
+                        cudaMemcpyDeviceToHost));
     *n_out = n;
+    return QW3_OK;
+}
+
+int qw3_decode_plan(const qw3_model *m, int32_t B, int32_t *persistent, int32_t *launches_per_step) {
+    if (!m || !persistent || !launches_per_step || B < 1 || B > m->cfg.max_seqs) return QW3_ERR_INVALID_ARG;
+    const qw3_config &c = m->cfg;
+    if (m->mega && B == 1) {
+        *persistent = 1;
+        *launches_per_step = 0;
+        return QW3_OK;
+    }
+    *persistent = 0;
+    *launches_per_step = use_gemv(c, B) ? 2 + 5 * c.n_layers : 4 + 7 * c.n_layers;
     return QW3_OK;
 }
 

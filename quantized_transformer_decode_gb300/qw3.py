@@ -31,12 +31,13 @@ QW3_ERR_TIMEOUT = 8
 QW3_FLAG_NO_GRAPH = 0x1
 QW3_FLAG_NO_PDL = 0x2
 QW3_FLAG_TRACE = 0x4
+QW3_FLAG_NO_MEGA = 0x8
 
 # Every entry point of include/qw3.h, in declaration order.
 EXPORTS = (
     "qw3_create", "qw3_destroy", "qw3_prefill", "qw3_decode", "qw3_generate_greedy",
     "qw3_reset", "qw3_truncate", "qw3_seq_len", "qw3_debug_read_kv", "qw3_debug_read_trace",
-    "qw3_sync", "qw3_stream", "qw3_status_string", "qw3_last_error",
+    "qw3_decode_plan", "qw3_sync", "qw3_stream", "qw3_status_string", "qw3_last_error",
     "qw3_q8_0_quantize", "qw3_q8_0_dequantize", "qw3_q8_0_gemv", "qw3_q8_0_gemv_splitk_noalloc",
 )
 
@@ -99,6 +100,7 @@ def lib() -> ctypes.CDLL:
         "qw3_seq_len": (ctypes.c_int, [_P, _I32, ctypes.POINTER(_I32)]),
         "qw3_debug_read_kv": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P]),
         "qw3_debug_read_trace": (ctypes.c_int, [_P, _P, _I32, ctypes.POINTER(_I32)]),
+        "qw3_decode_plan": (ctypes.c_int, [_P, _I32, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
         "qw3_sync": (ctypes.c_int, [_P]),
         "qw3_stream": (_P, [_P]),
         "qw3_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -181,6 +183,13 @@ def qw3_debug_read_trace(h: int, max_records: int) -> np.ndarray:
     n = _I32()
     _check(lib().qw3_debug_read_trace(h, out.ctypes.data, max_records, ctypes.byref(n)), h)
     return out[:n.value]
+
+
+def qw3_decode_plan(h: int, B: int) -> tuple[bool, int]:
+    """(uses the persistent kernel, kernel launches per step otherwise)."""
+    pers, lps = _I32(), _I32()
+    _check(lib().qw3_decode_plan(h, B, ctypes.byref(pers), ctypes.byref(lps)), h)
+    return bool(pers.value), lps.value
 
 
 def qw3_sync(h: int) -> None:
@@ -387,6 +396,9 @@ class Qw3Model:
 
     def read_trace(self, max_records: int = 4096) -> np.ndarray:
         return qw3_debug_read_trace(self.h, max_records)
+
+    def decode_plan(self, B: int = 1) -> tuple[bool, int]:
+        return qw3_decode_plan(self.h, B)
 
     def sync(self) -> None:
         qw3_sync(self.h)

@@ -70,13 +70,44 @@ def test_tiny_greedy_and_logits(torch):
     gm.close()
 
 
-@pytest.mark.parametrize("flags", [0x1, 0x2, 0x3])
-def test_tiny_launch_modes_agree(torch, flags):
-    """Direct launches and launches without programmatic dependent launch
-    compute the same numbers as the captured graph."""
+@pytest.mark.parametrize("flags", [0x8, 0x8 | 0x1, 0x8 | 0x2, 0x8 | 0x3])
+def test_tiny_per_kernel_launch_modes(torch, flags):
+    """The per-kernel decode path (captured graph, direct launches, with and
+    without programmatic dependent launch) against the oracle."""
     w = inputs.WORKLOADS["tiny"]
     _, gm, _ = run_greedy_case(torch, w.shape, w.seed, w.prompt_len, 6, flags=flags)
+    assert gm.decode_plan(1)[0] is False
     gm.close()
+
+
+def test_persistent_kernel_is_the_batch1_path(torch):
+    w = inputs.WORKLOADS["tiny"]
+    _, gm = build_pair(w.shape, w.seed, max_seq_len=64, max_prefill=32)
+    assert gm.decode_plan(1) == (True, 0)
+    gm.close()
+
+
+def test_mid_long_context_multi_chunk_kv(torch):
+    """Positions per CTA above one ring slot of K/V rows (hd 128)."""
+    _, gm, _ = run_greedy_case(torch, MID, 6, prompt_len=460, steps=5, max_prefill=256)
+    gm.close()
+
+
+def test_paths_agree_bitwise_on_ids(torch):
+    """Persistent kernel and per-kernel path: same greedy ids, logits close."""
+    shape = MID
+    prompt = inputs.prompt_tokens(shape, 4, 40)
+    outs = []
+    for flags in (0, 0x8):
+        _, gm = build_pair(shape, 4, max_seq_len=64, max_prefill=64, flags=flags)
+        _, am = gm.prefill(0, cuda_ints(prompt), want_logits=False)
+        lg, am2 = gm.decode(am, [40])
+        out = gm.generate_greedy(am2, 8)
+        gm.sync()
+        outs.append((_np(lg)[0], [int(v) for v in _np(out)[:, 0]]))
+        gm.close()
+    assert outs[0][1] == outs[1][1]
+    assert_logits_close(outs[0][0], outs[1][0], "persistent vs per-kernel", max_abs=1e-4, rel_l2=1e-5)
 
 
 def test_mid_greedy_and_logits(torch):
@@ -238,7 +269,8 @@ def test_truncate_then_redecode_is_reproducible(torch):
 
 def test_trace_records_every_kernel(torch):
     shape = inputs.TINY
-    _, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=32, flags=0x4)
+    _, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=32, flags=0x4 | 0x8)
+    assert gm.decode_plan(1)[0] is False
     gm.prefill(0, cuda_ints(inputs.prompt_tokens(shape, 0, 8)), want_logits=False)
     gm.decode(cuda_ints([3]), [8])
     tr = gm.read_trace()
@@ -247,4 +279,21 @@ def test_trace_records_every_kernel(torch):
     entry = tr[0:2 * n_kernels:2, 0].astype(np.int64)
     exits = tr[0:2 * n_kernels:2, 4].astype(np.int64)
     assert np.all(entry > 0) and np.all(exits >= entry)
+    gm.close()
+
+
+def test_persistent_kernel_trace(torch):
+    shape = inputs.TINY
+    _, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=32, flags=0x4)
+    assert gm.decode_plan(1)[0] is True
+    _, am = gm.prefill(0, cuda_ints(inputs.prompt_tokens(shape, 0, 8)), want_logits=False)
+    gm.generate_greedy(am, 3)
+    tr = gm.read_trace().astype(np.int64)
+    L = shape.n_layers
+    attn0 = tr[0]                     # CTA 0, layer 0 attention record
+    assert np.all(attn0[:7] > 0) and np.all(np.diff(attn0[:7]) >= 0)
+    lm = tr[2 * L]
+    assert np.all(lm[:4] > 0) and np.all(np.diff(lm[:4]) >= 0)
+    totals = tr[2 * (2 * L + 1):]
+    assert totals.shape[0] >= 16 and np.all(totals[:, 5] >= totals[:, 4])
     gm.close()
