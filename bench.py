@@ -284,7 +284,7 @@ def run_decode(a, w: inputs.Workload):
     s, B, P = w.shape, w.batch, w.prompt_len
     K, W = a.steps, a.warmup
     cap = P + max(K, 1) + W + 2
-    flags = (qw3.QW3_FLAG_NO_MEGA | qw3.QW3_FLAG_TRACE) if a.per_kernel else 0
+    flags = qw3.QW3_FLAG_PERSISTENT if a.persistent else qw3.QW3_FLAG_TRACE
     model = qw3.Qw3Model.from_f32(s, inputs.iter_weights(s, w.seed), max_seqs=B, max_seq_len=cap,
                                   max_prefill=min(P, 4096), flags=flags)
     persistent, launches_per_step = model.decode_plan(B)
@@ -328,7 +328,7 @@ def run_decode(a, w: inputs.Workload):
 
     # per-kernel durations of the last timed step from the device trace
     kernel_stats = None
-    if a.per_kernel and B == 1:
+    if not persistent and B == 1:
         tr = model.read_trace(4096).astype(np.int64)
         n_k = decode_launches_per_step(s, B)
         if tr.shape[0] >= 2 * n_k:
@@ -503,9 +503,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="qwen3-0.6b-decode", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--cpu-steps", type=int, default=8, help="oracle decode steps timed for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--per-kernel", action="store_true",
-                    help="batch-1 decode through per-kernel launches (with a device trace) instead of the "
-                         "persistent kernel")
+    ap.add_argument("--persistent", action="store_true",
+                    help="batch-1 decode through the persistent decode kernel (one launch per call)")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")

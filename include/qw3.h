@@ -96,8 +96,9 @@ typedef struct qw3_config {
 #define QW3_FLAG_NO_GRAPH 0x1  /* launch decode kernels directly, no CUDA graph */
 #define QW3_FLAG_NO_PDL   0x2  /* no programmatic dependent launch               */
 #define QW3_FLAG_TRACE    0x4  /* record timestamps of decode steps          */
-#define QW3_FLAG_NO_MEGA  0x8  /* batch-1 decode through per-kernel launches
-                                  instead of the persistent decode kernel       */
+#define QW3_FLAG_PERSISTENT 0x8 /* batch-1 decode through the persistent decode
+                                  kernel (one launch per call) instead of one
+                                  launch per kernel of each step              */
 
 /* One decoder layer (minfer section 1). Q8_0 matrices [out][in]:
  *   attn_q [n_heads*head_dim][H], attn_k and attn_v [n_kv_heads*head_dim][H],
@@ -176,11 +177,11 @@ QW3_API int qw3_debug_read_kv(qw3_model *m, int32_t layer, int32_t seq, int32_t 
 
 /* Timestamps recorded when the model was created with QW3_FLAG_TRACE, in
  * records of 8 u64 (%globaltimer ns unless stated).
- * Per-kernel decode path (B > 1, or QW3_FLAG_NO_MEGA): the most recent step;
+ * Per-kernel decode path (the default; B > 1 always): the most recent step;
  * for each kernel, in launch order, two records (its first and its last CTA):
  * entry, after the wait for the previous kernel, after the prologue, after the
  * weight/KV stream, exit, two kernel-specific words, SM id.
- * Persistent batch-1 kernel: the last step of the most recent call, for two
+ * Persistent batch-1 kernel (QW3_FLAG_PERSISTENT): the last step of the most recent call, for two
  * CTAs (slot 0: the first CTA of KV head group 0; slot 1: the last CTA), each
  * 2L+1 records: per layer an attention record (block start, QKV done, q/k/v
  * gathered, scores done, values done, partials combined, o_proj done) and an

@@ -79,7 +79,7 @@ __device__ __forceinline__ uint32_t dsmem_map(const void *local, uint32_t rank) 
 
 __device__ __forceinline__ float dsmem_ld(uint32_t addr) {
     float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
 }
 
@@ -107,61 +107,30 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// --------------------------------------------------------------- dot16
-
-struct X16 {
-    unsigned long long v[8];
+// Activation vectors enter the GEMVs as three int8 digit planes per 32-value
+// block: x = s * (h + m / 254 + l / 254^2), s = max|x| / 127, |h|, |m|, |l|
+// <= 127, which represents x to within s / (2 * 254^2) ~ 6e-8 of the block
+// maximum (about f32 rounding). Plane q of values [16c, 16c + 16) is the
+// uint4 at planes[3c + q]; the block scale s is at scales[k / 32]. A dot of
+// 16 codes with the planes is then 12 exact int8 dot-products (dp4a).
+struct Planes {
+    const uint4 *pl;
+    const float *sc;
 };
 
-__device__ __forceinline__ X16 load_x16(const float *xr) {
-    X16 x;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const ulonglong2 t = *reinterpret_cast<const ulonglong2 *>(xr + 4 * i);
-        x.v[2 * i] = t.x;
-        x.v[2 * i + 1] = t.y;
-    }
-    return x;
+// Split the 32 values a warp holds (lane i: value v of block element i) into
+// digit planes; writes the block's 3 x 32 plane bytes and its scale.
+__device__ __forceinline__ void to_planes(float v, int block, uint8_t *planes, float *scales, int lane) {
+    const float amax = warp_max(fabsf(v));
+    const float sb = amax / 127.0f;
+    int h = 0, m = 0, l = 0;
+    if (sb > 0.0f) digit_planes(v, 1.0f / sb, h, m, l);
+    uint8_t *dst = planes + static_cast<size_t>(block * 2 + (lane >> 4)) * 48 + (lane & 15);
+    dst[0] = static_cast<uint8_t>(static_cast<int8_t>(h));
+    dst[16] = static_cast<uint8_t>(static_cast<int8_t>(m));
+    dst[32] = static_cast<uint8_t>(static_cast<int8_t>(l));
+    if (lane == 0) scales[block] = sb;
 }
-
-#define QW3M_PAIR(WORD, SEL_LO, SEL_HI, X, ACC)             \
-    "prmt.b32 l, " WORD ", 0x4B000000, " SEL_LO ";\n\t"      \
-    "prmt.b32 h, " WORD ", 0x4B000000, " SEL_HI ";\n\t"      \
-    "mov.b64 p, {l, h};\n\t"                                 \
-    "add.rn.f32x2 p, p, bias;\n\t"                           \
-    "fma.rn.f32x2 " ACC ", p, " X ", " ACC ";\n\t"
-
-// Sum over 16 int8 codes w of q * x in f32 (exact code conversion).
-__device__ __forceinline__ float mdot16(const uint4 w, const X16 &x) {
-    float r;
-    asm("{\n\t"
-        ".reg .b32 t0, t1, t2, t3, l, h;\n\t"
-        ".reg .b64 p, a, b, bias;\n\t"
-        "mov.b64 bias, {%13, %13};\n\t"
-        "mov.b64 a, 0;\n\t"
-        "mov.b64 b, 0;\n\t"
-        "xor.b32 t0, %1, 0x80808080;\n\t"
-        "xor.b32 t1, %2, 0x80808080;\n\t"
-        "xor.b32 t2, %3, 0x80808080;\n\t"
-        "xor.b32 t3, %4, 0x80808080;\n\t"
-        QW3M_PAIR("t0", "0x7440", "0x7441", "%5", "a")
-        QW3M_PAIR("t0", "0x7442", "0x7443", "%6", "b")
-        QW3M_PAIR("t1", "0x7440", "0x7441", "%7", "a")
-        QW3M_PAIR("t1", "0x7442", "0x7443", "%8", "b")
-        QW3M_PAIR("t2", "0x7440", "0x7441", "%9", "a")
-        QW3M_PAIR("t2", "0x7442", "0x7443", "%10", "b")
-        QW3M_PAIR("t3", "0x7440", "0x7441", "%11", "a")
-        QW3M_PAIR("t3", "0x7442", "0x7443", "%12", "b")
-        "add.rn.f32x2 a, a, b;\n\t"
-        "mov.b64 {l, h}, a;\n\t"
-        "add.rn.f32 %0, l, h;\n\t"
-        "}"
-        : "=f"(r)
-        : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "l"(x.v[0]), "l"(x.v[1]), "l"(x.v[2]), "l"(x.v[3]),
-          "l"(x.v[4]), "l"(x.v[5]), "l"(x.v[6]), "l"(x.v[7]), "f"(-8388736.0f));
-    return r;
-}
-#undef QW3M_PAIR
 
 // ------------------------------------------------------------ item plan
 
@@ -186,14 +155,18 @@ __device__ __forceinline__ uint32_t tile_bytes(int kt) { return static_cast<uint
 
 __device__ __forceinline__ int ffn_a(const MegaParams &P, int c) { return (c * P.act_units / P.NC) * 32; }
 
+template <typename T>
+__device__ __forceinline__ const T *at_layer(const T *base, int l, size_t stride) {
+    return reinterpret_cast<const T *>(reinterpret_cast<const uint8_t *>(base) + static_cast<size_t>(l) * stride);
+}
+
 __device__ Run make_run(const MegaParams &P, const Role &R, int kind, int l, int p) {
     Run r{};
-    const MegaLayer &Ly = P.layers[l];
     switch (kind) {
         case MI_QKV: {
             const int row0 = R.c * P.RG + R.j * P.RPC;
             r.unit = tile_bytes(P.H);
-            r.src = Ly.qkv + static_cast<size_t>(row0 / 8) * r.unit;
+            r.src = at_layer(P.qkv0, l, P.mstride) + static_cast<size_t>(row0 / 8) * r.unit;
             r.n = P.RPC / 8;
             break;
         }
@@ -211,21 +184,21 @@ __device__ Run make_run(const MegaParams &P, const Role &R, int kind, int l, int
         }
         case MI_O: {
             r.unit = tile_bytes(P.G * P.hd);
-            r.src = Ly.o + (static_cast<size_t>(R.c) * P.o_groups + R.j * (P.ORPC / 8)) * r.unit;
+            r.src = at_layer(P.o0, l, P.mstride) + (static_cast<size_t>(R.c) * P.o_groups + R.j * (P.ORPC / 8)) * r.unit;
             r.n = P.ORPC / 8;
             break;
         }
         case MI_GU: {
             const int row0 = 2 * (R.a0 + R.j * R.apc);
             r.unit = tile_bytes(P.H);
-            r.src = Ly.gu + static_cast<size_t>(row0 / 8) * r.unit;
+            r.src = at_layer(P.gu0, l, P.wstride) + static_cast<size_t>(row0 / 8) * r.unit;
             r.n = 2 * R.apc / 8;
             break;
         }
         case MI_DOWN: {
             r.unit = tile_bytes(R.kt_c);
             const size_t cl_base = static_cast<size_t>(P.o_groups) * 17u * static_cast<size_t>(R.a0) / 2u;
-            r.src = Ly.down + cl_base + static_cast<size_t>(R.j * (P.ORPC / 8)) * r.unit;
+            r.src = at_layer(P.down0, l, P.mstride) + cl_base + static_cast<size_t>(R.j * (P.ORPC / 8)) * r.unit;
             r.n = P.ORPC / 8;
             break;
         }
@@ -250,7 +223,9 @@ __device__ __forceinline__ uint32_t run_chunks(const Run &r) { return (r.n + r.u
 
 struct Smem {
     uint64_t *full, *empty, *clbar;   // clbar[2]
-    float *x, *xn, *qkvpub, *qkv, *scores, *apub, *vred, *oall, *guout, *actpub, *act, *red;
+    float *x, *wbuf, *qkvpub, *qkv, *scores, *apub, *vred, *guout, *actpub, *red;
+    uint8_t *xpl, *opl, *apl;   // digit planes of the GEMV inputs (normed x, attention output, channels)
+    float *xsc, *osc, *asc;     // their block scales
     unsigned long long *keys;
     volatile int *err;
     int *tok;
@@ -263,16 +238,20 @@ __device__ Smem carve(const MegaParams &P, uint8_t *s) {
     m.empty = m.full + P.NS;
     m.clbar = m.empty + P.NS;
     m.x = reinterpret_cast<float *>(s + P.o_x);
-    m.xn = reinterpret_cast<float *>(s + P.o_xn);
+    m.xpl = s + P.o_xn;
+    m.xsc = reinterpret_cast<float *>(s + P.o_xn + static_cast<size_t>(P.H) * 3);
+    m.wbuf = reinterpret_cast<float *>(s + P.o_wbuf);
     m.qkvpub = reinterpret_cast<float *>(s + P.o_qkvpub);
     m.qkv = reinterpret_cast<float *>(s + P.o_qkv);
     m.scores = reinterpret_cast<float *>(s + P.o_scores);
     m.apub = reinterpret_cast<float *>(s + P.o_apub);
     m.vred = reinterpret_cast<float *>(s + P.o_vred);
-    m.oall = reinterpret_cast<float *>(s + P.o_oall);
+    m.opl = s + P.o_oall;
+    m.osc = reinterpret_cast<float *>(s + P.o_oall + static_cast<size_t>(P.G) * P.hd * 3);
     m.guout = reinterpret_cast<float *>(s + P.o_guout);
     m.actpub = reinterpret_cast<float *>(s + P.o_actpub);
-    m.act = reinterpret_cast<float *>(s + P.o_act);
+    m.apl = s + P.o_act;
+    m.asc = reinterpret_cast<float *>(s + P.o_act + static_cast<size_t>(P.o_act_cap) * 3);
     m.red = reinterpret_cast<float *>(s + P.o_red);
     m.keys = reinterpret_cast<unsigned long long *>(s + P.o_red + 256);
     m.err = reinterpret_cast<volatile int *>(s + P.o_red + 512);
@@ -287,6 +266,25 @@ __device__ bool wait_full(const Smem &S, uint64_t *bar, uint32_t parity, int32_t
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*S.err) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *S.err = 1;
+            record_status(status, QW3_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Producer-side bounded wait for a free ring slot. It backs off between
+// polls: the producer shares a scheduler with two consumer warps, and a
+// tight poll loop would take their issue slots for the whole step.
+__device__ bool wait_free_slot(const Smem &S, uint64_t *bar, uint32_t parity, int32_t *status) {
+    if (*S.err) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(128);
         if (mbar_try_wait(bar, parity)) return true;
         if (*S.err) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -382,14 +380,35 @@ struct Cons {
         mcons_sync();
     }
 
-    // x += sum over n partial vectors (fixed order), read from L2.
+    // x += sum over n partial vectors (fixed order), read from L2: the loads
+    // of up to four elements per thread are issued before their stores.
     __device__ void add_partials(const float *part, int n) {
-        for (int i = tid; i < P.H; i += kMegaConsumers) {
-            float s = __ldcg(part + i);
-            for (int k = 1; k < n; ++k) s += __ldcg(part + static_cast<size_t>(k) * P.H + i);
-            S.x[i] += s;
+        for (int i0 = tid; i0 < P.H; i0 += 4 * kMegaConsumers) {
+            float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int g = 0; g < n; ++g) {
+                const float *pg = part + static_cast<size_t>(g) * P.H;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = i0 + k * kMegaConsumers;
+                    if (i < P.H) v[k] += __ldcg(pg + i);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int i = i0 + k * kMegaConsumers;
+                if (i < P.H) S.x[i] += v[k];
+            }
         }
         mcons_sync();
+    }
+
+    // Norm weights for the next rmsnorm: cp.async into shared memory, issued
+    // ahead of the wait before the norm.
+    __device__ void prefetch_w(const float *w) {
+        for (int i = tid * 4; i < P.H; i += 4 * kMegaConsumers)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(S.wbuf + i)), "l"(w + i)
+                         : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
 
     __device__ float block_sum(float v) {
@@ -403,26 +422,32 @@ struct Cons {
         return t;
     }
 
-    // xn = x / sqrt(mean(x^2) + eps) * w  (course 12.3.2)
-    __device__ void rmsnorm(const float *w) {
+    // xn = x / sqrt(mean(x^2) + eps) * w (course 12.3.2), w from prefetch_w,
+    // written as digit planes: warp w handles blocks w, w + 8, ...
+    __device__ void rmsnorm() {
         float ss = 0.0f;
         for (int i = tid; i < P.H; i += kMegaConsumers) ss = fmaf(S.x[i], S.x[i], ss);
+        asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's weights; block_sum syncs all
         const float r = 1.0f / sqrtf(block_sum(ss) / static_cast<float>(P.H) + P.eps);
-        for (int i = tid; i < P.H; i += kMegaConsumers) S.xn[i] = S.x[i] * r * w[i];
+        for (int i = tid; i < P.H; i += kMegaConsumers) to_planes(S.x[i] * r * S.wbuf[i], i >> 5, S.xpl, S.xsc, lane);
         mcons_sync();
     }
 
-    // One chunk of tiles (8 rows x kt): warp w takes row w of each tile. Up to
-    // four tiles share each x load; with kt <= 256 a half-warp per tile.
+    // One chunk of tiles (8 rows x kt): warp w takes row w of each tile, four
+    // tiles (eight on the half-warp path, kt <= 256) per pass sharing each
+    // load of the activation planes.
     template <typename Sink>
-    __device__ void gemv_chunk(const uint8_t *stage, int ntiles, int kt, const float *xin, int tile0, Sink sink) {
+    __device__ void gemv_chunk(const uint8_t *stage, int ntiles, int kt, const Planes xin, int tile0, Sink sink) {
         const uint32_t tb = tile_bytes(kt);
         if (kt > 256) {
             for (int t0 = 0; t0 < ntiles; t0 += 4) {
                 const int T = min(4, ntiles - t0);
                 float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 for (int k = lane * 16; k < kt; k += 512) {
-                    const X16 xv = load_x16(xin + k);
+                    uint4 Pq[3];
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) Pq[q] = xin.pl[(k >> 4) * 3 + q];
+                    const float sx = xin.sc[k >> 5];
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
                         if (t < T) {
@@ -430,42 +455,56 @@ struct Cons {
                             const uint4 w = *reinterpret_cast<const uint4 *>(tile + warp * kt + k);
                             const float d = __half2float(
                                 reinterpret_cast<const __half *>(tile + 8 * kt)[warp * (kt >> 5) + (k >> 5)]);
-                            acc[t] = fmaf(d, mdot16(w, xv), acc[t]);
+                            acc[t] = fmaf(d * sx, pdot16(w, Pq), acc[t]);
                         }
                     }
                 }
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    if (t < T) {
-                        const float v = warp_sum(acc[t]);
-                        if (lane == 0) sink(tile0 + t0 + t, warp, v);
-                    }
+                for (int t = 0; t < 4; ++t) acc[t] = warp_sum(acc[t]);
+                if (lane == 0) {
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        if (t < T) sink(tile0 + t0 + t, warp, acc[t]);
                 }
             }
         } else {
             const int half = lane >> 4, hl = lane & 15;
-            for (int t0 = 0; t0 < ntiles; t0 += 2) {
-                const int t = t0 + half;
-                float acc = 0.0f;
-                if (t < ntiles) {
-                    const uint8_t *tile = stage + static_cast<size_t>(t) * tb;
-                    for (int k = hl * 16; k < kt; k += 256) {
-                        const X16 xv = load_x16(xin + k);
-                        const uint4 w = *reinterpret_cast<const uint4 *>(tile + warp * kt + k);
-                        const float d = __half2float(
-                            reinterpret_cast<const __half *>(tile + 8 * kt)[warp * (kt >> 5) + (k >> 5)]);
-                        acc = fmaf(d, mdot16(w, xv), acc);
+            for (int t0 = 0; t0 < ntiles; t0 += 8) {
+                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                for (int k = hl * 16; k < kt; k += 256) {
+                    uint4 Pq[3];
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) Pq[q] = xin.pl[(k >> 4) * 3 + q];
+                    const float sx = xin.sc[k >> 5];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int t = t0 + 2 * u + half;
+                        if (t < ntiles) {
+                            const uint8_t *tile = stage + static_cast<size_t>(t) * tb;
+                            const uint4 w = *reinterpret_cast<const uint4 *>(tile + warp * kt + k);
+                            const float d = __half2float(
+                                reinterpret_cast<const __half *>(tile + 8 * kt)[warp * (kt >> 5) + (k >> 5)]);
+                            acc[u] = fmaf(d * sx, pdot16(w, Pq), acc[u]);
+                        }
                     }
                 }
 #pragma unroll
-                for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                if (hl == 0 && t < ntiles) sink(tile0 + t, warp, acc);
+                for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
+                if (hl == 0) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int t = t0 + 2 * u + half;
+                        if (t < ntiles) sink(tile0 + t, warp, acc[u]);
+                    }
+                }
             }
         }
     }
 
     template <typename Sink>
-    __device__ void gemv_item(const Run &r, int kt, const float *xin, Sink sink) {
+    __device__ void gemv_item(const Run &r, int kt, const Planes xin, Sink sink) {
         const uint32_t nch = run_chunks(r);
         for (uint32_t ch = 0; ch < nch; ++ch) {
             const uint8_t *st = stage_wait();
@@ -477,63 +516,80 @@ struct Cons {
     }
 };
 
-// Q/K RMSNorm over head_dim then NeoX RoPE at position p (minfer 2.2;
-// course 12.3.4): one warp per head vector, lane holds HD/32 consecutive
-// dims; the rotation partner of dim i < HD/2 is i + HD/2, in lane ^ 16.
-template <int HD>
-__device__ void norm_rope(float *v, const float *w, float eps, const float2 *rope_p, int lane) {
-    constexpr int E = HD / 32;
-    float a[E];
-    float ss = 0.0f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        a[e] = v[lane * E + e];
-        ss = fmaf(a[e], a[e], ss);
-    }
-    ss = warp_sum(ss);
-    const float r = 1.0f / sqrtf(ss / static_cast<float>(HD) + eps);
-#pragma unroll
-    for (int e = 0; e < E; ++e) a[e] = a[e] * r * w[lane * E + e];
-    const bool first = lane < 16;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const float o = __shfl_xor_sync(0xffffffffu, a[e], 16);
-        const float2 cs = rope_p[(lane & 15) * E + e];
-        a[e] = first ? (a[e] * cs.x - o * cs.y) : (o * cs.y + a[e] * cs.x);
-    }
-    __syncwarp();
-#pragma unroll
-    for (int e = 0; e < E; ++e) v[lane * E + e] = a[e];
-}
-
-template <int HD>
+template <int HD, int G>
 __device__ void phase_attention(Cons &C, int l, int p) {
     const MegaParams &P = C.P;
     const Smem &S = C.S;
     const Role &R = C.R;
-    const MegaLayer &Ly = P.layers[l];
-    const int G = P.G;
     constexpr int E = HD / 32;
+
+    // RoPE row of position p and the Q/K norm weights, ahead of their use
+    float2 rp[E];
+    {
+        const float2 *rope_p = P.rope + static_cast<size_t>(p) * (HD / 2);
+#pragma unroll
+        for (int e = 0; e < E; ++e) rp[e] = __ldg(rope_p + (C.lane & 15) * E + e);
+    }
+    const float *qn = at_layer(P.q_norm0, l, P.wstride), *kn = at_layer(P.k_norm0, l, P.wstride);
+    const float *nw = C.warp < G ? qn : kn;
+    float nwr[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) nwr[e] = __ldg(nw + C.lane * E + e);
 
     // QKV rows of this CTA -> qkvpub
     C.mark(2 * l, 0);
-    C.rmsnorm(Ly.attn_norm);
+    C.rmsnorm();
     {
         const Run r = make_run(P, R, MI_QKV, l, p);
         float *pub = S.qkvpub;
-        C.gemv_item(r, P.H, S.xn, [pub](int tile, int w, float v) { pub[tile * 8 + w] = v; });
+        C.gemv_item(r, P.H, Planes{reinterpret_cast<const uint4 *>(S.xpl), S.xsc},
+                    [pub](int tile, int w, float v) { pub[tile * 8 + w] = v; });
     }
     C.mark(2 * l, 1);
     C.cluster_sync();
-    // gather the group's q, k, v from the cluster
-    for (int i = C.tid; i < P.RG; i += kMegaConsumers) {
-        const int src = i / P.RPC, off = i - src * P.RPC;
-        S.qkv[i] = dsmem_ld(dsmem_map(S.qkvpub + off, static_cast<uint32_t>(src)));
+    // gather the group's q, k, v from the cluster: issue every remote load first
+    {
+        float g[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = C.tid + u * kMegaConsumers;
+            g[u] = 0.0f;
+            if (i < P.RG) {
+                const int src = i / P.RPC, off = i - src * P.RPC;
+                g[u] = dsmem_ld(dsmem_map(S.qkvpub + off, static_cast<uint32_t>(src)));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = C.tid + u * kMegaConsumers;
+            if (i < P.RG) S.qkv[i] = g[u];
+        }
     }
     mcons_sync();
-    const float2 *rope_p = P.rope + static_cast<size_t>(p) * (HD / 2);
-    if (C.warp < G) norm_rope<HD>(S.qkv + C.warp * HD, Ly.q_norm, P.eps, rope_p, C.lane);
-    else if (C.warp == G) norm_rope<HD>(S.qkv + G * HD, Ly.k_norm, P.eps, rope_p, C.lane);
+    // Q/K RMSNorm over head_dim then RoPE (warp h < G: query head h; warp G: k)
+    if (C.warp <= G) {
+        float *v = S.qkv + C.warp * HD;
+        float a[E];
+        float ss = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            a[e] = v[C.lane * E + e];
+            ss = fmaf(a[e], a[e], ss);
+        }
+        ss = warp_sum(ss);
+        const float r = 1.0f / sqrtf(ss / static_cast<float>(HD) + P.eps);
+#pragma unroll
+        for (int e = 0; e < E; ++e) a[e] = a[e] * r * nwr[e];
+        const bool first = C.lane < 16;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const float o = __shfl_xor_sync(0xffffffffu, a[e], 16);
+            a[e] = first ? (a[e] * rp[e].x - o * rp[e].y) : (o * rp[e].y + a[e] * rp[e].x);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[C.lane * E + e] = a[e];
+    }
     mcons_sync();
     const float *knew = S.qkv + G * HD, *vnew = S.qkv + (G + 1) * HD;
     if (R.j == 0 && C.tid < 2 * HD) {
@@ -550,46 +606,78 @@ __device__ void phase_attention(Cons &C, int l, int p) {
     const int nk = static_cast<int>(rk.n);
     const bool has_new = (R.j == P.CS - 1);
     const int ntot = nk + (has_new ? 1 : 0);
-    float qreg[8][E];
+    float qreg[G][E];
 #pragma unroll
-    for (int h = 0; h < 8; ++h)
+    for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int e = 0; e < E; ++e) qreg[h][e] = (h < G) ? S.qkv[h * HD + C.lane * E + e] : 0.0f;
+        for (int e = 0; e < E; ++e) qreg[h][e] = S.qkv[h * HD + C.lane * E + e];
     {
         const uint32_t nch = run_chunks(rk);
         for (uint32_t ch = 0; ch < nch; ++ch) {
             const uint8_t *st = C.stage_wait();
             const int u0 = static_cast<int>(ch * rk.upc);
             const int nr = min(static_cast<int>(rk.upc), nk - u0);
-            for (int i = C.warp; i < nr; i += 8) {
-                const float *krow = reinterpret_cast<const float *>(st) + static_cast<size_t>(i) * HD;
-                float kv[E];
+            // four rows per warp per pass: 4 x G independent reductions
+            for (int i0 = C.warp; i0 < nr; i0 += 32) {
+                float sc[4][G];
 #pragma unroll
-                for (int e = 0; e < E; ++e) kv[e] = krow[C.lane * E + e];
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + 8 * u;
+                    float kv[E];
+                    if (i < nr) {
+                        const float *krow = reinterpret_cast<const float *>(st) + static_cast<size_t>(i) * HD + C.lane * E;
+                        if constexpr (E == 4) {
+                            const float4 t = *reinterpret_cast<const float4 *>(krow);
+                            kv[0] = t.x; kv[1] = t.y; kv[2] = t.z; kv[3] = t.w;
+                        } else {
 #pragma unroll
-                for (int h = 0; h < 8; ++h) {
-                    if (h < G) {
-                        float s = 0.0f;
+                            for (int e = 0; e < E; ++e) kv[e] = krow[e];
+                        }
+                    } else {
 #pragma unroll
-                        for (int e = 0; e < E; ++e) s = fmaf(qreg[h][e], kv[e], s);
-                        s = warp_sum(s);
-                        if (C.lane == 0) S.scores[h * P.maxpos + u0 + i] = s * P.scale;
+                        for (int e = 0; e < E; ++e) kv[e] = 0.0f;
                     }
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        float a = 0.0f;
+#pragma unroll
+                        for (int e = 0; e < E; ++e) a = fmaf(qreg[h][e], kv[e], a);
+                        sc[u][h] = a;
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int h = 0; h < G; ++h) sc[u][h] += __shfl_xor_sync(0xffffffffu, sc[u][h], o);
+                if (C.lane == 0) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int h = 0; h < G; ++h)
+                            if (i0 + 8 * u < nr) S.scores[h * P.maxpos + u0 + i0 + 8 * u] = sc[u][h] * P.scale;
                 }
             }
             C.stage_release();
         }
     }
     if (has_new && C.warp == 0) {
+        float sc[G];
 #pragma unroll
-        for (int h = 0; h < 8; ++h) {
-            if (h < G) {
-                float s = 0.0f;
+        for (int h = 0; h < G; ++h) {
+            float a = 0.0f;
 #pragma unroll
-                for (int e = 0; e < E; ++e) s = fmaf(qreg[h][e], knew[C.lane * E + e], s);
-                s = warp_sum(s);
-                if (C.lane == 0) S.scores[h * P.maxpos + nk] = s * P.scale;
-            }
+            for (int e = 0; e < E; ++e) a = fmaf(qreg[h][e], knew[C.lane * E + e], a);
+            sc[h] = a;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int h = 0; h < G; ++h) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], o);
+        if (C.lane == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) S.scores[h * P.maxpos + nk] = sc[h] * P.scale;
         }
     }
     mcons_sync();
@@ -614,9 +702,9 @@ __device__ void phase_attention(Cons &C, int l, int p) {
     }
     mcons_sync();
     // acc = sum_i e_i v_i : warp w takes rows i = w mod 8
-    float acc[8][E];
+    float acc[G][E];
 #pragma unroll
-    for (int h = 0; h < 8; ++h)
+    for (int h = 0; h < G; ++h)
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[h][e] = 0.0f;
     {
@@ -629,15 +717,18 @@ __device__ void phase_attention(Cons &C, int l, int p) {
             for (int i = C.warp; i < nr; i += 8) {
                 const float *vrow = reinterpret_cast<const float *>(st) + static_cast<size_t>(i) * HD;
                 float vv[E];
+                if constexpr (E == 4) {
+                    const float4 t = *reinterpret_cast<const float4 *>(vrow + C.lane * E);
+                    vv[0] = t.x; vv[1] = t.y; vv[2] = t.z; vv[3] = t.w;
+                } else {
 #pragma unroll
-                for (int e = 0; e < E; ++e) vv[e] = vrow[C.lane * E + e];
+                    for (int e = 0; e < E; ++e) vv[e] = vrow[C.lane * E + e];
+                }
 #pragma unroll
-                for (int h = 0; h < 8; ++h) {
-                    if (h < G) {
-                        const float wgt = S.scores[h * P.maxpos + u0 + i];
+                for (int h = 0; h < G; ++h) {
+                    const float wgt = S.scores[h * P.maxpos + u0 + i];
 #pragma unroll
-                        for (int e = 0; e < E; ++e) acc[h][e] = fmaf(wgt, vv[e], acc[h][e]);
-                    }
+                    for (int e = 0; e < E; ++e) acc[h][e] = fmaf(wgt, vv[e], acc[h][e]);
                 }
             }
             C.stage_release();
@@ -645,19 +736,16 @@ __device__ void phase_attention(Cons &C, int l, int p) {
     }
     if (has_new && C.warp == 0) {
 #pragma unroll
-        for (int h = 0; h < 8; ++h) {
-            if (h < G) {
-                const float wgt = S.scores[h * P.maxpos + nk];
+        for (int h = 0; h < G; ++h) {
+            const float wgt = S.scores[h * P.maxpos + nk];
 #pragma unroll
-                for (int e = 0; e < E; ++e) acc[h][e] = fmaf(wgt, vnew[C.lane * E + e], acc[h][e]);
-            }
+            for (int e = 0; e < E; ++e) acc[h][e] = fmaf(wgt, vnew[C.lane * E + e], acc[h][e]);
         }
     }
 #pragma unroll
-    for (int h = 0; h < 8; ++h)
-        if (h < G)
+    for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int e = 0; e < E; ++e) S.vred[(C.warp * G + h) * HD + C.lane * E + e] = acc[h][e];
+        for (int e = 0; e < E; ++e) S.vred[(C.warp * G + h) * HD + C.lane * E + e] = acc[h][e];
     mcons_sync();
     for (int i = C.tid; i < G * HD; i += kMegaConsumers) {
         const int h = i / HD, d = i - h * HD;
@@ -690,7 +778,7 @@ __device__ void phase_attention(Cons &C, int l, int p) {
             L = fmaf(lr[r], f, L);
             O = fmaf(ar[r], f, O);
         }
-        S.oall[i] = O / L;
+        to_planes(O / L, i >> 5, S.opl, S.osc, C.lane);
     }
     mcons_sync();
     C.mark(2 * l, 5);
@@ -698,7 +786,8 @@ __device__ void phase_attention(Cons &C, int l, int p) {
     {
         const Run r = make_run(P, R, MI_O, l, p);
         float *dst = P.opart + static_cast<size_t>(R.c) * P.H + R.j * P.ORPC;
-        C.gemv_item(r, G * HD, S.oall, [dst](int tile, int w, float v) { dst[tile * 8 + w] = v; });
+        C.gemv_item(r, G * HD, Planes{reinterpret_cast<const uint4 *>(S.opl), S.osc},
+                    [dst](int tile, int w, float v) { dst[tile * 8 + w] = v; });
     }
     C.mark(2 * l, 6);
 }
@@ -707,14 +796,14 @@ __device__ void phase_ffn(Cons &C, int l, int p) {
     const MegaParams &P = C.P;
     const Smem &S = C.S;
     const Role &R = C.R;
-    const MegaLayer &Ly = P.layers[l];
     C.mark(2 * l + 1, 0);
-    C.rmsnorm(Ly.ffn_norm);
+    C.rmsnorm();
     C.mark(2 * l + 1, 1);
     {
         const Run r = make_run(P, R, MI_GU, l, p);
         float *gu = S.guout;
-        C.gemv_item(r, P.H, S.xn, [gu](int tile, int w, float v) { gu[tile * 8 + w] = v; });
+        C.gemv_item(r, P.H, Planes{reinterpret_cast<const uint4 *>(S.xpl), S.xsc},
+                    [gu](int tile, int w, float v) { gu[tile * 8 + w] = v; });
     }
     mcons_sync();
     C.mark(2 * l + 1, 2);
@@ -723,16 +812,30 @@ __device__ void phase_ffn(Cons &C, int l, int p) {
         S.actpub[a] = g / (1.0f + expf(-g)) * u;   // SwiGLU (course 12.3.6)
     }
     C.cluster_sync();
-    for (int i = C.tid; i < R.kt_c; i += kMegaConsumers) {
-        const int src = i / R.apc, off = i - src * R.apc;
-        S.act[i] = dsmem_ld(dsmem_map(S.actpub + off, static_cast<uint32_t>(src)));
+    {
+        float g[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = C.tid + u * kMegaConsumers;
+            g[u] = 0.0f;
+            if (i < R.kt_c) {
+                const int src = i / R.apc, off = i - src * R.apc;
+                g[u] = dsmem_ld(dsmem_map(S.actpub + off, static_cast<uint32_t>(src)));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i0 = u * kMegaConsumers + C.warp * 32;   // warp-uniform block start
+            if (i0 < R.kt_c) to_planes(g[u], (C.tid + u * kMegaConsumers) >> 5, S.apl, S.asc, C.lane);
+        }
     }
     mcons_sync();
     C.mark(2 * l + 1, 3);
     {
         const Run r = make_run(P, R, MI_DOWN, l, p);
         float *dst = P.dpart + static_cast<size_t>(R.c) * P.H + R.j * P.ORPC;
-        C.gemv_item(r, R.kt_c, S.act, [dst](int tile, int w, float v) { dst[tile * 8 + w] = v; });
+        C.gemv_item(r, R.kt_c, Planes{reinterpret_cast<const uint4 *>(S.apl), S.asc},
+                    [dst](int tile, int w, float v) { dst[tile * 8 + w] = v; });
     }
     C.mark(2 * l + 1, 4);
 }
@@ -744,13 +847,13 @@ __device__ void embed(Cons &C, int tok) {
     mcons_sync();
 }
 
-// lm_head rows of this CTA with the argmax fold; returns after the arrive.
+// lm_head rows of this CTA with the argmax fold (before the arrive).
 __device__ void phase_lm(Cons &C, int s) {
     const MegaParams &P = C.P;
     const Smem &S = C.S;
     const Role &R = C.R;
     C.mark(2 * P.L, 0);
-    C.rmsnorm(P.out_norm);
+    C.rmsnorm();
     C.mark(2 * P.L, 1);
     const Run r = make_run(P, R, MI_LM, 0, 0);
     const int ng = (P.V + 7) / 8;
@@ -758,7 +861,7 @@ __device__ void phase_lm(Cons &C, int s) {
     unsigned long long best = 0ull;
     float *logits = P.logits;
     const int V = P.V;
-    C.gemv_item(r, P.H, S.xn, [&best, logits, V, g0](int tile, int w, float v) {
+    C.gemv_item(r, P.H, Planes{reinterpret_cast<const uint4 *>(S.xpl), S.xsc}, [&best, logits, V, g0](int tile, int w, float v) {
         const int row = (g0 + tile) * 8 + w;
         if (row < V) {
             if (logits) logits[row] = v;
@@ -780,10 +883,9 @@ __device__ void phase_lm(Cons &C, int s) {
         if (b) atomicMax(P.key + (s & 1), b);
     }
     C.mark(2 * P.L, 2);
-    (void)S;
 }
 
-template <int HD>
+template <int HD, int G>
 __global__ void __launch_bounds__(kMegaThreads, 1) k_decode_mega(const MegaParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
     const Smem S = carve(P, smem);
@@ -824,7 +926,7 @@ __global__ void __launch_bounds__(kMegaThreads, 1) k_decode_mega(const MegaParam
                     const int s = static_cast<int>(q % static_cast<uint32_t>(P.NS));
                     const uint32_t n = q / static_cast<uint32_t>(P.NS);
                     const uint64_t tw0 = P.trace ? globaltimer_ns() : 0;
-                    if (n >= 1 && !wait_full(S, S.empty + s, (n - 1) & 1u, P.status)) {
+                    if (n >= 1 && !wait_free_slot(S, S.empty + s, (n - 1) & 1u, P.status)) {
                         stop = true;
                         break;
                     }
@@ -877,19 +979,23 @@ __global__ void __launch_bounds__(kMegaThreads, 1) k_decode_mega(const MegaParam
             const int p = P.pos0 + st;
             C.last_step = (st == P.n_steps - 1);
             tok = tok < 0 ? 0 : (tok >= P.V ? P.V - 1 : tok);
+            if (R.att) C.prefetch_w(P.attn_norm0);
             embed(C, tok);
             for (int l = 0; l < P.L; ++l) {
                 if (l > 0) {
+                    if (R.att) C.prefetch_w(at_layer(P.attn_norm0, l, P.wstride));
                     C.grid_wait();
                     C.add_partials(P.dpart, P.NC);
                 }
-                if (R.att) phase_attention<HD>(C, l, p);
+                if (R.att) phase_attention<HD, G>(C, l, p);
                 C.grid_arrive();
+                C.prefetch_w(at_layer(P.ffn_norm0, l, P.wstride));
                 C.grid_wait();
                 C.add_partials(P.opart, P.NA);
                 phase_ffn(C, l, p);
                 C.grid_arrive();
             }
+            C.prefetch_w(P.out_norm);
             C.grid_wait();
             C.add_partials(P.dpart, P.NC);
             phase_lm(C, st);
@@ -931,13 +1037,31 @@ __global__ void __launch_bounds__(kMegaThreads, 1) k_decode_mega(const MegaParam
 
 size_t mega_smem_bytes(const MegaParams &P) { return P.o_ring + static_cast<size_t>(P.NS) * P.SB; }
 
+// Instantiations: head_dim 64 or 128, query heads per KV head 1, 2 or 4.
+template <typename F>
+static cudaError_t mega_dispatch(int hd, int G, F f) {
+    if (hd == 128 && G == 1) return f(k_decode_mega<128, 1>);
+    if (hd == 128 && G == 2) return f(k_decode_mega<128, 2>);
+    if (hd == 128 && G == 4) return f(k_decode_mega<128, 4>);
+    if (hd == 64 && G == 1) return f(k_decode_mega<64, 1>);
+    if (hd == 64 && G == 2) return f(k_decode_mega<64, 2>);
+    if (hd == 64 && G == 4) return f(k_decode_mega<64, 4>);
+    return cudaErrorInvalidValue;
+}
+
+bool mega_supported_heads(int hd, int G) { return (hd == 64 || hd == 128) && (G == 1 || G == 2 || G == 4); }
+
 cudaError_t configure_mega() {
-    cudaError_t e = cudaFuncSetAttribute(k_decode_mega<128>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_decode_mega<64>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_decode_mega<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMegaMaxSmem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_decode_mega<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMegaMaxSmem);
+    cudaError_t e = cudaSuccess;
+    for (int hd : {64, 128})
+        for (int G : {1, 2, 4}) {
+            if (e == cudaSuccess)
+                e = mega_dispatch(hd, G, [](auto k) {
+                    cudaError_t r = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                    if (r == cudaSuccess) r = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMegaMaxSmem);
+                    return r;
+                });
+        }
     return e;
 }
 
@@ -960,16 +1084,14 @@ cudaError_t mega_max_clusters(const MegaParams &P, int *n) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     mega_launch_config(P, cfg, attr, nullptr);
-    if (P.hd == 128) return cudaOccupancyMaxActiveClusters(n, k_decode_mega<128>, &cfg);
-    return cudaOccupancyMaxActiveClusters(n, k_decode_mega<64>, &cfg);
+    return mega_dispatch(P.hd, P.G, [&](auto k) { return cudaOccupancyMaxActiveClusters(n, k, &cfg); });
 }
 
 cudaError_t launch_mega(const MegaParams &P, cudaStream_t s) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     mega_launch_config(P, cfg, attr, s);
-    if (P.hd == 128) return cudaLaunchKernelEx(&cfg, k_decode_mega<128>, P);
-    return cudaLaunchKernelEx(&cfg, k_decode_mega<64>, P);
+    return mega_dispatch(P.hd, P.G, [&](auto k) { return cudaLaunchKernelEx(&cfg, k, P); });
 }
 
 // Column-partitioned down matrix: cluster c owns channels [a_c, a_{c+1}),

@@ -5,17 +5,16 @@
 
 namespace qw3 {
 
-// Per-layer weights in the layouts the persistent kernel streams.
-struct MegaLayer {
-    const uint8_t *qkv;    // rows grouped per KV head g: [G query heads | k | v], tiles 8 x H, row-group-major
-    const uint8_t *o;      // W_o, tiles 8 x (G*head_dim), k-tile-major (one k-tile per KV head group)
-    const uint8_t *gu;     // gate/up rows interleaved (2i gate, 2i+1 up), tiles 8 x H, row-group-major
-    const uint8_t *down;   // W_down, column-partitioned over the NC clusters (see k_repack_colpart)
-    const float *attn_norm, *q_norm, *k_norm, *ffn_norm;
-};
-
 struct MegaParams {
-    const MegaLayer *layers;  // device array [L]
+    // Per-layer weights in the layouts the kernel streams; layer l of each
+    // array sits at base + l * stride (bytes).
+    const uint8_t *qkv0;      // rows grouped per KV head g: [G query heads | k | v], tiles 8 x H, row-group-major
+    const uint8_t *o0;        // W_o, tiles 8 x (G*head_dim), k-tile-major (one k-tile per KV head group)
+    const uint8_t *down0;     // W_down, column-partitioned over the NC clusters (see k_repack_colpart)
+    size_t mstride;
+    const uint8_t *gu0;       // gate/up rows interleaved (2i gate, 2i+1 up), tiles 8 x H, row-group-major
+    const float *attn_norm0, *q_norm0, *k_norm0, *ffn_norm0;
+    size_t wstride;
     QMat embd, out;           // token embedding, lm_head (row-group-major, kt = H)
     const float *out_norm;
     const float2 *rope;       // [max_seq_len][hd/2] (cos, sin)
@@ -31,6 +30,7 @@ struct MegaParams {
     int o_groups;             // H / 8
     int act_units;            // I / 32
     int maxpos;               // score slots per head (>= positions per CTA + 1)
+    int o_act_cap;            // capacity (values) of the channel plane buffer
     float eps, scale;
     int seq, pos0, n_steps;
     const int32_t *first_token;   // device [1]
@@ -46,7 +46,7 @@ struct MegaParams {
     uint32_t SB;                  // ring slot bytes
     int NS;                       // ring slots
     // shared-memory layout (byte offsets)
-    uint32_t o_bar, o_x, o_xn, o_qkvpub, o_qkv, o_scores, o_apub, o_vred, o_oall, o_guout, o_actpub, o_act, o_red,
+    uint32_t o_bar, o_x, o_xn, o_wbuf, o_qkvpub, o_qkv, o_scores, o_apub, o_vred, o_oall, o_guout, o_actpub, o_act, o_red,
         o_ring;
 };
 
@@ -55,6 +55,7 @@ constexpr int kMegaCS = 8;
 
 size_t mega_smem_bytes(const MegaParams &P);
 cudaError_t configure_mega();
+bool mega_supported_heads(int hd, int G);
 cudaError_t mega_max_clusters(const MegaParams &P, int *n);
 cudaError_t launch_mega(const MegaParams &P, cudaStream_t s);
 cudaError_t launch_repack_colpart(const uint8_t *raw, int rows, int cols, int NC, uint8_t *dst, cudaStream_t s);

@@ -19,11 +19,16 @@
 //    never more than one phase ahead of its waiters: warp w takes row w of
 //    each tile, four tiles at once for independent chains.
 //  * Consumers wait for the previous kernel, then stage the input rows in
-//    shared memory (optionally RMS-normalised, 12.3.2) in a padded layout (36
-//    floats per 32-value block) that keeps 128-bit reads conflict-free.
-//  * Per 16 codes a lane converts int8 -> f32 by byte-permuting q + 128 into
-//    the mantissa of 2^23 and subtracting (exact), then accumulates with
-//    packed fma.rn.f32x2; f32 accumulation throughout.
+//    shared memory (optionally RMS-normalised, 12.3.2), in one of two forms.
+//    Small slices (the per-layer projections at 0.6B): f32 in a padded
+//    layout (36 floats per 32-value block, conflict-free 128-bit reads); per
+//    16 codes a lane converts int8 -> f32 by byte-permuting q + 128 into the
+//    mantissa of 2^23 and subtracting (exact) and accumulates with packed
+//    fma.rn.f32x2. Large slices (lm_head; every projection at 8B): int8
+//    digit planes (x = s (h + m/254 + l/254^2) per 32-block, within ~6e-8 of
+//    the block maximum), so that 16 codes cost 12 exact dp4a and one f32
+//    combination: about twice the f32 path's throughput, for a staging cost
+//    that only a large slice amortises. f32 accumulation throughout.
 //  * Row sums land in shared memory; one epilogue after the stream: store,
 //    residual add (12.3.7, the residual rows are fetched early), SwiGLU over
 //    interleaved gate/up rows (12.3.6), or argmax with packed (value, index)
@@ -40,6 +45,7 @@ constexpr int kThreads = kConsumers + 32;   // + producer warp
 constexpr size_t kOneShot = 100 * 1024;     // slices up to this size: one copy
 constexpr size_t kStageTarget = 36 * 1024;  // ring stage size otherwise
 constexpr int kRingStages = 3;
+constexpr size_t kPlanesMinSlice = 192 * 1024;   // digit-plane activations from this CTA slice size
 constexpr int kTilesPerPass = 4;            // tiles a warp reduces at once
 // shared-memory header: 4 full + 4 empty mbarriers, flags, argmax keys
 constexpr int kHeader = 256;
@@ -51,11 +57,15 @@ struct GemvPlan {
     int NG;           // 8-row groups
     int max_rows;     // rows of the largest CTA slice
     int resid_off;    // byte offset of the residual buffer (RESID mode)
+    int planes;       // 1: activations as digit planes (large slices)
     size_t stage_bytes;
     size_t smem;
 };
 
+// Activation row in shared memory, in floats: f32 padded (36 per 32 values),
+// or digit planes (3 bytes per value) then block scales (f32 per 32 values).
 __host__ __device__ inline int xs_floats_per_row(int K) { return (K / 32) * 36; }
+__host__ __device__ inline int xs_plane_floats_per_row(int K) { return ((K * 3 + K / 8) / 4 + 3) / 4 * 4; }
 
 __host__ __device__ inline size_t align128(size_t v) { return (v + 127) & ~static_cast<size_t>(127); }
 
@@ -77,7 +87,9 @@ GemvPlan make_plan(const QMat &W, int N, int K, int B, int mode) {
         p.S = kRingStages;
     }
     p.stage_bytes = static_cast<size_t>(p.sg) * tb;
-    size_t off = kHeader + align128(p.stage_bytes) * p.S + static_cast<size_t>(B) * xs_floats_per_row(K) * 4;
+    p.planes = slice >= kPlanesMinSlice ? 1 : 0;
+    const int xrow = p.planes ? xs_plane_floats_per_row(K) : xs_floats_per_row(K);
+    size_t off = kHeader + align128(p.stage_bytes) * p.S + static_cast<size_t>(B) * xrow * 4;
     off += align128(static_cast<size_t>(p.max_rows) * B * 4) + 128 /*norm scratch*/;
     p.resid_off = static_cast<int>(off);
     if (mode == GEMV_RESID) off += align128(static_cast<size_t>(p.max_rows) * B * 4);
@@ -151,7 +163,7 @@ __device__ __forceinline__ void consumers_sync() {
 // Largest number of float4 loads of one activation row per consumer thread.
 constexpr int kMaxXLoads = 12;   // K <= 12288
 
-template <int B, int MODE>
+template <int B, int MODE, bool PL>
 __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int K = a.K;
@@ -172,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
     unsigned long long *best = reinterpret_cast<unsigned long long *>(smem + 96);      // [4]
     uint8_t *ring = smem + kHeader;
     float *xs = reinterpret_cast<float *>(ring + slot * p.S);
-    const int xrow = xs_floats_per_row(K);
+    const int xrow = PL ? xs_plane_floats_per_row(K) : xs_floats_per_row(K);
     float *red = xs + B * xrow;                                    // [rows][B]
     float *nscr = red + align128(static_cast<size_t>(p.max_rows) * B * 4) / 4;  // [32]
     float *resid = reinterpret_cast<float *>(smem + p.resid_off);  // [rows][B] (RESID)
@@ -262,20 +274,62 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
                 t = warp_sum(t);
                 scale = 1.0f / sqrtf(t / static_cast<float>(K) + a.eps);
             }
-            float *xd = xs + b * xrow;
+            if constexpr (!PL) {
+                float *xd = xs + b * xrow;
 #pragma unroll
-            for (int i = 0; i < kMaxXLoads; ++i) {
-                const int k = (tid + i * kConsumers) * 4;
-                if (i < nld && k < K) {
-                    float4 u = v[i];
-                    if (a.norm_w) {
-                        const float4 w = *reinterpret_cast<const float4 *>(a.norm_w + k);
-                        u.x = u.x * scale * w.x;
-                        u.y = u.y * scale * w.y;
-                        u.z = u.z * scale * w.z;
-                        u.w = u.w * scale * w.w;
+                for (int i = 0; i < kMaxXLoads; ++i) {
+                    const int k = (tid + i * kConsumers) * 4;
+                    if (i < nld && k < K) {
+                        float4 u = v[i];
+                        if (a.norm_w) {
+                            const float4 w = *reinterpret_cast<const float4 *>(a.norm_w + k);
+                            u.x = u.x * scale * w.x;
+                            u.y = u.y * scale * w.y;
+                            u.z = u.z * scale * w.z;
+                            u.w = u.w * scale * w.w;
+                        }
+                        *reinterpret_cast<float4 *>(xd + (k >> 5) * 36 + (k & 31)) = u;
                     }
-                    *reinterpret_cast<float4 *>(xd + (k >> 5) * 36 + (k & 31)) = u;
+                }
+            } else {
+                // digit planes of the (normalised) row: 8 threads hold a 32-block
+                uint8_t *xd = reinterpret_cast<uint8_t *>(xs + b * xrow);
+                float *xsc = reinterpret_cast<float *>(xd + static_cast<size_t>(K) * 3);
+#pragma unroll
+                for (int i = 0; i < kMaxXLoads; ++i) {
+                    if (i < nld) {
+                        const int k = (tid + i * kConsumers) * 4;
+                        const bool act = k < K;
+                        float4 u = act ? v[i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        if (a.norm_w && act) {
+                            const float4 w = *reinterpret_cast<const float4 *>(a.norm_w + k);
+                            u.x = u.x * scale * w.x;
+                            u.y = u.y * scale * w.y;
+                            u.z = u.z * scale * w.z;
+                            u.w = u.w * scale * w.w;
+                        }
+                        float amax = fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w)));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+                        if (act) {
+                            const float sb = amax / 127.0f;
+                            int h[4] = {0, 0, 0, 0}, m[4] = {0, 0, 0, 0}, l[4] = {0, 0, 0, 0};
+                            if (sb > 0.0f) {
+                                const float inv = 1.0f / sb;
+                                digit_planes(u.x, inv, h[0], m[0], l[0]);
+                                digit_planes(u.y, inv, h[1], m[1], l[1]);
+                                digit_planes(u.z, inv, h[2], m[2], l[2]);
+                                digit_planes(u.w, inv, h[3], m[3], l[3]);
+                            }
+                            uint32_t *pw =
+                                reinterpret_cast<uint32_t *>(xd + static_cast<size_t>(k >> 4) * 48) + ((k & 15) >> 2);
+                            pw[0] = pack4_s8(h[0], h[1], h[2], h[3]);
+                            pw[4] = pack4_s8(m[0], m[1], m[2], m[3]);
+                            pw[8] = pack4_s8(l[0], l[1], l[2], l[3]);
+                            if ((k & 31) == 0) xsc[k >> 5] = sb;
+                        }
+                    }
                 }
             }
         }
@@ -328,10 +382,21 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
                         }
 #pragma unroll
                         for (int b = 0; b < B; ++b) {
-                            const X16 x = load_x16(xs + b * xrow + (kk >> 5) * 36 + (kk & 31));
+                            if constexpr (!PL) {
+                                const X16 x = load_x16(xs + b * xrow + (kk >> 5) * 36 + (kk & 31));
 #pragma unroll
-                            for (int j = 0; j < kTilesPerPass; ++j)
-                                if (j < np) acc[j][b] = fmaf(d[j], dot16(w[j], x), acc[j][b]);
+                                for (int j = 0; j < kTilesPerPass; ++j)
+                                    if (j < np) acc[j][b] = fmaf(d[j], dot16(w[j], x), acc[j][b]);
+                            } else {
+                                const uint8_t *xd = reinterpret_cast<const uint8_t *>(xs + b * xrow);
+                                uint4 Pq[3];
+#pragma unroll
+                                for (int q = 0; q < 3; ++q) Pq[q] = reinterpret_cast<const uint4 *>(xd)[(kk >> 4) * 3 + q];
+                                const float sx = reinterpret_cast<const float *>(xd + static_cast<size_t>(K) * 3)[kk >> 5];
+#pragma unroll
+                                for (int j = 0; j < kTilesPerPass; ++j)
+                                    if (j < np) acc[j][b] = fmaf(d[j] * sx, pdot16(w[j], Pq), acc[j][b]);
+                            }
                         }
                     } else {
 #pragma unroll
@@ -344,8 +409,19 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
                                     reinterpret_cast<const __half *>(tp + 8 * kt)[warp * (kt / 32) + (kk >> 5)]);
 #pragma unroll
                                 for (int b = 0; b < B; ++b) {
-                                    const X16 x = load_x16(xs + b * xrow + (kcol >> 5) * 36 + (kcol & 31));
-                                    acc[j][b] = fmaf(d, dot16(w, x), acc[j][b]);
+                                    if constexpr (!PL) {
+                                        const X16 x = load_x16(xs + b * xrow + (kcol >> 5) * 36 + (kcol & 31));
+                                        acc[j][b] = fmaf(d, dot16(w, x), acc[j][b]);
+                                    } else {
+                                        const uint8_t *xd = reinterpret_cast<const uint8_t *>(xs + b * xrow);
+                                        uint4 Pq[3];
+#pragma unroll
+                                        for (int q = 0; q < 3; ++q)
+                                            Pq[q] = reinterpret_cast<const uint4 *>(xd)[(kcol >> 4) * 3 + q];
+                                        const float sx =
+                                            reinterpret_cast<const float *>(xd + static_cast<size_t>(K) * 3)[kcol >> 5];
+                                        acc[j][b] = fmaf(d * sx, pdot16(w, Pq), acc[j][b]);
+                                    }
                                 }
                             }
                         }
@@ -480,23 +556,27 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
     if (tr) tr[4] = globaltimer_ns();
 }
 
-template <int B, int MODE>
+template <int B, int MODE, bool PL>
 cudaError_t configure_one() {
-    cudaError_t e = cudaFuncSetAttribute(k_gemv<B, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(k_gemv<B, MODE, PL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     // Same carveout for every decode kernel: an SM never has to drain to
     // reconfigure L1/shared memory between PDL-overlapped kernels.
-    return cudaFuncSetAttribute(k_gemv<B, MODE>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    return cudaFuncSetAttribute(k_gemv<B, MODE, PL>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                 cudaSharedmemCarveoutMaxShared);
 }
 
 template <int B>
 cudaError_t configure_b() {
     cudaError_t e;
-    if ((e = configure_one<B, GEMV_STORE>()) != cudaSuccess) return e;
-    if ((e = configure_one<B, GEMV_RESID>()) != cudaSuccess) return e;
-    if ((e = configure_one<B, GEMV_SWIGLU>()) != cudaSuccess) return e;
-    return configure_one<B, GEMV_ARGMAX>();
+    if ((e = configure_one<B, GEMV_STORE, false>()) != cudaSuccess) return e;
+    if ((e = configure_one<B, GEMV_RESID, false>()) != cudaSuccess) return e;
+    if ((e = configure_one<B, GEMV_SWIGLU, false>()) != cudaSuccess) return e;
+    if ((e = configure_one<B, GEMV_ARGMAX, false>()) != cudaSuccess) return e;
+    if ((e = configure_one<B, GEMV_STORE, true>()) != cudaSuccess) return e;
+    if ((e = configure_one<B, GEMV_RESID, true>()) != cudaSuccess) return e;
+    if ((e = configure_one<B, GEMV_SWIGLU, true>()) != cudaSuccess) return e;
+    return configure_one<B, GEMV_ARGMAX, true>();
 }
 
 template <int B, int MODE>
@@ -511,7 +591,8 @@ cudaError_t launch_one(const GemvArgs &a, const GemvPlan &p, bool pdl, cudaStrea
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_gemv<B, MODE>, a, p);
+    if (p.planes) return cudaLaunchKernelEx(&cfg, k_gemv<B, MODE, true>, a, p);
+    return cudaLaunchKernelEx(&cfg, k_gemv<B, MODE, false>, a, p);
 }
 
 template <int B>

@@ -132,7 +132,6 @@ struct qw3_model {
     // persistent batch-1 decode kernel (decode_mega.cu)
     bool mega = false;
     MegaParams mp{};
-    MegaLayer *d_mega_layers = nullptr;
     int mega_trace_records = 0;
     int32_t *d_first = nullptr;
 };
@@ -401,16 +400,18 @@ bool mega_layout(MegaParams &P, int max_seq_len) {
     };
     take(P.o_bar, 512);
     take(P.o_x, static_cast<size_t>(H) * 4);
-    take(P.o_xn, static_cast<size_t>(H) * 4);
+    take(P.o_xn, static_cast<size_t>(H) * 3 + static_cast<size_t>(H) / 32 * 4);
+    take(P.o_wbuf, static_cast<size_t>(H) * 4);
     take(P.o_qkvpub, static_cast<size_t>(P.RPC) * 4);
     take(P.o_qkv, static_cast<size_t>(P.RG) * 4);
     take(P.o_scores, static_cast<size_t>(G) * P.maxpos * 4);
     take(P.o_apub, static_cast<size_t>(G) * (hd + 4) * 4);
     take(P.o_vred, static_cast<size_t>(8) * G * hd * 4);
-    take(P.o_oall, static_cast<size_t>(G) * hd * 4);
+    take(P.o_oall, static_cast<size_t>(G) * hd * 3 + static_cast<size_t>(G) * hd / 32 * 4);
     take(P.o_guout, static_cast<size_t>(2) * apc_max * 4);
     take(P.o_actpub, static_cast<size_t>(apc_max) * 4);
-    take(P.o_act, static_cast<size_t>(kt_max) * 4);
+    P.o_act_cap = kt_max;
+    take(P.o_act, static_cast<size_t>(kt_max) * 3 + static_cast<size_t>(kt_max) / 32 * 4);
     take(P.o_red, 1024);
     P.o_ring = static_cast<uint32_t>(off);
     const size_t tbH = static_cast<size_t>(H) * 17 / 2;
@@ -424,11 +425,22 @@ bool mega_layout(MegaParams &P, int max_seq_len) {
 
 int setup_mega(qw3_model *m, const qw3_weights *w, bool on_dev, uint8_t *staging) {
     const qw3_config &c = m->cfg;
-    if (c.flags & QW3_FLAG_NO_MEGA) return QW3_OK;
+    if (!(c.flags & QW3_FLAG_PERSISTENT)) return QW3_OK;
     const int H = c.hidden, hd = c.head_dim, nh = c.n_heads, nkv = c.n_kv_heads, I = c.intermediate;
     const int G = nh / nkv, CS = kMegaCS;
     const int RG = (G + 2) * hd;
-    if (G > 7 || H > 4096 || H % (8 * CS) || RG % (8 * CS) || I % 32 || I / 32 < nkv) return QW3_OK;
+    if (!mega_supported_heads(hd, G) || H > 4096 || H % 256 || RG % (8 * CS) || RG > 8 * 256 || I % 32 || I / 32 < nkv) return QW3_OK;
+    // per-layer arrays must sit at one stride (they do: every layer has the same sizes)
+    for (int l = 1; l < c.n_layers; ++l) {
+        const LayerDev &a = m->layers[l - 1], &b = m->layers[l];
+        const ptrdiff_t st = m->layers[1].gu.base - m->layers[0].gu.base;
+        if (b.gu.base - a.gu.base != st ||
+            reinterpret_cast<const uint8_t *>(b.attn_norm) - reinterpret_cast<const uint8_t *>(a.attn_norm) != st ||
+            reinterpret_cast<const uint8_t *>(b.ffn_norm) - reinterpret_cast<const uint8_t *>(a.ffn_norm) != st ||
+            reinterpret_cast<const uint8_t *>(b.q_norm) - reinterpret_cast<const uint8_t *>(a.q_norm) != st ||
+            reinterpret_cast<const uint8_t *>(b.k_norm) - reinterpret_cast<const uint8_t *>(a.k_norm) != st)
+            return QW3_OK;
+    }
     MegaParams P{};
     P.L = c.n_layers; P.H = H; P.I = I; P.V = c.vocab; P.hd = hd; P.G = G;
     P.NA = nkv; P.CS = CS; P.RG = RG; P.RPC = RG / CS; P.ORPC = H / CS; P.o_groups = H / 8;
@@ -466,7 +478,6 @@ int setup_mega(qw3_model *m, const qw3_weights *w, bool on_dev, uint8_t *staging
     uint8_t *arena = nullptr;
     M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&arena), per_layer * c.n_layers));
     M_TRY(m, cudaMemsetAsync(arena, 0, per_layer * c.n_layers, m->stream));
-    std::vector<MegaLayer> hl(c.n_layers);
     const size_t qrow = static_cast<size_t>(H / 32) * 34;
     for (int l = 0; l < c.n_layers; ++l) {
         const qw3_layer_weights &lw = w->layers[l];
@@ -491,17 +502,18 @@ int setup_mega(qw3_model *m, const qw3_weights *w, bool on_dev, uint8_t *staging
         if (int rc = raw_on_device(m, lw.ffn_down, H, I, on_dev, staging, &raw)) return rc;
         M_TRY(m, launch_repack_colpart(raw, H, I, P.NC, down, m->stream));
         M_TRY(m, cudaStreamSynchronize(m->stream));
-        hl[l].qkv = qkv_m.base;
-        hl[l].o = o_m.base;
-        hl[l].gu = L.gu.base;
-        hl[l].down = down;
-        hl[l].attn_norm = L.attn_norm;
-        hl[l].q_norm = L.q_norm;
-        hl[l].k_norm = L.k_norm;
-        hl[l].ffn_norm = L.ffn_norm;
+        (void)L;
     }
-    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&m->d_mega_layers), sizeof(MegaLayer) * c.n_layers));
-    M_TRY(m, cudaMemcpy(m->d_mega_layers, hl.data(), sizeof(MegaLayer) * c.n_layers, cudaMemcpyHostToDevice));
+    P.qkv0 = arena;
+    P.o0 = arena + b_qkv;
+    P.down0 = arena + b_qkv + b_o;
+    P.mstride = per_layer;
+    P.gu0 = m->layers[0].gu.base;
+    P.attn_norm0 = m->layers[0].attn_norm;
+    P.q_norm0 = m->layers[0].q_norm;
+    P.k_norm0 = m->layers[0].k_norm;
+    P.ffn_norm0 = m->layers[0].ffn_norm;
+    P.wstride = c.n_layers > 1 ? static_cast<size_t>(m->layers[1].gu.base - m->layers[0].gu.base) : 0;
     M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&P.opart), static_cast<size_t>(P.NA) * H * 4));
     M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&P.dpart), static_cast<size_t>(P.NC) * H * 4));
     M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&P.gctr), 256));
@@ -512,7 +524,6 @@ int setup_mega(qw3_model *m, const qw3_weights *w, bool on_dev, uint8_t *staging
         M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&P.trace), tb));
         M_TRY(m, cudaMemsetAsync(P.trace, 0, tb, m->stream));
     }
-    P.layers = m->d_mega_layers;
     P.embd = m->embd;
     P.out = m->out;
     P.out_norm = m->out_norm;

@@ -303,5 +303,49 @@ __device__ __forceinline__ void record_status(int32_t *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
+// ---- activation digit planes (decode GEMVs)
+//
+// A GEMV input vector enters the decode GEMVs as three int8 digit planes per
+// 32-value block: x = s * (h + m / 254 + l / 254^2) with s = max|x| / 127 and
+// |h|, |m|, |l| <= 127, which represents x to within s / (2 * 254^2), about
+// 6e-8 of the block's largest value (the size of an f32 rounding). The dot
+// of 16 int8 codes with 16 such values is then 12 exact int8 dot products
+// (dp4a) and one f32 combination. Layout: plane q of values [16c, 16c + 16)
+// is the uint4 at planes[3c + q]; s of values [32b, 32b + 32) is scales[b].
+
+// Digit planes of v (|v| <= 127 s), packed one byte per value.
+__device__ __forceinline__ void digit_planes(float v, float inv_s, int &h, int &m, int &l) {
+    const float t = v * inv_s;
+    const float th = rintf(t);
+    const float r1 = (t - th) * 254.0f;
+    const float tm = rintf(r1);
+    const float r2 = (r1 - tm) * 254.0f;
+    h = static_cast<int>(fminf(fmaxf(th, -127.0f), 127.0f));
+    m = static_cast<int>(fminf(fmaxf(tm, -127.0f), 127.0f));
+    l = static_cast<int>(fminf(fmaxf(rintf(r2), -127.0f), 127.0f));
+}
+
+__device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
+    return (static_cast<uint32_t>(a) & 0xffu) | ((static_cast<uint32_t>(b) & 0xffu) << 8) |
+           ((static_cast<uint32_t>(c) & 0xffu) << 16) | ((static_cast<uint32_t>(d) & 0xffu) << 24);
+}
+
+// sum over 16 codes w of q * (h + m / 254 + l / 254^2), planes P[0..2]
+__device__ __forceinline__ float pdot16(const uint4 w, const uint4 *P) {
+    int a = __dp4a(static_cast<int>(w.x), static_cast<int>(P[0].x), 0);
+    a = __dp4a(static_cast<int>(w.y), static_cast<int>(P[0].y), a);
+    a = __dp4a(static_cast<int>(w.z), static_cast<int>(P[0].z), a);
+    a = __dp4a(static_cast<int>(w.w), static_cast<int>(P[0].w), a);
+    int b = __dp4a(static_cast<int>(w.x), static_cast<int>(P[1].x), 0);
+    b = __dp4a(static_cast<int>(w.y), static_cast<int>(P[1].y), b);
+    b = __dp4a(static_cast<int>(w.z), static_cast<int>(P[1].z), b);
+    b = __dp4a(static_cast<int>(w.w), static_cast<int>(P[1].w), b);
+    int c = __dp4a(static_cast<int>(w.x), static_cast<int>(P[2].x), 0);
+    c = __dp4a(static_cast<int>(w.y), static_cast<int>(P[2].y), c);
+    c = __dp4a(static_cast<int>(w.z), static_cast<int>(P[2].z), c);
+    c = __dp4a(static_cast<int>(w.w), static_cast<int>(P[2].w), c);
+    return fmaf(static_cast<float>(c), 1.0f / 64516.0f, fmaf(static_cast<float>(b), 1.0f / 254.0f, static_cast<float>(a)));
+}
+
 }  // namespace qw3
 #endif

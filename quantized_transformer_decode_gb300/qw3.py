@@ -31,7 +31,7 @@ QW3_ERR_TIMEOUT = 8
 QW3_FLAG_NO_GRAPH = 0x1
 QW3_FLAG_NO_PDL = 0x2
 QW3_FLAG_TRACE = 0x4
-QW3_FLAG_NO_MEGA = 0x8
+QW3_FLAG_PERSISTENT = 0x8
 
 # Every entry point of include/qw3.h, in declaration order.
 EXPORTS = (

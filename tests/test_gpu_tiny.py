@@ -70,26 +70,44 @@ def test_tiny_greedy_and_logits(torch):
     gm.close()
 
 
-@pytest.mark.parametrize("flags", [0x8, 0x8 | 0x1, 0x8 | 0x2, 0x8 | 0x3])
+PERSISTENT = 0x8
+
+
+@pytest.mark.parametrize("flags", [0x1, 0x2, 0x3])
 def test_tiny_per_kernel_launch_modes(torch, flags):
-    """The per-kernel decode path (captured graph, direct launches, with and
-    without programmatic dependent launch) against the oracle."""
+    """The per-kernel decode path with direct launches, with and without
+    programmatic dependent launch, against the oracle."""
     w = inputs.WORKLOADS["tiny"]
     _, gm, _ = run_greedy_case(torch, w.shape, w.seed, w.prompt_len, 6, flags=flags)
     assert gm.decode_plan(1)[0] is False
     gm.close()
 
 
-def test_persistent_kernel_is_the_batch1_path(torch):
+def test_decode_plans(torch):
     w = inputs.WORKLOADS["tiny"]
     _, gm = build_pair(w.shape, w.seed, max_seq_len=64, max_prefill=32)
+    assert gm.decode_plan(1) == (False, 2 + 5 * w.shape.n_layers)
+    gm.close()
+    _, gm = build_pair(w.shape, w.seed, max_seq_len=64, max_prefill=32, flags=PERSISTENT)
     assert gm.decode_plan(1) == (True, 0)
     gm.close()
 
 
-def test_mid_long_context_multi_chunk_kv(torch):
-    """Positions per CTA above one ring slot of K/V rows (hd 128)."""
-    _, gm, _ = run_greedy_case(torch, MID, 6, prompt_len=460, steps=5, max_prefill=256)
+@pytest.mark.parametrize("case", ["tiny", "mid", "mid_long", "untied"])
+def test_persistent_kernel_greedy_and_logits(torch, case):
+    """The persistent batch-1 kernel against the oracle (ids bit-exact,
+    teacher-forced logits); mid_long puts more positions per CTA than one
+    ring slot of K/V rows holds."""
+    if case == "tiny":
+        w = inputs.WORKLOADS["tiny"]
+        _, gm, _ = run_greedy_case(torch, w.shape, w.seed, w.prompt_len, w.decode_steps, flags=PERSISTENT)
+    elif case == "mid":
+        _, gm, _ = run_greedy_case(torch, MID, 4, prompt_len=70, steps=12, max_prefill=32, flags=PERSISTENT)
+    elif case == "mid_long":
+        _, gm, _ = run_greedy_case(torch, MID, 6, prompt_len=460, steps=5, max_prefill=256, flags=PERSISTENT)
+    else:
+        _, gm, _ = run_greedy_case(torch, MID_UNTIED, 5, prompt_len=40, steps=6, flags=PERSISTENT)
+    assert gm.decode_plan(1)[0] is True
     gm.close()
 
 
@@ -98,7 +116,7 @@ def test_paths_agree_bitwise_on_ids(torch):
     shape = MID
     prompt = inputs.prompt_tokens(shape, 4, 40)
     outs = []
-    for flags in (0, 0x8):
+    for flags in (0, PERSISTENT):
         _, gm = build_pair(shape, 4, max_seq_len=64, max_prefill=64, flags=flags)
         _, am = gm.prefill(0, cuda_ints(prompt), want_logits=False)
         lg, am2 = gm.decode(am, [40])
@@ -269,7 +287,7 @@ def test_truncate_then_redecode_is_reproducible(torch):
 
 def test_trace_records_every_kernel(torch):
     shape = inputs.TINY
-    _, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=32, flags=0x4 | 0x8)
+    _, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=32, flags=0x4)
     assert gm.decode_plan(1)[0] is False
     gm.prefill(0, cuda_ints(inputs.prompt_tokens(shape, 0, 8)), want_logits=False)
     gm.decode(cuda_ints([3]), [8])
@@ -284,7 +302,7 @@ def test_trace_records_every_kernel(torch):
 
 def test_persistent_kernel_trace(torch):
     shape = inputs.TINY
-    _, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=32, flags=0x4)
+    _, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=32, flags=0x4 | PERSISTENT)
     assert gm.decode_plan(1)[0] is True
     _, am = gm.prefill(0, cuda_ints(inputs.prompt_tokens(shape, 0, 8)), want_logits=False)
     gm.generate_greedy(am, 3)
