@@ -315,3 +315,24 @@ def test_persistent_kernel_trace(torch):
     totals = tr[2 * (2 * L + 1):]
     assert totals.shape[0] >= 16 and np.all(totals[:, 5] >= totals[:, 4])
     gm.close()
+
+
+@pytest.mark.parametrize("n", [1, 2, 7, 15])
+def test_create_failure_cleans_up(torch, n, monkeypatch):
+    """A failed device allocation during qw3_create returns QW3_ERR_OOM and
+    frees what was allocated (QW3_FAULT_ALLOC_AT makes the n-th one fail);
+    the next create succeeds."""
+    from quantized_transformer_decode_gb300.qw3 import Qw3Error, QW3_ERR_OOM
+    shape = inputs.TINY
+    monkeypatch.setenv("QW3_FAULT_ALLOC_AT", str(n))
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        with pytest.raises(Qw3Error) as e:
+            build_pair(shape, 0, max_seq_len=64, max_prefill=32)
+        assert e.value.status == QW3_ERR_OOM
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    assert torch.cuda.mem_get_info()[0] >= free0 - (64 << 20)
+    monkeypatch.delenv("QW3_FAULT_ALLOC_AT")
+    _, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=32)
+    gm.close()
