@@ -66,6 +66,7 @@ cudaError_t configure_all() {
         if (e == cudaSuccess) e = configure_attention();
         if (e == cudaSuccess) e = configure_misc();
         if (e == cudaSuccess) e = configure_mega();
+        if (e == cudaSuccess) e = configure_gemm_tc();
         g_cfg_err = e;
     });
     return g_cfg_err;
@@ -303,7 +304,7 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
             M_TRY(m, launch_gemv(a, GEMV_STORE, pdl, s));
         } else {
             M_TRY(m, launch_rmsnorm_rows(m->x, B, H, L.attn_norm, c.rms_eps, m->h, s));
-            M_TRY(m, launch_gemm(m->h, B, H, L.qkv, m->qkv, GEMV_STORE, nullptr, nullptr, s));
+            M_TRY(m, launch_gemm(m->h, B, H, L.qkv, m->qkv, GEMV_STORE, nullptr, nullptr, s, m->d_status));
         }
         AttnDecodeArgs at{};
         at.qkv = m->qkv; at.qkv_stride = m->qkv_w; at.q_norm = L.q_norm; at.k_norm = L.k_norm; at.eps = c.rms_eps;
@@ -331,10 +332,10 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
             dn.trace = tr();
             M_TRY(m, launch_gemv(dn, GEMV_RESID, pdl, s));
         } else {
-            M_TRY(m, launch_gemm(m->o, B, qw, L.o, m->x, GEMV_RESID, nullptr, nullptr, s));
+            M_TRY(m, launch_gemm(m->o, B, qw, L.o, m->x, GEMV_RESID, nullptr, nullptr, s, m->d_status));
             M_TRY(m, launch_rmsnorm_rows(m->x, B, H, L.ffn_norm, c.rms_eps, m->h, s));
-            M_TRY(m, launch_gemm(m->h, B, H, L.gu, m->act, GEMV_SWIGLU, nullptr, nullptr, s));
-            M_TRY(m, launch_gemm(m->act, B, I, L.down, m->x, GEMV_RESID, nullptr, nullptr, s));
+            M_TRY(m, launch_gemm(m->h, B, H, L.gu, m->act, GEMV_SWIGLU, nullptr, nullptr, s, m->d_status));
+            M_TRY(m, launch_gemm(m->act, B, I, L.down, m->x, GEMV_RESID, nullptr, nullptr, s, m->d_status));
         }
     }
     if (gv) {
@@ -347,7 +348,7 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
         M_TRY(m, launch_gemv(a, GEMV_ARGMAX, pdl, s));
     } else {
         M_TRY(m, launch_rmsnorm_rows(m->x, B, H, m->out_norm, c.rms_eps, m->h, s));
-        M_TRY(m, launch_gemm(m->h, B, H, m->out, nullptr, GEMV_ARGMAX, m->argmax_key, m->d_io, s));
+        M_TRY(m, launch_gemm(m->h, B, H, m->out, nullptr, GEMV_ARGMAX, m->argmax_key, m->d_io, s, m->d_status));
         M_TRY(m, launch_argmax_finalize(m->argmax_key, B, m->d_io, m->d_tok, m->d_step, m->d_pos, m->d_status, s));
     }
     return QW3_OK;
@@ -806,16 +807,16 @@ int qw3_prefill(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n,
             const LayerDev &L = m->layers[l];
             float *kvl = m->kv + static_cast<size_t>(l) * m->layer_stride;
             M_TRY(m, launch_rmsnorm_rows(m->px, M, H, L.attn_norm, c.rms_eps, m->ph, s));
-            M_TRY(m, launch_gemm(m->ph, M, H, L.qkv, m->pqkv, GEMV_STORE, nullptr, nullptr, s));
+            M_TRY(m, launch_gemm(m->ph, M, H, L.qkv, m->pqkv, GEMV_STORE, nullptr, nullptr, s, m->d_status));
             M_TRY(m, launch_qk_rope_append(m->pqkv, M, m->qkv_w, L.q_norm, L.k_norm, c.rms_eps, m->rope, nullptr, seq,
                                            nullptr, pos0, kvl, m->seq_stride, m->kvsel_stride, m->head_stride, nh,
                                            nkv, hd, s));
             M_TRY(m, launch_attn_prefill(m->pqkv, M, m->qkv_w, kvl, 0, static_cast<size_t>(seq) * m->seq_stride,
                                          m->kvsel_stride, m->head_stride, pos0, nh, nkv, hd, scale, m->po, s));
-            M_TRY(m, launch_gemm(m->po, M, qw, L.o, m->px, GEMV_RESID, nullptr, nullptr, s));
+            M_TRY(m, launch_gemm(m->po, M, qw, L.o, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status));
             M_TRY(m, launch_rmsnorm_rows(m->px, M, H, L.ffn_norm, c.rms_eps, m->ph, s));
-            M_TRY(m, launch_gemm(m->ph, M, H, L.gu, m->pact, GEMV_SWIGLU, nullptr, nullptr, s));
-            M_TRY(m, launch_gemm(m->pact, M, I, L.down, m->px, GEMV_RESID, nullptr, nullptr, s));
+            M_TRY(m, launch_gemm(m->ph, M, H, L.gu, m->pact, GEMV_SWIGLU, nullptr, nullptr, s, m->d_status));
+            M_TRY(m, launch_gemm(m->pact, M, I, L.down, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status));
         }
         if (off + M == n && (last_logits_dev || argmax_dev)) {
             GemvArgs a{};

@@ -158,8 +158,16 @@ cudaError_t launch_embed(const int32_t *tokens, int n, const QMat &E, float *x, 
 // prefill / batched path
 cudaError_t launch_rmsnorm_rows(const float *x, int M, int K, const float *w, float eps, float *y,
                                 cudaStream_t s);
+// Dense contraction C[M][N] = A[M][K] . W[N][K]^T with the GEMV epilogue
+// modes; tensor cores (tcgen05) from kGemmTcMinRows rows, CUDA cores below.
 cudaError_t launch_gemm(const float *A, int M, int K, const QMat &W, float *C, int mode,
-                        unsigned long long *argmax_key, const DecodeIO *io, cudaStream_t s);
+                        unsigned long long *argmax_key, const DecodeIO *io, cudaStream_t s,
+                        int32_t *status = nullptr);
+constexpr int kGemmTcMinRows = 32;
+bool gemm_tc_supported(int M, int K, const QMat &W);
+cudaError_t configure_gemm_tc();
+cudaError_t launch_gemm_tc(const float *A, int M, int K, const QMat &W, float *C, int mode,
+                           unsigned long long *argmax_key, const DecodeIO *io, int32_t *status, cudaStream_t s);
 cudaError_t launch_qk_rope_append(float *qkv, int M, int qkv_stride, const float *q_norm,
                                   const float *k_norm, float eps, const float2 *rope,
                                   const int32_t *row_seq, int seq0, const int32_t *row_pos, int pos0,
