@@ -132,9 +132,11 @@ __global__ void __launch_bounds__(256) k_gemm(const float *__restrict__ A, int M
 }  // namespace
 
 cudaError_t launch_gemm(const float *A, int M, int K, const QMat &W, float *C, int mode,
-                        unsigned long long *argmax_key, const DecodeIO *io, cudaStream_t s, int32_t *status) {
+                        unsigned long long *argmax_key, const DecodeIO *io, cudaStream_t s, int32_t *status,
+                        uint8_t *apack) {
     if (M <= 0) return cudaSuccess;
-    if (gemm_tc_supported(M, K, W)) return launch_gemm_tc(A, M, K, W, C, mode, argmax_key, io, status, s);
+    if (apack && gemm_tc_supported(M, K, W))
+        return launch_gemm_tc(A, M, K, W, C, mode, argmax_key, io, status, apack, s);
     dim3 grid((W.rows + BN - 1) / BN, (M + BM - 1) / BM);
     switch (mode) {
         case GEMV_STORE: k_gemm<GEMV_STORE><<<grid, 256, 0, s>>>(A, M, K, W, W.rows, W.rows_pad, C, nullptr, nullptr); break;
@@ -154,26 +156,29 @@ cudaError_t launch_gemm(const float *A, int M, int K, const QMat &W, float *C, i
 // activations are f32, so both operands are split into bf16 pairs, a = ah + al
 // and w = wh + wl (w = d * q formed exactly in f32 first), and each 16-deep
 // step issues three MMAs, ah.wh + ah.wl + al.wh, accumulated in f32 in tensor
-// memory; the dropped al.wl term and the split residues are ~2^-17 of each
-// product, the size of f32 rounding.
+// memory; the dropped al.wl term and the split residues are ~2^-16 of each
+// product.
 //
-// CTA tile 128 (activation rows, TMEM lanes) x 128 (weight rows, TMEM
-// columns), K steps of 64. Two shared-memory stages of four 128 x 64 bf16
-// operands (A hi/lo, W hi/lo) in the no-swizzle K-major core-matrix layout:
-// element (r, k) at (r / 8) * 1024 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2.
-// All 256 threads build the next stage (loads, dequantisation, splits) while
-// the tensor core consumes the current one; thread 0 issues the 12 MMAs of a
-// step and commits them to the stage's mbarrier, which frees the stage. The
-// epilogue reads the accumulator from tensor memory (32x32b loads: warp w
-// reads TMEM lanes 32 (w % 4).., columns half (w / 4)).
+// Operands are packed once into "UMMA tiles": 128 rows x 64 K of bf16 in the
+// no-swizzle K-major core-matrix layout (element (r, k) at (r / 8) * 1024 +
+// (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2, 16 KB), hi then lo (32 KB), tile
+// (row tile t, K step s) at ((t * K / 64 + s) * 32 KB). Weights are packed at
+// model creation from the repacked Q8_0 tiles (4 bytes per weight); each GEMM
+// input is packed by k_pack_act. The GEMM then streams 64 KB per K step (A and
+// W, hi and lo) with two 1-D bulk copies into a 3-stage ring; one thread
+// issues the 12 MMAs of a step and commits them to the stage's "empty"
+// barrier. CTA tile 128 x 128, accumulator in 128 TMEM columns; the epilogue
+// (store / residual / SwiGLU pairs / argmax keys) reads it with 32x32b loads.
 // ===========================================================================
 namespace {
 
 constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 64;
-constexpr int TC_THREADS = 256;
-constexpr uint32_t TC_OPERAND = TC_BM * TC_BK * 2;          // 16 KB per bf16 operand
-constexpr uint32_t TC_STAGE = 4 * TC_OPERAND;               // A hi, A lo, W hi, W lo
-constexpr uint32_t TC_SMEM = 2 * TC_STAGE + 2048;           // + barriers, alignment slack
+constexpr int TC_THREADS = 128;
+constexpr uint32_t TC_OPERAND = 128 * TC_BK * 2;            // 16 KB: one bf16 operand tile
+constexpr uint32_t TC_PAIR = 2 * TC_OPERAND;                // hi + lo
+constexpr uint32_t TC_STAGE = 2 * TC_PAIR;                  // A pair + W pair
+constexpr int TC_STAGES = 3;
+constexpr uint32_t TC_SMEM = TC_STAGES * TC_STAGE + 2048;   // + barriers, alignment slack
 
 __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
     // start >> 4; leading byte offset 128 (next 8-deep K core); stride byte
@@ -207,24 +212,80 @@ __device__ __forceinline__ void split8(const float *v, uint4 &hi, uint4 &lo) {
     lo = make_uint4(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]), pack_bf16(l[4], l[5]), pack_bf16(l[6], l[7]));
 }
 
-__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity) { return mbar_wait_bounded(bar, parity); }
+__device__ __forceinline__ size_t ut_tile(int t, int s, int ksteps) {
+    return (static_cast<size_t>(t) * ksteps + s) * TC_PAIR;
+}
+
+// One thread per (row, 8-column group): weights of a repacked Q8_0 matrix.
+__global__ void k_pack_w(const QMat W, int N, int K, uint8_t *__restrict__ dst) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int groups = K / 8;
+    const int rows = (N + TC_BM - 1) / TC_BM * TC_BM;
+    if (i >= static_cast<int64_t>(rows) * groups) return;
+    const int r = static_cast<int>(i / groups), k = static_cast<int>(i % groups) * 8;
+    float v[8];
+    if (r < N) {
+        const float d = __half2float(*qm_scale(W, r, k));
+        const int8_t *q = qm_codes(W, r, k);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = d * static_cast<float>(q[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+    }
+    uint4 hi, lo;
+    split8(v, hi, lo);
+    uint8_t *t = dst + ut_tile(r / TC_BM, k / TC_BK, K / TC_BK);
+    *reinterpret_cast<uint4 *>(t + core_off(r % TC_BM, k % TC_BK)) = hi;
+    *reinterpret_cast<uint4 *>(t + TC_OPERAND + core_off(r % TC_BM, k % TC_BK)) = lo;
+}
+
+// One thread per (row, 8-column group) of an f32 activation matrix.
+__global__ void k_pack_act(const float *__restrict__ A, int M, int K, uint8_t *__restrict__ dst) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int groups = K / 8;
+    const int rows = (M + TC_BM - 1) / TC_BM * TC_BM;
+    if (i >= static_cast<int64_t>(rows) * groups) return;
+    const int r = static_cast<int>(i / groups), k = static_cast<int>(i % groups) * 8;
+    float v[8];
+    if (r < M) {
+        const float4 a = *reinterpret_cast<const float4 *>(A + static_cast<size_t>(r) * K + k);
+        const float4 b = *reinterpret_cast<const float4 *>(A + static_cast<size_t>(r) * K + k + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+    }
+    uint4 hi, lo;
+    split8(v, hi, lo);
+    uint8_t *t = dst + ut_tile(r / TC_BM, k / TC_BK, K / TC_BK);
+    *reinterpret_cast<uint4 *>(t + core_off(r % TC_BM, k % TC_BK)) = hi;
+    *reinterpret_cast<uint4 *>(t + TC_OPERAND + core_off(r % TC_BM, k % TC_BK)) = lo;
+}
 
 template <int MODE>
-__global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const float *__restrict__ A, int M, int K, const QMat W,
-                                                           int N, float *C, unsigned long long *__restrict__ argmax_key,
+__global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__restrict__ Ap, int M, int K,
+                                                           const uint8_t *__restrict__ Wp, int N, float *C,
+                                                           unsigned long long *__restrict__ argmax_key,
                                                            const DecodeIO *io, int32_t *status) {
     extern __shared__ __align__(1024) uint8_t tc_smem[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_smem) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(base + 2 * TC_STAGE);   // [2]
-    uint32_t *tbase = reinterpret_cast<uint32_t *>(base + 2 * TC_STAGE + 64);
-    int *err = reinterpret_cast<int *>(base + 2 * TC_STAGE + 128);
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + TC_STAGES * TC_STAGE);   // [3]
+    uint64_t *empty = full + TC_STAGES;                                             // [3]
+    uint64_t *done = empty + TC_STAGES;                                             // [1]
+    uint32_t *tbase = reinterpret_cast<uint32_t *>(done + 1);
+    volatile int *err = reinterpret_cast<volatile int *>(tbase + 1);
     if (MODE == GEMV_ARGMAX && io) C = io->logits;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int m0 = blockIdx.y * TC_BM, n0 = blockIdx.x * TC_BN;
+    const int mt = blockIdx.y, nt = blockIdx.x;
+    const int ksteps = K / TC_BK;
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int i = 0; i < TC_STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(done, 1);
         *err = 0;
         fence_mbar_init();
     }
@@ -238,72 +299,42 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const float *__restri
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tbase;
 
-    // staging roles: thread t fills row t / 2, columns (t % 2) * 32 .. + 32 of
-    // the 128 x 64 A tile and of the 128 x 64 W tile
-    const int sr = tid >> 1, sh = (tid & 1) * 32;
-    const int am = m0 + sr, wn = n0 + sr;
-    const int nsteps = K / TC_BK;
-    for (int ks = 0; ks < nsteps; ++ks) {
-        const int st = ks & 1;
-        uint8_t *sb = base + st * TC_STAGE;
-        if (ks >= 2 && !*err && !tc_wait(&bars[st], static_cast<uint32_t>(((ks - 2) >> 1) & 1))) {
-            *err = 1;
-            record_status(status, QW3_ERR_TIMEOUT);
+    if (warp == 0 && lane == 0) {
+        // producer: A tile pair and W tile pair of each K step
+        const uint64_t pol_a = 0, pol_w = 0;
+        (void)pol_a;
+        (void)pol_w;
+        for (int ks = 0; ks < ksteps; ++ks) {
+            const int st = ks % TC_STAGES;
+            if (ks >= TC_STAGES && !mbar_wait_bounded(&empty[st], static_cast<uint32_t>(((ks / TC_STAGES) - 1) & 1))) {
+                *err = 1;
+                record_status(status, QW3_ERR_TIMEOUT);
+                break;
+            }
+            if (*err) break;
+            uint8_t *sb = base + st * TC_STAGE;
+            mbar_arrive_expect_tx(&full[st], TC_STAGE);
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                         ::"r"(smem_u32(sb)), "l"(Ap + ut_tile(mt, ks, ksteps)), "r"(TC_PAIR), "r"(smem_u32(&full[st]))
+                         : "memory");
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                         ::"r"(smem_u32(sb + TC_PAIR)), "l"(Wp + ut_tile(nt, ks, ksteps)), "r"(TC_PAIR),
+                           "r"(smem_u32(&full[st]))
+                         : "memory");
         }
-        const int k0 = ks * TC_BK + sh;
-        // activations
-        {
-            float v[32];
-            if (am < M) {
-                const float4 *src = reinterpret_cast<const float4 *>(A + static_cast<size_t>(am) * K + k0);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 t = src[i];
-                    v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer
+        int issued = 0;
+        for (int ks = 0; ks < ksteps; ++ks) {
+            const int st = ks % TC_STAGES;
+            if (!mbar_wait_bounded(&full[st], static_cast<uint32_t>((ks / TC_STAGES) & 1)) || *err) {
+                *err = 1;
+                record_status(status, QW3_ERR_TIMEOUT);
+                break;
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint4 hi, lo;
-                split8(v + 8 * j, hi, lo);
-                *reinterpret_cast<uint4 *>(sb + core_off(sr, sh + 8 * j)) = hi;
-                *reinterpret_cast<uint4 *>(sb + TC_OPERAND + core_off(sr, sh + 8 * j)) = lo;
-            }
-        }
-        // weights: one Q8_0 block of row wn, dequantised exactly, split
-        {
-            float v[32];
-            if (wn < W.rows_pad) {
-                const uint4 *q = reinterpret_cast<const uint4 *>(qm_codes(W, wn, k0));
-                const float d = __half2float(*qm_scale(W, wn, k0));
-                const uint4 c0 = q[0], c1 = q[1];
-                const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-#pragma unroll
-                    for (int b = 0; b < 4; ++b)
-                        v[4 * i + b] = d * static_cast<float>(static_cast<int8_t>((w[i] >> (8 * b)) & 0xffu));
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint4 hi, lo;
-                split8(v + 8 * j, hi, lo);
-                *reinterpret_cast<uint4 *>(sb + 2 * TC_OPERAND + core_off(sr, sh + 8 * j)) = hi;
-                *reinterpret_cast<uint4 *>(sb + 3 * TC_OPERAND + core_off(sr, sh + 8 * j)) = lo;
-            }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor core reads
-        __syncthreads();
-        if (tid == 0 && !*err) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t a_hi = smem_u32(sb), a_lo = a_hi + TC_OPERAND;
-            const uint32_t w_hi = a_hi + 2 * TC_OPERAND, w_lo = a_hi + 3 * TC_OPERAND;
+            const uint32_t a_hi = smem_u32(base + st * TC_STAGE), a_lo = a_hi + TC_OPERAND;
+            const uint32_t w_hi = a_hi + TC_PAIR, w_lo = w_hi + TC_OPERAND;
 #pragma unroll
             for (int sub = 0; sub < TC_BK / 16; ++sub) {
                 const uint32_t off = sub * 256;   // two 8-deep K cores per 16-deep step
@@ -318,29 +349,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const float *__restri
                     : "memory");
             }
             asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                             smem_u32(&bars[st]))
+                             smem_u32(&empty[st]))
                          : "memory");
+            ++issued;
         }
+        // completion of everything issued (commit tracks all prior MMAs)
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(done))
+                     : "memory");
+        (void)issued;
     }
-    // the last commit covers every MMA issued before it
-    if (nsteps > 0 && !*err) {
-        const int last = nsteps - 1;
-        if (!tc_wait(&bars[last & 1], static_cast<uint32_t>((last >> 1) & 1))) {
-            *err = 1;
-            record_status(status, QW3_ERR_TIMEOUT);
-        }
+    __syncwarp();
+    // all threads: wait for the accumulator (or give up after 1 s), then the
+    // producer's copies must have landed before the CTA may exit
+    if (!mbar_wait_bounded(done, 0u)) {
+        *err = 1;
+        record_status(status, QW3_ERR_TIMEOUT);
     }
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     __syncthreads();
+    if (tid == 0 && *err) {
+        // drain copies that may still be in flight (bounded)
+        for (int ks = ksteps > TC_STAGES ? ksteps - TC_STAGES : 0; ks < ksteps; ++ks)
+            (void)mbar_wait_bounded(&full[ks % TC_STAGES], static_cast<uint32_t>((ks / TC_STAGES) & 1));
+    }
 
-    // ---- epilogue: row m0 + 32 (warp % 4) + lane, columns half (warp / 4)
-    const int row = 32 * (warp & 3) + lane;
-    const int m = m0 + row;
-    const int cbase = (warp >> 2) * (TC_BN / 2);
+    // ---- epilogue: thread (warp, lane) owns row 32 warp + lane, all 128 columns
+    const int row = 32 * warp + lane;
+    const int m = mt * TC_BM + row;
     unsigned long long best = 0ull;
-    for (int c0 = 0; c0 < TC_BN / 2; c0 += 16) {
+    for (int c0 = 0; c0 < TC_BN; c0 += 16) {
         uint32_t r[16];
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + static_cast<uint32_t>(cbase + c0);
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * warp) << 16) + static_cast<uint32_t>(c0);
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
             "tcgen05.wait::ld.sync.aligned;"
@@ -349,7 +388,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const float *__restri
             : "r"(taddr)
             : "memory");
         if (m >= M || *err) continue;
-        const int nb = n0 + cbase + c0;
+        const int nb = nt * TC_BN + c0;
         if (MODE == GEMV_SWIGLU) {
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
@@ -385,10 +424,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const float *__restri
 }
 
 template <int MODE>
-cudaError_t launch_tc_mode(const float *A, int M, int K, const QMat &W, float *C, unsigned long long *argmax_key,
-                           const DecodeIO *io, int32_t *status, cudaStream_t s) {
-    const dim3 grid((W.rows + TC_BN - 1) / TC_BN, (M + TC_BM - 1) / TC_BM);
-    k_gemm_tc<MODE><<<grid, TC_THREADS, TC_SMEM, s>>>(A, M, K, W, W.rows, C, argmax_key, io, status);
+cudaError_t launch_tc_mode(const uint8_t *Ap, int M, int K, const uint8_t *Wp, int N, float *C,
+                           unsigned long long *argmax_key, const DecodeIO *io, int32_t *status, cudaStream_t s) {
+    const dim3 grid((N + TC_BN - 1) / TC_BN, (M + TC_BM - 1) / TC_BM);
+    k_gemm_tc<MODE><<<grid, TC_THREADS, TC_SMEM, s>>>(Ap, M, K, Wp, N, C, argmax_key, io, status);
     return cudaGetLastError();
 }
 
@@ -402,18 +441,37 @@ cudaError_t configure_gemm_tc() {
     return e;
 }
 
+size_t ut_bytes(int rows, int K) {
+    return static_cast<size_t>((rows + TC_BM - 1) / TC_BM) * TC_BM * static_cast<size_t>(K) * 4;
+}
+
 bool gemm_tc_supported(int M, int K, const QMat &W) {
-    return M >= kGemmTcMinRows && K % TC_BK == 0 && W.kt % TC_BK == 0 && W.cols == K;
+    return W.ut != nullptr && M >= kGemmTcMinRows && K % TC_BK == 0 && W.cols == K;
+}
+
+cudaError_t launch_pack_w(const QMat &W, uint8_t *dst, cudaStream_t s) {
+    const int rows = (W.rows + TC_BM - 1) / TC_BM * TC_BM;
+    const int64_t n = static_cast<int64_t>(rows) * (W.cols / 8);
+    k_pack_w<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(W, W.rows, W.cols, dst);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_tc(const float *A, int M, int K, const QMat &W, float *C, int mode,
-                           unsigned long long *argmax_key, const DecodeIO *io, int32_t *status, cudaStream_t s) {
+                           unsigned long long *argmax_key, const DecodeIO *io, int32_t *status, uint8_t *apack,
+                           cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
+    {
+        const int rows = (M + TC_BM - 1) / TC_BM * TC_BM;
+        const int64_t n = static_cast<int64_t>(rows) * (K / 8);
+        k_pack_act<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(A, M, K, apack);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     switch (mode) {
-        case GEMV_STORE: return launch_tc_mode<GEMV_STORE>(A, M, K, W, C, argmax_key, io, status, s);
-        case GEMV_RESID: return launch_tc_mode<GEMV_RESID>(A, M, K, W, C, argmax_key, io, status, s);
-        case GEMV_SWIGLU: return launch_tc_mode<GEMV_SWIGLU>(A, M, K, W, C, argmax_key, io, status, s);
-        case GEMV_ARGMAX: return launch_tc_mode<GEMV_ARGMAX>(A, M, K, W, C, argmax_key, io, status, s);
+        case GEMV_STORE: return launch_tc_mode<GEMV_STORE>(apack, M, K, W.ut, W.rows, C, argmax_key, io, status, s);
+        case GEMV_RESID: return launch_tc_mode<GEMV_RESID>(apack, M, K, W.ut, W.rows, C, argmax_key, io, status, s);
+        case GEMV_SWIGLU: return launch_tc_mode<GEMV_SWIGLU>(apack, M, K, W.ut, W.rows, C, argmax_key, io, status, s);
+        case GEMV_ARGMAX: return launch_tc_mode<GEMV_ARGMAX>(apack, M, K, W.ut, W.rows, C, argmax_key, io, status, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -123,6 +123,7 @@ struct qw3_model {
 
     // prefill scratch
     float *px = nullptr, *ph = nullptr, *pqkv = nullptr, *po = nullptr, *pact = nullptr;
+    uint8_t *apack = nullptr;   // tensor-core GEMM input, packed (nullptr: CUDA-core GEMM only)
 
     std::map<int, cudaGraphExec_t> graphs;
 
@@ -304,7 +305,7 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
             M_TRY(m, launch_gemv(a, GEMV_STORE, pdl, s));
         } else {
             M_TRY(m, launch_rmsnorm_rows(m->x, B, H, L.attn_norm, c.rms_eps, m->h, s));
-            M_TRY(m, launch_gemm(m->h, B, H, L.qkv, m->qkv, GEMV_STORE, nullptr, nullptr, s, m->d_status));
+            M_TRY(m, launch_gemm(m->h, B, H, L.qkv, m->qkv, GEMV_STORE, nullptr, nullptr, s, m->d_status, m->apack));
         }
         AttnDecodeArgs at{};
         at.qkv = m->qkv; at.qkv_stride = m->qkv_w; at.q_norm = L.q_norm; at.k_norm = L.k_norm; at.eps = c.rms_eps;
@@ -332,10 +333,10 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
             dn.trace = tr();
             M_TRY(m, launch_gemv(dn, GEMV_RESID, pdl, s));
         } else {
-            M_TRY(m, launch_gemm(m->o, B, qw, L.o, m->x, GEMV_RESID, nullptr, nullptr, s, m->d_status));
+            M_TRY(m, launch_gemm(m->o, B, qw, L.o, m->x, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack));
             M_TRY(m, launch_rmsnorm_rows(m->x, B, H, L.ffn_norm, c.rms_eps, m->h, s));
-            M_TRY(m, launch_gemm(m->h, B, H, L.gu, m->act, GEMV_SWIGLU, nullptr, nullptr, s, m->d_status));
-            M_TRY(m, launch_gemm(m->act, B, I, L.down, m->x, GEMV_RESID, nullptr, nullptr, s, m->d_status));
+            M_TRY(m, launch_gemm(m->h, B, H, L.gu, m->act, GEMV_SWIGLU, nullptr, nullptr, s, m->d_status, m->apack));
+            M_TRY(m, launch_gemm(m->act, B, I, L.down, m->x, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack));
         }
     }
     if (gv) {
@@ -348,7 +349,7 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
         M_TRY(m, launch_gemv(a, GEMV_ARGMAX, pdl, s));
     } else {
         M_TRY(m, launch_rmsnorm_rows(m->x, B, H, m->out_norm, c.rms_eps, m->h, s));
-        M_TRY(m, launch_gemm(m->h, B, H, m->out, nullptr, GEMV_ARGMAX, m->argmax_key, m->d_io, s, m->d_status));
+        M_TRY(m, launch_gemm(m->h, B, H, m->out, nullptr, GEMV_ARGMAX, m->argmax_key, m->d_io, s, m->d_status, m->apack));
         M_TRY(m, launch_argmax_finalize(m->argmax_key, B, m->d_io, m->d_tok, m->d_step, m->d_pos, m->d_status, s));
     }
     return QW3_OK;
@@ -376,6 +377,41 @@ int run_decode_step(qw3_model *m, int B) {
         it = m->graphs.emplace(B, ex).first;
     }
     M_TRY(m, cudaGraphLaunch(it->second, m->stream));
+    return QW3_OK;
+}
+
+// ---- tensor-core GEMM (prefill, batches from kGemmTcMinRows rows): every
+// layer matrix (and the lm_head when batches that large are possible) gets a
+// copy as bf16 hi/lo tensor-core tiles, 4 bytes per weight.
+int setup_tensor_core_gemm(qw3_model *m) {
+    const qw3_config &c = m->cfg;
+    const bool prefill_tc = c.max_prefill >= kGemmTcMinRows;
+    const bool batch_tc = c.max_seqs >= kGemmTcMinRows;
+    if (!prefill_tc && !batch_tc) return QW3_OK;
+    const int H = c.hidden, qw = c.n_heads * c.head_dim, I = c.intermediate;
+    if (H % 64 || qw % 64 || I % 64) return QW3_OK;
+    auto pack = [&](QMat &q) -> int {
+        uint8_t *p = nullptr;
+        M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&p), ut_bytes(q.rows, q.cols)));
+        M_TRY(m, launch_pack_w(q, p, m->stream));
+        q.ut = p;
+        return QW3_OK;
+    };
+    for (int l = 0; l < c.n_layers; ++l) {
+        LayerDev &L = m->layers[l];
+        if (int rc = pack(L.qkv)) return rc;
+        if (int rc = pack(L.o)) return rc;
+        if (int rc = pack(L.gu)) return rc;
+        if (int rc = pack(L.down)) return rc;
+    }
+    if (batch_tc) {
+        if (int rc = pack(m->out)) return rc;
+        if (c.tied_lm_head) m->embd.ut = m->out.ut;
+    }
+    const int rows = std::max(c.max_prefill, c.max_seqs);
+    const int kmax = std::max(H, std::max(qw, I));
+    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&m->apack), ut_bytes(rows, kmax)));
+    M_TRY(m, cudaStreamSynchronize(m->stream));
     return QW3_OK;
 }
 
@@ -763,6 +799,7 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->po), P * qw * 4);
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->pact), P * I * 4);
     if (e != cudaSuccess) return bail(cuda_err(m, e, "scratch allocation"));
+    if (int rc = setup_tensor_core_gemm(m)) return bail(rc);
     if (int rc = setup_mega(m, w, on_dev, staging)) return bail(rc);
     e = cudaMemsetAsync(m->counters, 0, static_cast<size_t>(Bm) * nkv * 4, m->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->done_counter, 0, 64, m->stream);
@@ -807,16 +844,16 @@ int qw3_prefill(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n,
             const LayerDev &L = m->layers[l];
             float *kvl = m->kv + static_cast<size_t>(l) * m->layer_stride;
             M_TRY(m, launch_rmsnorm_rows(m->px, M, H, L.attn_norm, c.rms_eps, m->ph, s));
-            M_TRY(m, launch_gemm(m->ph, M, H, L.qkv, m->pqkv, GEMV_STORE, nullptr, nullptr, s, m->d_status));
+            M_TRY(m, launch_gemm(m->ph, M, H, L.qkv, m->pqkv, GEMV_STORE, nullptr, nullptr, s, m->d_status, m->apack));
             M_TRY(m, launch_qk_rope_append(m->pqkv, M, m->qkv_w, L.q_norm, L.k_norm, c.rms_eps, m->rope, nullptr, seq,
                                            nullptr, pos0, kvl, m->seq_stride, m->kvsel_stride, m->head_stride, nh,
                                            nkv, hd, s));
             M_TRY(m, launch_attn_prefill(m->pqkv, M, m->qkv_w, kvl, 0, static_cast<size_t>(seq) * m->seq_stride,
                                          m->kvsel_stride, m->head_stride, pos0, nh, nkv, hd, scale, m->po, s));
-            M_TRY(m, launch_gemm(m->po, M, qw, L.o, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status));
+            M_TRY(m, launch_gemm(m->po, M, qw, L.o, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack));
             M_TRY(m, launch_rmsnorm_rows(m->px, M, H, L.ffn_norm, c.rms_eps, m->ph, s));
-            M_TRY(m, launch_gemm(m->ph, M, H, L.gu, m->pact, GEMV_SWIGLU, nullptr, nullptr, s, m->d_status));
-            M_TRY(m, launch_gemm(m->pact, M, I, L.down, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status));
+            M_TRY(m, launch_gemm(m->ph, M, H, L.gu, m->pact, GEMV_SWIGLU, nullptr, nullptr, s, m->d_status, m->apack));
+            M_TRY(m, launch_gemm(m->pact, M, I, L.down, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack));
         }
         if (off + M == n && (last_logits_dev || argmax_dev)) {
             GemvArgs a{};

@@ -29,6 +29,7 @@ struct QMat {
     int cols = 0;
     int kt = 0;           // tile width: divides cols, multiple of 32
     int ktile_major = 0;  // 0: row-group-major, 1: k-tile-major
+    uint8_t *ut = nullptr;  // nullable: the same weights as bf16 hi/lo tensor-core tiles
 };
 
 constexpr int kRowAlign = 16;
@@ -160,14 +161,19 @@ cudaError_t launch_rmsnorm_rows(const float *x, int M, int K, const float *w, fl
                                 cudaStream_t s);
 // Dense contraction C[M][N] = A[M][K] . W[N][K]^T with the GEMV epilogue
 // modes; tensor cores (tcgen05) from kGemmTcMinRows rows, CUDA cores below.
+// apack: scratch for the packed activations (ut_bytes(M, K)); nullptr keeps
+// the CUDA-core path.
 cudaError_t launch_gemm(const float *A, int M, int K, const QMat &W, float *C, int mode,
                         unsigned long long *argmax_key, const DecodeIO *io, cudaStream_t s,
-                        int32_t *status = nullptr);
+                        int32_t *status = nullptr, uint8_t *apack = nullptr);
 constexpr int kGemmTcMinRows = 32;
 bool gemm_tc_supported(int M, int K, const QMat &W);
+size_t ut_bytes(int rows, int K);   // bytes of a matrix packed into bf16 hi/lo UMMA tiles
 cudaError_t configure_gemm_tc();
+cudaError_t launch_pack_w(const QMat &W, uint8_t *dst, cudaStream_t s);
 cudaError_t launch_gemm_tc(const float *A, int M, int K, const QMat &W, float *C, int mode,
-                           unsigned long long *argmax_key, const DecodeIO *io, int32_t *status, cudaStream_t s);
+                           unsigned long long *argmax_key, const DecodeIO *io, int32_t *status, uint8_t *apack,
+                           cudaStream_t s);
 cudaError_t launch_qk_rope_append(float *qkv, int M, int qkv_stride, const float *q_norm,
                                   const float *k_norm, float eps, const float2 *rope,
                                   const int32_t *row_seq, int seq0, const int32_t *row_pos, int pos0,
