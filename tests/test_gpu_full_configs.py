@@ -1,0 +1,154 @@
+"""GPU parity at the full sizes of the prefill, batched-decode and 8B
+workloads, through the C ABI, in the launch configuration the benchmark uses.
+
+Where the oracle cannot finish the full workload (it is a plain f64 numpy
+statement of the model), the check uses outputs it can compute one by one
+(sampled sequences of the batch, layer-0 K/V rows, which depend on their own
+token only) and properties that hold at any size (a decode step after a
+prefill equals the last row of the prefill that includes its token).
+"""
+import numpy as np
+import pytest
+
+from oracle import qw3_oracle as orc
+from quantized_transformer_decode_gb300 import inputs
+from parity import assert_logits_close, cuda_ints
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_transformer_decode_gb300 import build
+    build.build()
+    return t
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def test_prefill_4096_last_row(torch):
+    """0.6B shape, one 4096-token prompt (tensor-core GEMMs): last-row logits
+    and argmax against the oracle, and sampled KV rows of two layers."""
+    from quantized_transformer_decode_gb300.qw3 import Qw3Model
+    w = inputs.WORKLOADS["qwen3-0.6b-prefill4096"]
+    S = w.prompt_len
+    om = orc.OracleModel.from_f32(w.shape, inputs.generate_weights(w.shape, w.seed))
+    cache = om.new_cache(S)
+    prompt = inputs.prompt_tokens(w.shape, w.seed, S)
+    want = om.forward(cache, prompt, 0)
+    with Qw3Model.from_f32(w.shape, inputs.iter_weights(w.shape, w.seed), max_seq_len=S + 1, max_prefill=S) as gm:
+        lg, am = gm.prefill(0, cuda_ints(prompt))
+        gm.sync()
+        assert_logits_close(_np(lg), want, "prefill 4096 last row")
+        assert int(_np(am)[0]) == orc.argmax_lowest(want)
+        pos = np.array([0, 1, 777, 2048, S - 1])
+        for layer in (0, w.shape.n_layers - 1):
+            k, v = gm.read_kv(layer, 0, 0, S)
+            k, v = _np(k), _np(v)
+            assert_logits_close(k[pos], cache.k[layer, pos], f"K layer {layer}")
+            assert_logits_close(v[pos], cache.v[layer, pos], f"V layer {layer}")
+
+
+def test_batch64_decode_sampled_sequences(torch):
+    """0.6B shape, 64 sequences with their own 2048-token prefixes, decoded
+    together (tensor-core GEMMs at 64 rows, batched attention): three
+    sampled sequences against the oracle run per sequence, 3 steps."""
+    from quantized_transformer_decode_gb300.qw3 import Qw3Model
+    w = inputs.WORKLOADS["qwen3-0.6b-batch64"]
+    B, P, steps = w.batch, w.prompt_len, 3
+    sample = (0, 37, 63)
+    om = orc.OracleModel.from_f32(w.shape, inputs.generate_weights(w.shape, w.seed))
+    with Qw3Model.from_f32(w.shape, inputs.iter_weights(w.shape, w.seed), max_seqs=B, max_seq_len=P + steps + 1,
+                           max_prefill=P) as gm:
+        firsts = []
+        for b in range(B):
+            _, am = gm.prefill(b, cuda_ints(inputs.batch_prefix_tokens(w.shape, w.seed, b, P)), want_logits=False)
+            firsts.append(am)
+        import torch as t
+        toks = t.cat(firsts)
+        caches = {}
+        for b in sample:
+            c = om.new_cache(P + steps + 1)
+            lg = om.forward(c, inputs.batch_prefix_tokens(w.shape, w.seed, b, P), 0)
+            caches[b] = c
+            assert int(_np(toks)[b]) == orc.argmax_lowest(lg), f"prefill argmax of sequence {b}"
+        for s in range(steps):
+            lg, am = gm.decode(toks, [P + s] * B)
+            lgn, amn = _np(lg), _np(am)
+            for b in sample:
+                want = om.forward(caches[b], [int(_np(toks)[b])], P + s)
+                assert_logits_close(lgn[b], want, f"sequence {b} step {s}")
+                assert int(amn[b]) == orc.argmax_lowest(want)
+            toks = am
+        gm.sync()
+
+
+QWEN3_8B_2L = inputs.QWEN3_8B.with_layers(2)
+
+
+def test_8b_geometry_two_layers(torch):
+    """Every kernel at the 8B widths (hidden 4096, 32/8 heads, intermediate
+    12288, untied lm_head) against the oracle on a 2-layer model: prefill
+    (tensor cores), teacher-forced decode, greedy ids."""
+    from quantized_transformer_decode_gb300.qw3 import Qw3Model
+    shape, seed, P, steps = QWEN3_8B_2L, 2, 96, 6
+    om = orc.OracleModel.from_f32(shape, inputs.generate_weights(shape, seed))
+    prompt = inputs.prompt_tokens(shape, seed, P)
+    ids, logits = om.generate_greedy(om.new_cache(P + steps + 1), prompt, steps)
+    with Qw3Model.from_f32(shape, inputs.iter_weights(shape, seed), max_seq_len=P + steps + 1, max_prefill=64) as gm:
+        lg, am = gm.prefill(0, cuda_ints(prompt))
+        assert_logits_close(_np(lg), logits[0], "8B-geometry prefill")
+        assert int(_np(am)[0]) == ids[0]
+        for s in range(steps):
+            lg, am = gm.decode(cuda_ints([ids[s]]), [P + s])
+            assert_logits_close(_np(lg)[0], logits[s + 1], f"8B-geometry step {s + 1}")
+            assert int(_np(am)[0]) == ids[s + 1]
+        gm.reset(0)
+        _, am = gm.prefill(0, cuda_ints(prompt), want_logits=False)
+        out = gm.generate_greedy(am, steps)
+        gm.sync()
+        assert [int(_np(am)[0])] + [int(v) for v in _np(out)[:, 0]] == ids
+
+
+def test_8b_full_size_properties(torch):
+    """Qwen3-8B shape at full size (36 layers, 8.7 GB of Q8_0 weights, an
+    8192-token prompt): layer-0 K/V rows at sampled positions against the
+    oracle's layer 0 for those tokens, and the cached == uncached property
+    (course 12.4): decoding token t after the 8192-token prefill gives the
+    logits of the last row of an 8193-token prefill."""
+    from quantized_transformer_decode_gb300.qw3 import Qw3Model
+    w = inputs.WORKLOADS["qwen3-8b"]
+    s, P = w.shape, w.prompt_len
+    prompt = inputs.prompt_tokens(s, w.seed, P + 1)
+    with Qw3Model.from_f32(s, inputs.iter_weights(s, w.seed), max_seqs=2, max_seq_len=P + 2, max_prefill=4096) as gm:
+        _, am = gm.prefill(0, cuda_ints(prompt[:P]), want_logits=False)
+        lg_dec, am_dec = gm.decode(cuda_ints(prompt[P:P + 1]), [P], seqs=[0])
+        lg_full, am_full = gm.prefill(1, cuda_ints(prompt))
+        gm.sync()
+        assert_logits_close(_np(lg_dec)[0], _np(lg_full), "decode after prefill vs longer prefill")
+        assert int(_np(am_dec)[0]) == int(_np(am_full)[0])
+        k, v = gm.read_kv(0, 0, 0, P)
+        k, v = _np(k), _np(v)
+    # the oracle's layer 0 for single tokens at their own positions
+    w0 = {}
+    for name, kind, arr in inputs.iter_weights(s, w.seed):
+        if name in ("token_embd", "blk.0.attn_norm", "blk.0.attn_k", "blk.0.attn_v", "blk.0.attn_k_norm"):
+            w0[name] = orc.q8_0_quantize(arr) if kind == "linear" else np.asarray(arr, np.float32)
+        if name.startswith("blk.1."):
+            break
+    emb = orc.QLinear(w0["token_embd"], s.vocab, s.hidden, keep_f64=False)
+    wk = orc.QLinear(w0["blk.0.attn_k"], s.kv_width, s.hidden, keep_f64=True)
+    wv = orc.QLinear(w0["blk.0.attn_v"], s.kv_width, s.hidden, keep_f64=True)
+    for p in (0, 1, 4095, P - 1):
+        x = emb.row(np.array([prompt[p]]))
+        h = orc.rms_norm(x, w0["blk.0.attn_norm"], s.rms_eps)
+        kk = orc.rms_norm(wk(h).reshape(1, s.n_kv_heads, s.head_dim), w0["blk.0.attn_k_norm"], s.rms_eps)
+        kk = orc.rope_neox(kk, [p], s.rope_theta)
+        vv = wv(h).reshape(1, s.n_kv_heads, s.head_dim)
+        assert_logits_close(k[p], kk[0], f"8B layer-0 K at {p}")
+        assert_logits_close(v[p], vv[0], f"8B layer-0 V at {p}")
