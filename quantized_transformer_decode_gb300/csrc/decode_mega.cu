@@ -83,8 +83,11 @@ __device__ __forceinline__ float dsmem_ld(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+// Relaxed remote arrive: the caller publishes its writes with one
+// fence.acq_rel.cluster before a series of these (a release per arrive would
+// pay a cluster-scope fence each time).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
@@ -334,7 +337,8 @@ struct Cons {
         mcons_sync();
         uint64_t *bar = S.clbar + (clround & 1u);
         if (tid == 0) {
-            for (int r = 0; r < P.CS; ++r) mbar_arrive_remote(dsmem_map(bar, static_cast<uint32_t>(r)));
+            asm volatile("fence.acq_rel.cluster;" ::: "memory");   // publishes the CTA's writes (ordered by the bar.sync)
+            for (int r = 0; r < P.CS; ++r) mbar_arrive_remote_relaxed(dsmem_map(bar, static_cast<uint32_t>(r)));
         }
         const uint32_t parity = (clround >> 1) & 1u;
         const uint64_t tw0 = (P.trace && tid == 0) ? globaltimer_ns() : 0;
@@ -429,8 +433,38 @@ struct Cons {
         for (int i = tid; i < P.H; i += kMegaConsumers) ss = fmaf(S.x[i], S.x[i], ss);
         asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's weights; block_sum syncs all
         const float r = 1.0f / sqrtf(block_sum(ss) / static_cast<float>(P.H) + P.eps);
-        for (int i = tid; i < P.H; i += kMegaConsumers) to_planes(S.x[i] * r * S.wbuf[i], i >> 5, S.xpl, S.xsc, lane);
+        for (int i0 = tid; i0 < P.H; i0 += 4 * kMegaConsumers) to_planes4(i0, r);
         mcons_sync();
+    }
+
+    // Digit planes of up to four normalised values per thread (elements i0,
+    // i0 + 256, ...): the four warp reductions run as independent chains.
+    __device__ void to_planes4(int i0, float r) {
+        float v[4], am[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kMegaConsumers;
+            v[u] = (i < P.H) ? S.x[i] * r * S.wbuf[i] : 0.0f;
+            am[u] = fabsf(v[u]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) am[u] = fmaxf(am[u], __shfl_xor_sync(0xffffffffu, am[u], o));
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kMegaConsumers;
+            if (i < P.H) {
+                const float sb = am[u] / 127.0f;
+                int h = 0, m = 0, l = 0;
+                if (sb > 0.0f) digit_planes(v[u], 1.0f / sb, h, m, l);
+                uint8_t *dst = S.xpl + static_cast<size_t>((i >> 5) * 2 + (lane >> 4)) * 48 + (lane & 15);
+                dst[0] = static_cast<uint8_t>(static_cast<int8_t>(h));
+                dst[16] = static_cast<uint8_t>(static_cast<int8_t>(m));
+                dst[32] = static_cast<uint8_t>(static_cast<int8_t>(l));
+                if (lane == 0) S.xsc[i >> 5] = sb;
+            }
+        }
     }
 
     // One chunk of tiles (8 rows x kt): warp w takes row w of each tile, four
