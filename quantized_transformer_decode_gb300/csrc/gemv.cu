@@ -313,20 +313,17 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
                         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
                         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
                         if (act) {
-                            const float sb = amax / 127.0f;
-                            int h[4] = {0, 0, 0, 0}, m[4] = {0, 0, 0, 0}, l[4] = {0, 0, 0, 0};
+                            const float sb = amax * (1.0f / 127.0f);
+                            uint32_t ph = 0, pm = 0, pl = 0;
                             if (sb > 0.0f) {
-                                const float inv = 1.0f / sb;
-                                digit_planes(u.x, inv, h[0], m[0], l[0]);
-                                digit_planes(u.y, inv, h[1], m[1], l[1]);
-                                digit_planes(u.z, inv, h[2], m[2], l[2]);
-                                digit_planes(u.w, inv, h[3], m[3], l[3]);
+                                const float vv[4] = {u.x, u.y, u.z, u.w};
+                                digit_planes4(vv, __frcp_rn(sb), ph, pm, pl);
                             }
                             uint32_t *pw =
                                 reinterpret_cast<uint32_t *>(xd + static_cast<size_t>(k >> 4) * 48) + ((k & 15) >> 2);
-                            pw[0] = pack4_s8(h[0], h[1], h[2], h[3]);
-                            pw[4] = pack4_s8(m[0], m[1], m[2], m[3]);
-                            pw[8] = pack4_s8(l[0], l[1], l[2], l[3]);
+                            pw[0] = ph;
+                            pw[4] = pm;
+                            pw[8] = pl;
                             if ((k & 31) == 0) xsc[k >> 5] = sb;
                         }
                     }

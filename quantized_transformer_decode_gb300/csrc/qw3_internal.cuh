@@ -339,6 +339,33 @@ __device__ __forceinline__ void digit_planes(float v, float inv_s, int &h, int &
     l = static_cast<int>(fminf(fmaxf(rintf(r2), -127.0f), 127.0f));
 }
 
+// Digit planes of four values at once, packed one byte per value into the
+// three plane words (value j in byte j). inv_s = 1 / s with s >= max|v| / 127
+// (any such s: the digits represent v / s). Rounding to nearest by the 1.5 *
+// 2^23 shift, exact for |t| < 2^22; every digit lies in [-127, 127] because
+// |t| <= 127 (1 + 2^-23) and each residual is at most 0.5 * 254.
+__device__ __forceinline__ void digit_planes4(const float (&v)[4], float inv_s, uint32_t &ph, uint32_t &pm,
+                                              uint32_t &pl) {
+    constexpr float kShift = 12582912.0f;   // 1.5 * 2^23
+    uint32_t bh[4], bm[4], bl[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float t = v[j] * inv_s;
+        const float sh = __fadd_rn(t, kShift);
+        const float r1 = __fmul_rn(__fsub_rn(t, __fsub_rn(sh, kShift)), 254.0f);
+        const float sm = __fadd_rn(r1, kShift);
+        const float r2 = __fmul_rn(__fsub_rn(r1, __fsub_rn(sm, kShift)), 254.0f);
+        const float sl = __fadd_rn(r2, kShift);
+        bh[j] = __float_as_uint(sh);
+        bm[j] = __float_as_uint(sm);
+        bl[j] = __float_as_uint(sl);
+    }
+    // the low byte of each shifted float is the digit in two's complement
+    ph = __byte_perm(__byte_perm(bh[0], bh[1], 0x0040), __byte_perm(bh[2], bh[3], 0x0040), 0x5410);
+    pm = __byte_perm(__byte_perm(bm[0], bm[1], 0x0040), __byte_perm(bm[2], bm[3], 0x0040), 0x5410);
+    pl = __byte_perm(__byte_perm(bl[0], bl[1], 0x0040), __byte_perm(bl[2], bl[3], 0x0040), 0x5410);
+}
+
 __device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
     return (static_cast<uint32_t>(a) & 0xffu) | ((static_cast<uint32_t>(b) & 0xffu) << 8) |
            ((static_cast<uint32_t>(c) & 0xffu) << 16) | ((static_cast<uint32_t>(d) & 0xffu) << 24);
