@@ -14,18 +14,25 @@
 // (TMA) issued before griddepcontrol.wait: they were written by earlier
 // steps. After the wait the CTA applies the per-head Q/K RMSNorm and RoPE to
 // the new q/k (minfer 2.2, course 12.3.4); the CTA whose range holds the new
-// position also appends k, v to the cache. Partial (max, sum, acc) per head
-// and split go to global memory; the last CTA of (b, g) to arrive merges
-// them (flash-decoding combine) and writes o.
+// position also appends k, v to the cache. The nsplit CTAs of one (g, b)
+// form a thread-block cluster: each keeps its partial (max, sum, acc) per
+// head in shared memory, and after one cluster barrier every CTA merges a
+// 1/nsplit share of the outputs from its peers' partials (flash-decoding
+// combine through distributed shared memory; no global round trip).
 #include "qw3_internal.cuh"
 
 namespace qw3 {
 
 namespace {
 
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 256;
+constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kTileP = 32;   // positions per staged tile
 constexpr int kStages = 2;
+
+// Splits of one (sequence, kv head) form one cluster; its leader holds a
+// partial row per split and head, which caps the cluster at 8 for G = 8.
+__host__ __device__ constexpr int attn_max_cluster(int G) { return G <= 4 ? 16 : 8; }
 
 // A partial row holds acc[HD], then m and l; padded to HD + 4 floats so every
 // row starts on a 16-byte boundary for the vector stores.
@@ -54,27 +61,38 @@ __device__ __forceinline__ void store_lane(float *dst, const float (&v)[HD / 32]
     }
 }
 
-// Per-head RMSNorm over head_dim then NeoX rotation at position p; the lane
-// holds dims [lane*E, lane*E+E), its rotation partner sits in lane ^ 16.
+// Preloaded operands of one per-head norm + RoPE: the lane's norm weights
+// and (cos, sin) pairs (neither depends on the previous kernel).
 template <int HD>
-__device__ __forceinline__ void norm_rope_lane(float (&v)[HD / 32], const float *w, float eps,
-                                               const float2 *rope_row, int lane) {
+struct NormRope {
+    float w[HD / 32];
+    float2 cs[HD / 32];
+};
+
+template <int HD>
+__device__ __forceinline__ void load_norm_rope(NormRope<HD> &nr, const float *w, const float2 *rope_row, int lane) {
+    constexpr int E = HD / 32;
+    load_lane<HD>(w, nr.w, lane);
+#pragma unroll
+    for (int e = 0; e < E; ++e) nr.cs[e] = rope_row[(lane & 15) * E + e];
+}
+
+// Per-head RMSNorm over head_dim then NeoX rotation, from preloaded operands.
+template <int HD>
+__device__ __forceinline__ void norm_rope_pre(float (&v)[HD / 32], const NormRope<HD> &nr, float eps, int lane) {
     constexpr int E = HD / 32;
     float ss = 0.0f;
 #pragma unroll
     for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
     ss = warp_sum(ss);
     const float r = 1.0f / sqrtf(ss / static_cast<float>(HD) + eps);
-    float wl[E];
-    load_lane<HD>(w, wl, lane);
 #pragma unroll
-    for (int e = 0; e < E; ++e) v[e] = v[e] * r * wl[e];
+    for (int e = 0; e < E; ++e) v[e] = v[e] * r * nr.w[e];
     const bool first_half = lane < 16;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         const float other = __shfl_xor_sync(0xffffffffu, v[e], 16);
-        const float2 cs = rope_row[(lane & 15) * E + e];
-        v[e] = first_half ? (v[e] * cs.x - other * cs.y) : (other * cs.y + v[e] * cs.x);
+        v[e] = first_half ? (v[e] * nr.cs[e].x - other * nr.cs[e].y) : (other * nr.cs[e].y + v[e] * nr.cs[e].x);
     }
 }
 
@@ -82,28 +100,36 @@ template <int HD, int G>
 __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, int nsplit) {
     constexpr int E = HD / 32;
     constexpr int PS = part_stride<HD>();
+    constexpr int CM = attn_max_cluster(G);
+    static_assert(kAttnWarps * G * PS <= 2 * kStages * kTileP * HD, "warp-merge rows must fit in the K/V tiles");
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);                 // [kStages] K/V tiles
+    uint64_t *rbar = bars + kStages;                                      // partials received (leader)
+    int *flags = reinterpret_cast<int *>(smem + 64);
     float *ktile = reinterpret_cast<float *>(smem + 128);               // [kStages][kTileP][HD]
     float *vtile = ktile + kStages * kTileP * HD;                         // [kStages][kTileP][HD]
     float *qn = vtile + kStages * kTileP * HD;                            // [G][HD]
     float *knew = qn + G * HD;                                            // [HD]
     float *vnew = knew + HD;                                              // [HD]
-    float *mrg = vnew + HD;                                               // [4][G][PS]
-    int *flags = reinterpret_cast<int *>(mrg + 4 * G * PS);
+    float *mrg = ktile;                     // [kAttnWarps][G][PS], in the K/V tiles once they are consumed
+    float *recv = vnew + HD;                                              // [CM][G][PS] split partials (leader)
+    float *wts = recv + CM * G * PS;                                      // [G][CM] merge weights (leader)
 
     const int g = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int C = nsplit;                        // the cluster spans the splits: rank == s
     unsigned long long *tr = (tid == 0) ? trace_slot(a.trace) : nullptr;
     if (tr) {
         tr[0] = globaltimer_ns();
         tr[5] = clock64();
         tr[7] = smid();
     }
+    // seq_ids and pos are step inputs: the embedding kernel at the head of the
+    // step waits for the previous step before it lets later kernels start.
     const int seq = a.seq_ids[b];
     const int p = a.pos[b];
     const int ctx = p + 1;
-    const int chunk = (ctx + nsplit - 1) / nsplit;
+    const int chunk = (ctx + C - 1) / C;
     const int start = s * chunk;
     const int end = min(ctx, start + chunk);
     const bool has_new = (start <= p) && (p < end);
@@ -115,9 +141,11 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) mbar_init(&bars[i], 1);
+        mbar_init(rbar, 1);
         fence_mbar_init();
         flags[0] = 0;
         flags[1] = 0;
+        flags[2] = 0;
     }
     __syncthreads();
     const uint64_t pol = policy_evict_first();
@@ -130,22 +158,31 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
             bulk_g2s(ktile + t * kTileP * HD, kbase + off, bytes, &bars[t], pol);
             bulk_g2s(vtile + t * kTileP * HD, vbase + off, bytes, &bars[t], pol);
         }
+        // the leader expects every peer's partial rows (acc, m, l per head)
+        if (s == 0) mbar_arrive_expect_tx(rbar, static_cast<uint32_t>((C - 1) * G * (HD * 4 + 8)));
     }
+    // norm weights and rotation of this warp's first head task, before the wait
+    const float2 *rope_row = a.rope + static_cast<size_t>(p) * (HD / 2);
+    NormRope<HD> nr;
+    if (warp <= G) load_norm_rope<HD>(nr, warp < G ? a.q_norm : a.k_norm, rope_row, lane);
+    // the leader's barrier is initialised and armed before any peer sends:
+    // arrive now, wait just before the push (long after every CTA arrived)
+    cluster_arrive_release();
     pdl_wait();
     if (tr) tr[1] = globaltimer_ns();
 
     // ---- new token: per-head norm + RoPE of q (and k), append k and v
-    const float2 *rope_row = a.rope + static_cast<size_t>(p) * (HD / 2);
     const float *qkv_b = a.qkv + static_cast<size_t>(b) * a.qkv_stride;
-    for (int t = warp; t < G + 2; t += kAttnThreads / 32) {
+    for (int t = warp; t < G + 2; t += kAttnWarps) {
+        if (t != warp && t <= G) load_norm_rope<HD>(nr, t < G ? a.q_norm : a.k_norm, rope_row, lane);
         float v[E];
         if (t < G) {
             load_lane<HD>(qkv_b + (g * G + t) * HD, v, lane);
-            norm_rope_lane<HD>(v, a.q_norm, a.eps, rope_row, lane);
+            norm_rope_pre<HD>(v, nr, a.eps, lane);
             store_lane<HD>(qn + t * HD, v, lane);
         } else if (has_new && t == G) {
             load_lane<HD>(qkv_b + a.nh * HD + g * HD, v, lane);
-            norm_rope_lane<HD>(v, a.k_norm, a.eps, rope_row, lane);
+            norm_rope_pre<HD>(v, nr, a.eps, lane);
             store_lane<HD>(knew, v, lane);
             store_lane<HD>(const_cast<float *>(kbase) + static_cast<size_t>(p) * HD, v, lane);
         } else if (has_new && t == G + 1) {
@@ -236,8 +273,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
         if (!ok) flags[0] = 1, flags[1] = t;
         if (ok) {
             const int rows = min(kTileP, n_cached - t * kTileP);
-            // warp w takes positions [w*NP, w*NP+NP), then every 4th batch
-            for (int j0 = warp * NP; j0 < rows; j0 += (kAttnThreads / 32) * NP)
+            // warp w takes positions [w*NP, w*NP+NP), then every kAttnWarps-th batch
+            for (int j0 = warp * NP; j0 < rows; j0 += kAttnWarps * NP)
                 consume(ktile + (si * kTileP + j0) * HD, vtile + (si * kTileP + j0) * HD, min(NP, rows - j0));
         }
         __syncthreads();
@@ -254,18 +291,30 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
         __syncthreads();
     }
     if (flags[0]) {
+        // A stage never completed: report, drain the copies that may still
+        // be in flight (bounded), and contribute an empty partial so that
+        // the leader's combine still completes.
         if (tid == 0) {
             record_status(a.status, QW3_ERR_TIMEOUT);
             const int first = flags[1];
             for (int t = first; t < ntiles && t < first + kStages; ++t)
                 (void)mbar_wait_bounded(&bars[t % kStages], static_cast<uint32_t>((t / kStages) & 1));
         }
-        return;
+#pragma unroll
+        for (int t = 0; t < G; ++t) {
+            m[t] = -INFINITY;
+            l[t] = 0.0f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[t][e] = 0.0f;
+        }
+    } else if (has_new && warp == kAttnWarps - 1) {
+        consume(knew, vnew, 1);
     }
-    if (has_new && warp == (kAttnThreads / 32) - 1) consume(knew, vnew, 1);
+    __syncthreads();   // no copy in flight and no warp reading the K/V tiles: they hold mrg next
     if (tr) tr[3] = globaltimer_ns();
 
-    // ---- merge the four warps, write this split's partial
+    // ---- merge the warps into this split's partial and push it to the
+    // leader (split 0): acc, then (m, l), into its slot s of recv
 #pragma unroll
     for (int t = 0; t < G; ++t) {
         float *mw = mrg + (warp * G + t) * PS;
@@ -276,14 +325,16 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
         }
     }
     __syncthreads();
-    for (int t = warp; t < G; t += kAttnThreads / 32) {
+    cluster_wait_acquire();
+    const uint32_t rbar_leader = dsmem_map(rbar, 0u);
+    for (int t = warp; t < G; t += kAttnWarps) {
         float M = -INFINITY;
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, mrg[(w * G + t) * PS + HD]);
+        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mrg[(w * G + t) * PS + HD]);
         float L = 0.0f, o[E];
 #pragma unroll
         for (int e = 0; e < E; ++e) o[e] = 0.0f;
         if (M != -INFINITY) {
-            for (int w = 0; w < 4; ++w) {
+            for (int w = 0; w < kAttnWarps; ++w) {
                 const float *mw = mrg + (w * G + t) * PS;
                 const float f = expf(mw[HD] - M);
                 L = fmaf(mw[HD + 1], f, L);
@@ -293,66 +344,67 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
                 for (int e = 0; e < E; ++e) o[e] = fmaf(aw[e], f, o[e]);
             }
         }
-        const int h = g * G + t;
-        float *pp = a.partial + ((static_cast<size_t>(b) * a.nh + h) * nsplit + s) * PS;
-        store_lane<HD>(pp, o, lane);
-        if (lane == 0) {
-            pp[HD] = M;
-            pp[HD + 1] = L;
+        float *slot = recv + (s * G + t) * PS;
+        if (s == 0) {
+            store_lane<HD>(slot, o, lane);
+            if (lane == 0) {
+                slot[HD] = M;
+                slot[HD + 1] = L;
+            }
+        } else {
+            const uint32_t dst = dsmem_map(slot, 0u);
+            if constexpr (E == 4) {
+                st_async_f32x4(dst + 16u * lane, o[0], o[1], o[2], o[3], rbar_leader);
+            } else {
+                st_async_f32x2(dst + 8u * lane, o[0], o[1], rbar_leader);
+            }
+            if (lane == 0) st_async_f32x2(dst + 4u * HD, M, L, rbar_leader);
         }
     }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const unsigned prev = atomicAdd(&a.counters[b * a.nkv + g], 1u);
-        flags[2] = (prev == static_cast<unsigned>(nsplit - 1)) ? 1 : 0;
+    if (s == 0) {
+        // ---- leader: flash-decoding combine of the C split partials
+        if (tid == 0 && !mbar_wait_bounded_cluster(rbar, 0u)) flags[2] = 1;
+        __syncthreads();
+        if (flags[2]) {
+            if (tid == 0) record_status(a.status, QW3_ERR_TIMEOUT);
+        } else {
+            if (warp < G) {
+                // warp t: lane j holds split j's (m, l) of head t
+                const int t = warp;
+                const float mj = lane < C ? recv[(lane * G + t) * PS + HD] : -INFINITY;
+                const float lj = lane < C ? recv[(lane * G + t) * PS + HD + 1] : 0.0f;
+                const float M = warp_max(mj);
+                const float f = (mj == -INFINITY) ? 0.0f : expf(mj - M);
+                const float L = warp_sum(lj * f);
+                if (lane < C) wts[t * CM + lane] = L > 0.0f ? f * (1.0f / L) : 0.0f;
+            }
+            __syncthreads();
+            float *ob = a.out + static_cast<size_t>(b) * a.nh * HD + static_cast<size_t>(g) * G * HD;
+            for (int o = tid; o < G * HD; o += kAttnThreads) {
+                const int t = o / HD, d = o - (o / HD) * HD;
+                float v[CM];
+#pragma unroll
+                for (int j = 0; j < CM; ++j) v[j] = j < C ? recv[(j * G + t) * PS + d] : 0.0f;
+                float sum = 0.0f;
+#pragma unroll
+                for (int j = 0; j < CM; ++j)
+                    if (j < C) sum = fmaf(wts[t * CM + j], v[j], sum);
+                ob[o] = sum;
+            }
+        }
     }
-    __syncthreads();
     if (tr) {
         tr[4] = globaltimer_ns();
         tr[6] = clock64();
     }
-    if (!flags[2]) return;
-    __threadfence();
-    // ---- last CTA of (b, g): merge the splits. The G heads' partials are
-    // contiguous ([h][split][PS]); pull them into the (now free) K/V tile
-    // buffer with one coalesced pass, then reduce from shared memory.
-    {
-        const float *src = a.partial + (static_cast<size_t>(b) * a.nh + g * G) * nsplit * PS;
-        const int nf = G * nsplit * PS;
-        float *stage = ktile;   // 2 * kStages * kTileP * HD floats available
-        for (int i = tid * 4; i < nf; i += kAttnThreads * 4)
-            *reinterpret_cast<float4 *>(stage + i) = __ldcg(reinterpret_cast<const float4 *>(src + i));
-        __syncthreads();
-        for (int t = warp; t < G; t += kAttnThreads / 32) {
-            const float *base = stage + t * nsplit * PS;
-            float M = -INFINITY;
-            for (int j = lane; j < nsplit; j += 32) M = fmaxf(M, base[j * PS + HD]);
-            M = warp_max(M);
-            float L = 0.0f, o[E];
-#pragma unroll
-            for (int e = 0; e < E; ++e) o[e] = 0.0f;
-            for (int j = 0; j < nsplit; ++j) {
-                const float mj = base[j * PS + HD];
-                if (mj == -INFINITY) continue;
-                const float f = expf(mj - M);
-                L = fmaf(base[j * PS + HD + 1], f, L);
-                float aw[E];
-                load_lane<HD>(base + j * PS, aw, lane);
-#pragma unroll
-                for (int e = 0; e < E; ++e) o[e] = fmaf(aw[e], f, o[e]);
-            }
-            const float inv = 1.0f / L;
-#pragma unroll
-            for (int e = 0; e < E; ++e) o[e] *= inv;
-            store_lane<HD>(a.out + static_cast<size_t>(b) * a.nh * HD + (g * G + t) * HD, o, lane);
-        }
-    }
-    if (tid == 0) a.counters[b * a.nkv + g] = 0u;
 }
 
 size_t attn_decode_smem(int HD, int G) {
-    return 128 + static_cast<size_t>(2 * kStages * kTileP * HD + G * HD + 2 * HD + 4 * G * (HD + 4)) * 4 + 16;
+    const int PS = HD + 4;
+    // the warp-merge rows reuse the K/V tiles (kAttnWarps * G * PS <= 2 * kStages * kTileP * HD)
+    const size_t floats = static_cast<size_t>(2) * kStages * kTileP * HD + static_cast<size_t>(G) * HD + 2 * HD +
+                          static_cast<size_t>(attn_max_cluster(G)) * G * PS + static_cast<size_t>(G) * attn_max_cluster(G);
+    return 128 + floats * 4;
 }
 
 template <int HD, int G>
@@ -360,8 +412,39 @@ cudaError_t configure_attn_t() {
     cudaError_t e = cudaFuncSetAttribute(k_attn_decode<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(attn_decode_smem(HD, G)));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_attn_decode<HD, G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(k_attn_decode<HD, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                 cudaSharedmemCarveoutMaxShared);
+}
+
+// Largest cluster (splits per kv head) of at most attn_max_cluster(G) CTAs
+// such that `units` clusters run at once on this device (one wave for batch
+// 1); else the largest that fits at all.
+template <int HD, int G>
+int max_cluster_t(int units) {
+    int fallback = 1;
+    for (int c = attn_max_cluster(G); c > 1; c /= 2) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(1, c, 1);
+        cfg.blockDim = dim3(kAttnThreads);
+        cfg.dynamicSmemBytes = attn_decode_smem(HD, G);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = static_cast<unsigned>(c);
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_attn_decode<HD, G>, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        if (n >= units) return c;
+        if (n >= 1 && fallback == 1) fallback = c;
+    }
+    return fallback;
 }
 
 template <int HD, int G>
@@ -372,11 +455,15 @@ cudaError_t launch_attn_t(const AttnDecodeArgs &a, int B, int nsplit, bool pdl, 
     cfg.blockDim = dim3(kAttnThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = static_cast<unsigned>(nsplit);
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, k_attn_decode<HD, G>, a, nsplit);
 }
 
@@ -512,11 +599,25 @@ cudaError_t launch_prefill_t(const float *qkv, int M, int qkv_stride, const floa
 
 }  // namespace
 
-int attn_decode_max_nsplit(int hd, int G) {
-    // the last CTA stages G * nsplit partial rows in its K/V tile buffer
-    const int cap = 2 * kStages * kTileP * hd;
-    const int n = cap / (G * (hd + 4));
-    return n < 1 ? 1 : (n > 64 ? 64 : n);
+int attn_decode_max_nsplit(int hd, int G, int units) {
+    if (hd == 128) {
+        switch (G) {
+            case 1: return max_cluster_t<128, 1>(units);
+            case 2: return max_cluster_t<128, 2>(units);
+            case 4: return max_cluster_t<128, 4>(units);
+            case 8: return max_cluster_t<128, 8>(units);
+            default: break;
+        }
+    } else if (hd == 64) {
+        switch (G) {
+            case 1: return max_cluster_t<64, 1>(units);
+            case 2: return max_cluster_t<64, 2>(units);
+            case 4: return max_cluster_t<64, 4>(units);
+            case 8: return max_cluster_t<64, 8>(units);
+            default: break;
+        }
+    }
+    return 8;
 }
 
 cudaError_t configure_attention() {
@@ -540,7 +641,7 @@ cudaError_t configure_attention() {
 
 cudaError_t launch_attn_decode(const AttnDecodeArgs &a, int B, int nsplit, bool pdl, cudaStream_t s) {
     const int G = a.nh / a.nkv;
-    if (nsplit < 1 || nsplit > attn_decode_max_nsplit(a.hd, G)) return cudaErrorInvalidValue;
+    if (nsplit < 1 || nsplit > attn_max_cluster(G)) return cudaErrorInvalidValue;
     if (a.hd == 128) {
         switch (G) {
             case 1: return launch_attn_t<128, 1>(a, B, nsplit, pdl, s);

@@ -55,32 +55,10 @@ constexpr int kMegaThreads = 288;     // + 1 producer warp
 
 __device__ __forceinline__ void mcons_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
 __device__ __forceinline__ uint32_t cluster_id_x() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
     return r;
-}
-
-__device__ __forceinline__ void hw_cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t dsmem_map(const void *local, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ float dsmem_ld(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-    return v;
 }
 
 // Relaxed remote arrive: the caller publishes its writes with one
@@ -88,16 +66,6 @@ __device__ __forceinline__ float dsmem_ld(uint32_t addr) {
 // pay a cluster-scope fence each time).
 __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t addr) {
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
-    return ok != 0;
 }
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {

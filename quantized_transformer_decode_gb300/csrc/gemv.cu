@@ -3,9 +3,11 @@
 // projection is a matrix-vector product and the weight stream is the cost).
 //
 // Design (GB300):
-//  * At most one CTA per SM; CTA c owns a contiguous run of 8-row groups. In
-//    the tiled weight layout (8 rows x kt columns per tile, codes then
-//    scales) that slice is one contiguous range.
+//  * Two CTAs per SM (one where the layout needs more than half the SM's
+//    shared memory): 18 warps per SM hide the dequantise-and-dot latency
+//    that 9 cannot. CTA c owns a contiguous run of 8-row groups; in the
+//    tiled weight layout (8 rows x kt columns per tile, codes then scales)
+//    that slice is one contiguous range.
 //  * The slice streams through shared memory in stages of whole tiles, one
 //    1-D bulk copy (TMA, cp.async.bulk, L2 evict-first) per stage. A bulk
 //    copy pays a fixed cost of a few hundred ns, so stages are large: a slice
@@ -46,6 +48,8 @@ constexpr size_t kOneShot = 100 * 1024;     // slices up to this size: one copy
 constexpr size_t kStageTarget = 36 * 1024;  // ring stage size otherwise
 constexpr int kRingStages = 3;
 constexpr size_t kPlanesMinSlice = 192 * 1024;   // digit-plane activations from this CTA slice size
+constexpr size_t kSmemMax = 227 * 1024;     // dynamic shared memory of one CTA
+constexpr size_t kSmemPair = 112 * 1024;    // per CTA when two share an SM (228 KB, 1 KB reserved each)
 constexpr int kTilesPerPass = 4;            // tiles a warp reduces at once
 // shared-memory header: 4 full + 4 empty mbarriers, flags, argmax keys
 constexpr int kHeader = 256;
@@ -69,32 +73,50 @@ __host__ __device__ inline int xs_plane_floats_per_row(int K) { return ((K * 3 +
 
 __host__ __device__ inline size_t align128(size_t v) { return (v + 127) & ~static_cast<size_t>(127); }
 
-GemvPlan make_plan(const QMat &W, int N, int K, int B, int mode) {
+// Plan for cps CTAs per SM: the slice of each CTA, one copy or a ring of
+// stages, and the shared-memory layout within budget bytes. smem = 0 when the
+// layout does not fit.
+GemvPlan plan_for(const QMat &W, int N, int K, int B, int mode, int cps, size_t budget) {
     GemvPlan p{};
     p.NG = (N + 7) / 8;
-    p.G = p.NG < num_sms() ? p.NG : num_sms();
+    p.G = p.NG < cps * num_sms() ? p.NG : cps * num_sms();
     const int max_groups = (p.NG + p.G - 1) / p.G;
     p.max_rows = max_groups * 8;
     const size_t tb = qm_tile_bytes(W.kt);
     const int ntk = K / W.kt;
     const size_t slice = static_cast<size_t>(max_groups) * ntk * tb;
-    if (slice <= kOneShot) {
+    p.planes = slice >= kPlanesMinSlice ? 1 : 0;
+    const int xrow = p.planes ? xs_plane_floats_per_row(K) : xs_floats_per_row(K);
+    size_t fixed = kHeader + static_cast<size_t>(B) * xrow * 4 + align128(static_cast<size_t>(p.max_rows) * B * 4) + 128;
+    if (mode == GEMV_RESID) fixed += align128(static_cast<size_t>(p.max_rows) * B * 4);
+    if (fixed >= budget) return p;
+    const size_t avail = budget - fixed;
+    if (slice <= kOneShot && align128(slice) <= avail) {
         p.sg = max_groups * ntk;
         p.S = 1;
     } else {
-        p.sg = static_cast<int>(kStageTarget / tb);
-        if (p.sg < 1) p.sg = 1;
+        size_t stage = avail / kRingStages;
+        if (stage > kStageTarget) stage = kStageTarget;
+        p.sg = static_cast<int>(stage / tb);
+        if (p.sg < 1) return p;
         p.S = kRingStages;
     }
     p.stage_bytes = static_cast<size_t>(p.sg) * tb;
-    p.planes = slice >= kPlanesMinSlice ? 1 : 0;
-    const int xrow = p.planes ? xs_plane_floats_per_row(K) : xs_floats_per_row(K);
     size_t off = kHeader + align128(p.stage_bytes) * p.S + static_cast<size_t>(B) * xrow * 4;
     off += align128(static_cast<size_t>(p.max_rows) * B * 4) + 128 /*norm scratch*/;
     p.resid_off = static_cast<int>(off);
     if (mode == GEMV_RESID) off += align128(static_cast<size_t>(p.max_rows) * B * 4);
-    p.smem = off;
+    if (off <= budget) p.smem = off;
     return p;
+}
+
+// Two CTAs per SM where the layout fits in half the SM's shared memory (twice
+// the warps to hide the dequantise-and-dot latency, and twice the copies in
+// flight), else one.
+GemvPlan make_plan(const QMat &W, int N, int K, int B, int mode) {
+    const GemvPlan p2 = plan_for(W, N, K, B, mode, 2, kSmemPair);
+    if (p2.smem) return p2;
+    return plan_for(W, N, K, B, mode, 1, kSmemMax);
 }
 
 // 16 activations of one lane, as 8 f32 pairs (read straight into 64-bit
@@ -162,6 +184,7 @@ __device__ __forceinline__ void consumers_sync() {
 
 // Largest number of float4 loads of one activation row per consumer thread.
 constexpr int kMaxXLoads = 12;   // K <= 12288
+constexpr int kNormPre = 4;      // norm-weight float4 per thread fetched before the dependency wait (K <= 4096)
 
 template <int B, int MODE, bool PL>
 __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
@@ -234,6 +257,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
         pdl_trigger();
     } else {
         // ------------------------------------------------------ consumers
+        // the norm weights do not depend on the previous kernel: fetch them
+        // before the wait (rows up to kNormPre float4 per thread)
+        const int nld = (K / 4 + kConsumers - 1) / kConsumers;   // float4 per thread
+        const bool npre = a.norm_w != nullptr && nld <= kNormPre;
+        float4 nw[kNormPre];
+#pragma unroll
+        for (int i = 0; i < kNormPre; ++i) {
+            const int k = (tid + i * kConsumers) * 4;
+            if (npre && i < nld && k < K) nw[i] = __ldg(reinterpret_cast<const float4 *>(a.norm_w + k));
+        }
         pdl_trigger();
         pdl_wait();
         if (tr) tr[1] = globaltimer_ns();
@@ -245,7 +278,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
             }
         }
         // activations: every load of a row in flight at once, then the norm
-        const int nld = (K / 4 + kConsumers - 1) / kConsumers;   // float4 per thread
         for (int b = 0; b < B; ++b) {
             const float *xb = a.x + static_cast<int64_t>(b) * K;
             float4 v[kMaxXLoads];
@@ -282,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
                     if (i < nld && k < K) {
                         float4 u = v[i];
                         if (a.norm_w) {
-                            const float4 w = *reinterpret_cast<const float4 *>(a.norm_w + k);
+                            const float4 w = (i < kNormPre && npre) ? nw[i & (kNormPre - 1)]
+                                                                    : *reinterpret_cast<const float4 *>(a.norm_w + k);
                             u.x = u.x * scale * w.x;
                             u.y = u.y * scale * w.y;
                             u.z = u.z * scale * w.z;
@@ -302,7 +335,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
                         const bool act = k < K;
                         float4 u = act ? v[i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                         if (a.norm_w && act) {
-                            const float4 w = *reinterpret_cast<const float4 *>(a.norm_w + k);
+                            const float4 w = (i < kNormPre && npre) ? nw[i & (kNormPre - 1)]
+                                                                    : *reinterpret_cast<const float4 *>(a.norm_w + k);
                             u.x = u.x * scale * w.x;
                             u.y = u.y * scale * w.y;
                             u.z = u.z * scale * w.z;
@@ -619,7 +653,7 @@ cudaError_t launch_gemv(const GemvArgs &a, int mode, bool pdl, cudaStream_t s) {
     // rows must fit in shared memory next to the ring
     if (a.K > kMaxXLoads * 4 * kConsumers || a.B * a.K > kGemvMaxBK) return cudaErrorInvalidValue;
     const GemvPlan p = make_plan(a.W, a.N, a.K, a.B, mode);
-    if (p.smem > 227 * 1024) return cudaErrorInvalidValue;
+    if (p.smem == 0) return cudaErrorInvalidValue;
     switch (a.B) {
         case 1: return launch_b<1>(a, mode, p, pdl, s);
         case 2: return launch_b<2>(a, mode, p, pdl, s);

@@ -114,12 +114,12 @@ struct qw3_model {
 
     // decode scratch
     int qkv_w = 0;
-    float *x = nullptr, *h = nullptr, *qkv = nullptr, *o = nullptr, *act = nullptr, *partial = nullptr;
-    unsigned int *counters = nullptr, *done_counter = nullptr;
+    float *x = nullptr, *h = nullptr, *qkv = nullptr, *o = nullptr, *act = nullptr;
+    unsigned int *done_counter = nullptr;
     unsigned long long *argmax_key = nullptr;
     int32_t *d_tok = nullptr, *d_pos = nullptr, *d_seq = nullptr, *d_step = nullptr, *d_status = nullptr;
     DecodeIO *d_io = nullptr;
-    int max_nsplit = 0;
+    int attn_max_split = 8;   // largest decode-attention cluster (splits per kv head)
 
     // prefill scratch
     float *px = nullptr, *ph = nullptr, *pqkv = nullptr, *po = nullptr, *pact = nullptr;
@@ -262,11 +262,10 @@ int validate_config(const qw3_config *c, std::string &why) {
     return QW3_OK;
 }
 
-int pick_nsplit(int B, int nkv, int hd, int G) {
+int pick_nsplit(int B, int nkv, int cap) {
     const int sms = num_sms();
     const int units = B * nkv;
     int ns = units >= sms ? (4 * sms + units - 1) / units : (sms + units - 1) / units;
-    const int cap = attn_decode_max_nsplit(hd, G);
     if (ns > cap) ns = cap;
     if (ns < 1) ns = 1;
     return ns;
@@ -286,7 +285,7 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
     const bool pdl = !(c.flags & QW3_FLAG_NO_PDL);
     const int H = c.hidden, hd = c.head_dim, nh = c.n_heads, nkv = c.n_kv_heads, I = c.intermediate;
     const int qw = nh * hd;
-    const int nsplit = pick_nsplit(B, nkv, hd, nh / nkv);
+    const int nsplit = pick_nsplit(B, nkv, m->attn_max_split);
     const bool gv = use_gemv(c, B);
     int kidx = 0;
     auto tr = [&]() -> unsigned long long * {
@@ -313,7 +312,7 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
         at.seq_stride = m->seq_stride; at.kvsel_stride = m->kvsel_stride; at.head_stride = m->head_stride;
         at.seq_ids = m->d_seq; at.pos = m->d_pos; at.nh = nh; at.nkv = nkv; at.hd = hd;
         at.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(hd)));
-        at.partial = m->partial; at.counters = m->counters; at.out = m->o; at.status = m->d_status;
+        at.out = m->o; at.status = m->d_status;
         at.trace = tr();
         M_TRY(m, launch_attn_decode(at, B, nsplit, pdl && gv, s));
         if (gv) {
@@ -766,7 +765,7 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
 
     // ---- decode scratch
     const int Bm = c.max_seqs;
-    m->max_nsplit = 64;
+    m->attn_max_split = attn_decode_max_nsplit(hd, nh / nkv, nkv);
     auto A = [&](void **p, size_t bytes) { return model_alloc(m, p, bytes); };
     cudaError_t e = cudaSuccess;
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->x), static_cast<size_t>(Bm) * H * 4);
@@ -774,9 +773,6 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->qkv), static_cast<size_t>(Bm) * m->qkv_w * 4);
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->o), static_cast<size_t>(Bm) * qw * 4);
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->act), static_cast<size_t>(Bm) * I * 4);
-    if (e == cudaSuccess)
-        e = A(reinterpret_cast<void **>(&m->partial), static_cast<size_t>(Bm) * nh * m->max_nsplit * (hd + 4) * 4);
-    if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->counters), static_cast<size_t>(Bm) * nkv * 4);
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->done_counter), 64);
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->argmax_key), static_cast<size_t>(Bm) * 8);
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->d_tok), static_cast<size_t>(Bm) * 4);
@@ -801,8 +797,7 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
     if (e != cudaSuccess) return bail(cuda_err(m, e, "scratch allocation"));
     if (int rc = setup_tensor_core_gemm(m)) return bail(rc);
     if (int rc = setup_mega(m, w, on_dev, staging)) return bail(rc);
-    e = cudaMemsetAsync(m->counters, 0, static_cast<size_t>(Bm) * nkv * 4, m->stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(m->done_counter, 0, 64, m->stream);
+    e = cudaMemsetAsync(m->done_counter, 0, 64, m->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->argmax_key, 0, static_cast<size_t>(Bm) * 8, m->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->d_step, 0, 64, m->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->d_status, 0, 64, m->stream);

@@ -112,8 +112,6 @@ struct AttnDecodeArgs {
     const int32_t *pos;      // [B] position of the new token
     int nh, nkv, hd;
     float scale;
-    float *partial;          // [B][nh][nsplit][hd+4]: acc[hd], m, l, pad
-    unsigned int *counters;  // [B][nkv]
     float *out;              // [B][nh*hd]
     int32_t *status;
     unsigned long long *trace;  // nullable: 2 records of 8 u64 (first, last CTA)
@@ -151,8 +149,10 @@ cudaError_t launch_gemv(const GemvArgs &a, int mode, bool pdl, cudaStream_t s);
 // largest B * K the decode GEMV stages (activations live in shared memory)
 constexpr int kGemvMaxBK = 16384;
 cudaError_t launch_attn_decode(const AttnDecodeArgs &a, int B, int nsplit, bool pdl, cudaStream_t s);
-// largest split count the decode attention kernel accepts for (head_dim, group)
-int attn_decode_max_nsplit(int hd, int G);
+// largest split count (= cluster size) of the decode attention kernel for
+// (head_dim, group) on the current device such that `units` clusters (one per
+// kv head and sequence) run at once
+int attn_decode_max_nsplit(int hd, int G, int units);
 cudaError_t launch_embed(const int32_t *tokens, int n, const QMat &E, float *x, bool pdl, cudaStream_t s,
                          unsigned long long *trace = nullptr);
 
@@ -246,6 +246,39 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait with cluster-scope acquire: for phases completed by peers of
+// the cluster (remote arrives, st.async bytes).
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// Asynchronous stores into a peer CTA's shared memory (shared::cluster
+// addresses from dsmem_map); each completes its bytes on the peer's mbarrier.
+__device__ __forceinline__ void st_async_f32x4(uint32_t addr, float a, float b, float c, float d, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32x2(uint32_t addr, float a, float b, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+                 ::"r"(addr), "f"(a), "f"(b), "r"(bar) : "memory");
+}
+
 // 1-D bulk copy global -> shared (TMA), completion counted on `bar` in bytes.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
@@ -263,6 +296,40 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 }
 
 // Programmatic dependent launch controls (no-ops without the launch attribute).
+// ---- thread-block clusters: rank, the hardware cluster barrier (every
+// thread of every CTA of the cluster arrives; release/acquire order shared
+// memory across the cluster), and loads from a peer CTA's shared memory.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void hw_cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The two halves of the cluster barrier, for work between them.
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t dsmem_map(const void *local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float dsmem_ld(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
