@@ -394,7 +394,30 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
                 int kcol0[kTilesPerPass];
 #pragma unroll
                 for (int j = 0; j < kTilesPerPass; ++j) kcol0[j] = ntk == 1 ? 0 : ((t0 + j0 + j) % ntk) * kt;
-                for (int c = 0; c < nchunk; ++c) {
+                // A lone tile (o_proj, down at 0.6B: one row group per CTA)
+                // has no second tile to overlap with: take its chunks two at
+                // a time as independent chains instead. Lanes past the row
+                // end read column 0 with zero codes and scale.
+                const bool lone = !PL && B == 1 && ntk == 1 && np == 1;
+                if (lone) {
+                    const __half *dsc = reinterpret_cast<const __half *>(tp0 + 8 * kt) + warp * (kt / 32);
+                    float s0 = 0.0f, s1 = 0.0f;
+                    for (int c = 0; c < nchunk; c += 2) {
+                        const int k0 = c * 512 + lane * 16, k1 = k0 + 512;
+                        const bool v0 = k0 < kt, v1 = k1 < kt;
+                        const int c0 = v0 ? k0 : 0, c1 = v1 ? k1 : 0;
+                        uint4 w0 = *reinterpret_cast<const uint4 *>(tp0 + warp * kt + c0);
+                        uint4 w1 = *reinterpret_cast<const uint4 *>(tp0 + warp * kt + c1);
+                        const float d0 = v0 ? __half2float(dsc[c0 >> 5]) : 0.0f;
+                        const float d1 = v1 ? __half2float(dsc[c1 >> 5]) : 0.0f;
+                        const X16 x0 = load_x16(xs + (c0 >> 5) * 36 + (c0 & 31));
+                        const X16 x1 = load_x16(xs + (c1 >> 5) * 36 + (c1 & 31));
+                        s0 = fmaf(d0, dot16(w0, x0), s0);
+                        s1 = fmaf(d1, dot16(w1, x1), s1);
+                    }
+                    acc[0][0] = s0 + s1;
+                }
+                for (int c = 0; c < (lone ? 0 : nchunk); ++c) {
                     const int kk = c * 512 + lane * 16;       // column within the tile
                     if (kk >= kt) continue;
                     if (ntk == 1) {
