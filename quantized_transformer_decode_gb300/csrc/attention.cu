@@ -28,7 +28,7 @@ namespace {
 constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kTileP = 32;   // positions per staged tile
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 
 // Splits of one (sequence, kv head) form one cluster; its leader holds a
 // partial row per split and head, which caps the cluster at 8 for G = 8.
@@ -101,7 +101,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
     constexpr int E = HD / 32;
     constexpr int PS = part_stride<HD>();
     constexpr int CM = attn_max_cluster(G);
-    static_assert(kAttnWarps * G * PS <= 2 * kStages * kTileP * HD, "warp-merge rows must fit in the K/V tiles");
+    static_assert(kAttnWarps * G * PS <= kStages * kTileP * HD, "warp-merge rows must fit in the K tiles");
+    static_assert(CM * G * PS <= kStages * kTileP * HD, "the leader's partial rows must fit in the V tiles");
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);                 // [kStages] K/V tiles
     uint64_t *rbar = bars + kStages;                                      // partials received (leader)
@@ -111,9 +112,13 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
     float *qn = vtile + kStages * kTileP * HD;                            // [G][HD]
     float *knew = qn + G * HD;                                            // [HD]
     float *vnew = knew + HD;                                              // [HD]
-    float *mrg = ktile;                     // [kAttnWarps][G][PS], in the K/V tiles once they are consumed
-    float *recv = vnew + HD;                                              // [CM][G][PS] split partials (leader)
-    float *wts = recv + CM * G * PS;                                      // [G][CM] merge weights (leader)
+    // once the tiles are consumed: the warp-merge rows in the K tiles, the
+    // split partials pushed to the leader in the V tiles
+    float *mrg = ktile;                                                   // [kAttnWarps][G][PS]
+    float *recv = vtile;                                                  // [CM][G][PS] (leader)
+    float *wts = vnew + HD;                                               // [G][CM] merge weights (leader)
+    float *pbuf = wts + G * CM;                                           // [kAttnWarps][32] probabilities
+    float *cbuf = pbuf + kAttnWarps * 32;                                 // [kAttnWarps][8] rescale factors
 
     const int g = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -165,9 +170,6 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
     const float2 *rope_row = a.rope + static_cast<size_t>(p) * (HD / 2);
     NormRope<HD> nr;
     if (warp <= G) load_norm_rope<HD>(nr, warp < G ? a.q_norm : a.k_norm, rope_row, lane);
-    // the leader's barrier is initialised and armed before any peer sends:
-    // arrive now, wait just before the push (long after every CTA arrived)
-    cluster_arrive_release();
     pdl_wait();
     if (tr) tr[1] = globaltimer_ns();
 
@@ -198,95 +200,137 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
     float qv[G][E];
 #pragma unroll
     for (int t = 0; t < G; ++t) load_lane<HD>(qn + t * HD, qv[t], lane);
-    float m[G], l[G], acc[G][E];
+    float acc[G][E];
 #pragma unroll
-    for (int t = 0; t < G; ++t) {
-        m[t] = -INFINITY;
-        l[t] = 0.0f;
+    for (int t = 0; t < G; ++t)
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[t][e] = 0.0f;
-    }
 
-    // Score NP positions at once: NP * G independent butterfly reductions
-    // keep the shuffle pipe busy; one online-softmax update per batch.
-    constexpr int NP = 4;
+    // A warp scores NP positions at once: the G*NP dot products (each spread
+    // over the lanes' dims) are summed by one reduce-scatter butterfly, after
+    // which lane k (k < V = G*NP, repeated above V) holds the score of head
+    // k / NP at position k % NP. Each lane keeps the running max and sum of
+    // its own head (online softmax, one exp per lane per batch); the
+    // probabilities and rescale factors reach every lane through the warp's
+    // shared-memory slots for the P.V accumulation over the lanes' dims.
+    constexpr int NP = G <= 4 ? 8 : 4;
+    constexpr int V = G * NP;
+    static_assert(V <= 32, "one score per lane");
+    float *pb = pbuf + warp * 32;
+    float *cb = cbuf + warp * 8;
+    const int k_own = lane & (V - 1);
+    const int t_own = k_own / NP, j_own = k_own % NP;
+    float m_own = -INFINITY, l_own = 0.0f;
     auto consume = [&](const float *krows, const float *vrows, int n) {
-        float kv_[NP][E];
-#pragma unroll
-        for (int j = 0; j < NP; ++j) {
-            if (j < n) {
-                load_lane<HD>(krows + j * HD, kv_[j], lane);
-            } else {
-#pragma unroll
-                for (int e = 0; e < E; ++e) kv_[j][e] = 0.0f;
-            }
-        }
-        float sc[G][NP];
-#pragma unroll
-        for (int t = 0; t < G; ++t)
-#pragma unroll
-            for (int j = 0; j < NP; ++j) {
-                float d = 0.0f;
-#pragma unroll
-                for (int e = 0; e < E; ++e) d = fmaf(qv[t][e], kv_[j][e], d);
-                sc[t][j] = d;
-            }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int t = 0; t < G; ++t)
-#pragma unroll
-                for (int j = 0; j < NP; ++j) sc[t][j] += __shfl_xor_sync(0xffffffffu, sc[t][j], o);
-        float vv[NP][E];
-#pragma unroll
-        for (int j = 0; j < NP; ++j) {
-            if (j < n) load_lane<HD>(vrows + j * HD, vv[j], lane);
-        }
-#pragma unroll
-        for (int t = 0; t < G; ++t) {
-            float mx = m[t];
-#pragma unroll
-            for (int j = 0; j < NP; ++j) {
-                sc[t][j] = (j < n) ? sc[t][j] * a.scale : -INFINITY;
-                mx = fmaxf(mx, sc[t][j]);
-            }
-            const float corr = expf(m[t] - mx);
-            l[t] *= corr;
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[t][e] *= corr;
+        float sc[V];
+        {
+            float kv_[NP][E];
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
                 if (j < n) {
-                    const float pr = expf(sc[t][j] - mx);
-                    l[t] += pr;
+                    load_lane<HD>(krows + j * HD, kv_[j], lane);
+                } else {
 #pragma unroll
-                    for (int e = 0; e < E; ++e) acc[t][e] = fmaf(pr, vv[j][e], acc[t][e]);
+                    for (int e = 0; e < E; ++e) kv_[j][e] = 0.0f;
                 }
             }
-            m[t] = mx;
+#pragma unroll
+            for (int t = 0; t < G; ++t)
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    float d = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) d = fmaf(qv[t][e], kv_[j][e], d);
+                    sc[t * NP + j] = d;
+                }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            if (o >= V) {
+#pragma unroll
+                for (int i = 0; i < V; ++i) sc[i] += __shfl_xor_sync(0xffffffffu, sc[i], o);
+            } else {
+                // keep the upper half of the 2o values when lane bit o is set
+                const bool up = (lane & o) != 0;
+#pragma unroll
+                for (int i = 0; i < o; ++i) {
+                    const float send = up ? sc[i] : sc[i + o];
+                    const float keep = up ? sc[i + o] : sc[i];
+                    sc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+        }
+        const bool valid = j_own < n;
+        const float sv = valid ? sc[0] * a.scale : -INFINITY;
+        float mx = sv;
+#pragma unroll
+        for (int o = 1; o < NP; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float m_new = fmaxf(m_own, mx);
+        const float pr = valid ? expf(sv - m_new) : 0.0f;
+        const float corr = expf(m_own - m_new);
+        float ps = pr;
+#pragma unroll
+        for (int o = 1; o < NP; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+        l_own = fmaf(l_own, corr, ps);
+        m_own = m_new;
+        if (lane < V) {
+            pb[lane] = pr;
+            if (j_own == 0) cb[t_own] = corr;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < G; ++t) {
+            const float c = cb[t];
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[t][e] *= c;
+        }
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            if (j < n) {
+                float vv[E];
+                load_lane<HD>(vrows + j * HD, vv, lane);
+#pragma unroll
+                for (int t = 0; t < G; ++t) {
+                    const float pj = pb[t * NP + j];
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[t][e] = fmaf(pj, vv[e], acc[t][e]);
+                }
+            }
+        }
+        __syncwarp();
     };
 
-    for (int t = 0; t < ntiles; ++t) {
-        const int si = t % kStages;
-        const bool ok = mbar_wait_bounded(&bars[si], static_cast<uint32_t>((t / kStages) & 1));
-        if (!ok) flags[0] = 1, flags[1] = t;
-        if (ok) {
-            const int rows = min(kTileP, n_cached - t * kTileP);
-            // warp w takes positions [w*NP, w*NP+NP), then every kAttnWarps-th batch
-            for (int j0 = warp * NP; j0 < rows; j0 += kAttnWarps * NP)
-                consume(ktile + (si * kTileP + j0) * HD, vtile + (si * kTileP + j0) * HD, min(NP, rows - j0));
+    // WPT warps share a tile (NP positions each); TPI tiles are consumed per
+    // round, the next ones already in flight in the remaining stages.
+    constexpr int WPT = kTileP / NP;
+    constexpr int TPI = kAttnWarps / WPT;
+    static_assert(TPI >= 1 && TPI < kStages, "a stage stays in flight while a round is consumed");
+    for (int t0 = 0; t0 < ntiles; t0 += TPI) {
+        const int t = t0 + warp / WPT;
+        if (t < ntiles) {
+            const int si = t % kStages;
+            if (!mbar_wait_bounded(&bars[si], static_cast<uint32_t>((t / kStages) & 1))) {
+                flags[0] = 1;
+                flags[1] = t0;
+            } else {
+                const int rows = min(kTileP, n_cached - t * kTileP);
+                const int j0 = (warp % WPT) * NP;
+                if (j0 < rows)
+                    consume(ktile + (si * kTileP + j0) * HD, vtile + (si * kTileP + j0) * HD, min(NP, rows - j0));
+            }
         }
         __syncthreads();
         if (flags[0]) break;
-        if (tid == 0 && t + kStages < ntiles) {
-            const int tt = t + kStages;
-            const int rows = min(kTileP, n_cached - tt * kTileP);
-            const uint32_t bytes = static_cast<uint32_t>(rows * HD * 4);
-            const size_t off = static_cast<size_t>(start + tt * kTileP) * HD;
-            mbar_arrive_expect_tx(&bars[si], 2 * bytes);
-            bulk_g2s(ktile + si * kTileP * HD, kbase + off, bytes, &bars[si], pol);
-            bulk_g2s(vtile + si * kTileP * HD, vbase + off, bytes, &bars[si], pol);
+        if (tid == 0) {
+            for (int tt = t0 + kStages; tt < t0 + kStages + TPI && tt < ntiles; ++tt) {
+                const int si = tt % kStages;
+                const int rows = min(kTileP, n_cached - tt * kTileP);
+                const uint32_t bytes = static_cast<uint32_t>(rows * HD * 4);
+                const size_t off = static_cast<size_t>(start + tt * kTileP) * HD;
+                mbar_arrive_expect_tx(&bars[si], 2 * bytes);
+                bulk_g2s(ktile + si * kTileP * HD, kbase + off, bytes, &bars[si], pol);
+                bulk_g2s(vtile + si * kTileP * HD, vbase + off, bytes, &bars[si], pol);
+            }
         }
         __syncthreads();
     }
@@ -300,17 +344,19 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
             for (int t = first; t < ntiles && t < first + kStages; ++t)
                 (void)mbar_wait_bounded(&bars[t % kStages], static_cast<uint32_t>((t / kStages) & 1));
         }
+        m_own = -INFINITY;
+        l_own = 0.0f;
 #pragma unroll
-        for (int t = 0; t < G; ++t) {
-            m[t] = -INFINITY;
-            l[t] = 0.0f;
+        for (int t = 0; t < G; ++t)
 #pragma unroll
             for (int e = 0; e < E; ++e) acc[t][e] = 0.0f;
-        }
     } else if (has_new && warp == kAttnWarps - 1) {
         consume(knew, vnew, 1);
     }
-    __syncthreads();   // no copy in flight and no warp reading the K/V tiles: they hold mrg next
+    __syncthreads();   // no copy in flight and no warp reading the K/V tiles: they hold mrg and recv next
+    // the leader's V tiles take partials only once it is done with them (and
+    // its barrier is armed): arrive now, wait just before the push
+    cluster_arrive_release();
     if (tr) tr[3] = globaltimer_ns();
 
     // ---- merge the warps into this split's partial and push it to the
@@ -319,9 +365,9 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
     for (int t = 0; t < G; ++t) {
         float *mw = mrg + (warp * G + t) * PS;
         store_lane<HD>(mw, acc[t], lane);
-        if (lane == 0) {
-            mw[HD] = m[t];
-            mw[HD + 1] = l[t];
+        if (lane == t * NP) {   // a lane of head t's group holds its (m, l)
+            mw[HD] = m_own;
+            mw[HD + 1] = l_own;
         }
     }
     __syncthreads();
@@ -400,10 +446,10 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
 }
 
 size_t attn_decode_smem(int HD, int G) {
-    const int PS = HD + 4;
-    // the warp-merge rows reuse the K/V tiles (kAttnWarps * G * PS <= 2 * kStages * kTileP * HD)
+    // K/V tiles (the warp-merge rows and the leader's partials reuse them),
+    // q rows, new k and v, merge weights, per-warp probabilities and factors
     const size_t floats = static_cast<size_t>(2) * kStages * kTileP * HD + static_cast<size_t>(G) * HD + 2 * HD +
-                          static_cast<size_t>(attn_max_cluster(G)) * G * PS + static_cast<size_t>(G) * attn_max_cluster(G);
+                          static_cast<size_t>(G) * attn_max_cluster(G) + kAttnWarps * 32 + kAttnWarps * 8;
     return 128 + floats * 4;
 }
 
