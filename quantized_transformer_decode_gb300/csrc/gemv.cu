@@ -12,7 +12,8 @@
 //    1-D bulk copy (TMA, cp.async.bulk, L2 evict-first) per stage. A bulk
 //    copy pays a fixed cost of a few hundred ns, so stages are large: a slice
 //    that fits (up to ~100 KB) is a single copy; bigger slices use a ring of
-//    three ~35 KB stages.
+//    up to six stages of up to 36 KB, sized to keep the most bytes in flight
+//    within the CTA's share of shared memory.
 //  * Warp specialisation: warp 8 is the producer; its first copies are
 //    issued before griddepcontrol.wait (weights never depend on the previous
 //    kernel), so under programmatic dependent launch the weight stream
@@ -35,6 +36,8 @@
 //    residual add (12.3.7, the residual rows are fetched early), SwiGLU over
 //    interleaved gate/up rows (12.3.6), or argmax with packed (value, index)
 //    u64 keys and a last-CTA finish that emits the greedy token (12.6).
+#include <algorithm>
+
 #include "qw3_internal.cuh"
 
 namespace qw3 {
@@ -46,12 +49,12 @@ constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;   // + producer warp
 constexpr size_t kOneShot = 100 * 1024;     // slices up to this size: one copy
 constexpr size_t kStageTarget = 36 * 1024;  // ring stage size otherwise
-constexpr int kRingStages = 3;
+constexpr int kMaxStages = 6;             // ring stages at most
 constexpr size_t kPlanesMinSlice = 192 * 1024;   // digit-plane activations from this CTA slice size
 constexpr size_t kSmemMax = 227 * 1024;     // dynamic shared memory of one CTA
 constexpr size_t kSmemPair = 112 * 1024;    // per CTA when two share an SM (228 KB, 1 KB reserved each)
 constexpr int kTilesPerPass = 4;            // tiles a warp reduces at once
-// shared-memory header: 4 full + 4 empty mbarriers, flags, argmax keys
+// shared-memory header: 8 full + 8 empty mbarriers, flags, argmax keys
 constexpr int kHeader = 256;
 
 struct GemvPlan {
@@ -95,11 +98,32 @@ GemvPlan plan_for(const QMat &W, int N, int K, int B, int mode, int cps, size_t 
         p.sg = max_groups * ntk;
         p.S = 1;
     } else {
-        size_t stage = avail / kRingStages;
-        if (stage > kStageTarget) stage = kStageTarget;
-        p.sg = static_cast<int>(stage / tb);
-        if (p.sg < 1) return p;
-        p.S = kRingStages;
+        // ring: the largest stage (whole tiles, at most kStageTarget) that
+        // still gives three stages or more; failing that, the stage size and
+        // count (at most kMaxStages) with the most bytes in flight while one
+        // stage is consumed. (Measured: six 17 KB stages stream the 0.6B
+        // lm_head at 4.3 TB/s, three 35 KB stages at 6.2 TB/s.)
+        size_t best_fly = 0;
+        int sg_max = static_cast<int>(kStageTarget / tb);
+        if (sg_max < 1) sg_max = 1;
+        for (int sg = sg_max; sg >= 1; --sg) {
+            const size_t st = align128(static_cast<size_t>(sg) * tb);
+            const int S = static_cast<int>(std::min<size_t>(kMaxStages, avail / st));
+            if (S < 2) continue;
+            const size_t fly = static_cast<size_t>(S - 1) * sg * tb;
+            if (S >= 3) {
+                p.sg = sg;
+                p.S = S;
+                best_fly = fly;
+                break;
+            }
+            if (fly > best_fly) {
+                best_fly = fly;
+                p.sg = sg;
+                p.S = S;
+            }
+        }
+        if (best_fly == 0) return p;
     }
     p.stage_bytes = static_cast<size_t>(p.sg) * tb;
     size_t off = kHeader + align128(p.stage_bytes) * p.S + static_cast<size_t>(B) * xrow * 4;
@@ -201,10 +225,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
     const int ntk = K / kt;                      // tiles per row group
     const size_t tb = qm_tile_bytes(kt);
     const size_t slot = align128(p.stage_bytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem);          // [4]
-    uint64_t *empty = full + 4;                                    // [4]
-    volatile int *flags = reinterpret_cast<volatile int *>(smem + 64);                  // [8]
-    unsigned long long *best = reinterpret_cast<unsigned long long *>(smem + 96);      // [4]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);          // [kMaxStages]
+    uint64_t *empty = full + 8;                                    // [kMaxStages]
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + 128);                 // [8]
+    unsigned long long *best = reinterpret_cast<unsigned long long *>(smem + 160);     // [4]
     uint8_t *ring = smem + kHeader;
     float *xs = reinterpret_cast<float *>(ring + slot * p.S);
     const int xrow = PL ? xs_plane_floats_per_row(K) : xs_floats_per_row(K);
@@ -394,26 +418,41 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
                 int kcol0[kTilesPerPass];
 #pragma unroll
                 for (int j = 0; j < kTilesPerPass; ++j) kcol0[j] = ntk == 1 ? 0 : ((t0 + j0 + j) % ntk) * kt;
-                // A lone tile (o_proj, down at 0.6B: one row group per CTA)
-                // has no second tile to overlap with: take its chunks two at
-                // a time as independent chains instead. Lanes past the row
-                // end read column 0 with zero codes and scale.
-                const bool lone = !PL && B == 1 && ntk == 1 && np == 1;
+                // A lone tile per pass (one row group per CTA, or one tile per
+                // ring stage) has no second tile to overlap with: take its
+                // chunks two at a time as independent chains instead. Lanes
+                // past the tile's end read column 0 with zero codes and scale.
+                const bool lone = B == 1 && np == 1;
                 if (lone) {
                     const __half *dsc = reinterpret_cast<const __half *>(tp0 + 8 * kt) + warp * (kt / 32);
+                    const int kc = kcol0[0];   // the tile's first column in the row
                     float s0 = 0.0f, s1 = 0.0f;
                     for (int c = 0; c < nchunk; c += 2) {
                         const int k0 = c * 512 + lane * 16, k1 = k0 + 512;
                         const bool v0 = k0 < kt, v1 = k1 < kt;
                         const int c0 = v0 ? k0 : 0, c1 = v1 ? k1 : 0;
-                        uint4 w0 = *reinterpret_cast<const uint4 *>(tp0 + warp * kt + c0);
-                        uint4 w1 = *reinterpret_cast<const uint4 *>(tp0 + warp * kt + c1);
+                        const uint4 w0 = *reinterpret_cast<const uint4 *>(tp0 + warp * kt + c0);
+                        const uint4 w1 = *reinterpret_cast<const uint4 *>(tp0 + warp * kt + c1);
                         const float d0 = v0 ? __half2float(dsc[c0 >> 5]) : 0.0f;
                         const float d1 = v1 ? __half2float(dsc[c1 >> 5]) : 0.0f;
-                        const X16 x0 = load_x16(xs + (c0 >> 5) * 36 + (c0 & 31));
-                        const X16 x1 = load_x16(xs + (c1 >> 5) * 36 + (c1 & 31));
-                        s0 = fmaf(d0, dot16(w0, x0), s0);
-                        s1 = fmaf(d1, dot16(w1, x1), s1);
+                        const int x0c = kc + c0, x1c = kc + c1;
+                        if constexpr (!PL) {
+                            const X16 x0 = load_x16(xs + (x0c >> 5) * 36 + (x0c & 31));
+                            const X16 x1 = load_x16(xs + (x1c >> 5) * 36 + (x1c & 31));
+                            s0 = fmaf(d0, dot16(w0, x0), s0);
+                            s1 = fmaf(d1, dot16(w1, x1), s1);
+                        } else {
+                            const uint8_t *xd = reinterpret_cast<const uint8_t *>(xs);
+                            const float *xsc = reinterpret_cast<const float *>(xd + static_cast<size_t>(K) * 3);
+                            uint4 P0[3], P1[3];
+#pragma unroll
+                            for (int q = 0; q < 3; ++q) {
+                                P0[q] = reinterpret_cast<const uint4 *>(xd)[(x0c >> 4) * 3 + q];
+                                P1[q] = reinterpret_cast<const uint4 *>(xd)[(x1c >> 4) * 3 + q];
+                            }
+                            s0 = fmaf(d0 * xsc[x0c >> 5], pdot16(w0, P0), s0);
+                            s1 = fmaf(d1 * xsc[x1c >> 5], pdot16(w1, P1), s1);
+                        }
                     }
                     acc[0][0] = s0 + s1;
                 }

@@ -174,10 +174,13 @@ void free_all(qw3_model *m) {
     m->stream = nullptr;
 }
 
-// Tile width of the repacked layout: the whole row up to 4096 columns.
+// Tile width of the repacked layout: the whole row up to 3072 columns; wider
+// rows are halved to at most 2048 columns (17 KB tiles), so that the decode
+// GEMV's shared-memory ring holds several stages at two CTAs per SM.
 int tile_width(int cols) {
     int kt = cols;
-    while (kt > 4096 && kt % 2 == 0 && (kt / 2) % 32 == 0) kt /= 2;
+    if (cols > 3072)
+        while (kt > 2048 && kt % 2 == 0 && (kt / 2) % 32 == 0) kt /= 2;
     return kt;
 }
 
@@ -466,6 +469,8 @@ int setup_mega(qw3_model *m, const qw3_weights *w, bool on_dev, uint8_t *staging
     const int G = nh / nkv, CS = kMegaCS;
     const int RG = (G + 2) * hd;
     if (!mega_supported_heads(hd, G) || H > 4096 || H % 256 || RG % (8 * CS) || RG > 8 * 256 || I % 32 || I / 32 < nkv) return QW3_OK;
+    // it streams gate/up and the lm_head as whole-row tiles (8 x H)
+    if (m->layers.empty() || m->layers[0].gu.kt != H || m->out.kt != H) return QW3_OK;
     // per-layer arrays must sit at one stride (they do: every layer has the same sizes)
     for (int l = 1; l < c.n_layers; ++l) {
         const LayerDev &a = m->layers[l - 1], &b = m->layers[l];
