@@ -65,6 +65,8 @@ struct GemvPlan {
     int max_rows;     // rows of the largest CTA slice
     int resid_off;    // byte offset of the residual buffer (RESID mode)
     int planes;       // 1: activations as digit planes (large slices)
+    int cs;           // 1: column-split consumer (batch 1, 2048-column tiles, several per row)
+    int red8_off;     // byte offset of its per-warp row partials
     size_t stage_bytes;
     size_t smem;
 };
@@ -92,6 +94,9 @@ GemvPlan plan_for(const QMat &W, int N, int K, int B, int mode, int cps, size_t 
     const int xrow = p.planes ? xs_plane_floats_per_row(K) : xs_floats_per_row(K);
     size_t fixed = kHeader + static_cast<size_t>(B) * xrow * 4 + align128(static_cast<size_t>(p.max_rows) * B * 4) + 128;
     if (mode == GEMV_RESID) fixed += align128(static_cast<size_t>(p.max_rows) * B * 4);
+    p.cs = (B == 1 && ntk > 1 && W.kt == 2048) ? 1 : 0;
+    const size_t red8 = p.cs ? align128(static_cast<size_t>(max_groups) * 64 * 4) : 0;
+    fixed += red8;
     if (fixed >= budget) return p;
     const size_t avail = budget - fixed;
     if (slice <= kOneShot && align128(slice) <= avail) {
@@ -116,6 +121,8 @@ GemvPlan plan_for(const QMat &W, int N, int K, int B, int mode, int cps, size_t 
     off += align128(static_cast<size_t>(p.max_rows) * B * 4) + 128 /*norm scratch*/;
     p.resid_off = static_cast<int>(off);
     if (mode == GEMV_RESID) off += align128(static_cast<size_t>(p.max_rows) * B * 4);
+    p.red8_off = static_cast<int>(off);
+    off += red8;
     if (off <= budget) p.smem = off;
     return p;
 }
@@ -196,7 +203,7 @@ __device__ __forceinline__ void consumers_sync() {
 constexpr int kMaxXLoads = 12;   // K <= 12288
 constexpr int kNormPre = 4;      // norm-weight float4 per thread fetched before the dependency wait (K <= 4096)
 
-template <int B, int MODE, bool PL>
+template <int B, int MODE, bool PL, bool CS>
 __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int K = a.K;
@@ -382,6 +389,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
         float carry[B];                       // running sum across k-tiles of a group
 #pragma unroll
         for (int b = 0; b < B; ++b) carry[b] = 0.0f;
+        // column-split consumer (batch 1, rows split into 2048-column tiles):
+        // warp w takes the 256-column slice w of every tile for all 8 rows,
+        // half-warp h rows h, h+2, h+4, h+6, so each lane's 16 activations
+        // are read from shared memory once for four rows instead of once per
+        // row; per-warp row partials of each group go to red8 and are summed
+        // in a fixed order before the epilogue
+        static_assert(!CS || B == 1, "the column-split consumer is for batch 1");
+        float cacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float *red8 = reinterpret_cast<float *>(smem + p.red8_off);   // [groups][8 warps][8 rows]
         for (int st = 0; st < nst; ++st) {
             const int si = st % p.S;
             if (!mbar_wait_bounded(&full[si], static_cast<uint32_t>((st / p.S) & 1))) {
@@ -392,7 +408,55 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
             const uint8_t *stage = ring + slot * si;
             const int t0 = st * p.sg;
             const int nt = min(p.sg, ntiles - t0);
-            for (int j0 = 0; j0 < nt; j0 += kTilesPerPass) {
+            if constexpr (CS) {
+                const int h = lane >> 4;
+                const int cin = warp * 256 + (lane & 15) * 16;   // column within the tile
+                for (int j = 0; j < nt; ++j) {
+                    const int tile = t0 + j;
+                    const int kti = tile % ntk;
+                    const uint8_t *tp = stage + static_cast<size_t>(j) * tb;
+                    const __half *sc = reinterpret_cast<const __half *>(tp + 8 * kt);
+                    const int col = kti * kt + cin;               // column within the row
+                    if constexpr (PL) {
+                        const uint8_t *xd = reinterpret_cast<const uint8_t *>(xs);
+                        const float sx = reinterpret_cast<const float *>(xd + static_cast<size_t>(K) * 3)[col >> 5];
+                        uint4 P[3];
+#pragma unroll
+                        for (int q = 0; q < 3; ++q) P[q] = reinterpret_cast<const uint4 *>(xd)[(col >> 4) * 3 + q];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = h + 2 * i;
+                            const uint4 w = *reinterpret_cast<const uint4 *>(tp + r * kt + cin);
+                            const float d = __half2float(sc[r * (kt / 32) + (cin >> 5)]);
+                            cacc[i] = fmaf(d * sx, pdot16(w, P), cacc[i]);
+                        }
+                    } else {
+                        const X16 x = load_x16(xs + (col >> 5) * 36 + (col & 31));
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = h + 2 * i;
+                            const uint4 w = *reinterpret_cast<const uint4 *>(tp + r * kt + cin);
+                            const float d = __half2float(sc[r * (kt / 32) + (cin >> 5)]);
+                            cacc[i] = fmaf(d, dot16(w, x), cacc[i]);
+                        }
+                    }
+                    if (kti == ntk - 1) {
+                        // the group's last k-tile: sum the 16 lanes of each half-warp
+#pragma unroll
+                        for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) cacc[i] += __shfl_xor_sync(0xffffffffu, cacc[i], o);
+                        if ((lane & 15) == 0) {
+                            float *dst = red8 + (tile / ntk) * 64 + warp * 8;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) dst[h + 2 * i] = cacc[i];
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) cacc[i] = 0.0f;
+                    }
+                }
+            }
+            for (int j0 = 0; j0 < (CS ? 0 : nt); j0 += kTilesPerPass) {
                 const int np = min(kTilesPerPass, nt - j0);
                 const uint8_t *tp0 = stage + static_cast<size_t>(j0) * tb;
                 float acc[kTilesPerPass][B];
@@ -552,6 +616,19 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
         return;
     }
 
+    if constexpr (CS) {
+        // row sums of the column-split consumer: the 8 warps' partials in order
+        const float *red8 = reinterpret_cast<const float *>(smem + p.red8_off);
+        for (int t = tid; t < nrows; t += kThreads) {
+            const float *src = red8 + (t >> 3) * 64 + (t & 7);
+            float v = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) v += src[w * 8];
+            red[t] = v;
+        }
+        __syncthreads();
+    }
+
     // ---- epilogue over the CTA's rows
     float *yout = a.y;
     if (MODE == GEMV_ARGMAX && a.io) yout = a.io->logits;
@@ -635,13 +712,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
     if (tr) tr[4] = globaltimer_ns();
 }
 
-template <int B, int MODE, bool PL>
+template <int B, int MODE, bool PL, bool CS = false>
 cudaError_t configure_one() {
-    cudaError_t e = cudaFuncSetAttribute(k_gemv<B, MODE, PL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(k_gemv<B, MODE, PL, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     // Same carveout for every decode kernel: an SM never has to drain to
     // reconfigure L1/shared memory between PDL-overlapped kernels.
-    return cudaFuncSetAttribute(k_gemv<B, MODE, PL>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    return cudaFuncSetAttribute(k_gemv<B, MODE, PL, CS>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                 cudaSharedmemCarveoutMaxShared);
 }
 
@@ -655,7 +732,18 @@ cudaError_t configure_b() {
     if ((e = configure_one<B, GEMV_STORE, true>()) != cudaSuccess) return e;
     if ((e = configure_one<B, GEMV_RESID, true>()) != cudaSuccess) return e;
     if ((e = configure_one<B, GEMV_SWIGLU, true>()) != cudaSuccess) return e;
-    return configure_one<B, GEMV_ARGMAX, true>();
+    if ((e = configure_one<B, GEMV_ARGMAX, true>()) != cudaSuccess) return e;
+    if constexpr (B == 1) {
+        if ((e = configure_one<1, GEMV_STORE, false, true>()) != cudaSuccess) return e;
+        if ((e = configure_one<1, GEMV_RESID, false, true>()) != cudaSuccess) return e;
+        if ((e = configure_one<1, GEMV_SWIGLU, false, true>()) != cudaSuccess) return e;
+        if ((e = configure_one<1, GEMV_ARGMAX, false, true>()) != cudaSuccess) return e;
+        if ((e = configure_one<1, GEMV_STORE, true, true>()) != cudaSuccess) return e;
+        if ((e = configure_one<1, GEMV_RESID, true, true>()) != cudaSuccess) return e;
+        if ((e = configure_one<1, GEMV_SWIGLU, true, true>()) != cudaSuccess) return e;
+        if ((e = configure_one<1, GEMV_ARGMAX, true, true>()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 template <int B, int MODE>
@@ -670,8 +758,14 @@ cudaError_t launch_one(const GemvArgs &a, const GemvPlan &p, bool pdl, cudaStrea
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (p.planes) return cudaLaunchKernelEx(&cfg, k_gemv<B, MODE, true>, a, p);
-    return cudaLaunchKernelEx(&cfg, k_gemv<B, MODE, false>, a, p);
+    if constexpr (B == 1) {
+        if (p.cs) {
+            if (p.planes) return cudaLaunchKernelEx(&cfg, k_gemv<1, MODE, true, true>, a, p);
+            return cudaLaunchKernelEx(&cfg, k_gemv<1, MODE, false, true>, a, p);
+        }
+    }
+    if (p.planes) return cudaLaunchKernelEx(&cfg, k_gemv<B, MODE, true, false>, a, p);
+    return cudaLaunchKernelEx(&cfg, k_gemv<B, MODE, false, false>, a, p);
 }
 
 template <int B>

@@ -175,12 +175,15 @@ void free_all(qw3_model *m) {
 }
 
 // Tile width of the repacked layout: the whole row up to 3072 columns; wider
-// rows are halved to at most 2048 columns (17 KB tiles), so that the decode
-// GEMV's shared-memory ring holds several stages at two CTAs per SM.
+// rows are cut into the widest tiles of at most 2048 columns (a multiple of
+// 256 that divides the row; 17 KB tiles), so that the decode GEMV's
+// shared-memory ring holds two stages or more at two CTAs per SM.
 int tile_width(int cols) {
+    if (cols <= 3072) return cols;
+    for (int kt = 2048; kt >= 256; kt -= 256)
+        if (cols % kt == 0) return kt;
     int kt = cols;
-    if (cols > 3072)
-        while (kt > 2048 && kt % 2 == 0 && (kt / 2) % 32 == 0) kt /= 2;
+    while (kt > 2048 && kt % 2 == 0 && (kt / 2) % 32 == 0) kt /= 2;
     return kt;
 }
 
