@@ -28,6 +28,7 @@ namespace {
 constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kTileP = 32;   // positions per staged tile
+constexpr int kAttnMaxClusters = 8;   // clusters per (sequence, kv head): their partials merge in global memory
 constexpr int kStages = 3;
 
 // Splits of one (sequence, kv head) form one cluster; its leader holds a
@@ -97,7 +98,7 @@ __device__ __forceinline__ void norm_rope_pre(float (&v)[HD / 32], const NormRop
 }
 
 template <int HD, int G>
-__global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, int nsplit) {
+__global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, int nsplit, int csize) {
     constexpr int E = HD / 32;
     constexpr int PS = part_stride<HD>();
     constexpr int CM = attn_max_cluster(G);
@@ -122,7 +123,9 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
 
     const int g = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int C = nsplit;                        // the cluster spans the splits: rank == s
+    // nsplit splits of the context per (b, g), in nsplit / csize clusters of
+    // csize CTAs: cluster kc = s / C, rank r = s % C (rank 0 leads)
+    const int C = csize, r = s % csize, kc = s / csize, K2 = nsplit / csize;
     unsigned long long *tr = (tid == 0) ? trace_slot(a.trace) : nullptr;
     if (tr) {
         tr[0] = globaltimer_ns();
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
     const int seq = a.seq_ids[b];
     const int p = a.pos[b];
     const int ctx = p + 1;
-    const int chunk = (ctx + C - 1) / C;
+    const int chunk = (ctx + nsplit - 1) / nsplit;
     const int start = s * chunk;
     const int end = min(ctx, start + chunk);
     const bool has_new = (start <= p) && (p < end);
@@ -151,6 +154,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
         flags[0] = 0;
         flags[1] = 0;
         flags[2] = 0;
+        flags[3] = 0;
     }
     __syncthreads();
     const uint64_t pol = policy_evict_first();
@@ -164,7 +168,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
             bulk_g2s(vtile + t * kTileP * HD, vbase + off, bytes, &bars[t], pol);
         }
         // the leader expects every peer's partial rows (acc, m, l per head)
-        if (s == 0) mbar_arrive_expect_tx(rbar, static_cast<uint32_t>((C - 1) * G * (HD * 4 + 8)));
+        if (r == 0) mbar_arrive_expect_tx(rbar, static_cast<uint32_t>((C - 1) * G * (HD * 4 + 8)));
     }
     // norm weights and rotation of this warp's first head task, before the wait
     const float2 *rope_row = a.rope + static_cast<size_t>(p) * (HD / 2);
@@ -390,8 +394,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
                 for (int e = 0; e < E; ++e) o[e] = fmaf(aw[e], f, o[e]);
             }
         }
-        float *slot = recv + (s * G + t) * PS;
-        if (s == 0) {
+        float *slot = recv + (r * G + t) * PS;
+        if (r == 0) {
             store_lane<HD>(slot, o, lane);
             if (lane == 0) {
                 slot[HD] = M;
@@ -407,8 +411,10 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
             if (lane == 0) st_async_f32x2(dst + 4u * HD, M, L, rbar_leader);
         }
     }
-    if (s == 0) {
-        // ---- leader: flash-decoding combine of the C split partials
+    if (r == 0) {
+        // ---- leader: flash-decoding combine of the C split partials (with
+        // several clusters per (b, g): the cluster's unnormalised partial to
+        // global memory, the last leader to arrive merges them)
         if (tid == 0 && !mbar_wait_bounded_cluster(rbar, 0u)) flags[2] = 1;
         __syncthreads();
         if (flags[2]) {
@@ -422,10 +428,16 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
                 const float M = warp_max(mj);
                 const float f = (mj == -INFINITY) ? 0.0f : expf(mj - M);
                 const float L = warp_sum(lj * f);
-                if (lane < C) wts[t * CM + lane] = L > 0.0f ? f * (1.0f / L) : 0.0f;
+                if (lane < C) wts[t * CM + lane] = K2 > 1 ? f : (L > 0.0f ? f * (1.0f / L) : 0.0f);
+                if (K2 > 1 && lane == 0) {
+                    float *cp = a.cpart + ((static_cast<size_t>(b) * a.nkv + g) * K2 + kc) * G * PS + t * PS;
+                    cp[HD] = M;
+                    cp[HD + 1] = L;
+                }
             }
             __syncthreads();
-            float *ob = a.out + static_cast<size_t>(b) * a.nh * HD + static_cast<size_t>(g) * G * HD;
+            float *ob = K2 > 1 ? a.cpart + ((static_cast<size_t>(b) * a.nkv + g) * K2 + kc) * G * PS
+                               : a.out + static_cast<size_t>(b) * a.nh * HD + static_cast<size_t>(g) * G * HD;
             for (int o = tid; o < G * HD; o += kAttnThreads) {
                 const int t = o / HD, d = o - (o / HD) * HD;
                 float v[CM];
@@ -435,7 +447,43 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
 #pragma unroll
                 for (int j = 0; j < CM; ++j)
                     if (j < C) sum = fmaf(wts[t * CM + j], v[j], sum);
-                ob[o] = sum;
+                if (K2 > 1) {
+                    ob[t * PS + d] = sum;
+                } else {
+                    ob[o] = sum;
+                }
+            }
+            if (K2 > 1) {
+                // second level: the last of the K2 leaders merges the clusters
+                __threadfence();
+                __syncthreads();
+                if (tid == 0) {
+                    const unsigned prev = atomicAdd(&a.ccnt[b * a.nkv + g], 1u);
+                    flags[3] = (prev == static_cast<unsigned>(K2 - 1)) ? 1 : 0;
+                }
+                __syncthreads();
+                if (flags[3]) {
+                    __threadfence();
+                    const float *cp = a.cpart + (static_cast<size_t>(b) * a.nkv + g) * K2 * G * PS;
+                    if (warp < G) {
+                        const int t = warp;
+                        const float mc = lane < K2 ? __ldcg(cp + (lane * G + t) * PS + HD) : -INFINITY;
+                        const float lc = lane < K2 ? __ldcg(cp + (lane * G + t) * PS + HD + 1) : 0.0f;
+                        const float M = warp_max(mc);
+                        const float f = (mc == -INFINITY) ? 0.0f : expf(mc - M);
+                        const float L = warp_sum(lc * f);
+                        if (lane < K2) wts[t * CM + lane] = L > 0.0f ? f * (1.0f / L) : 0.0f;
+                    }
+                    __syncthreads();
+                    float *out = a.out + static_cast<size_t>(b) * a.nh * HD + static_cast<size_t>(g) * G * HD;
+                    for (int o = tid; o < G * HD; o += kAttnThreads) {
+                        const int t = o / HD, d = o - (o / HD) * HD;
+                        float sum = 0.0f;
+                        for (int c = 0; c < K2; ++c) sum = fmaf(wts[t * CM + c], __ldcg(cp + (c * G + t) * PS + d), sum);
+                        out[o] = sum;
+                    }
+                    if (tid == 0) a.ccnt[b * a.nkv + g] = 0u;
+                }
             }
         }
     }
@@ -494,7 +542,7 @@ int max_cluster_t(int units) {
 }
 
 template <int HD, int G>
-cudaError_t launch_attn_t(const AttnDecodeArgs &a, int B, int nsplit, bool pdl, cudaStream_t s) {
+cudaError_t launch_attn_t(const AttnDecodeArgs &a, int B, int nsplit, int csize, bool pdl, cudaStream_t s) {
     const size_t smem = attn_decode_smem(HD, G);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(a.nkv, nsplit, B);
@@ -504,13 +552,13 @@ cudaError_t launch_attn_t(const AttnDecodeArgs &a, int B, int nsplit, bool pdl, 
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = static_cast<unsigned>(nsplit);
+    attr[0].val.clusterDim.y = static_cast<unsigned>(csize);
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, k_attn_decode<HD, G>, a, nsplit);
+    return cudaLaunchKernelEx(&cfg, k_attn_decode<HD, G>, a, nsplit, csize);
 }
 
 // ------------------------------------------------------------- prefill
@@ -685,23 +733,25 @@ cudaError_t configure_attention() {
     return cudaSuccess;
 }
 
-cudaError_t launch_attn_decode(const AttnDecodeArgs &a, int B, int nsplit, bool pdl, cudaStream_t s) {
+cudaError_t launch_attn_decode(const AttnDecodeArgs &a, int B, int nsplit, int csize, bool pdl, cudaStream_t s) {
     const int G = a.nh / a.nkv;
-    if (nsplit < 1 || nsplit > attn_max_cluster(G)) return cudaErrorInvalidValue;
+    if (csize < 1 || csize > attn_max_cluster(G) || nsplit % csize != 0 || nsplit / csize > kAttnMaxClusters ||
+        (nsplit > csize && (!a.cpart || !a.ccnt)))
+        return cudaErrorInvalidValue;
     if (a.hd == 128) {
         switch (G) {
-            case 1: return launch_attn_t<128, 1>(a, B, nsplit, pdl, s);
-            case 2: return launch_attn_t<128, 2>(a, B, nsplit, pdl, s);
-            case 4: return launch_attn_t<128, 4>(a, B, nsplit, pdl, s);
-            case 8: return launch_attn_t<128, 8>(a, B, nsplit, pdl, s);
+            case 1: return launch_attn_t<128, 1>(a, B, nsplit, csize, pdl, s);
+            case 2: return launch_attn_t<128, 2>(a, B, nsplit, csize, pdl, s);
+            case 4: return launch_attn_t<128, 4>(a, B, nsplit, csize, pdl, s);
+            case 8: return launch_attn_t<128, 8>(a, B, nsplit, csize, pdl, s);
             default: break;
         }
     } else if (a.hd == 64) {
         switch (G) {
-            case 1: return launch_attn_t<64, 1>(a, B, nsplit, pdl, s);
-            case 2: return launch_attn_t<64, 2>(a, B, nsplit, pdl, s);
-            case 4: return launch_attn_t<64, 4>(a, B, nsplit, pdl, s);
-            case 8: return launch_attn_t<64, 8>(a, B, nsplit, pdl, s);
+            case 1: return launch_attn_t<64, 1>(a, B, nsplit, csize, pdl, s);
+            case 2: return launch_attn_t<64, 2>(a, B, nsplit, csize, pdl, s);
+            case 4: return launch_attn_t<64, 4>(a, B, nsplit, csize, pdl, s);
+            case 8: return launch_attn_t<64, 8>(a, B, nsplit, csize, pdl, s);
             default: break;
         }
     }

@@ -120,6 +120,9 @@ struct qw3_model {
     int32_t *d_tok = nullptr, *d_pos = nullptr, *d_seq = nullptr, *d_step = nullptr, *d_status = nullptr;
     DecodeIO *d_io = nullptr;
     int attn_max_split = 8;   // largest decode-attention cluster (splits per kv head)
+    int attn_long_c = 0;      // cluster size of the batch-1 long-context split (0: none)
+    float *attn_cpart = nullptr;          // cluster partials of the long-context split
+    unsigned int *attn_ccnt = nullptr;    // their arrival counters
 
     // prefill scratch
     float *px = nullptr, *ph = nullptr, *pqkv = nullptr, *po = nullptr, *pact = nullptr;
@@ -279,6 +282,11 @@ int pick_nsplit(int B, int nkv, int cap) {
 
 // The decode GEMV path stages B activation rows of up to max(H, I, n_heads*hd)
 // floats in shared memory; larger batches use the tiled GEMM path.
+// Batch-1 decode at contexts of this capacity or more splits each kv head's
+// positions over kAttnLongClusters clusters.
+constexpr int kAttnLongCtx = 4096;
+constexpr int kAttnLongClusters = 4;
+
 bool use_gemv(const qw3_config &c, int B) {
     const int kmax = std::max(c.hidden, std::max(c.intermediate, c.n_heads * c.head_dim));
     return B <= 4 && B * kmax <= kGemvMaxBK;
@@ -291,7 +299,14 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
     const bool pdl = !(c.flags & QW3_FLAG_NO_PDL);
     const int H = c.hidden, hd = c.head_dim, nh = c.n_heads, nkv = c.n_kv_heads, I = c.intermediate;
     const int qw = nh * hd;
-    const int nsplit = pick_nsplit(B, nkv, m->attn_max_split);
+    int nsplit = pick_nsplit(B, nkv, m->attn_max_split), csize = nsplit;
+    if (B == 1 && m->attn_long_c > 0) {
+        // long contexts at batch 1: kAttnLongClusters clusters per kv head,
+        // merged in global memory (more CTAs stream the cache than one
+        // cluster holds)
+        csize = m->attn_long_c;
+        nsplit = csize * kAttnLongClusters;
+    }
     const bool gv = use_gemv(c, B);
     int kidx = 0;
     auto tr = [&]() -> unsigned long long * {
@@ -318,9 +333,9 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
         at.seq_stride = m->seq_stride; at.kvsel_stride = m->kvsel_stride; at.head_stride = m->head_stride;
         at.seq_ids = m->d_seq; at.pos = m->d_pos; at.nh = nh; at.nkv = nkv; at.hd = hd;
         at.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(hd)));
-        at.out = m->o; at.status = m->d_status;
+        at.out = m->o; at.status = m->d_status; at.cpart = m->attn_cpart; at.ccnt = m->attn_ccnt;
         at.trace = tr();
-        M_TRY(m, launch_attn_decode(at, B, nsplit, pdl && gv, s));
+        M_TRY(m, launch_attn_decode(at, B, nsplit, csize, pdl && gv, s));
         if (gv) {
             GemvArgs a{};
             a.W = L.o; a.N = H; a.K = qw; a.B = B; a.x = m->o; a.norm_w = nullptr;
@@ -774,6 +789,10 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
     // ---- decode scratch
     const int Bm = c.max_seqs;
     m->attn_max_split = attn_decode_max_nsplit(hd, nh / nkv, nkv);
+    if (c.max_seq_len >= kAttnLongCtx) {
+        const int lc = attn_decode_max_nsplit(hd, nh / nkv, nkv * kAttnLongClusters);
+        if (lc >= 4) m->attn_long_c = lc;
+    }
     auto A = [&](void **p, size_t bytes) { return model_alloc(m, p, bytes); };
     cudaError_t e = cudaSuccess;
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->x), static_cast<size_t>(Bm) * H * 4);
@@ -782,6 +801,10 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->o), static_cast<size_t>(Bm) * qw * 4);
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->act), static_cast<size_t>(Bm) * I * 4);
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->done_counter), 64);
+    if (e == cudaSuccess && m->attn_long_c > 0)
+        e = A(reinterpret_cast<void **>(&m->attn_cpart),
+              static_cast<size_t>(nkv) * kAttnLongClusters * (nh / nkv) * (hd + 4) * 4);
+    if (e == cudaSuccess && m->attn_long_c > 0) e = A(reinterpret_cast<void **>(&m->attn_ccnt), 64 * 4);
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->argmax_key), static_cast<size_t>(Bm) * 8);
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->d_tok), static_cast<size_t>(Bm) * 4);
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->d_pos), static_cast<size_t>(Bm) * 4);
@@ -806,6 +829,7 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
     if (int rc = setup_tensor_core_gemm(m)) return bail(rc);
     if (int rc = setup_mega(m, w, on_dev, staging)) return bail(rc);
     e = cudaMemsetAsync(m->done_counter, 0, 64, m->stream);
+    if (e == cudaSuccess && m->attn_ccnt) e = cudaMemsetAsync(m->attn_ccnt, 0, 64 * 4, m->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->argmax_key, 0, static_cast<size_t>(Bm) * 8, m->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->d_step, 0, 64, m->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->d_status, 0, 64, m->stream);

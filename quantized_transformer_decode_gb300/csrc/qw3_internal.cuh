@@ -113,6 +113,10 @@ struct AttnDecodeArgs {
     int nh, nkv, hd;
     float scale;
     float *out;              // [B][nh*hd]
+    // several clusters per (b, g) (nsplit > cluster size): their partials
+    // [B][nkv][clusters][G][hd+4] and arrival counters [B][nkv] (zero)
+    float *cpart;
+    unsigned int *ccnt;
     int32_t *status;
     unsigned long long *trace;  // nullable: 2 records of 8 u64 (first, last CTA)
 };
@@ -148,7 +152,9 @@ cudaError_t launch_gemv_raw(const uint8_t *W, int rows, int cols, const float *x
 cudaError_t launch_gemv(const GemvArgs &a, int mode, bool pdl, cudaStream_t s);
 // largest B * K the decode GEMV stages (activations live in shared memory)
 constexpr int kGemvMaxBK = 16384;
-cudaError_t launch_attn_decode(const AttnDecodeArgs &a, int B, int nsplit, bool pdl, cudaStream_t s);
+// nsplit splits of each (sequence, kv head) in clusters of csize CTAs
+// (csize divides nsplit; nsplit / csize <= 8 clusters merge through cpart)
+cudaError_t launch_attn_decode(const AttnDecodeArgs &a, int B, int nsplit, int csize, bool pdl, cudaStream_t s);
 // largest split count (= cluster size) of the decode attention kernel for
 // (head_dim, group) on the current device such that `units` clusters (one per
 // kv head and sequence) run at once
