@@ -1,0 +1,435 @@
+// Causal prefill attention on the 5th-generation tensor cores ("A transformer
+// from scratch", 12.3.5: scores q.k / sqrt(head_dim) over keys 0..p, softmax
+// with the running maximum subtracted, weighted sum of V; GQA maps query head
+// h to kv head h / (n_heads / n_kv_heads)).
+//
+// Flash-attention over 64-key tiles, one CTA per (128-query tile, query
+// head), f32 accuracy from bf16 operands: every operand x is split into
+// hi = bf16(x) and lo = bf16(x - hi), and each product is hi.hi + hi.lo +
+// lo.hi (three tcgen05.mma, f32 accumulation in TMEM), as in the GEMMs.
+//  * Per layer, k_pack_kv converts the cached K and V of the sequence into
+//    per-(kv head, 64-key tile) UMMA operand tiles (K as B of S = Q K^T,
+//    V transposed as B of O = P V), so attention CTAs fetch each tile with
+//    one bulk copy into a two-buffer ring.
+//  * The CTA packs its 128 query rows once; per key tile: S = Q K^T into 64
+//    TMEM columns; each thread owns one query row (its TMEM lane) and runs
+//    the online softmax on it without shuffles; P (hi/lo) goes to shared
+//    memory; O (in TMEM) is rescaled only where the row maximum moved; then
+//    O += P V. The row's 1/l scaling is applied when O is read back.
+//  * Every wait is bounded (1 s -> QW3_ERR_TIMEOUT, then the kernel drains
+//    and frees its tensor memory without waiting further).
+#include <cuda_bf16.h>
+
+#include "qw3_internal.cuh"
+
+namespace qw3 {
+
+namespace {
+
+constexpr int kQT = 128;          // queries per CTA (TMEM lanes)
+constexpr int kKT = 64;           // keys per tile
+constexpr int kPaThreads = 128;
+
+// Bytes of the packed operand tiles.
+template <int HD>
+struct PaSizes {
+    static constexpr uint32_t kq = (HD / 64) * 2 * (kQT * 128);   // Q: per 64-dim step hi + lo, 128 rows x 128 B
+    static constexpr uint32_t kk = (HD / 64) * 2 * (kKT * 128);   // K tile: per 64-dim step hi + lo, 64 rows
+    static constexpr uint32_t kv = 2 * (HD * 128);                // V^T tile: hi + lo, HD rows x 64 keys
+    static constexpr uint32_t kkv = kk + kv;                      // one packed (K, V) tile
+    static constexpr uint32_t kp = 2 * (kQT * 128);               // P: hi + lo, 128 rows x 64 keys
+    static constexpr uint32_t smem = kq + 2 * kkv + kp + 1024 + 256;
+};
+
+// Byte offset of element (row r, column k) in a K-major no-swizzle UMMA tile
+// of 64 columns: 8x8 core matrices (128 B), 8-row groups 1024 B apart.
+__device__ __forceinline__ uint32_t pa_core(int r, int k) {
+    return static_cast<uint32_t>((r >> 3) * 1024 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+
+__device__ __forceinline__ uint64_t pa_desc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128 >> 4) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46);
+}
+
+// kind::f16 instruction descriptor: f32 accumulate, bf16 A and B, K-major.
+__host__ __device__ constexpr uint32_t pa_idesc(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t bf16x2(float a, float b) {
+    const __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&p);
+}
+
+// hi/lo bf16 parts of 8 values as two uint4 (value j in halfword j).
+__device__ __forceinline__ void split8_hl(const float (&v)[8], uint4 &hi, uint4 &lo) {
+    float h[8], l[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        h[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+        l[i] = v[i] - h[i];
+    }
+    hi = make_uint4(bf16x2(h[0], h[1]), bf16x2(h[2], h[3]), bf16x2(h[4], h[5]), bf16x2(h[6], h[7]));
+    lo = make_uint4(bf16x2(l[0], l[1]), bf16x2(l[2], l[3]), bf16x2(l[4], l[5]), bf16x2(l[6], l[7]));
+}
+
+// Pack keys [0, ntiles * 64) of every kv head: thread = (head, tile, part, row,
+// 8-column group). Keys at or past ctx are zero.
+template <int HD>
+__global__ void k_pack_kv(const float *__restrict__ kc, const float *__restrict__ vc, size_t head_stride, int nkv,
+                          int ctx, int ntiles, uint8_t *__restrict__ dst) {
+    using Z = PaSizes<HD>;
+    constexpr int kItems = kKT * (HD / 8);   // K: rows x 8-dim groups (= V^T: HD rows x 8-key groups)
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t total = static_cast<int64_t>(nkv) * ntiles * 2 * kItems;
+    if (i >= total) return;
+    const int item = static_cast<int>(i % kItems);
+    const int part = static_cast<int>((i / kItems) % 2);
+    const int tile = static_cast<int>((i / (2 * kItems)) % ntiles);
+    const int g = static_cast<int>(i / (2 * static_cast<int64_t>(kItems) * ntiles));
+    uint8_t *t = dst + (static_cast<size_t>(g) * ntiles + tile) * Z::kkv;
+    float v[8];
+    uint4 hi, lo;
+    if (part == 0) {
+        // K: row = key, columns = dims
+        const int r = item / (HD / 8), d0 = (item % (HD / 8)) * 8;
+        const int key = tile * kKT + r;
+        const float *src = kc + static_cast<size_t>(g) * head_stride + static_cast<size_t>(key) * HD + d0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = key < ctx ? src[j] : 0.0f;
+        split8_hl(v, hi, lo);
+        const int s = d0 / 64, kk = d0 % 64;
+        uint8_t *base = t + s * 2 * (kKT * 128);
+        *reinterpret_cast<uint4 *>(base + pa_core(r, kk)) = hi;
+        *reinterpret_cast<uint4 *>(base + kKT * 128 + pa_core(r, kk)) = lo;
+    } else {
+        // V^T: row = dim, columns = keys
+        const int d = item / (kKT / 8), k0 = (item % (kKT / 8)) * 8;
+        const float *src = vc + static_cast<size_t>(g) * head_stride;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int key = tile * kKT + k0 + j;
+            v[j] = key < ctx ? src[static_cast<size_t>(key) * HD + d] : 0.0f;
+        }
+        split8_hl(v, hi, lo);
+        uint8_t *base = t + Z::kk;
+        *reinterpret_cast<uint4 *>(base + pa_core(d, k0)) = hi;
+        *reinterpret_cast<uint4 *>(base + HD * 128 + pa_core(d, k0)) = lo;
+    }
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+          "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+          "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+          "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+          "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+          "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
+// Three MMAs (hi.hi, hi.lo, lo.hi) over one 64-deep step: A at a_hi / a_lo,
+// B at b_hi / b_lo (each a K-major tile of 64 columns); accumulate unless
+// first.
+__device__ __forceinline__ void mma3(uint32_t tmem, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo,
+                                     uint32_t idesc, bool first) {
+#pragma unroll
+    for (int sub = 0; sub < 4; ++sub) {
+        const uint32_t off = sub * 256;
+        const uint32_t acc0 = (!first || sub > 0) ? 1u : 0u;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %3, 1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %2, %3, 1;\n\t}"
+            ::"r"(tmem), "l"(pa_desc(a_hi + off)), "l"(pa_desc(b_hi + off)), "r"(idesc), "r"(acc0),
+              "l"(pa_desc(b_lo + off)), "l"(pa_desc(a_lo + off))
+            : "memory");
+    }
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+template <int HD>
+__global__ void __launch_bounds__(kPaThreads, 1)
+    k_attn_prefill_tc(const float *__restrict__ qkv, int M, int qkv_stride, const uint8_t *__restrict__ kvpack,
+                      int ntiles, int pos0, int group, float scale, float *__restrict__ out, int32_t *status) {
+    using Z = PaSizes<HD>;
+    extern __shared__ __align__(1024) uint8_t pa_smem[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(pa_smem) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *Qs = base;                    // [HD/64][hi|lo] 128 x 64 tiles
+    uint8_t *KV0 = Qs + Z::kq;             // two packed (K, V^T) tiles
+    uint8_t *Ps = KV0 + 2 * Z::kkv;        // [hi|lo] 128 x 64
+    uint64_t *bars = reinterpret_cast<uint64_t *>(Ps + Z::kp);   // kv_full[2], s_done, o_done
+    uint64_t *kv_full = bars, *s_done = bars + 2, *o_done = bars + 3;
+    uint32_t *tbase = reinterpret_cast<uint32_t *>(bars + 4);
+    volatile int *err = reinterpret_cast<volatile int *>(tbase + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int qt = blockIdx.x, h = blockIdx.y, g = h / group;
+    const int row = tid;                                   // this thread's query (TMEM lane)
+    const int q = qt * kQT + row;                          // row of the chunk
+    const int qpos = pos0 + q;                             // its position
+    const int last_q = min(M - 1, qt * kQT + kQT - 1);
+    const int ntl = min(ntiles, (pos0 + last_q) / kKT + 1);   // key tiles this CTA needs
+    const uint8_t *kvg = kvpack + static_cast<size_t>(g) * ntiles * Z::kkv;
+
+    if (tid == 0) {
+        mbar_init(&kv_full[0], 1);
+        mbar_init(&kv_full[1], 1);
+        mbar_init(s_done, 1);
+        mbar_init(o_done, 1);
+        *err = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tbase)),
+                     "r"(256) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tbase;
+    const uint32_t tS = tmem, tO = tmem + 128;              // S: 64 columns, O: HD columns
+    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+
+    int last_issued[2] = {-1, -1};   // thread 0: the last tile fetched into each buffer
+    if (tid == 0) {
+        for (int j = 0; j < 2 && j < ntl; ++j) {
+            last_issued[j] = j;
+            mbar_arrive_expect_tx(&kv_full[j], Z::kkv);
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                         ::"r"(smem_u32(KV0 + j * Z::kkv)), "l"(kvg + static_cast<size_t>(j) * Z::kkv), "r"(Z::kkv),
+                           "r"(smem_u32(&kv_full[j]))
+                         : "memory");
+        }
+    }
+    // ---- this thread's query row -> Q tiles (hi / lo)
+    {
+        const float *src = qkv + static_cast<size_t>(q) * qkv_stride + static_cast<size_t>(h) * HD;
+#pragma unroll
+        for (int d0 = 0; d0 < HD; d0 += 8) {
+            float v[8];
+            if (q < M) {
+                const float4 a = *reinterpret_cast<const float4 *>(src + d0);
+                const float4 b = *reinterpret_cast<const float4 *>(src + d0 + 4);
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+            }
+            uint4 hi, lo;
+            split8_hl(v, hi, lo);
+            uint8_t *tq = Qs + (d0 / 64) * 2 * (kQT * 128);
+            *reinterpret_cast<uint4 *>(tq + pa_core(row, d0 % 64)) = hi;
+            *reinterpret_cast<uint4 *>(tq + kQT * 128 + pa_core(row, d0 % 64)) = lo;
+        }
+    }
+    fence_async_smem();
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+
+    constexpr uint32_t kIdS = pa_idesc(kQT, kKT), kIdO = pa_idesc(kQT, HD);
+    float m_run = -INFINITY, l_run = 0.0f;
+    for (int j = 0; j < ntl; ++j) {
+        const int buf = j & 1;
+        const uint8_t *KV = KV0 + buf * Z::kkv;
+        // ---- S = Q K_j^T (issued by one thread)
+        if (tid == 0) {
+            if (*err || !mbar_wait_bounded(&kv_full[buf], static_cast<uint32_t>((j >> 1) & 1))) {
+                *err = 1;
+            } else {
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+                for (int s = 0; s < HD / 64; ++s) {
+                    const uint32_t a = smem_u32(Qs + s * 2 * (kQT * 128));
+                    const uint32_t b = smem_u32(KV + s * 2 * (kKT * 128));
+                    mma3(tS, a, a + kQT * 128, b, b + kKT * 128, kIdS, s == 0);
+                }
+            }
+            mma_commit(s_done);
+        }
+        __syncwarp();
+        if (!mbar_wait_bounded(s_done, static_cast<uint32_t>(j & 1))) *err = 1;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        // ---- online softmax of this row over the tile's 64 keys
+        float sv[kKT];
+#pragma unroll
+        for (int c = 0; c < kKT; c += 16) {
+            float t16[16];
+            tmem_ld16(tS + lane_off + static_cast<uint32_t>(c), t16);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sv[c + e] = t16[e];
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kKT; ++c) {
+            const int key = j * kKT + c;
+            sv[c] = (key <= qpos) ? sv[c] * scale : -INFINITY;
+            mx = fmaxf(mx, sv[c]);
+        }
+        const float m_new = fmaxf(m_run, mx);
+        const float corr = (m_new == -INFINITY) ? 1.0f : expf(m_run - m_new);
+        float ps = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kKT; ++c) {
+            sv[c] = (sv[c] == -INFINITY) ? 0.0f : expf(sv[c] - m_new);
+            ps += sv[c];
+        }
+        l_run = fmaf(l_run, corr, ps);
+        m_run = m_new;
+        // ---- the previous O += P V must be complete before P and O change
+        if (j > 0) {
+            if (!mbar_wait_bounded(o_done, static_cast<uint32_t>((j - 1) & 1))) *err = 1;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            // its K/V buffer is free: fetch tile j + 1 into it
+            if (tid == 0 && j + 1 < ntl && !*err) {
+                const int nb = (j + 1) & 1;
+                last_issued[nb] = j + 1;
+                mbar_arrive_expect_tx(&kv_full[nb], Z::kkv);
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                    ::"r"(smem_u32(KV0 + nb * Z::kkv)), "l"(kvg + static_cast<size_t>(j + 1) * Z::kkv), "r"(Z::kkv),
+                      "r"(smem_u32(&kv_full[nb]))
+                    : "memory");
+            }
+            // rescale O where a row's maximum moved (warp-uniform skip)
+            if (__any_sync(0xffffffffu, corr != 1.0f)) {
+#pragma unroll
+                for (int c = 0; c < HD; c += 16) {
+                    float t16[16];
+                    tmem_ld16(tO + lane_off + static_cast<uint32_t>(c), t16);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) t16[e] *= corr;
+                    tmem_st16(tO + lane_off + static_cast<uint32_t>(c), t16);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+        }
+        // ---- P (hi / lo) of this row
+#pragma unroll
+        for (int c = 0; c < kKT; c += 8) {
+            const float v8[8] = {sv[c], sv[c + 1], sv[c + 2], sv[c + 3], sv[c + 4], sv[c + 5], sv[c + 6], sv[c + 7]};
+            uint4 hi, lo;
+            split8_hl(v8, hi, lo);
+            *reinterpret_cast<uint4 *>(Ps + pa_core(row, c)) = hi;
+            *reinterpret_cast<uint4 *>(Ps + kQT * 128 + pa_core(row, c)) = lo;
+        }
+        fence_async_smem();
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();
+        // ---- O += P V_j
+        if (tid == 0) {
+            if (!*err) {
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t a = smem_u32(Ps);
+                const uint32_t b = smem_u32(KV + Z::kk);
+                mma3(tO, a, a + kQT * 128, b, b + HD * 128, kIdO, j == 0);
+            }
+            mma_commit(o_done);
+        }
+        __syncwarp();
+    }
+    // ---- O / l of this row to global memory
+    if (ntl > 0) {
+        if (!mbar_wait_bounded(o_done, static_cast<uint32_t>((ntl - 1) & 1))) *err = 1;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    }
+    const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+    float *dst = out + static_cast<size_t>(q) * (static_cast<size_t>(gridDim.y) * HD) + static_cast<size_t>(h) * HD;
+#pragma unroll
+    for (int c = 0; c < HD; c += 16) {
+        float t16[16];
+        tmem_ld16(tO + lane_off + static_cast<uint32_t>(c), t16);
+        if (q < M && ntl > 0) {
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+                *reinterpret_cast<float4 *>(dst + c + e) =
+                    make_float4(t16[e] * inv, t16[e + 1] * inv, t16[e + 2] * inv, t16[e + 3] * inv);
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && *err) {
+        record_status(status, QW3_ERR_TIMEOUT);
+        // copies that may still be in flight (bounded)
+        for (int b = 0; b < 2; ++b)
+            if (last_issued[b] >= 0)
+                (void)mbar_wait_bounded(&kv_full[b], static_cast<uint32_t>((last_issued[b] >> 1) & 1));
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
+}
+
+template <int HD>
+cudaError_t launch_pa_t(const float *qkv, int M, int qkv_stride, const float *kc, const float *vc,
+                        size_t head_stride, int pos0, int nh, int nkv, float scale, float *out, uint8_t *kvpack,
+                        int32_t *status, cudaStream_t s) {
+    using Z = PaSizes<HD>;
+    const int ctx = pos0 + M;
+    const int ntiles = (ctx + kKT - 1) / kKT;
+    const int64_t items = static_cast<int64_t>(nkv) * ntiles * 2 * kKT * (HD / 8);
+    k_pack_kv<HD><<<static_cast<unsigned>((items + 255) / 256), 256, 0, s>>>(kc, vc, head_stride, nkv, ctx, ntiles,
+                                                                              kvpack);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const dim3 grid((M + kQT - 1) / kQT, nh);
+    k_attn_prefill_tc<HD><<<grid, kPaThreads, Z::smem, s>>>(qkv, M, qkv_stride, kvpack, ntiles, pos0, nh / nkv,
+                                                            scale, out, status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attn_prefill_tc_pack_bytes(int hd, int nkv, int max_seq_len) {
+    const size_t ntiles = (static_cast<size_t>(max_seq_len) + kKT - 1) / kKT;
+    const size_t tile = hd == 128 ? PaSizes<128>::kkv : PaSizes<64>::kkv;
+    return static_cast<size_t>(nkv) * ntiles * tile;
+}
+
+cudaError_t configure_attn_prefill_tc() {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_prefill_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(PaSizes<128>::smem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attn_prefill_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(PaSizes<64>::smem));
+    return e;
+}
+
+cudaError_t launch_attn_prefill_tc(const float *qkv, int M, int qkv_stride, const float *kv, size_t layer_off,
+                                   size_t seq_off, size_t kvsel_stride, size_t head_stride, int pos0, int nh, int nkv,
+                                   int hd, float scale, float *out, uint8_t *kvpack, int32_t *status, cudaStream_t s) {
+    const float *kc = kv + layer_off + seq_off;
+    const float *vc = kc + kvsel_stride;
+    if (hd == 128) return launch_pa_t<128>(qkv, M, qkv_stride, kc, vc, head_stride, pos0, nh, nkv, scale, out, kvpack,
+                                           status, s);
+    if (hd == 64) return launch_pa_t<64>(qkv, M, qkv_stride, kc, vc, head_stride, pos0, nh, nkv, scale, out, kvpack,
+                                         status, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace qw3

@@ -67,6 +67,7 @@ cudaError_t configure_all() {
         if (e == cudaSuccess) e = configure_misc();
         if (e == cudaSuccess) e = configure_mega();
         if (e == cudaSuccess) e = configure_gemm_tc();
+        if (e == cudaSuccess) e = configure_attn_prefill_tc();
         g_cfg_err = e;
     });
     return g_cfg_err;
@@ -127,6 +128,7 @@ struct qw3_model {
     // prefill scratch
     float *px = nullptr, *ph = nullptr, *pqkv = nullptr, *po = nullptr, *pact = nullptr;
     uint8_t *apack = nullptr;   // tensor-core GEMM input, packed (nullptr: CUDA-core GEMM only)
+    uint8_t *kvpack = nullptr;  // K/V operand tiles of the tensor-core prefill attention (nullptr: CUDA cores)
 
     std::map<int, cudaGraphExec_t> graphs;
 
@@ -827,6 +829,10 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
     if (e == cudaSuccess) e = A(reinterpret_cast<void **>(&m->pact), P * I * 4);
     if (e != cudaSuccess) return bail(cuda_err(m, e, "scratch allocation"));
     if (int rc = setup_tensor_core_gemm(m)) return bail(rc);
+    if (c.max_prefill >= kAttnPrefillTcMinRows && (hd == 64 || hd == 128)) {
+        e = model_alloc(m, reinterpret_cast<void **>(&m->kvpack), attn_prefill_tc_pack_bytes(hd, nkv, c.max_seq_len));
+        if (e != cudaSuccess) return bail(cuda_err(m, e, "prefill attention packing buffer"));
+    }
     if (int rc = setup_mega(m, w, on_dev, staging)) return bail(rc);
     e = cudaMemsetAsync(m->done_counter, 0, 64, m->stream);
     if (e == cudaSuccess && m->attn_ccnt) e = cudaMemsetAsync(m->attn_ccnt, 0, 64 * 4, m->stream);
@@ -875,8 +881,14 @@ int qw3_prefill(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n,
             M_TRY(m, launch_qk_rope_append(m->pqkv, M, m->qkv_w, L.q_norm, L.k_norm, c.rms_eps, m->rope, nullptr, seq,
                                            nullptr, pos0, kvl, m->seq_stride, m->kvsel_stride, m->head_stride, nh,
                                            nkv, hd, s));
-            M_TRY(m, launch_attn_prefill(m->pqkv, M, m->qkv_w, kvl, 0, static_cast<size_t>(seq) * m->seq_stride,
-                                         m->kvsel_stride, m->head_stride, pos0, nh, nkv, hd, scale, m->po, s));
+            if (m->kvpack && M >= kAttnPrefillTcMinRows) {
+                M_TRY(m, launch_attn_prefill_tc(m->pqkv, M, m->qkv_w, kvl, 0, static_cast<size_t>(seq) * m->seq_stride,
+                                                m->kvsel_stride, m->head_stride, pos0, nh, nkv, hd, scale, m->po,
+                                                m->kvpack, m->d_status, s));
+            } else {
+                M_TRY(m, launch_attn_prefill(m->pqkv, M, m->qkv_w, kvl, 0, static_cast<size_t>(seq) * m->seq_stride,
+                                             m->kvsel_stride, m->head_stride, pos0, nh, nkv, hd, scale, m->po, s));
+            }
             M_TRY(m, launch_gemm(m->po, M, qw, L.o, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack));
             M_TRY(m, launch_rmsnorm_rows(m->px, M, H, L.ffn_norm, c.rms_eps, m->ph, s));
             M_TRY(m, launch_gemm(m->ph, M, H, L.gu, m->pact, GEMV_SWIGLU, nullptr, nullptr, s, m->d_status, m->apack));

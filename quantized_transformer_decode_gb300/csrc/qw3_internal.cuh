@@ -189,6 +189,15 @@ cudaError_t launch_attn_prefill(const float *qkv, int M, int qkv_stride, const f
                                 size_t layer_off, size_t seq_off, size_t kvsel_stride,
                                 size_t head_stride, int pos0, int nh, int nkv, int hd,
                                 float scale, float *out, cudaStream_t s);
+// Causal prefill attention on tensor cores (attn_prefill_tc.cu): packs the
+// sequence's K/V of the layer into kvpack (attn_prefill_tc_pack_bytes) and
+// runs one CTA per (128-query tile, head); for chunks of >= 128 rows.
+constexpr int kAttnPrefillTcMinRows = 128;
+size_t attn_prefill_tc_pack_bytes(int hd, int nkv, int max_seq_len);
+cudaError_t configure_attn_prefill_tc();
+cudaError_t launch_attn_prefill_tc(const float *qkv, int M, int qkv_stride, const float *kv, size_t layer_off,
+                                   size_t seq_off, size_t kvsel_stride, size_t head_stride, int pos0, int nh, int nkv,
+                                   int hd, float scale, float *out, uint8_t *kvpack, int32_t *status, cudaStream_t s);
 cudaError_t launch_argmax_finalize(unsigned long long *key, int B, const DecodeIO *io,
                                    int32_t *next_token, int32_t *step_ctr, int32_t *pos_inc,
                                    int32_t *status, cudaStream_t s);
