@@ -8,6 +8,8 @@
 // vocabulary (packed (value, index) keys, lowest index on ties).
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "qw3_internal.cuh"
 
 namespace qw3 {
@@ -133,10 +135,10 @@ __global__ void __launch_bounds__(256) k_gemm(const float *__restrict__ A, int M
 
 cudaError_t launch_gemm(const float *A, int M, int K, const QMat &W, float *C, int mode,
                         unsigned long long *argmax_key, const DecodeIO *io, cudaStream_t s, int32_t *status,
-                        uint8_t *apack) {
+                        uint8_t *apack, const GemmSplitK *sk) {
     if (M <= 0) return cudaSuccess;
     if (apack && gemm_tc_supported(M, K, W))
-        return launch_gemm_tc(A, M, K, W, C, mode, argmax_key, io, status, apack, s);
+        return launch_gemm_tc(A, M, K, W, C, mode, argmax_key, io, status, apack, s, sk);
     dim3 grid((W.rows + BN - 1) / BN, (M + BM - 1) / BM);
     switch (mode) {
         case GEMV_STORE: k_gemm<GEMV_STORE><<<grid, 256, 0, s>>>(A, M, K, W, W.rows, W.rows_pad, C, nullptr, nullptr); break;
@@ -267,7 +269,7 @@ template <int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__restrict__ Ap, int M, int K,
                                                            const uint8_t *__restrict__ Wp, int N, float *C,
                                                            unsigned long long *__restrict__ argmax_key,
-                                                           const DecodeIO *io, int32_t *status) {
+                                                           const DecodeIO *io, int32_t *status, float *ws) {
     extern __shared__ __align__(1024) uint8_t tc_smem[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_smem) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(base + TC_STAGES * TC_STAGE);   // [3]
@@ -279,7 +281,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__rest
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mt = blockIdx.y, nt = blockIdx.x;
-    const int ksteps = K / TC_BK;
+    // split K over gridDim.z CTAs (small M: too few output tiles to fill the
+    // GPU); each takes a contiguous run of k-steps
+    const int ksteps_all = K / TC_BK;
+    const int kz = blockIdx.z, nks = gridDim.z;
+    const int kb = static_cast<int>(static_cast<int64_t>(kz) * ksteps_all / nks);
+    const int ksteps = static_cast<int>(static_cast<int64_t>(kz + 1) * ksteps_all / nks) - kb;
     if (tid == 0) {
         for (int i = 0; i < TC_STAGES; ++i) {
             mbar_init(&full[i], 1);
@@ -315,10 +322,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__rest
             uint8_t *sb = base + st * TC_STAGE;
             mbar_arrive_expect_tx(&full[st], TC_STAGE);
             asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                         ::"r"(smem_u32(sb)), "l"(Ap + ut_tile(mt, ks, ksteps)), "r"(TC_PAIR), "r"(smem_u32(&full[st]))
+                         ::"r"(smem_u32(sb)), "l"(Ap + ut_tile(mt, kb + ks, ksteps_all)), "r"(TC_PAIR),
+                           "r"(smem_u32(&full[st]))
                          : "memory");
             asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                         ::"r"(smem_u32(sb + TC_PAIR)), "l"(Wp + ut_tile(nt, ks, ksteps)), "r"(TC_PAIR),
+                         ::"r"(smem_u32(sb + TC_PAIR)), "l"(Wp + ut_tile(nt, kb + ks, ksteps_all)), "r"(TC_PAIR),
                            "r"(smem_u32(&full[st]))
                          : "memory");
         }
@@ -377,33 +385,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__rest
     const int row = 32 * warp + lane;
     const int m = mt * TC_BM + row;
     unsigned long long best = 0ull;
-    for (int c0 = 0; c0 < TC_BN; c0 += 16) {
-        uint32_t r[16];
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * warp) << 16) + static_cast<uint32_t>(c0);
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-            "tcgen05.wait::ld.sync.aligned;"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-            : "r"(taddr)
-            : "memory");
-        if (m >= M || *err) continue;
+    auto emit = [&](const float (&v)[16], int c0) {
+        if (m >= M || *err) return;
         const int nb = nt * TC_BN + c0;
         if (MODE == GEMV_SWIGLU) {
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
                 const int n = nb + j;
-                if (n < N) {
-                    const float g = __uint_as_float(r[j]), u = __uint_as_float(r[j + 1]);
-                    C[static_cast<size_t>(m) * (N / 2) + n / 2] = g / (1.0f + expf(-g)) * u;
-                }
+                if (n < N) C[static_cast<size_t>(m) * (N / 2) + n / 2] = v[j] / (1.0f + expf(-v[j])) * v[j + 1];
             }
         } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int n = nb + j;
                 if (n < N) {
-                    const float y = __uint_as_float(r[j]);
+                    const float y = v[j];
                     float *c = C ? C + static_cast<size_t>(m) * N + n : nullptr;
                     if (MODE == GEMV_STORE) *c = y;
                     else if (MODE == GEMV_RESID) *c += y;
@@ -415,6 +411,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__rest
                 }
             }
         }
+    };
+    const int Np = gridDim.x * TC_BN;   // workspace row stride
+    for (int c0 = 0; c0 < TC_BN; c0 += 16) {
+        uint32_t r[16];
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * warp) << 16) + static_cast<uint32_t>(c0);
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+            "tcgen05.wait::ld.sync.aligned;"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(taddr)
+            : "memory");
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+        if (nks > 1) {
+            // this split's partial tile (valid rows) to the workspace [z][m][n]
+            if (m >= M) continue;
+            float4 *w4 = reinterpret_cast<float4 *>(
+                ws + (static_cast<size_t>(kz) * gridDim.y * TC_BM + static_cast<size_t>(m)) * Np + nt * TC_BN + c0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) w4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        } else {
+            emit(v, c0);
+        }
     }
     if (MODE == GEMV_ARGMAX && m < M && best) atomicMax(&argmax_key[m], best);
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -423,11 +444,61 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__rest
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_BN) : "memory");
 }
 
+// Sum of the K splits of a tensor-core GEMM in split order (deterministic),
+// then the epilogue: thread = (row, 4 columns).
+template <int MODE>
+__global__ void k_splitk_reduce(const float *__restrict__ ws, int nks, int M, int N, int Np, int Mp, float *C) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int cols4 = N / 4;
+    if (i >= static_cast<int64_t>(M) * cols4) return;
+    const int m = static_cast<int>(i / cols4), n = static_cast<int>(i % cols4) * 4;
+    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int z = 0; z < nks; ++z) {
+        const float4 t = __ldcg(reinterpret_cast<const float4 *>(ws + (static_cast<size_t>(z) * Mp + m) * Np + n));
+        v.x += t.x;
+        v.y += t.y;
+        v.z += t.z;
+        v.w += t.w;
+    }
+    if (MODE == GEMV_SWIGLU) {
+        float *c = C + static_cast<size_t>(m) * (N / 2) + n / 2;
+        c[0] = v.x / (1.0f + expf(-v.x)) * v.y;
+        c[1] = v.z / (1.0f + expf(-v.z)) * v.w;
+    } else {
+        float4 *c = reinterpret_cast<float4 *>(C + static_cast<size_t>(m) * N + n);
+        if (MODE == GEMV_RESID) {
+            const float4 o = *c;
+            v.x += o.x;
+            v.y += o.y;
+            v.z += o.z;
+            v.w += o.w;
+        }
+        *c = v;
+    }
+}
+
 template <int MODE>
 cudaError_t launch_tc_mode(const uint8_t *Ap, int M, int K, const uint8_t *Wp, int N, float *C,
-                           unsigned long long *argmax_key, const DecodeIO *io, int32_t *status, cudaStream_t s) {
-    const dim3 grid((N + TC_BN - 1) / TC_BN, (M + TC_BM - 1) / TC_BM);
-    k_gemm_tc<MODE><<<grid, TC_THREADS, TC_SMEM, s>>>(Ap, M, K, Wp, N, C, argmax_key, io, status);
+                           unsigned long long *argmax_key, const DecodeIO *io, int32_t *status,
+                           const GemmSplitK *sk, cudaStream_t s) {
+    const int nt = (N + TC_BN - 1) / TC_BN, mt = (M + TC_BM - 1) / TC_BM, ksteps = K / TC_BK;
+    // split K while the output tiles leave SMs idle (>= 4 k-steps per split,
+    // partials within the workspace); the reduction is its own kernel
+    int nks = 1;
+    if (MODE != GEMV_ARGMAX && sk && sk->ws && nt * mt < num_sms() && N % 4 == 0) {
+        nks = (num_sms() + nt * mt - 1) / (nt * mt);
+        nks = std::min(nks, ksteps / 4);
+        while (nks > 1 && static_cast<size_t>(nks) * mt * TC_BM * nt * TC_BN > sk->ws_floats) --nks;
+        if (nks < 1) nks = 1;
+    }
+    const dim3 grid(nt, mt, nks);
+    k_gemm_tc<MODE><<<grid, TC_THREADS, TC_SMEM, s>>>(Ap, M, K, Wp, N, C, argmax_key, io, status,
+                                                      nks > 1 ? sk->ws : nullptr);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || nks == 1) return e;
+    const int64_t items = static_cast<int64_t>(M) * (N / 4);
+    k_splitk_reduce<MODE><<<static_cast<unsigned>((items + 255) / 256), 256, 0, s>>>(sk->ws, nks, M, N, nt * TC_BN,
+                                                                                      mt * TC_BM, C);
     return cudaGetLastError();
 }
 
@@ -458,7 +529,7 @@ cudaError_t launch_pack_w(const QMat &W, uint8_t *dst, cudaStream_t s) {
 
 cudaError_t launch_gemm_tc(const float *A, int M, int K, const QMat &W, float *C, int mode,
                            unsigned long long *argmax_key, const DecodeIO *io, int32_t *status, uint8_t *apack,
-                           cudaStream_t s) {
+                           cudaStream_t s, const GemmSplitK *sk) {
     if (M <= 0) return cudaSuccess;
     {
         const int rows = (M + TC_BM - 1) / TC_BM * TC_BM;
@@ -468,10 +539,10 @@ cudaError_t launch_gemm_tc(const float *A, int M, int K, const QMat &W, float *C
         if (e != cudaSuccess) return e;
     }
     switch (mode) {
-        case GEMV_STORE: return launch_tc_mode<GEMV_STORE>(apack, M, K, W.ut, W.rows, C, argmax_key, io, status, s);
-        case GEMV_RESID: return launch_tc_mode<GEMV_RESID>(apack, M, K, W.ut, W.rows, C, argmax_key, io, status, s);
-        case GEMV_SWIGLU: return launch_tc_mode<GEMV_SWIGLU>(apack, M, K, W.ut, W.rows, C, argmax_key, io, status, s);
-        case GEMV_ARGMAX: return launch_tc_mode<GEMV_ARGMAX>(apack, M, K, W.ut, W.rows, C, argmax_key, io, status, s);
+        case GEMV_STORE: return launch_tc_mode<GEMV_STORE>(apack, M, K, W.ut, W.rows, C, argmax_key, io, status, sk, s);
+        case GEMV_RESID: return launch_tc_mode<GEMV_RESID>(apack, M, K, W.ut, W.rows, C, argmax_key, io, status, sk, s);
+        case GEMV_SWIGLU: return launch_tc_mode<GEMV_SWIGLU>(apack, M, K, W.ut, W.rows, C, argmax_key, io, status, sk, s);
+        case GEMV_ARGMAX: return launch_tc_mode<GEMV_ARGMAX>(apack, M, K, W.ut, W.rows, C, argmax_key, io, status, sk, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -129,6 +129,7 @@ struct qw3_model {
     float *px = nullptr, *ph = nullptr, *pqkv = nullptr, *po = nullptr, *pact = nullptr;
     uint8_t *apack = nullptr;   // tensor-core GEMM input, packed (nullptr: CUDA-core GEMM only)
     uint8_t *kvpack = nullptr;  // K/V operand tiles of the tensor-core prefill attention (nullptr: CUDA cores)
+    GemmSplitK gsk;             // split-K workspace of the small-M tensor-core GEMMs
 
     std::map<int, cudaGraphExec_t> graphs;
 
@@ -327,7 +328,7 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
             M_TRY(m, launch_gemv(a, GEMV_STORE, pdl, s));
         } else {
             M_TRY(m, launch_rmsnorm_rows(m->x, B, H, L.attn_norm, c.rms_eps, m->h, s));
-            M_TRY(m, launch_gemm(m->h, B, H, L.qkv, m->qkv, GEMV_STORE, nullptr, nullptr, s, m->d_status, m->apack));
+            M_TRY(m, launch_gemm(m->h, B, H, L.qkv, m->qkv, GEMV_STORE, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
         }
         AttnDecodeArgs at{};
         at.qkv = m->qkv; at.qkv_stride = m->qkv_w; at.q_norm = L.q_norm; at.k_norm = L.k_norm; at.eps = c.rms_eps;
@@ -355,10 +356,10 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
             dn.trace = tr();
             M_TRY(m, launch_gemv(dn, GEMV_RESID, pdl, s));
         } else {
-            M_TRY(m, launch_gemm(m->o, B, qw, L.o, m->x, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack));
+            M_TRY(m, launch_gemm(m->o, B, qw, L.o, m->x, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
             M_TRY(m, launch_rmsnorm_rows(m->x, B, H, L.ffn_norm, c.rms_eps, m->h, s));
-            M_TRY(m, launch_gemm(m->h, B, H, L.gu, m->act, GEMV_SWIGLU, nullptr, nullptr, s, m->d_status, m->apack));
-            M_TRY(m, launch_gemm(m->act, B, I, L.down, m->x, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack));
+            M_TRY(m, launch_gemm(m->h, B, H, L.gu, m->act, GEMV_SWIGLU, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
+            M_TRY(m, launch_gemm(m->act, B, I, L.down, m->x, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
         }
     }
     if (gv) {
@@ -371,7 +372,7 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
         M_TRY(m, launch_gemv(a, GEMV_ARGMAX, pdl, s));
     } else {
         M_TRY(m, launch_rmsnorm_rows(m->x, B, H, m->out_norm, c.rms_eps, m->h, s));
-        M_TRY(m, launch_gemm(m->h, B, H, m->out, nullptr, GEMV_ARGMAX, m->argmax_key, m->d_io, s, m->d_status, m->apack));
+        M_TRY(m, launch_gemm(m->h, B, H, m->out, nullptr, GEMV_ARGMAX, m->argmax_key, m->d_io, s, m->d_status, m->apack, &m->gsk));
         M_TRY(m, launch_argmax_finalize(m->argmax_key, B, m->d_io, m->d_tok, m->d_step, m->d_pos, m->d_status, s));
     }
     return QW3_OK;
@@ -433,6 +434,9 @@ int setup_tensor_core_gemm(qw3_model *m) {
     const int rows = std::max(c.max_prefill, c.max_seqs);
     const int kmax = std::max(H, std::max(qw, I));
     M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&m->apack), ut_bytes(rows, kmax)));
+    // split-K partials of products with few output tiles (batched decode, short prefill chunks)
+    m->gsk.ws_floats = static_cast<size_t>(4) << 20;
+    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&m->gsk.ws), m->gsk.ws_floats * 4));
     M_TRY(m, cudaStreamSynchronize(m->stream));
     return QW3_OK;
 }
@@ -877,7 +881,7 @@ int qw3_prefill(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n,
             const LayerDev &L = m->layers[l];
             float *kvl = m->kv + static_cast<size_t>(l) * m->layer_stride;
             M_TRY(m, launch_rmsnorm_rows(m->px, M, H, L.attn_norm, c.rms_eps, m->ph, s));
-            M_TRY(m, launch_gemm(m->ph, M, H, L.qkv, m->pqkv, GEMV_STORE, nullptr, nullptr, s, m->d_status, m->apack));
+            M_TRY(m, launch_gemm(m->ph, M, H, L.qkv, m->pqkv, GEMV_STORE, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
             M_TRY(m, launch_qk_rope_append(m->pqkv, M, m->qkv_w, L.q_norm, L.k_norm, c.rms_eps, m->rope, nullptr, seq,
                                            nullptr, pos0, kvl, m->seq_stride, m->kvsel_stride, m->head_stride, nh,
                                            nkv, hd, s));
@@ -889,10 +893,10 @@ int qw3_prefill(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n,
                 M_TRY(m, launch_attn_prefill(m->pqkv, M, m->qkv_w, kvl, 0, static_cast<size_t>(seq) * m->seq_stride,
                                              m->kvsel_stride, m->head_stride, pos0, nh, nkv, hd, scale, m->po, s));
             }
-            M_TRY(m, launch_gemm(m->po, M, qw, L.o, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack));
+            M_TRY(m, launch_gemm(m->po, M, qw, L.o, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
             M_TRY(m, launch_rmsnorm_rows(m->px, M, H, L.ffn_norm, c.rms_eps, m->ph, s));
-            M_TRY(m, launch_gemm(m->ph, M, H, L.gu, m->pact, GEMV_SWIGLU, nullptr, nullptr, s, m->d_status, m->apack));
-            M_TRY(m, launch_gemm(m->pact, M, I, L.down, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack));
+            M_TRY(m, launch_gemm(m->ph, M, H, L.gu, m->pact, GEMV_SWIGLU, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
+            M_TRY(m, launch_gemm(m->pact, M, I, L.down, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
         }
         if (off + M == n && (last_logits_dev || argmax_dev)) {
             GemvArgs a{};

@@ -165,13 +165,19 @@ cudaError_t launch_embed(const int32_t *tokens, int n, const QMat &E, float *x, 
 // prefill / batched path
 cudaError_t launch_rmsnorm_rows(const float *x, int M, int K, const float *w, float eps, float *y,
                                 cudaStream_t s);
+// Workspace of the split-K tensor-core GEMM: partial tiles [split][M][N].
+struct GemmSplitK {
+    float *ws = nullptr;
+    size_t ws_floats = 0;
+};
+
 // Dense contraction C[M][N] = A[M][K] . W[N][K]^T with the GEMV epilogue
 // modes; tensor cores (tcgen05) from kGemmTcMinRows rows, CUDA cores below.
 // apack: scratch for the packed activations (ut_bytes(M, K)); nullptr keeps
-// the CUDA-core path.
+// the CUDA-core path. sk (nullable): lets small-M products split K.
 cudaError_t launch_gemm(const float *A, int M, int K, const QMat &W, float *C, int mode,
                         unsigned long long *argmax_key, const DecodeIO *io, cudaStream_t s,
-                        int32_t *status = nullptr, uint8_t *apack = nullptr);
+                        int32_t *status = nullptr, uint8_t *apack = nullptr, const GemmSplitK *sk = nullptr);
 constexpr int kGemmTcMinRows = 32;
 bool gemm_tc_supported(int M, int K, const QMat &W);
 size_t ut_bytes(int rows, int K);   // bytes of a matrix packed into bf16 hi/lo UMMA tiles
@@ -179,7 +185,7 @@ cudaError_t configure_gemm_tc();
 cudaError_t launch_pack_w(const QMat &W, uint8_t *dst, cudaStream_t s);
 cudaError_t launch_gemm_tc(const float *A, int M, int K, const QMat &W, float *C, int mode,
                            unsigned long long *argmax_key, const DecodeIO *io, int32_t *status, uint8_t *apack,
-                           cudaStream_t s);
+                           cudaStream_t s, const GemmSplitK *sk = nullptr);
 cudaError_t launch_qk_rope_append(float *qkv, int M, int qkv_stride, const float *q_norm,
                                   const float *k_norm, float eps, const float2 *rope,
                                   const int32_t *row_seq, int seq0, const int32_t *row_pos, int pos0,
