@@ -490,8 +490,8 @@ def run_prefill(a, w: inputs.Workload):
                          "frac": achieved / tf_peak,
                          "peak_source": f"{peak_kind} bf16 sustained (MEASURED_PEAKS.json bf16_tflops_sustained)",
                          "note": "achieved counts the model's FLOPs (linear + causal attention + last-row lm_head); "
-                                 "the GEMMs run as three bf16 MMAs per product (hi/lo split for f32 accuracy) and "
-                                 "the causal attention on CUDA cores",
+                                 "the GEMMs and the causal attention (chunks of 128+ rows) run as three bf16 MMAs "
+                                 "per product (hi/lo split for f32 accuracy)",
                          "algorithmic_flops_per_step": flops, "traffic": None},
             "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
             "gpu_launches": launches_per_step * a.steps, "cpu_baseline": None,

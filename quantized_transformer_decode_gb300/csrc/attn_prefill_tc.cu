@@ -13,7 +13,7 @@
 //    one bulk copy into a two-buffer ring.
 //  * The CTA packs its 128 query rows once; per key tile: S = Q K^T into 64
 //    TMEM columns; each thread owns one query row (its TMEM lane) and runs
-//    the online softmax on it without shuffles; P (hi/lo) goes to shared
+//    the online softmax on it without shuffles (in base 2); P (hi/lo) goes to shared
 //    memory; O (in TMEM) is rescaled only where the row maximum moved; then
 //    O += P V. The row's 1/l scaling is applied when O is read back.
 //  * Every wait is bounded (1 s -> QW3_ERR_TIMEOUT, then the kernel drains
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kPaThreads, 1)
     volatile int *err = reinterpret_cast<volatile int *>(tbase + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int qt = blockIdx.x, h = blockIdx.y, g = h / group;
+    const int qt = gridDim.x - 1 - blockIdx.x, h = blockIdx.y, g = h / group;   // late (heavy) query tiles first
     const int row = tid;                                   // this thread's query (TMEM lane)
     const int q = qt * kQT + row;                          // row of the chunk
     const int qpos = pos0 + q;                             // its position
@@ -253,6 +253,8 @@ __global__ void __launch_bounds__(kPaThreads, 1)
     __syncthreads();
 
     constexpr uint32_t kIdS = pa_idesc(kQT, kKT), kIdO = pa_idesc(kQT, HD);
+    // softmax in base 2: exp(x) = 2^(x log2 e), scores pre-scaled by log2 e
+    const float scale2 = scale * 1.4426950408889634f;
     float m_run = -INFINITY, l_run = 0.0f;
     for (int j = 0; j < ntl; ++j) {
         const int buf = j & 1;
@@ -288,15 +290,15 @@ __global__ void __launch_bounds__(kPaThreads, 1)
 #pragma unroll
         for (int c = 0; c < kKT; ++c) {
             const int key = j * kKT + c;
-            sv[c] = (key <= qpos) ? sv[c] * scale : -INFINITY;
+            sv[c] = (key <= qpos) ? sv[c] * scale2 : -INFINITY;
             mx = fmaxf(mx, sv[c]);
         }
         const float m_new = fmaxf(m_run, mx);
-        const float corr = (m_new == -INFINITY) ? 1.0f : expf(m_run - m_new);
+        const float corr = (m_new == -INFINITY) ? 1.0f : exp2f(m_run - m_new);
         float ps = 0.0f;
 #pragma unroll
         for (int c = 0; c < kKT; ++c) {
-            sv[c] = (sv[c] == -INFINITY) ? 0.0f : expf(sv[c] - m_new);
+            sv[c] = (sv[c] == -INFINITY) ? 0.0f : exp2f(sv[c] - m_new);
             ps += sv[c];
         }
         l_run = fmaf(l_run, corr, ps);
