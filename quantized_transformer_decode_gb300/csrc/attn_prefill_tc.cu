@@ -14,7 +14,8 @@
 //  * The CTA packs its 128 query rows once; per key tile: S = Q K^T into 64
 //    TMEM columns; each thread owns one query row (its TMEM lane) and runs
 //    the online softmax on it without shuffles (in base 2); P (hi/lo) goes to shared
-//    memory; O (in TMEM) is rescaled only where the row maximum moved; then
+//    memory; O (in TMEM) is rescaled only where the row's reference maximum
+//    moved (it trails the true maximum by at most 8 in base 2); then
 //    O += P V. The row's 1/l scaling is applied when O is read back.
 //  * Every wait is bounded (1 s -> QW3_ERR_TIMEOUT, then the kernel drains
 //    and frees its tensor memory without waiting further).
@@ -293,8 +294,11 @@ __global__ void __launch_bounds__(kPaThreads, 1)
             sv[c] = (key <= qpos) ? sv[c] * scale2 : -INFINITY;
             mx = fmaxf(mx, sv[c]);
         }
-        const float m_new = fmaxf(m_run, mx);
-        const float corr = (m_new == -INFINITY) ? 1.0f : exp2f(m_run - m_new);
+        // The reference maximum moves only when the tile's maximum exceeds it
+        // by more than 8 (probabilities up to 2^8 are exact to represent and
+        // cancel in O / l): most tiles then need no rescale of O.
+        const float m_new = (mx > m_run + 8.0f) ? mx : m_run;
+        const float corr = (m_new == m_run || m_new == -INFINITY) ? 1.0f : exp2f(m_run - m_new);
         float ps = 0.0f;
 #pragma unroll
         for (int c = 0; c < kKT; ++c) {
