@@ -178,9 +178,12 @@ constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 64;
 constexpr int TC_THREADS = 128;
 constexpr uint32_t TC_OPERAND = 128 * TC_BK * 2;            // 16 KB: one bf16 operand tile
 constexpr uint32_t TC_PAIR = 2 * TC_OPERAND;                // hi + lo
-constexpr uint32_t TC_STAGE = 2 * TC_PAIR;                  // A pair + W pair
-constexpr int TC_STAGES = 3;
-constexpr uint32_t TC_SMEM = TC_STAGES * TC_STAGE + 2048;   // + barriers, alignment slack
+// NH = 128-column halves of the output tile (1: 128 x 128, 2: 128 x 256 with
+// the A tile shared by two N=128 products): a stage holds the A pair and NH
+// W pairs; three stages for NH = 1, two for NH = 2.
+template <int NH> __host__ __device__ constexpr uint32_t tc_stage() { return (1 + NH) * TC_PAIR; }
+template <int NH> __host__ __device__ constexpr int tc_stages() { return NH == 1 ? 3 : 2; }
+template <int NH> __host__ __device__ constexpr uint32_t tc_smem() { return tc_stages<NH>() * tc_stage<NH>() + 2048; }
 
 __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
     // start >> 4; leading byte offset 128 (next 8-deep K core); stride byte
@@ -265,15 +268,18 @@ __global__ void k_pack_act(const float *__restrict__ A, int M, int K, uint8_t *_
     *reinterpret_cast<uint4 *>(t + TC_OPERAND + core_off(r % TC_BM, k % TC_BK)) = lo;
 }
 
-template <int MODE>
+template <int MODE, int NH>
 __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__restrict__ Ap, int M, int K,
                                                            const uint8_t *__restrict__ Wp, int N, float *C,
                                                            unsigned long long *__restrict__ argmax_key,
                                                            const DecodeIO *io, int32_t *status, float *ws) {
     extern __shared__ __align__(1024) uint8_t tc_smem[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_smem) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(base + TC_STAGES * TC_STAGE);   // [3]
-    uint64_t *empty = full + TC_STAGES;                                             // [3]
+    constexpr int TC_STAGES = tc_stages<NH>();
+    constexpr uint32_t TC_STAGE = tc_stage<NH>();
+    constexpr int BNE = TC_BN * NH;                                                 // output columns per CTA
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + TC_STAGES * TC_STAGE);   // [TC_STAGES]
+    uint64_t *empty = full + TC_STAGES;                                             // [TC_STAGES]
     uint64_t *done = empty + TC_STAGES;                                             // [1]
     uint32_t *tbase = reinterpret_cast<uint32_t *>(done + 1);
     volatile int *err = reinterpret_cast<volatile int *>(tbase + 1);
@@ -298,7 +304,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__rest
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tbase)),
-                     "r"(TC_BN) : "memory");
+                     "r"(BNE) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -325,10 +331,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__rest
                          ::"r"(smem_u32(sb)), "l"(Ap + ut_tile(mt, kb + ks, ksteps_all)), "r"(TC_PAIR),
                            "r"(smem_u32(&full[st]))
                          : "memory");
-            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                         ::"r"(smem_u32(sb + TC_PAIR)), "l"(Wp + ut_tile(nt, kb + ks, ksteps_all)), "r"(TC_PAIR),
-                           "r"(smem_u32(&full[st]))
-                         : "memory");
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+                asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                             ::"r"(smem_u32(sb + (1 + h) * TC_PAIR)), "l"(Wp + ut_tile(nt * NH + h, kb + ks, ksteps_all)),
+                               "r"(TC_PAIR), "r"(smem_u32(&full[st]))
+                             : "memory");
         }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer
@@ -342,19 +350,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__rest
             }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t a_hi = smem_u32(base + st * TC_STAGE), a_lo = a_hi + TC_OPERAND;
-            const uint32_t w_hi = a_hi + TC_PAIR, w_lo = w_hi + TC_OPERAND;
 #pragma unroll
-            for (int sub = 0; sub < TC_BK / 16; ++sub) {
-                const uint32_t off = sub * 256;   // two 8-deep K cores per 16-deep step
-                const uint32_t acc0 = (ks > 0 || sub > 0) ? 1u : 0u;
-                asm volatile(
-                    "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                    "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
-                    "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %3, 1;\n\t"
-                    "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %2, %3, 1;\n\t}"
-                    ::"r"(tmem), "l"(umma_desc(a_hi + off)), "l"(umma_desc(w_hi + off)), "r"(kTcIdesc), "r"(acc0),
-                      "l"(umma_desc(w_lo + off)), "l"(umma_desc(a_lo + off))
-                    : "memory");
+            for (int h = 0; h < NH; ++h) {
+                // output columns 128 h.. of the tile from W pair h (TMEM columns 128 h..)
+                const uint32_t w_hi = a_hi + (1 + h) * TC_PAIR, w_lo = w_hi + TC_OPERAND;
+                const uint32_t th = tmem + static_cast<uint32_t>(TC_BN * h);
+#pragma unroll
+                for (int sub = 0; sub < TC_BK / 16; ++sub) {
+                    const uint32_t off = sub * 256;   // two 8-deep K cores per 16-deep step
+                    const uint32_t acc0 = (ks > 0 || sub > 0) ? 1u : 0u;
+                    asm volatile(
+                        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %3, 1;\n\t"
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %2, %3, 1;\n\t}"
+                        ::"r"(th), "l"(umma_desc(a_hi + off)), "l"(umma_desc(w_hi + off)), "r"(kTcIdesc), "r"(acc0),
+                          "l"(umma_desc(w_lo + off)), "l"(umma_desc(a_lo + off))
+                        : "memory");
+                }
             }
             asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                              smem_u32(&empty[st]))
@@ -387,7 +400,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__rest
     unsigned long long best = 0ull;
     auto emit = [&](const float (&v)[16], int c0) {
         if (m >= M || *err) return;
-        const int nb = nt * TC_BN + c0;
+        const int nb = nt * BNE + c0;
         if (MODE == GEMV_SWIGLU) {
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
@@ -412,8 +425,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__rest
             }
         }
     };
-    const int Np = gridDim.x * TC_BN;   // workspace row stride
-    for (int c0 = 0; c0 < TC_BN; c0 += 16) {
+    const int Np = gridDim.x * BNE;   // workspace row stride
+    for (int c0 = 0; c0 < BNE; c0 += 16) {
         uint32_t r[16];
         const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * warp) << 16) + static_cast<uint32_t>(c0);
         asm volatile(
@@ -430,7 +443,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__rest
             // this split's partial tile (valid rows) to the workspace [z][m][n]
             if (m >= M) continue;
             float4 *w4 = reinterpret_cast<float4 *>(
-                ws + (static_cast<size_t>(kz) * gridDim.y * TC_BM + static_cast<size_t>(m)) * Np + nt * TC_BN + c0);
+                ws + (static_cast<size_t>(kz) * gridDim.y * TC_BM + static_cast<size_t>(m)) * Np + nt * BNE + c0);
 #pragma unroll
             for (int j = 0; j < 4; ++j) w4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         } else {
@@ -441,7 +454,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__rest
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_BN) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BNE) : "memory");
 }
 
 // Sum of the K splits of a tensor-core GEMM in split order (deterministic),
@@ -481,23 +494,31 @@ template <int MODE>
 cudaError_t launch_tc_mode(const uint8_t *Ap, int M, int K, const uint8_t *Wp, int N, float *C,
                            unsigned long long *argmax_key, const DecodeIO *io, int32_t *status,
                            const GemmSplitK *sk, cudaStream_t s) {
-    const int nt = (N + TC_BN - 1) / TC_BN, mt = (M + TC_BM - 1) / TC_BM, ksteps = K / TC_BK;
+    const int wt = (N + TC_BN - 1) / TC_BN, mt = (M + TC_BM - 1) / TC_BM, ksteps = K / TC_BK;
+    // 128 x 256 tiles (A shared by two W tiles) where enough of them fill the
+    // GPU; 128 x 128 otherwise
+    const bool wide = wt % 2 == 0 && (wt / 2) * mt >= num_sms();
+    const int nt = wide ? wt / 2 : wt, bne = wide ? 2 * TC_BN : TC_BN;
     // split K while the output tiles leave SMs idle (>= 4 k-steps per split,
     // partials within the workspace); the reduction is its own kernel
     int nks = 1;
     if (MODE != GEMV_ARGMAX && sk && sk->ws && nt * mt < num_sms() && N % 4 == 0) {
         nks = (num_sms() + nt * mt - 1) / (nt * mt);
         nks = std::min(nks, ksteps / 4);
-        while (nks > 1 && static_cast<size_t>(nks) * mt * TC_BM * nt * TC_BN > sk->ws_floats) --nks;
+        while (nks > 1 && static_cast<size_t>(nks) * mt * TC_BM * nt * bne > sk->ws_floats) --nks;
         if (nks < 1) nks = 1;
     }
     const dim3 grid(nt, mt, nks);
-    k_gemm_tc<MODE><<<grid, TC_THREADS, TC_SMEM, s>>>(Ap, M, K, Wp, N, C, argmax_key, io, status,
-                                                      nks > 1 ? sk->ws : nullptr);
+    if (wide)
+        k_gemm_tc<MODE, 2><<<grid, TC_THREADS, tc_smem<2>(), s>>>(Ap, M, K, Wp, N, C, argmax_key, io, status,
+                                                                nks > 1 ? sk->ws : nullptr);
+    else
+        k_gemm_tc<MODE, 1><<<grid, TC_THREADS, tc_smem<1>(), s>>>(Ap, M, K, Wp, N, C, argmax_key, io, status,
+                                                                nks > 1 ? sk->ws : nullptr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || nks == 1) return e;
     const int64_t items = static_cast<int64_t>(M) * (N / 4);
-    k_splitk_reduce<MODE><<<static_cast<unsigned>((items + 255) / 256), 256, 0, s>>>(sk->ws, nks, M, N, nt * TC_BN,
+    k_splitk_reduce<MODE><<<static_cast<unsigned>((items + 255) / 256), 256, 0, s>>>(sk->ws, nks, M, N, nt * bne,
                                                                                       mt * TC_BM, C);
     return cudaGetLastError();
 }
@@ -505,10 +526,17 @@ cudaError_t launch_tc_mode(const uint8_t *Ap, int M, int K, const uint8_t *Wp, i
 }  // namespace
 
 cudaError_t configure_gemm_tc() {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<GEMV_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<GEMV_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<GEMV_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<GEMV_ARGMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+    cudaError_t e = cudaSuccess;
+#define QW3_TC_CFG(MODE)                                                                                          \
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<MODE, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                                    static_cast<int>(tc_smem<1>()));                                \
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<MODE, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                                    static_cast<int>(tc_smem<2>()));
+    QW3_TC_CFG(GEMV_STORE)
+    QW3_TC_CFG(GEMV_RESID)
+    QW3_TC_CFG(GEMV_SWIGLU)
+    QW3_TC_CFG(GEMV_ARGMAX)
+#undef QW3_TC_CFG
     return e;
 }
 
