@@ -171,6 +171,13 @@ cudaError_t launch_gemm(const float *A, int M, int K, const QMat &W, float *C, i
 // issues the 12 MMAs of a step and commits them to the stage's "empty"
 // barrier. CTA tile 128 x 128, accumulator in 128 TMEM columns; the epilogue
 // (store / residual / SwiGLU pairs / argmax keys) reads it with 32x32b loads.
+// Where 128 x 256 tiles still fill the GPU (long prefills), a CTA takes two
+// W tiles per K step against one A tile (96 KB per step, 2 stages, 256 TMEM
+// columns): a CTA's bulk copies complete at a roughly fixed rate, so sharing
+// A raises the work per byte copied. Where the tiles cannot fill the GPU
+// (batched decode), K is split over several CTAs that write f32 partial tiles
+// to a workspace; k_splitk_reduce sums them in split order and applies the
+// epilogue.
 // ===========================================================================
 namespace {
 
