@@ -225,6 +225,11 @@ def run_reference(a, w: inputs.Workload):
     if w.decode_steps == 0:
         print(json.dumps({"impl": "reference", "unavailable": "prefill workload has no oracle decode arm"}))
         return 0
+    s = w.shape
+    if s.n_layers * (s.hidden * (2 * s.q_width + 2 * s.kv_width) + 3 * s.hidden * s.intermediate) > 1e9:
+        print(json.dumps({"impl": "reference", "unavailable": "the f64 oracle of a model past 1e9 weights takes "
+                                                               "~10 min to build on the host; not a bounded run"}))
+        return 0
     steps, warm = a.steps, a.warmup
     # Batched workloads: one sequence of the batch stands for the step's cost per token.
     P = min(w.prompt_len, 512) if w.batch > 1 else w.prompt_len
@@ -415,12 +420,18 @@ def run_decode(a, w: inputs.Workload):
                                      "step_us": tot / 1e3, "kernels": ks}
     if rank == 0:
         cb = None
-        if not a.no_cpu_baseline and world >= 1:
+        big = s.n_layers * (s.hidden * (2 * s.q_width + 2 * s.kv_width) + 3 * s.hidden * s.intermediate) > 1e9
+        if big and not a.no_cpu_baseline:
+            # not a bounded sample: building the f64 oracle of this model takes ~10 minutes on the host
+            line["cpu_baseline_note"] = ("skipped for models past 1e9 weights (the oracle alone takes ~10 min to "
+                                         "build); the 0.6B line carries the CPU baseline")
+        elif not a.no_cpu_baseline and world >= 1:
             n_cpu = a.cpu_steps
-            secs, n = oracle_decode(w, 0, n_cpu, P if B == 1 else min(P, 512))
+            pre = P if B == 1 else min(P, 512)
+            secs, n = oracle_decode(w, 0, n_cpu, pre)
             cb = {"value": n / secs, "unit": "tok/s", "cores": oracle_cores(), "kind": "oracle",
-                  "sample": f"oracle (f64 numpy) greedy decode at B=1 after an untimed {P if B == 1 else min(P, 512)}"
-                            f"-token prefill: {n} timed steps"}
+                  "sample": f"oracle (f64 numpy) greedy decode at B=1 after an untimed {pre}-token prefill: {n} timed "
+                            f"steps"}
         line["cpu_baseline"] = cb
         print(json.dumps(line), flush=True)
     model.close()
