@@ -261,7 +261,9 @@ def workload_config(w: inputs.Workload, steps: int) -> dict:
                        f"prefill {w.prompt_len} tokens untimed, then greedy decode at B={w.batch}",
            "batch": w.batch, "prompt_len": w.prompt_len, "timed_positions": [w.prompt_len, w.prompt_len + steps - 1],
            "weights": f"Q8_0, {weight_bytes_per_step(s) / 1e6:.1f} MB streamed per step", "kv_cache": "f32",
-           "l2": "inputs larger than L2 (the Q8_0 weights streamed every step exceed the 129 MB L2)"}
+           "l2": ("inputs larger than L2 (the Q8_0 weights streamed every step exceed the 129 MB L2)"
+                  if weight_bytes_per_step(s) > 129e6 else
+                  "inputs smaller than L2: the weights stay L2-resident between steps (a small test case)")}
     return cfg
 
 
