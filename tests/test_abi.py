@@ -124,3 +124,17 @@ def test_model_calls_reject_null_model(L):
     assert L.qw3_decode(None, 1, None, 16, None, None, None) == 1
     assert L.qw3_destroy(None) == 0
     assert L.qw3_stream(None) is None
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No fallback: with the shared library absent the binding raises instead
+    of computing anything on the CPU."""
+    import os
+    import subprocess
+    import sys
+    code = ("import quantized_transformer_decode_gb300.qw3 as q\n"
+            "try:\n    q.lib()\nexcept RuntimeError as e:\n    print('raised', e)\n")
+    env = dict(os.environ, QW3_LIB=str(tmp_path / "absent" / "libqw3.so"))
+    p = subprocess.run([sys.executable, "-c", code], cwd=str(ROOT), env=env, capture_output=True, text=True,
+                       timeout=120)
+    assert p.returncode == 0 and p.stdout.startswith("raised") and "not built" in p.stdout
