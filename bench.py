@@ -291,7 +291,7 @@ def run_decode(a, w: inputs.Workload):
     s, B, P = w.shape, w.batch, w.prompt_len
     K, W = a.steps, a.warmup
     cap = P + max(K, 1) + W + 2
-    flags = qw3.QW3_FLAG_PERSISTENT if a.persistent else qw3.QW3_FLAG_TRACE
+    flags = qw3.QW3_FLAG_PER_KERNEL if a.per_kernel else 0
     model = qw3.Qw3Model.from_f32(s, inputs.iter_weights(s, w.seed), max_seqs=B, max_seq_len=cap,
                                   max_prefill=min(P, 4096), flags=flags)
     persistent, launches_per_step = model.decode_plan(B)
@@ -378,9 +378,9 @@ def run_decode(a, w: inputs.Workload):
     del h_tok, h_out
     torch.cuda.synchronize()
 
-    gpu_launches = 1 if persistent else launches_per_step * K
-    kernel_desc = ("k_decode_mega: one persistent launch runs all K timed steps (every layer, attention, lm_head "
-                   "and argmax); its duration is the timed region" if persistent else
+    gpu_launches = launches_per_step * K
+    kernel_desc = ("k_step: one persistent launch per decode step (embedding, every layer's projections, "
+                   "attention, FFN, lm_head and argmax)" if persistent else
                    "decode step (per-kernel path: Q8_0 GEMVs, attention, embedding, lm_head + argmax)")
     line = {
         "metric": METRIC if w.name == "qwen3-0.6b-decode" else f"{w.name} decode tok/s",
@@ -394,7 +394,7 @@ def run_decode(a, w: inputs.Workload):
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_step": alg_bytes / K,
-                     "traffic": profiled_traffic("k_decode_mega" if persistent else "decode_step")},
+                     "traffic": profiled_traffic("k_step" if persistent else "decode_step")},
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "e2e": {"value": e2e_val, "unit": "tok/s", "h2d_bytes_per_step": 4 * B, "d2h_bytes_per_step": 4 * B,
                 "how": "per step: pinned host token -> device, qw3_decode, argmax -> pinned host, stream sync",
@@ -524,8 +524,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="qwen3-0.6b-decode", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--cpu-steps", type=int, default=8, help="oracle decode steps timed for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--persistent", action="store_true",
-                    help="batch-1 decode through the persistent decode kernel (one launch per call)")
+    ap.add_argument("--per-kernel", action="store_true",
+                    help="batch-1 decode through the per-kernel chain instead of the persistent step kernel")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")

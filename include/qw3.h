@@ -96,9 +96,14 @@ typedef struct qw3_config {
 #define QW3_FLAG_NO_GRAPH 0x1  /* launch decode kernels directly, no CUDA graph */
 #define QW3_FLAG_NO_PDL   0x2  /* no programmatic dependent launch               */
 #define QW3_FLAG_TRACE    0x4  /* record timestamps of decode steps          */
-#define QW3_FLAG_PERSISTENT 0x8 /* batch-1 decode through the persistent decode
-                                  kernel (one launch per call) instead of one
-                                  launch per kernel of each step              */
+#define QW3_FLAG_PER_KERNEL 0x8 /* batch-1 decode through the per-kernel
+                                  chain (one launch per projection and
+                                  attention) instead of the persistent
+                                  decode-step kernel                          */
+#define QW3_FLAG_TEST_NO_WAIT 0x10 /* testing only: a wait on another CTA's
+                                  data in the decode-step kernel gives up at
+                                  its first miss (QW3_ERR_TIMEOUT) instead
+                                  of after 1 s                                */
 
 /* One decoder layer (minfer section 1). Q8_0 matrices [out][in]:
  *   attn_q [n_heads*head_dim][H], attn_k and attn_v [n_kv_heads*head_dim][H],
@@ -176,28 +181,26 @@ QW3_API int qw3_debug_read_kv(qw3_model *m, int32_t layer, int32_t seq, int32_t 
                       int32_t n, float *k_out_dev, float *v_out_dev);
 
 /* Timestamps recorded when the model was created with QW3_FLAG_TRACE, in
- * records of 8 u64 (%globaltimer ns unless stated).
- * Per-kernel decode path (the default; B > 1 always): the most recent step;
- * for each kernel, in launch order, two records (its first and its last CTA):
- * entry, after the wait for the previous kernel, after the prologue, after the
- * weight/KV stream, exit, two kernel-specific words, SM id.
- * Persistent batch-1 kernel (QW3_FLAG_PERSISTENT): the last step of the most recent call, for two
- * CTAs (slot 0: the first CTA of KV head group 0; slot 1: the last CTA), each
- * 2L+1 records: per layer an attention record (block start, QKV done, q/k/v
- * gathered, scores done, values done, partials combined, o_proj done) and an
- * FFN record (block start, normed, gate/up done, channels gathered, down
- * done), then an lm_head record (start, normed, lm_head done, token known);
- * then one record per CTA of wait totals over the whole call (ring waits,
- * grid-sync waits, cluster-sync waits, producer waits for free slots), entry,
- * exit, cluster id, SM id.
+ * records of 8 u64.
+ * Per-kernel decode path (QW3_FLAG_PER_KERNEL at batch 1; B > 1 always): the
+ * most recent step; for each kernel, in launch order, two records (its first
+ * and its last CTA): entry, after the wait for the previous kernel, after the
+ * prologue, after the weight/KV stream, exit, two kernel-specific words, SM
+ * id (%globaltimer ns).
+ * Persistent step kernel (batch 1, the default): the most recent step, as a
+ * flat array of u64 words. With P = 6 * n_layers + 2 phases, for the first
+ * and then the last CTA, 4 * P + 64 words: per phase (0 = step start, 6 l + k
+ * for phase k = 1..6 of layer l, P - 1 = lm_head) inputs staged, first weight
+ * chunk in, dot products done, outputs published (SM cycle counter), then the
+ * issue and the take times of the first 32 ring chunks; after both, 16 words
+ * per CTA for layer 1 (%globaltimer ns).
  * out_host receives min(max_records, available) records; *n_out is the
  * number written. Synchronises the model's stream. */
 QW3_API int qw3_debug_read_trace(qw3_model *m, uint64_t *out_host, int32_t max_records, int32_t *n_out);
 
 /* How decode calls of batch B run: *persistent = 1 when they use the
- * persistent decode kernel (one kernel launch per qw3_decode or
- * qw3_generate_greedy call, whatever the step count), else 0 and
- * *launches_per_step kernels per decode step. */
+ * persistent decode-step kernel (one cooperative launch per step; then
+ * *launches_per_step = 1), else 0 and *launches_per_step kernels per step. */
 QW3_API int qw3_decode_plan(const qw3_model *m, int32_t B, int32_t *persistent,
                             int32_t *launches_per_step);
 

@@ -23,7 +23,7 @@
 #include <vector>
 
 #include "qw3_internal.cuh"
-#include "decode_mega.cuh"
+#include "decode_step.cuh"
 
 namespace qw3 {
 
@@ -65,7 +65,7 @@ cudaError_t configure_all() {
         cudaError_t e = configure_gemv();
         if (e == cudaSuccess) e = configure_attention();
         if (e == cudaSuccess) e = configure_misc();
-        if (e == cudaSuccess) e = configure_mega();
+        if (e == cudaSuccess) e = configure_step();
         if (e == cudaSuccess) e = configure_gemm_tc();
         if (e == cudaSuccess) e = configure_attn_prefill_tc();
         g_cfg_err = e;
@@ -137,11 +137,10 @@ struct qw3_model {
     unsigned long long *trace = nullptr;
     int trace_kernels = 0;
 
-    // persistent batch-1 decode kernel (decode_mega.cu)
-    bool mega = false;
-    MegaParams mp{};
-    int mega_trace_records = 0;
-    int32_t *d_first = nullptr;
+    // persistent batch-1 decode-step kernel (decode_step.cu)
+    bool step = false;
+    StepParams sp{};
+    int step_trace_words = 0;
 };
 
 namespace {
@@ -441,183 +440,81 @@ int setup_tensor_core_gemm(qw3_model *m) {
     return QW3_OK;
 }
 
-// ---- persistent batch-1 decode kernel: plan, weight copies, launch
+// ---- persistent batch-1 decode-step kernel: buffers and plan
 
-size_t align128h(size_t v) { return (v + 127) / 128 * 128; }
-
-// Shared-memory layout of the persistent kernel for NC clusters; false if it
-// does not fit.
-bool mega_layout(MegaParams &P, int max_seq_len) {
-    const int H = P.H, G = P.G, hd = P.hd;
-    int kt_max = 0;
-    for (int c = 0; c < P.NC; ++c) {
-        const int a = (c * P.act_units / P.NC) * 32, b = ((c + 1) * P.act_units / P.NC) * 32;
-        kt_max = std::max(kt_max, b - a);
-    }
-    const int apc_max = kt_max / P.CS;
-    P.maxpos = (max_seq_len + P.CS - 1) / P.CS + 2;
-    size_t off = 0;
-    auto take = [&](uint32_t &o, size_t bytes) {
-        o = static_cast<uint32_t>(off);
-        off = align128h(off + bytes);
-    };
-    take(P.o_bar, 512);
-    take(P.o_x, static_cast<size_t>(H) * 4);
-    take(P.o_xn, static_cast<size_t>(H) * 3 + static_cast<size_t>(H) / 32 * 4);
-    take(P.o_wbuf, static_cast<size_t>(H) * 4);
-    take(P.o_qkvpub, static_cast<size_t>(P.RPC) * 4);
-    take(P.o_qkv, static_cast<size_t>(P.RG) * 4);
-    take(P.o_scores, static_cast<size_t>(G) * P.maxpos * 4);
-    take(P.o_apub, static_cast<size_t>(G) * (hd + 4) * 4);
-    take(P.o_vred, static_cast<size_t>(8) * G * hd * 4);
-    take(P.o_oall, static_cast<size_t>(G) * hd * 3 + static_cast<size_t>(G) * hd / 32 * 4);
-    take(P.o_guout, static_cast<size_t>(2) * apc_max * 4);
-    take(P.o_actpub, static_cast<size_t>(apc_max) * 4);
-    P.o_act_cap = kt_max;
-    take(P.o_act, static_cast<size_t>(kt_max) * 3 + static_cast<size_t>(kt_max) / 32 * 4);
-    take(P.o_red, 1024);
-    P.o_ring = static_cast<uint32_t>(off);
-    const size_t tbH = static_cast<size_t>(H) * 17 / 2;
-    size_t sb = tbH * std::max<size_t>(1, 28672 / tbH);
-    sb = align128h(sb);
-    P.SB = static_cast<uint32_t>(sb);
-    if (static_cast<size_t>(kMegaMaxSmem) < off + 2 * sb) return false;
-    P.NS = static_cast<int>(std::min<size_t>(16, (kMegaMaxSmem - off) / sb));
-    return P.NS >= 2;
-}
-
-int setup_mega(qw3_model *m, const qw3_weights *w, bool on_dev, uint8_t *staging) {
+// Set up the step kernel unless the model opts out or its shape is not
+// covered; the per-kernel path then serves batch 1 too.
+int setup_step(qw3_model *m) {
     const qw3_config &c = m->cfg;
-    if (!(c.flags & QW3_FLAG_PERSISTENT)) return QW3_OK;
-    const int H = c.hidden, hd = c.head_dim, nh = c.n_heads, nkv = c.n_kv_heads, I = c.intermediate;
-    const int G = nh / nkv, CS = kMegaCS;
-    const int RG = (G + 2) * hd;
-    if (!mega_supported_heads(hd, G) || H > 4096 || H % 256 || RG % (8 * CS) || RG > 8 * 256 || I % 32 || I / 32 < nkv) return QW3_OK;
-    // it streams gate/up and the lm_head as whole-row tiles (8 x H)
-    if (m->layers.empty() || m->layers[0].gu.kt != H || m->out.kt != H) return QW3_OK;
-    // per-layer arrays must sit at one stride (they do: every layer has the same sizes)
-    for (int l = 1; l < c.n_layers; ++l) {
-        const LayerDev &a = m->layers[l - 1], &b = m->layers[l];
-        const ptrdiff_t st = m->layers[1].gu.base - m->layers[0].gu.base;
-        if (b.gu.base - a.gu.base != st ||
-            reinterpret_cast<const uint8_t *>(b.attn_norm) - reinterpret_cast<const uint8_t *>(a.attn_norm) != st ||
-            reinterpret_cast<const uint8_t *>(b.ffn_norm) - reinterpret_cast<const uint8_t *>(a.ffn_norm) != st ||
-            reinterpret_cast<const uint8_t *>(b.q_norm) - reinterpret_cast<const uint8_t *>(a.q_norm) != st ||
-            reinterpret_cast<const uint8_t *>(b.k_norm) - reinterpret_cast<const uint8_t *>(a.k_norm) != st)
-            return QW3_OK;
-    }
-    MegaParams P{};
-    P.L = c.n_layers; P.H = H; P.I = I; P.V = c.vocab; P.hd = hd; P.G = G;
-    P.NA = nkv; P.CS = CS; P.RG = RG; P.RPC = RG / CS; P.ORPC = H / CS; P.o_groups = H / 8;
-    P.act_units = I / 32;
+    if ((c.flags & QW3_FLAG_PER_KERNEL) || !step_supported(c)) return QW3_OK;
+    StepParams P{};
+    P.L = c.n_layers;
+    P.H = c.hidden;
+    P.I = c.intermediate;
+    P.V = c.vocab;
+    P.nh = c.n_heads;
+    P.nkv = c.n_kv_heads;
+    P.hd = c.head_dim;
+    P.G = c.n_heads / c.n_kv_heads;
+    P.qkv_w = m->qkv_w;
     P.eps = c.rms_eps;
-    P.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(hd)));
-    int nc = std::min(16, P.act_units);
-    for (int iter = 0; iter < 4; ++iter) {
-        P.NC = nc;
-        P.NCTA = nc * CS;
-        if (!mega_layout(P, c.max_seq_len)) return QW3_OK;
-        int maxc = 0;
-        if (mega_max_clusters(P, &maxc) != cudaSuccess) {
-            cudaGetLastError();
-            return QW3_OK;
-        }
-        if (maxc >= nc) break;
-        nc = maxc;
-        if (nc < nkv) return QW3_OK;
-    }
-    if (P.NC < nkv) return QW3_OK;
-    int maxc = 0;
-    if (mega_max_clusters(P, &maxc) != cudaSuccess || maxc < P.NC) {
-        cudaGetLastError();
-        return QW3_OK;
-    }
-
-    // weight copies in the streamed layouts
-    const int qw = nh * hd;
-    QMat qkv_m = qmat_shape(nkv * RG, H, H, 0);
-    QMat o_m = qmat_shape(H, qw, G * hd, 1);
-    const size_t b_qkv = align_up(qm_bytes(qkv_m), 256), b_o = align_up(qm_bytes(o_m), 256);
-    const size_t b_down = align_up(static_cast<size_t>(H) * I / 32 * 34, 256);
-    const size_t per_layer = b_qkv + b_o + b_down;
-    uint8_t *arena = nullptr;
-    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&arena), per_layer * c.n_layers));
-    M_TRY(m, cudaMemsetAsync(arena, 0, per_layer * c.n_layers, m->stream));
-    const size_t qrow = static_cast<size_t>(H / 32) * 34;
-    for (int l = 0; l < c.n_layers; ++l) {
-        const qw3_layer_weights &lw = w->layers[l];
-        const LayerDev &L = m->layers[l];
-        uint8_t *base = arena + per_layer * l;
-        qkv_m.base = base;
-        o_m.base = base + b_qkv;
-        uint8_t *down = base + b_qkv + b_o;
-        const uint8_t *raw = nullptr;
-        if (int rc = raw_on_device(m, lw.attn_q, qw, H, on_dev, staging, &raw)) return rc;
-        for (int g = 0; g < nkv; ++g)
-            M_TRY(m, launch_repack(raw + static_cast<size_t>(g) * G * hd * qrow, G * hd, H, qkv_m, g * RG, 1, m->stream));
-        if (int rc = raw_on_device(m, lw.attn_k, nkv * hd, H, on_dev, staging, &raw)) return rc;
-        for (int g = 0; g < nkv; ++g)
-            M_TRY(m, launch_repack(raw + static_cast<size_t>(g) * hd * qrow, hd, H, qkv_m, g * RG + G * hd, 1, m->stream));
-        if (int rc = raw_on_device(m, lw.attn_v, nkv * hd, H, on_dev, staging, &raw)) return rc;
-        for (int g = 0; g < nkv; ++g)
-            M_TRY(m, launch_repack(raw + static_cast<size_t>(g) * hd * qrow, hd, H, qkv_m, g * RG + (G + 1) * hd, 1,
-                                   m->stream));
-        if (int rc = raw_on_device(m, lw.attn_output, H, qw, on_dev, staging, &raw)) return rc;
-        M_TRY(m, launch_repack(raw, H, qw, o_m, 0, 1, m->stream));
-        if (int rc = raw_on_device(m, lw.ffn_down, H, I, on_dev, staging, &raw)) return rc;
-        M_TRY(m, launch_repack_colpart(raw, H, I, P.NC, down, m->stream));
-        M_TRY(m, cudaStreamSynchronize(m->stream));
-        (void)L;
-    }
-    P.qkv0 = arena;
-    P.o0 = arena + b_qkv;
-    P.down0 = arena + b_qkv + b_o;
-    P.mstride = per_layer;
-    P.gu0 = m->layers[0].gu.base;
-    P.attn_norm0 = m->layers[0].attn_norm;
-    P.q_norm0 = m->layers[0].q_norm;
-    P.k_norm0 = m->layers[0].k_norm;
-    P.ffn_norm0 = m->layers[0].ffn_norm;
-    P.wstride = c.n_layers > 1 ? static_cast<size_t>(m->layers[1].gu.base - m->layers[0].gu.base) : 0;
-    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&P.opart), static_cast<size_t>(P.NA) * H * 4));
-    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&P.dpart), static_cast<size_t>(P.NC) * H * 4));
-    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&P.gctr), 256));
-    P.key = reinterpret_cast<unsigned long long *>(reinterpret_cast<uint8_t *>(P.gctr) + 64);
-    if (c.flags & QW3_FLAG_TRACE) {
-        m->mega_trace_records = 2 * (2 * P.L + 1) + P.NCTA;
-        const size_t tb = static_cast<size_t>(m->mega_trace_records) * 64;
-        M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&P.trace), tb));
-        M_TRY(m, cudaMemsetAsync(P.trace, 0, tb, m->stream));
-    }
+    P.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(c.head_dim)));
     P.embd = m->embd;
     P.out = m->out;
     P.out_norm = m->out_norm;
+    if (!step_plan(P, m->layers[0])) return QW3_OK;
+    LayerDev *dl = nullptr;
+    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&dl), sizeof(LayerDev) * c.n_layers));
+    M_TRY(m, cudaMemcpyAsync(dl, m->layers.data(), sizeof(LayerDev) * c.n_layers, cudaMemcpyHostToDevice, m->stream));
+    P.layers = dl;
     P.rope = m->rope;
     P.kv = m->kv;
     P.seq_stride = m->seq_stride;
     P.kvsel_stride = m->kvsel_stride;
     P.head_stride = m->head_stride;
     P.layer_stride = m->layer_stride;
+    P.seq_ids = m->d_seq;
+    P.pos = m->d_pos;
+    P.tok = m->d_tok;
+    P.step_ctr = m->d_step;
+    P.io = m->d_io;
+    P.argmax_key = m->argmax_key;
+    P.done_counter = m->done_counter;
     P.status = m->d_status;
-    m->mp = P;
-    m->mega = true;
-    return QW3_OK;
-}
-
-// One launch of the persistent kernel: n_steps greedy steps of sequence seq
-// from position pos0, first input token at first_tok (device).
-int run_mega(qw3_model *m, int seq, int pos0, int n_steps, const int32_t *first_tok, int32_t *hist, float *logits,
-             int32_t *argmax_out) {
-    MegaParams P = m->mp;
-    P.seq = seq;
-    P.pos0 = pos0;
-    P.n_steps = n_steps;
-    P.first_token = first_tok;
-    P.hist = hist;
-    P.logits = logits;
-    P.argmax_out = argmax_out;
-    M_TRY(m, cudaMemsetAsync(P.gctr, 0, 256, m->stream));
-    M_TRY(m, launch_mega(P, m->stream));
+    P.wait_ns = (c.flags & QW3_FLAG_TEST_NO_WAIT) ? 0ull : kWaitLimitNs;
+    // exchange buffers, arrival counters (zero), the epoch and the abort word
+    const size_t floats = static_cast<size_t>(P.H) + P.qkv_w + static_cast<size_t>(P.nkv) * P.S * P.G * (P.hd + 2) +
+                          static_cast<size_t>(P.nh) * P.hd + P.I + 64;
+    float *fb = nullptr;
+    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&fb), floats * 8));
+    M_TRY(m, cudaMemsetAsync(fb, 0, floats * 8, m->stream));
+    auto take = [&](size_t n) {   // room for one 64-bit word per value
+        float *r = fb;
+        fb += (n + 3) / 4 * 8;
+        return r;
+    };
+    P.xb = take(P.H);
+    P.qkvb = take(P.qkv_w);
+    P.partb = take(static_cast<size_t>(P.nkv) * P.S * P.G * (P.hd + 2));
+    P.ob = take(static_cast<size_t>(P.nh) * P.hd);
+    P.actb = take(P.I);
+    const size_t cbytes = static_cast<size_t>(step_counters(P.nkv)) * 128 + 256;
+    unsigned *ew = nullptr;
+    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&ew), cbytes));
+    M_TRY(m, cudaMemsetAsync(ew, 0, cbytes, m->stream));
+    const unsigned init[2] = {1u, 0u};
+    M_TRY(m, cudaMemcpyAsync(ew, init, sizeof init, cudaMemcpyHostToDevice, m->stream));
+    P.epoch = ew;
+    P.abort_word = ew + 1;
+    P.ctrs = ew + 64;
+    if (c.flags & QW3_FLAG_TRACE) {
+        m->step_trace_words = 2 * ((kStepPhases * c.n_layers + 2) * 4 + 64) + P.NCTA * 16;
+        M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&P.trace), static_cast<size_t>(m->step_trace_words) * 8));
+        M_TRY(m, cudaMemsetAsync(P.trace, 0, static_cast<size_t>(m->step_trace_words) * 8, m->stream));
+    }
+    M_TRY(m, cudaStreamSynchronize(m->stream));
+    m->sp = P;
+    m->step = true;
     return QW3_OK;
 }
 
@@ -837,7 +734,7 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
         e = model_alloc(m, reinterpret_cast<void **>(&m->kvpack), attn_prefill_tc_pack_bytes(hd, nkv, c.max_seq_len));
         if (e != cudaSuccess) return bail(cuda_err(m, e, "prefill attention packing buffer"));
     }
-    if (int rc = setup_mega(m, w, on_dev, staging)) return bail(rc);
+    if (int rc = setup_step(m)) return bail(rc);
     e = cudaMemsetAsync(m->done_counter, 0, 64, m->stream);
     if (e == cudaSuccess && m->attn_ccnt) e = cudaMemsetAsync(m->attn_ccnt, 0, 64 * 4, m->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(m->argmax_key, 0, static_cast<size_t>(Bm) * 8, m->stream);
@@ -931,17 +828,16 @@ int qw3_decode(qw3_model *m, int32_t B, const int32_t *seqs_host, const int32_t 
         seqs[b] = sq;
         pos[b] = pos_host[b];
     }
-    if (m->mega && B == 1) {
-        if (int rc = run_mega(m, seqs[0], pos[0], 1, tokens_dev, nullptr, logits_dev, argmax_dev)) return rc;
-        m->seq_len[seqs[0]] += 1;
-        return QW3_OK;
-    }
     DecodeIO io{logits_dev, argmax_dev, nullptr, nullptr};
     M_TRY(m, cudaMemcpyAsync(m->d_seq, seqs.data(), B * 4, cudaMemcpyHostToDevice, m->stream));
     M_TRY(m, cudaMemcpyAsync(m->d_pos, pos.data(), B * 4, cudaMemcpyHostToDevice, m->stream));
     M_TRY(m, cudaMemcpyAsync(m->d_io, &io, sizeof io, cudaMemcpyHostToDevice, m->stream));
     M_TRY(m, cudaMemcpyAsync(m->d_tok, tokens_dev, B * 4, cudaMemcpyDeviceToDevice, m->stream));
-    if (int rc = run_decode_step(m, B)) return rc;
+    if (m->step && B == 1) {
+        M_TRY(m, launch_step(m->sp, m->stream));
+    } else if (int rc = run_decode_step(m, B)) {
+        return rc;
+    }
     for (int b = 0; b < B; ++b) m->seq_len[seqs[b]] += 1;
     return QW3_OK;
 }
@@ -968,11 +864,6 @@ int qw3_generate_greedy(qw3_model *m, int32_t B, const int32_t *seqs_host, int32
         seqs[b] = sq;
         pos[b] = m->seq_len[sq];
     }
-    if (m->mega && B == 1) {
-        if (int rc = run_mega(m, seqs[0], pos[0], n_steps, first_tokens_dev, out_tokens_dev, nullptr, nullptr)) return rc;
-        m->seq_len[seqs[0]] += n_steps;
-        return QW3_OK;
-    }
     DecodeIO io{nullptr, nullptr, out_tokens_dev, nullptr};
     const int32_t zero = 0;
     M_TRY(m, cudaMemcpyAsync(m->d_seq, seqs.data(), B * 4, cudaMemcpyHostToDevice, m->stream));
@@ -981,7 +872,11 @@ int qw3_generate_greedy(qw3_model *m, int32_t B, const int32_t *seqs_host, int32
     M_TRY(m, cudaMemcpyAsync(m->d_step, &zero, 4, cudaMemcpyHostToDevice, m->stream));
     M_TRY(m, cudaMemcpyAsync(m->d_tok, first_tokens_dev, B * 4, cudaMemcpyDeviceToDevice, m->stream));
     for (int sidx = 0; sidx < n_steps; ++sidx) {
-        if (int rc = run_decode_step(m, B)) return rc;
+        if (m->step && B == 1) {
+            M_TRY(m, launch_step(m->sp, m->stream));
+        } else if (int rc = run_decode_step(m, B)) {
+            return rc;
+        }
     }
     for (int b = 0; b < B; ++b) m->seq_len[seqs[b]] += n_steps;
     return QW3_OK;
@@ -1029,11 +924,11 @@ int qw3_debug_read_trace(qw3_model *m, uint64_t *out_host, int32_t max_records, 
         return fail(m, QW3_ERR_INVALID_ARG, "bad trace arguments");
     *n_out = 0;
     if (!m->trace) return fail(m, QW3_ERR_INVALID_ARG, "model was created without QW3_FLAG_TRACE");
-    const bool mega = m->mega && m->mp.trace;
-    const int avail = mega ? m->mega_trace_records : 2 * m->trace_kernels;
+    const bool stp = m->step && m->sp.trace;
+    const int avail = stp ? m->step_trace_words / kTraceWords : 2 * m->trace_kernels;
     const int n = std::min(max_records, avail);
     M_TRY(m, cudaStreamSynchronize(m->stream));
-    M_TRY(m, cudaMemcpy(out_host, mega ? m->mp.trace : m->trace, static_cast<size_t>(n) * kTraceWords * 8,
+    M_TRY(m, cudaMemcpy(out_host, stp ? m->sp.trace : m->trace, static_cast<size_t>(n) * kTraceWords * 8,
                         cudaMemcpyDeviceToHost));
     *n_out = n;
     return QW3_OK;
@@ -1042,9 +937,9 @@ int qw3_debug_read_trace(qw3_model *m, uint64_t *out_host, int32_t max_records, 
 int qw3_decode_plan(const qw3_model *m, int32_t B, int32_t *persistent, int32_t *launches_per_step) {
     if (!m || !persistent || !launches_per_step || B < 1 || B > m->cfg.max_seqs) return QW3_ERR_INVALID_ARG;
     const qw3_config &c = m->cfg;
-    if (m->mega && B == 1) {
+    if (m->step && B == 1) {
         *persistent = 1;
-        *launches_per_step = 0;
+        *launches_per_step = 1;
         return QW3_OK;
     }
     *persistent = 0;

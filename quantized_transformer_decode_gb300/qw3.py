@@ -31,7 +31,8 @@ QW3_ERR_TIMEOUT = 8
 QW3_FLAG_NO_GRAPH = 0x1
 QW3_FLAG_NO_PDL = 0x2
 QW3_FLAG_TRACE = 0x4
-QW3_FLAG_PERSISTENT = 0x8
+QW3_FLAG_PER_KERNEL = 0x8
+QW3_FLAG_TEST_NO_WAIT = 0x10
 
 # Every entry point of include/qw3.h, in declaration order.
 EXPORTS = (
@@ -186,7 +187,7 @@ def qw3_debug_read_trace(h: int, max_records: int) -> np.ndarray:
 
 
 def qw3_decode_plan(h: int, B: int) -> tuple[bool, int]:
-    """(uses the persistent kernel, kernel launches per step otherwise)."""
+    """(uses the persistent step kernel, kernel launches per step)."""
     pers, lps = _I32(), _I32()
     _check(lib().qw3_decode_plan(h, B, ctypes.byref(pers), ctypes.byref(lps)), h)
     return bool(pers.value), lps.value

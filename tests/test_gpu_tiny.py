@@ -71,7 +71,8 @@ def test_tiny_greedy_and_logits(torch):
     gm.close()
 
 
-PERSISTENT = 0x8
+PER_KERNEL = 0x8      # batch-1 decode through the per-kernel chain
+TEST_NO_WAIT = 0x10   # waits on other CTAs give up at their first miss
 
 
 @pytest.mark.parametrize("flags", [0x1, 0x2, 0x3])
@@ -79,7 +80,7 @@ def test_tiny_per_kernel_launch_modes(torch, flags):
     """The per-kernel decode path with direct launches, with and without
     programmatic dependent launch, against the oracle."""
     w = inputs.WORKLOADS["tiny"]
-    _, gm, _ = run_greedy_case(torch, w.shape, w.seed, w.prompt_len, 6, flags=flags)
+    _, gm, _ = run_greedy_case(torch, w.shape, w.seed, w.prompt_len, 6, flags=flags | PER_KERNEL)
     assert gm.decode_plan(1)[0] is False
     gm.close()
 
@@ -94,7 +95,7 @@ def test_long_capacity_split_over_clusters(torch, prompt_len):
     (at 600 tokens step 6 has two logits 1.7e-5 apart: either is the
     greedy token at f32 precision), and free-running ids up to that step."""
     shape, seed, steps = MID, 7, 8
-    om, gm = build_pair(shape, seed, max_seq_len=4200, max_prefill=256)
+    om, gm = build_pair(shape, seed, max_seq_len=4200, max_prefill=256, flags=PER_KERNEL)
     try:
         prompt = inputs.prompt_tokens(shape, seed, prompt_len)
         ids, ologits = om.generate_greedy(om.new_cache(prompt_len + steps + 1), prompt, steps)
@@ -125,37 +126,47 @@ def test_long_capacity_split_over_clusters(torch, prompt_len):
 def test_decode_plans(torch):
     w = inputs.WORKLOADS["tiny"]
     _, gm = build_pair(w.shape, w.seed, max_seq_len=64, max_prefill=32)
-    assert gm.decode_plan(1) == (False, 2 + 5 * w.shape.n_layers)
+    assert gm.decode_plan(1) == (True, 1)
+    assert gm.decode_plan(1)[0] is True
     gm.close()
-    _, gm = build_pair(w.shape, w.seed, max_seq_len=64, max_prefill=32, flags=PERSISTENT)
-    assert gm.decode_plan(1) == (True, 0)
+    _, gm = build_pair(w.shape, w.seed, max_seq_len=64, max_prefill=32, flags=PER_KERNEL)
+    assert gm.decode_plan(1) == (False, 2 + 5 * w.shape.n_layers)
     gm.close()
 
 
 @pytest.mark.parametrize("case", ["tiny", "mid", "mid_long", "untied"])
-def test_persistent_kernel_greedy_and_logits(torch, case):
-    """The persistent batch-1 kernel against the oracle (ids bit-exact,
-    teacher-forced logits); mid_long puts more positions per CTA than one
-    ring slot of K/V rows holds."""
+def test_per_kernel_chain_greedy_and_logits(torch, case):
+    """The per-kernel batch-1 chain (one launch per projection and
+    attention) against the oracle (ids bit-exact, teacher-forced logits);
+    the default batch-1 path, the persistent step kernel, runs the same
+    cases in the tests above and below."""
     if case == "tiny":
         w = inputs.WORKLOADS["tiny"]
-        _, gm, _ = run_greedy_case(torch, w.shape, w.seed, w.prompt_len, w.decode_steps, flags=PERSISTENT)
+        _, gm, _ = run_greedy_case(torch, w.shape, w.seed, w.prompt_len, w.decode_steps, flags=PER_KERNEL)
     elif case == "mid":
-        _, gm, _ = run_greedy_case(torch, MID, 4, prompt_len=70, steps=12, max_prefill=32, flags=PERSISTENT)
+        _, gm, _ = run_greedy_case(torch, MID, 4, prompt_len=70, steps=12, max_prefill=32, flags=PER_KERNEL)
     elif case == "mid_long":
-        _, gm, _ = run_greedy_case(torch, MID, 6, prompt_len=460, steps=5, max_prefill=256, flags=PERSISTENT)
+        _, gm, _ = run_greedy_case(torch, MID, 6, prompt_len=460, steps=5, max_prefill=256, flags=PER_KERNEL)
     else:
-        _, gm, _ = run_greedy_case(torch, MID_UNTIED, 5, prompt_len=40, steps=6, flags=PERSISTENT)
+        _, gm, _ = run_greedy_case(torch, MID_UNTIED, 5, prompt_len=40, steps=6, flags=PER_KERNEL)
+    assert gm.decode_plan(1)[0] is False
+    gm.close()
+
+
+def test_step_kernel_long_context(torch):
+    """The step kernel with more cached positions per attention unit than
+    one ring slot of K/V rows holds, against the oracle."""
+    _, gm, _ = run_greedy_case(torch, MID, 6, prompt_len=460, steps=5, max_prefill=256)
     assert gm.decode_plan(1)[0] is True
     gm.close()
 
 
 def test_paths_agree_bitwise_on_ids(torch):
-    """Persistent kernel and per-kernel path: same greedy ids, logits close."""
+    """Persistent step kernel and per-kernel path: same greedy ids, logits close."""
     shape = MID
     prompt = inputs.prompt_tokens(shape, 4, 40)
     outs = []
-    for flags in (0, PERSISTENT):
+    for flags in (0, PER_KERNEL):
         _, gm = build_pair(shape, 4, max_seq_len=64, max_prefill=64, flags=flags)
         _, am = gm.prefill(0, cuda_ints(prompt), want_logits=False)
         lg, am2 = gm.decode(am, [40])
@@ -326,7 +337,7 @@ def test_truncate_then_redecode_is_reproducible(torch):
 
 def test_trace_records_every_kernel(torch):
     shape = inputs.TINY
-    _, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=32, flags=0x4)
+    _, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=32, flags=0x4 | PER_KERNEL)
     assert gm.decode_plan(1)[0] is False
     gm.prefill(0, cuda_ints(inputs.prompt_tokens(shape, 0, 8)), want_logits=False)
     gm.decode(cuda_ints([3]), [8])
@@ -339,21 +350,55 @@ def test_trace_records_every_kernel(torch):
     gm.close()
 
 
-def test_persistent_kernel_trace(torch):
+def test_step_kernel_trace(torch):
+    """Step-kernel trace of the latest step: for the first CTA, per phase
+    (cycle counter) inputs staged <= outputs published, phases in order."""
     shape = inputs.TINY
-    _, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=32, flags=0x4 | PERSISTENT)
+    _, gm = build_pair(shape, 0, max_seq_len=64, max_prefill=32, flags=0x4)
     assert gm.decode_plan(1)[0] is True
     _, am = gm.prefill(0, cuda_ints(inputs.prompt_tokens(shape, 0, 8)), want_logits=False)
     gm.generate_greedy(am, 3)
-    tr = gm.read_trace().astype(np.int64)
-    L = shape.n_layers
-    attn0 = tr[0]                     # CTA 0, layer 0 attention record
-    assert np.all(attn0[:7] > 0) and np.all(np.diff(attn0[:7]) >= 0)
-    lm = tr[2 * L]
-    assert np.all(lm[:4] > 0) and np.all(np.diff(lm[:4]) >= 0)
-    totals = tr[2 * (2 * L + 1):]
-    assert totals.shape[0] >= 16 and np.all(totals[:, 5] >= totals[:, 4])
+    tr = gm.read_trace(100000).astype(np.int64).reshape(-1)
+    nph = 6 * shape.n_layers + 2
+    first = tr[: nph * 4].reshape(nph, 4)
+    assert first[0, 0] > 0 and first[0, 3] >= first[0, 0]
+    for ph in range(1, nph):
+        if ph % 6 in (1, 4, 5, 0) or ph == nph - 1:   # projection phases and the lm_head
+            assert first[ph, 0] > 0 and first[ph, 3] >= first[ph, 0], ph
+    outs = [first[ph, 3] for ph in range(1, nph) if first[ph, 3] > 0]
+    assert np.all(np.diff(outs) >= 0)
     gm.close()
+
+
+def test_step_kernel_wait_timeout_reported(torch):
+    """With QW3_FLAG_TEST_NO_WAIT every wait on another CTA's data gives up at
+    its first miss: the step runs to its end, qw3_sync reports
+    QW3_ERR_TIMEOUT once, and the model stays usable (a fresh prefill and a
+    batch-2 decode, which do not use the step kernel, match the oracle)."""
+    from quantized_transformer_decode_gb300.qw3 import Qw3Error, QW3_ERR_TIMEOUT
+    shape = inputs.TINY
+    om, gm = build_pair(shape, 0, max_seqs=2, max_seq_len=64, max_prefill=32, flags=TEST_NO_WAIT)
+    try:
+        assert gm.decode_plan(1)[0] is True
+        prompt = inputs.prompt_tokens(shape, 0, 20)
+        _, am = gm.prefill(0, cuda_ints(prompt), want_logits=False)
+        gm.generate_greedy(am, 4)
+        with pytest.raises(Qw3Error) as e:
+            gm.sync()
+        assert e.value.status == QW3_ERR_TIMEOUT
+        gm.sync()   # the status was cleared
+        gm.reset(0)
+        for b in range(2):
+            gm.prefill(b, cuda_ints(prompt), want_logits=False)
+        lg, _ = gm.decode(cuda_ints([5, 5]), [20, 20])
+        gm.sync()
+        cache = om.new_cache(32)
+        om.forward(cache, prompt, 0)
+        want = om.forward(cache, [5], 20)
+        assert_logits_close(_np(lg)[0], want, "batch-2 decode after a timed-out step")
+        assert_logits_close(_np(lg)[1], want, "batch-2 decode after a timed-out step")
+    finally:
+        gm.close()
 
 
 @pytest.mark.parametrize("n", [1, 2, 7, 15])
