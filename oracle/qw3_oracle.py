@@ -265,29 +265,50 @@ def argmax_lowest(logits: np.ndarray) -> int:
 # ---------------------------------------------------------------------------
 
 class QLinear:
-    """A Q8_0 weight [out][in], kept dequantised (exactly) for f64 matmuls."""
+    """A Q8_0 weight [out][in] for f64 matmuls.
 
-    def __init__(self, blocks: np.ndarray, rows: int, cols: int, keep_f64: bool):
+    Storage only, never arithmetic: keep_f64 holds the dequantised matrix in
+    f64, otherwise in f32, and lazy holds the Q8_0 blocks themselves and
+    dequantises a chunk of rows per call (for models whose dequantised
+    weights do not fit in host memory). d * q is exact in f32, so the three
+    give identical results.
+    """
+
+    def __init__(self, blocks: np.ndarray, rows: int, cols: int, keep_f64: bool, lazy: bool = False):
         if cols % QK8_0:
             raise InvalidShape(f"in-dimension {cols} is not a multiple of {QK8_0}")
         self.rows, self.cols = rows, cols
-        w32 = matrix_from_blocks(blocks, rows, cols)
-        self.w = w32.astype(np.float64) if keep_f64 else w32
+        self.lazy = lazy
+        if lazy:
+            self.blocks = np.asarray(blocks, dtype=np.uint8).reshape(rows, (cols // QK8_0) * Q8_0_BYTES)
+            self.w = None
+        else:
+            w32 = matrix_from_blocks(blocks, rows, cols)
+            self.w = w32.astype(np.float64) if keep_f64 else w32
+
+    def _rows32(self, r0: int, r1: int) -> np.ndarray:
+        if self.lazy:
+            return matrix_from_blocks(self.blocks[r0:r1].reshape(-1), r1 - r0, self.cols)
+        return self.w[r0:r1]
 
     def __call__(self, x: np.ndarray) -> np.ndarray:
         """y[m, n] = sum_k W[n, k] x[m, k] in f64 (a library matmul), f32 out."""
         x64 = np.asarray(x, np.float32).astype(np.float64)
-        if self.w.dtype == np.float64:
+        if self.w is not None and self.w.dtype == np.float64:
             return (x64 @ self.w.T).astype(np.float32)
         out = np.empty((x64.shape[0], self.rows), dtype=np.float32)
         step = 8192
         for r0 in range(0, self.rows, step):
-            wc = self.w[r0:r0 + step].astype(np.float64)
-            out[:, r0:r0 + step] = (x64 @ wc.T).astype(np.float32)
+            r1 = min(self.rows, r0 + step)
+            wc = self._rows32(r0, r1).astype(np.float64)
+            out[:, r0:r1] = (x64 @ wc.T).astype(np.float32)
         return out
 
     def row(self, r: np.ndarray) -> np.ndarray:
         """Rows of the dequantised matrix as f32 (the embedding gather)."""
+        if self.lazy:
+            rr = np.asarray(r, dtype=np.int64).reshape(-1)
+            return np.stack([self._rows32(int(i), int(i) + 1)[0] for i in rr]).astype(np.float32)
         return np.asarray(self.w[r], dtype=np.float32)
 
 
@@ -361,7 +382,7 @@ class OracleModel:
 
     F64_BUDGET_BYTES = 12 << 30
 
-    def __init__(self, shape, tensors: dict, keep_f64: bool | None = None):
+    def __init__(self, shape, tensors: dict, keep_f64: bool | None = None, lazy: bool = False):
         s = shape
         self.shape = s
         if s.head_dim % 2:
@@ -373,7 +394,7 @@ class OracleModel:
             keep_f64 = n_params * 8 <= self.F64_BUDGET_BYTES
 
         def lin(name, rows, cols):
-            return QLinear(tensors[name], rows, cols, keep_f64)
+            return QLinear(tensors[name], rows, cols, keep_f64, lazy)
 
         def norm(name, n):
             w = np.asarray(tensors[name], np.float32)
@@ -411,6 +432,19 @@ class OracleModel:
             w = weights[name]
             tensors[name] = q8_0_quantize(w) if kind == "linear" else np.asarray(w, np.float32)
         return cls(shape, tensors, keep_f64)
+
+    @classmethod
+    def from_f32_stream(cls, shape, named_weights) -> "OracleModel":
+        """The same model from an iterator of (name, f32 tensor): each linear
+        weight is quantised as it arrives and only its Q8_0 blocks are kept
+        (lazy storage), so a model far larger than host memory in f32 fits."""
+        from quantized_transformer_decode_gb300.inputs import tensor_specs
+        kinds = {name: kind for name, kind, _ in tensor_specs(shape)}
+        tensors = {}
+        for name, w in named_weights:
+            tensors[name] = q8_0_quantize(w) if kinds[name] == "linear" else np.asarray(w, np.float32)
+            del w
+        return cls(shape, tensors, keep_f64=False, lazy=True)
 
     def new_cache(self, capacity: int) -> KvCache:
         s = self.shape

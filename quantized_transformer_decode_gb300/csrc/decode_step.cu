@@ -128,21 +128,35 @@ __device__ __noinline__ void step_abort(const WaitCtx &w) {
     record_status(w.P->status, QW3_ERR_TIMEOUT);
 }
 
+// Limits of waits on other CTAs are kept in SM cycles (clock64 is cheap;
+// %globaltimer and the abort word are read only every 256 polls).
+// wait_ns == 0 (a test setting) gives up at the first miss.
+__device__ __forceinline__ bool wait_expired(const WaitCtx &w, long long c0, int it) {
+    if (w.P->wait_ns == 0) return true;
+    if ((it & 255) != 255) return false;
+    return clock64() - c0 > static_cast<long long>(w.P->wait_ns) * 4;   // >= 1 ns per 4 cycles up to 4 GHz
+}
+
 // Wait (one thread) until *ctr >= target (wrap-safe), with backoff.
 __device__ __forceinline__ void wait_count(const unsigned *ctr, unsigned target, const WaitCtx &w) {
     if (static_cast<int>(ld_relaxed_u32(ctr) - target) >= 0) return;
-    if (step_aborted(w)) return;
-    const uint64_t t0 = globaltimer_ns();
+    const long long c0 = clock64();
     for (int it = 1;; ++it) {
         if (it > 4) __nanosleep(32);
         if (static_cast<int>(ld_relaxed_u32(ctr) - target) >= 0) return;
-        if ((it & 15) == 0 && step_aborted(w)) return;
-        if (globaltimer_ns() - t0 > w.P->wait_ns) {
+        if ((it & 255) == 255 && step_aborted(w)) return;
+        if (wait_expired(w, c0, it)) {
             step_abort(w);
             return;
         }
     }
 }
+
+// A wait on n writers' counter stops once all but n / 4 of them arrived;
+// the readers then poll the few words still missing directly (their tags),
+// which skips one L2 round trip on the critical path while keeping the
+// polling to the tail of the hand-off.
+__device__ __forceinline__ unsigned gate(unsigned target, unsigned n) { return target - n / 4; }
 
 // Counter i of the step's counter array (128-byte apart).
 __device__ __forceinline__ unsigned *ctr_at(const StepParams &P, int i) { return P.ctrs + 32 * i; }
@@ -176,8 +190,8 @@ __device__ __forceinline__ void ll_read(const float *buf, int i, unsigned tag, f
     bool ok = true;
 #pragma unroll
     for (int k = 0; k < N; ++k) ok = ok && ll_ok(u[k], tag);
-    if (!ok && !step_aborted(w)) {
-        const uint64_t t0 = globaltimer_ns();
+    if (!ok) {
+        const long long c0 = clock64();
         for (int it = 1;; ++it) {
             __nanosleep(32);
             ll_ld2(p, u[0], u[1]);
@@ -186,8 +200,8 @@ __device__ __forceinline__ void ll_read(const float *buf, int i, unsigned tag, f
 #pragma unroll
             for (int k = 0; k < N; ++k) ok = ok && ll_ok(u[k], tag);
             if (ok) break;
-            if ((it & 15) == 0 && step_aborted(w)) break;
-            if (globaltimer_ns() - t0 > w.P->wait_ns) {
+            if ((it & 255) == 255 && step_aborted(w)) break;
+            if (wait_expired(w, c0, it)) {
                 step_abort(w);
                 break;
             }
@@ -200,14 +214,14 @@ __device__ __forceinline__ void ll_read(const float *buf, int i, unsigned tag, f
 __device__ __forceinline__ float ll_read1(const float *buf, int i, unsigned tag, const WaitCtx &w) {
     const unsigned long long *p = reinterpret_cast<const unsigned long long *>(buf) + i;
     unsigned long long u = ll_ld1(p);
-    if (!ll_ok(u, tag) && !step_aborted(w)) {
-        const uint64_t t0 = globaltimer_ns();
+    if (!ll_ok(u, tag)) {
+        const long long c0 = clock64();
         for (int it = 1;; ++it) {
             __nanosleep(32);
             u = ll_ld1(p);
             if (ll_ok(u, tag)) break;
-            if ((it & 15) == 0 && step_aborted(w)) break;
-            if (globaltimer_ns() - t0 > w.P->wait_ns) {
+            if ((it & 255) == 255 && step_aborted(w)) break;
+            if (wait_expired(w, c0, it)) {
                 step_abort(w);
                 break;
             }
@@ -231,14 +245,16 @@ struct Ring {
 // aborted (the chain is broken; the copies themselves complete in
 // microseconds).
 __device__ __noinline__ bool ring_bar_wait_slow(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
-    const uint64_t t0 = globaltimer_ns();
-    uint64_t limit = kWaitLimitNs;
+    const long long c0 = clock64();
+    long long limit = static_cast<long long>(kWaitLimitNs) * 4;
     for (int it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63) == 0 && step_aborted(w)) limit = 2000000ull;
-        if (globaltimer_ns() - t0 > limit) {
-            step_abort(w);
-            return false;
+        if ((it & 255) == 255) {
+            if (step_aborted(w)) limit = 2000000ll * 4;
+            if (clock64() - c0 > limit) {
+                step_abort(w);
+                return false;
+            }
         }
     }
 }
@@ -432,6 +448,18 @@ __device__ __forceinline__ Slice make_slice(const QMat &W, int c, int NCTA, uint
     return s;
 }
 
+// Layer l's copy of a layer-0 pointer (layers are laid out at a fixed stride).
+template <typename T>
+__device__ __forceinline__ T *at_layer(T *p0, int l, size_t lstride) {
+    return reinterpret_cast<T *>(reinterpret_cast<uintptr_t>(p0) + static_cast<uintptr_t>(l) * lstride);
+}
+
+__device__ __forceinline__ Slice slice_at(const Slice &s0, int l, size_t lstride) {
+    Slice s = s0;
+    s.src = at_layer(s0.src, l, lstride);
+    return s;
+}
+
 __device__ __forceinline__ int slice_chunks(const Slice &s) {
     return (s.ng * s.ntk + s.tpc - 1) / s.tpc;
 }
@@ -443,35 +471,53 @@ __device__ __forceinline__ int slice_chunks(const Slice &s) {
 template <int LC>
 __device__ __forceinline__ void gemv_tasks(const Slice sl, const Ring ring, uint32_t &n, const uint8_t *planes,
                                         const float *scales, float *red, const WaitCtx w, int warp, int lane,
-                                        unsigned long long *tr) {
+                                        unsigned long long *tr, unsigned long long *dd = nullptr) {
+    if (dd) dd[0] = clock64();
     constexpr int kSeg = 32 * LC;
     const int nseg = sl.kt / kSeg;
     const int ntile = sl.ng * sl.ntk;
     const int ntask = ntile * nseg;
     const int nch = slice_chunks(sl);
     int task = warp;
+    // (tile, segment) of `task` walked without runtime divisions
+    int tile = 0, seg = task;
+    while (seg >= nseg) {
+        seg -= nseg;
+        ++tile;
+    }
 #pragma unroll 1
     for (int c = 0; c < nch; ++c) {
+        if (dd && c == 0) dd[1] = clock64();
         const uint8_t *slot = ring_wait(ring, n, w);
         if (tr && c == 0) tr[1] = clock64();
+        if (dd && c == 0) dd[2] = clock64();
         const int tile_end = min(ntile, (c + 1) * sl.tpc);
 #pragma unroll 1
-        for (; task < ntask && task / nseg < tile_end; task += kCW) {
-            const int tile = task / nseg, seg = task - (task / nseg) * nseg;
-            const int kti = tile % sl.ntk;
+        for (; task < ntask && tile < tile_end; task += kCW) {
+            int kti = tile;
+            while (kti >= sl.ntk) kti -= sl.ntk;
             const uint8_t *tp = slot + static_cast<size_t>(tile - c * sl.tpc) * sl.tb;
             const int colt = seg * kSeg + lane * LC;
             float acc[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
             dot_rows8<LC>(tp, sl.kt, colt, kti * sl.kt + colt, planes, scales, acc);
+            if (dd && c == 0) dd[3] = clock64() + static_cast<long long>(acc[0] * 0.0f);
             const float t = reduce8(acc, lane);
             if ((lane & 3) == 0) red[task * 8 + red8_row(lane)] = t;
+            if (dd && c == 0) dd[4] = clock64();
+            seg += kCW;
+            while (seg >= nseg) {
+                seg -= nseg;
+                ++tile;
+            }
         }
         ring_release(ring, n, lane);
+        if (dd && c == 0) dd[5] = clock64();
         ++n;
     }
     if (tr) tr[2] = clock64();
+    if (dd) dd[6] = clock64();
 }
 
 // Sum of the task partials of local row t of the slice (fixed order).
@@ -591,16 +637,15 @@ __device__ __forceinline__ void attention_phase(const StepParams &P, int l, int 
     const bool role = warp < G || (u.has_new && warp < G + 2);
 
     // operands that do not depend on this layer's projection, then the wait
-    const LayerDev &Ld = P.layers[l];
     float nw[E];
     float2 cs[E];
     if (role && warp <= G) {
-        lane_load<HD>(warp < G ? Ld.q_norm : Ld.k_norm, nw, lane);
+        lane_load<HD>(at_layer(warp < G ? P.L0.q_norm : P.L0.k_norm, l, P.lstride), nw, lane);
         const float2 *rrow = P.rope + static_cast<size_t>(p) * (HD / 2);
 #pragma unroll
         for (int e = 0; e < E; ++e) cs[e] = __ldg(rrow + (lane & 15) * E + e);
     }
-    if (tid == 0) wait_count(ctr_at(P, 24 + u.g), static_cast<unsigned>(l + 1) * nq, w);
+    if (tid == 0) wait_count(ctr_at(P, 24 + u.g), gate(static_cast<unsigned>(l + 1) * nq, nq), w);
     csync();
     if (tr) tr[1] = globaltimer_ns();
     if (role) {
@@ -682,31 +727,34 @@ __device__ __forceinline__ void attention_phase(const StepParams &P, int l, int 
         }
     }
     csync();
-    if (warp < G) {
-        const int t = warp;
-        float M = -INFINITY;
-        for (int ww = 0; ww < kCW; ++ww) M = fmaxf(M, wp[(ww * G + t) * PW + HD]);
-        float L = 0.0f, A[E];
-#pragma unroll
-        for (int e = 0; e < E; ++e) A[e] = 0.0f;
-        if (M != -INFINITY) {
-            for (int ww = 0; ww < kCW; ++ww) {
-                const float *src = wp + (ww * G + t) * PW;
-                const float f = expf(src[HD] - M);
-                L = fmaf(src[HD + 1], f, L);
-                float aw[E];
-                lane_load<HD>(src, aw, lane);
-#pragma unroll
-                for (int e = 0; e < E; ++e) A[e] = fmaf(aw[e], f, A[e]);
-            }
-        }
-        const int dst = ((u.g * P.S + u.j) * G + t) * PS;
+    {
+        // one (head, dim) output per consumer thread: max and weights over
+        // the 16 warps' partials, independent loads and exps in flight
         const unsigned tag = step_tag(w.epoch, l, 2);
+        const int base = (u.g * P.S + u.j) * G;
+        for (int o = tid; o < G * HD; o += kCT) {
+            const int t = o / HD, d = o - (o / HD) * HD;
+            float mw[kCW];
+            float M = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < E; ++e) ll_st(P.partb, dst + lane * E + e, A[e], tag);
-        if (lane == 0) {
-            ll_st(P.partb, dst + HD, M, tag);
-            ll_st(P.partb, dst + HD + 1, L, tag);
+            for (int ww = 0; ww < kCW; ++ww) {
+                mw[ww] = wp[(ww * G + t) * PW + HD];
+                M = fmaxf(M, mw[ww]);
+            }
+            float L = 0.0f, A = 0.0f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int ww = 0; ww < kCW; ++ww) {
+                    const float f = expf(mw[ww] - M);
+                    L = fmaf(wp[(ww * G + t) * PW + HD + 1], f, L);
+                    A = fmaf(wp[(ww * G + t) * PW + d], f, A);
+                }
+            }
+            ll_st(P.partb, (base + t) * PS + d, A, tag);
+            if (d == 0) {
+                ll_st(P.partb, (base + t) * PS + HD, M, tag);
+                ll_st(P.partb, (base + t) * PS + HD + 1, L, tag);
+            }
         }
     }
     // the scratch is the next phase's plane buffer: arrive() synchronises
@@ -724,7 +772,7 @@ __device__ __forceinline__ void combine_phase(const StepParams &P, int l, int un
     const int S = P.S, g = unit / S, j = unit - (unit / S) * S;
     const int e0 = j * GD / S, e1 = (j + 1) * GD / S;
     const unsigned tag2 = step_tag(w.epoch, l, 2);
-    if (tid == 0) wait_count(ctr_at(P, 24 + P.nkv + g), static_cast<unsigned>((l + 1) * S), w);
+    if (tid == 0) wait_count(ctr_at(P, 24 + P.nkv + g), gate(static_cast<unsigned>((l + 1) * S), S), w);
     csync();
     bool wrote = false;
 #pragma unroll 1
@@ -825,6 +873,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
     auto rec1 = [&](int l, int k) {
         if (ctr1 && l == 1) ctr1[k] = globaltimer_ns();
     };
+    unsigned long long *dbg = (P.trace && tid == 0 && c == NCTA - 1) ? P.trace + 2 * (nph * 4 + 64) + static_cast<size_t>(NCTA) * 16 : nullptr;
+#define DBG(l_, i_) do { if (dbg && (l_) == 1) dbg[i_] = clock64(); } while (0)
     rec(0, 0);
 
     if (tid == 0) {
@@ -836,6 +886,14 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
         *best = 0ull;
         flags[0] = 0;
         flags[1] = 0;
+    }
+    // this CTA's slices of the five streamed matrices (layer 0; layer l adds
+    // l * lstride), computed once
+    Slice *sls = reinterpret_cast<Slice *>(smem + P.o_misc + 256);   // qkv, o, gu, down, lm_head
+    float *rsc = reinterpret_cast<float *>(smem + P.o_misc + 96);    // norm scale of the staged vector
+    if (tid < 5) {
+        const QMat *mats[5] = {&P.L0.qkv, &P.L0.o, &P.L0.gu, &P.L0.down, &P.out};
+        sls[tid] = make_slice(*mats[tid], c, NCTA, P.SB);
     }
     __syncthreads();
     const unsigned *nX = P.cnt_x, *nO = P.cnt_o, *nA = P.cnt_act;
@@ -856,8 +914,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
                 if (bytes2) bulk_g2s(dst + off2, src2, bytes2, &full[slot], pol);
                 ++n;
             };
-            auto tiles = [&](const QMat &W) {
-                const Slice sl = make_slice(W, c, NCTA, P.SB);
+            auto tiles = [&](const Slice &sl) {
                 const int nt = sl.ng * sl.ntk;
                 for (int t0 = 0; t0 < nt; t0 += sl.tpc) {
                     const int cnt_t = min(sl.tpc, nt - t0);
@@ -865,9 +922,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
                 }
             };
             for (int l = 0; l < P.L; ++l) {
-                const LayerDev &Ld = P.layers[l];
                 if (l == 1 && P.trace) P.trace[2 * (nph * 4 + 64) + static_cast<size_t>(c) * 16 + 13] = globaltimer_ns();
-                tiles(Ld.qkv);
+                tiles(slice_at(sls[0], l, P.lstride));
                 if (unit >= 0) {
                     const UnitRange u = unit_range(unit, P.S, p);
                     const float *kb = P.kv + static_cast<size_t>(l) * P.layer_stride +
@@ -880,11 +936,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
                              bytes, static_cast<uint32_t>(P.CP * HD * 4));
                     }
                 }
-                tiles(Ld.o);
-                tiles(Ld.gu);
-                tiles(Ld.down);
+                tiles(slice_at(sls[1], l, P.lstride));
+                tiles(slice_at(sls[2], l, P.lstride));
+                tiles(slice_at(sls[3], l, P.lstride));
             }
-            tiles(P.out);
+            tiles(sls[4]);
             // drain: every copy has landed before the CTA can exit
             const uint32_t first = n > static_cast<uint32_t>(P.NS) ? n - P.NS : 0;
             for (uint32_t k = first; k < n; ++k) (void)ring_bar_wait(&full[k % P.NS], (k / P.NS) & 1u, wc);
@@ -896,7 +952,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
     uint32_t n = 0;
     {
         // this CTA's rows of the residual stream: the embedding row
-        const Slice so = make_slice(P.layers[0].o, c, NCTA, P.SB);
+        const Slice so = sls[1];
         for (int t = tid; t < so.ng * 8; t += kCT) {
             const int r = so.row0 + t;
             xown[t] = __half2float(*qm_scale(P.embd, tok, r)) * static_cast<float>(*qm_codes(P.embd, tok, r));
@@ -905,25 +961,28 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
     rec(0, 1);
     const int xsub = c % kSub;
     for (int l = 0; l < P.L; ++l) {
-        const LayerDev &Ld = P.layers[l];
         const int ph = kStepPhases * l;
 
         // ---- P1: [q; k; v] = W_qkv RMSNorm(x)
         {
-            const Slice sl = make_slice(Ld.qkv, c, NCTA, P.SB);
-            if (l > 0 && sl.ng > 0 && tid < kSub) wait_count(ctr_at(P, tid), 2u * l * nX[tid], wc);
+            const Slice sl = slice_at(sls[0], l, P.lstride);
+            if (l > 0 && sl.ng > 0 && tid < kSub) wait_count(ctr_at(P, tid), gate(2u * l * nX[tid], nX[tid]), wc);
             csync();
             if (sl.ng > 0)
-                stage_planes<LC>(l == 0 ? nullptr : P.xb, step_tag(epoch, l - 1, 6), wc, &P.embd, tok, P.H, Ld.attn_norm,
+                stage_planes<LC>(l == 0 ? nullptr : P.xb, step_tag(epoch, l - 1, 6), wc, &P.embd, tok, P.H, at_layer(P.L0.attn_norm, l, P.lstride),
                                  planes, scales, ssw, tid);
             csync();
             rec(ph + 1, 0);
+            if (warp == kCW - 1 && sl.ng > 0) {
+                const float r = norm_scale(ssw, P.H, P.eps);
+                if (lane == 0) *rsc = r;
+            }
             rec1(l, 0);
             gemv_tasks<LC>(sl, ring, n, planes, scales, red, wc, warp, lane, trace ? trace + (ph + 1) * 4 : nullptr);
             csync();
             const int r0 = sl.row0, r1 = min(sl.row0 + 8 * sl.ng, P.qkv_w);
             if (sl.ng > 0) {
-                const float r = norm_scale(ssw, P.H, P.eps);
+                const float r = *rsc;
                 bool wrote = false;
                 for (int t = tid; t < r1 - r0; t += kCT) {
                     ll_st(P.qkvb, r0 + t, row_sum<LC>(sl, red, t) * r, step_tag(epoch, l, 1));
@@ -949,8 +1008,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
         }
         // ---- P4: x += W_o o
         {
-            const Slice sl = make_slice(Ld.o, c, NCTA, P.SB);
-            if (sl.ng > 0 && tid < kSub) wait_count(ctr_at(P, 8 + tid), static_cast<unsigned>(l + 1) * nO[tid], wc);
+            const Slice sl = slice_at(sls[1], l, P.lstride);
+            if (sl.ng > 0 && tid < kSub) wait_count(ctr_at(P, 8 + tid), gate(static_cast<unsigned>(l + 1) * nO[tid], nO[tid]), wc);
             csync();
             if (sl.ng > 0)
                 stage_planes<LC>(P.ob, step_tag(epoch, l, 3), wc, nullptr, 0, P.nh * HD, nullptr, planes, scales, ssw, tid);
@@ -973,38 +1032,56 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
         }
         // ---- P5: act = silu(W_gate h) * (W_up h), h = RMSNorm(x)
         {
-            const Slice sl = make_slice(Ld.gu, c, NCTA, P.SB);
-            if (sl.ng > 0 && tid < kSub) wait_count(ctr_at(P, tid), (2u * l + 1u) * nX[tid], wc);
+            const Slice sl = slice_at(sls[2], l, P.lstride);
+            DBG(l, 0);
+            if (sl.ng > 0 && tid < kSub) wait_count(ctr_at(P, tid), gate((2u * l + 1u) * nX[tid], nX[tid]), wc);
+            DBG(l, 1);
             csync();
+            DBG(l, 2);
             if (sl.ng > 0)
-                stage_planes<LC>(P.xb, step_tag(epoch, l, 4), wc, nullptr, 0, P.H, Ld.ffn_norm, planes, scales, ssw, tid);
+                stage_planes<LC>(P.xb, step_tag(epoch, l, 4), wc, nullptr, 0, P.H, at_layer(P.L0.ffn_norm, l, P.lstride), planes, scales, ssw, tid);
+            DBG(l, 3);
             csync();
+            DBG(l, 4);
             rec(ph + 5, 0);
-            rec1(l, 9);
-            gemv_tasks<LC>(sl, ring, n, planes, scales, red, wc, warp, lane, trace ? trace + (ph + 5) * 4 : nullptr);
-            csync();
-            bool wrote = false;
-            if (sl.ng > 0) {
+            if (warp == kCW - 1 && sl.ng > 0) {
                 const float r = norm_scale(ssw, P.H, P.eps);
+                if (lane == 0) *rsc = r;
+            }
+            rec1(l, 9);
+            gemv_tasks<LC>(sl, ring, n, planes, scales, red, wc, warp, lane, trace ? trace + (ph + 5) * 4 : nullptr,
+                           (dbg && l == 1) ? dbg + 5 : nullptr);
+            DBG(l, 12);
+            csync();
+            DBG(l, 13);
+            bool wrote = false;
+            for (int pass = 0; pass < ((P.trace && l == 1) ? 2 : 1); ++pass) {
+            if (pass == 1) DBG(l, 16);
+            if (sl.ng > 0) {
+                const float r = *rsc;
                 for (int t = 2 * tid; t < sl.ng * 8; t += 2 * kCT) {
                     const int row = sl.row0 + t;
                     if (row < 2 * P.I) {
                         const float gt = row_sum<LC>(sl, red, t) * r;
                         const float up = row_sum<LC>(sl, red, t + 1) * r;
-                        ll_st(P.actb, row / 2, gt / (1.0f + expf(-gt)) * up, step_tag(epoch, l, 5));
+                        ll_st(P.actb, row / 2, __fdividef(gt, 1.0f + __expf(-gt)) * up, step_tag(epoch, l, 5));
                         wrote = true;
                     }
                 }
             }
+            if (pass == 1) DBG(l, 17);
+            }
             (void)wrote;
+            DBG(l, 14);
             arrive(ctr_at(P, 16 + xsub), sl.ng > 0, tid);
+            DBG(l, 15);
             rec(ph + 5, 1);
             rec1(l, 10);
         }
         // ---- P6: x += W_down act
         {
-            const Slice sl = make_slice(Ld.down, c, NCTA, P.SB);
-            if (sl.ng > 0 && tid < kSub) wait_count(ctr_at(P, 16 + tid), static_cast<unsigned>(l + 1) * nA[tid], wc);
+            const Slice sl = slice_at(sls[3], l, P.lstride);
+            if (sl.ng > 0 && tid < kSub) wait_count(ctr_at(P, 16 + tid), gate(static_cast<unsigned>(l + 1) * nA[tid], nA[tid]), wc);
             csync();
             if (sl.ng > 0)
                 stage_planes<LC>(P.actb, step_tag(epoch, l, 5), wc, nullptr, 0, P.I, nullptr, planes, scales, ssw, tid);
@@ -1030,20 +1107,24 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
     // ---- final RMSNorm, lm_head, argmax (lowest index on ties)
     {
         const int phl = kStepPhases * P.L + 1;
-        const Slice sl = make_slice(P.out, c, NCTA, P.SB);
-        if (sl.ng > 0 && tid < kSub) wait_count(ctr_at(P, tid), 2u * P.L * nX[tid], wc);
+        const Slice sl = sls[4];
+        if (sl.ng > 0 && tid < kSub) wait_count(ctr_at(P, tid), gate(2u * P.L * nX[tid], nX[tid]), wc);
         csync();
         if (sl.ng > 0)
             stage_planes<LC>(P.xb, step_tag(epoch, P.L - 1, 6), wc, nullptr, 0, P.H, P.out_norm, planes, scales, ssw,
                              tid);
         csync();
         rec(phl, 0);
+        if (warp == kCW - 1 && sl.ng > 0) {
+            const float r = norm_scale(ssw, P.H, P.eps);
+            if (lane == 0) *rsc = r;
+        }
         gemv_tasks<LC>(sl, ring, n, planes, scales, red, wc, warp, lane, trace ? trace + phl * 4 : nullptr);
         csync();
         float *logits = P.io->logits;
         unsigned long long key = 0ull;
         if (sl.ng > 0) {
-            const float r = norm_scale(ssw, P.H, P.eps);
+            const float r = *rsc;
             for (int t = tid; t < sl.ng * 8; t += kCT) {
                 const int row = sl.row0 + t;
                 if (row < P.V) {

@@ -15,6 +15,8 @@ struct StepParams {
     int L, H, I, V, nh, nkv, hd, G, qkv_w;
     float eps, scale;
     const LayerDev *layers;     // device array [L]
+    LayerDev L0;                // layer 0; layer l's matrices and norms sit lstride bytes further per layer
+    size_t lstride;
     QMat embd, out;             // token embedding; lm_head (== embd when tied)
     const float *out_norm;
     const float2 *rope;         // [max_seq_len][hd/2] (cos, sin)
@@ -57,6 +59,9 @@ struct StepParams {
 };
 
 constexpr int kStepConsumerWarps = 16;
+// Largest per-SM share of one layer's weights for which batch-1 decode uses
+// the step kernel (0.6B geometry: ~110 KB; 8B: ~1.4 MB).
+constexpr size_t kStepMaxLayerBytesPerSm = 512 * 1024;
 constexpr int kStepThreads = (kStepConsumerWarps + 1) * 32;
 
 // Phases per layer (trace records).

@@ -426,3 +426,19 @@ def test_cached_equals_uncached_and_contract_errors():
     c2.truncate(6)
     lg = m.forward(c2, toks[6:7], 6)
     assert np.max(np.abs(lg - full[6])) < 1e-6
+
+
+def test_lazy_block_storage_gives_identical_outputs():
+    """The lazy storage mode (Q8_0 blocks kept, rows dequantised per call; for
+    models too large to hold dequantised on the host) changes no arithmetic:
+    the same greedy ids and bit-identical logits as the eager model."""
+    from quantized_transformer_decode_gb300 import inputs
+    s = inputs.TINY
+    eager = orc.OracleModel.from_f32(s, inputs.generate_weights(s, 0))
+    lazy = orc.OracleModel.from_f32_stream(s, ((n, w) for n, _, w in inputs.iter_weights(s, 0)))
+    prompt = inputs.prompt_tokens(s, 0, 12)
+    ia, la = eager.generate_greedy(eager.new_cache(20), prompt, 3)
+    ib, lb = lazy.generate_greedy(lazy.new_cache(20), prompt, 3)
+    assert ia == ib
+    for x, y in zip(la, lb):
+        np.testing.assert_array_equal(np.asarray(x), np.asarray(y))
