@@ -80,7 +80,7 @@ typedef struct qw3_config {
     int32_t hidden;         /* H, multiple of 32                            */
     int32_t n_layers;       /* L                                            */
     int32_t n_heads;        /* query heads                                  */
-    int32_t n_kv_heads;     /* key/value heads; n_heads % n_kv_heads == 0   */
+    int32_t n_kv_heads;     /* key/value heads, <= 64; n_heads % n_kv_heads == 0 */
     int32_t head_dim;       /* 64 or 128                                    */
     int32_t intermediate;   /* FFN width, multiple of 32                    */
     float rms_eps;          /* 1e-6 for Qwen3                               */
@@ -253,8 +253,10 @@ QW3_API int qw3_q8_0_gemv(const void *W_dev, int32_t rows, int32_t cols,
  * The counters must be zero when a call starts: static storage starts at
  * zero and every call leaves them at zero.
  * The first call on each device looks up the scratch address
- * (cudaGetSymbolAddress, which can load the module); make that first call
- * before any stream capture.
+ * (cudaGetSymbolAddress, which can load the module) and keeps it for the
+ * life of the process; make that first call before any stream capture, and
+ * do not call this entry on a device after cudaDeviceReset (the kept
+ * address belongs to the context that was reset).
  * Calls that overlap on one device (two streams, or two threads without
  * ordering) share the scratch and race: order them on one stream.
  * Arguments as qw3_q8_0_gemv, except that x_dev must be 8-byte aligned.

@@ -417,14 +417,17 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
         // global memory, the last leader to arrive merges them)
         if (tid == 0 && !mbar_wait_bounded_cluster(rbar, 0u)) flags[2] = 1;
         __syncthreads();
-        if (flags[2]) {
-            if (tid == 0) record_status(a.status, QW3_ERR_TIMEOUT);
-        } else {
+        // On a timeout the peers' partials are not trusted: every split
+        // counts as empty, but the merge (and, with several clusters, the
+        // arrival on the counter the last leader resets) still runs.
+        const bool tmo = flags[2] != 0;
+        if (tmo && tid == 0) record_status(a.status, QW3_ERR_TIMEOUT);
+        {
             if (warp < G) {
                 // warp t: lane j holds split j's (m, l) of head t
                 const int t = warp;
-                const float mj = lane < C ? recv[(lane * G + t) * PS + HD] : -INFINITY;
-                const float lj = lane < C ? recv[(lane * G + t) * PS + HD + 1] : 0.0f;
+                const float mj = (lane < C && !tmo) ? recv[(lane * G + t) * PS + HD] : -INFINITY;
+                const float lj = (lane < C && !tmo) ? recv[(lane * G + t) * PS + HD + 1] : 0.0f;
                 const float M = warp_max(mj);
                 const float f = (mj == -INFINITY) ? 0.0f : expf(mj - M);
                 const float L = warp_sum(lj * f);
@@ -442,7 +445,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
                 const int t = o / HD, d = o - (o / HD) * HD;
                 float v[CM];
 #pragma unroll
-                for (int j = 0; j < CM; ++j) v[j] = j < C ? recv[(j * G + t) * PS + d] : 0.0f;
+                for (int j = 0; j < CM; ++j) v[j] = (j < C && !tmo) ? recv[(j * G + t) * PS + d] : 0.0f;
                 float sum = 0.0f;
 #pragma unroll
                 for (int j = 0; j < CM; ++j)

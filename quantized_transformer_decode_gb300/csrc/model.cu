@@ -262,6 +262,7 @@ int validate_config(const qw3_config *c, std::string &why) {
     if (c->intermediate % 32) return bad("intermediate must be a multiple of 32");
     if ((c->n_heads * c->head_dim) % 32) return bad("n_heads*head_dim must be a multiple of 32");
     if (c->n_heads % c->n_kv_heads) return bad("n_heads must be a multiple of n_kv_heads");
+    if (c->n_kv_heads > 64) return bad("n_kv_heads must be at most 64");
     if (c->head_dim % 2) return bad("head_dim must be even");
     if (c->head_dim != 64 && c->head_dim != 128) return bad("head_dim must be 64 or 128");
     const int group = c->n_heads / c->n_kv_heads;

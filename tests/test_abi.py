@@ -81,6 +81,7 @@ def _weights(n_layers=2):
     (dict(n_heads=5), 2),                     # nh % nkv
     (dict(head_dim=96), 2),                   # head_dim not 64/128
     (dict(n_heads=32, n_kv_heads=2), 2),      # group 16 unsupported
+    (dict(n_heads=130, n_kv_heads=65), 2),    # more than 64 kv heads
     (dict(max_seq_len=0), 2),
     (dict(rope_theta=0.0), 2),
     (dict(vocab=0), 2),
