@@ -317,25 +317,34 @@ class QLinear:
 # ---------------------------------------------------------------------------
 
 class KvCache:
-    """Per-layer f32 K and V, each [capacity, kv_heads, head_dim].
+    """Per-layer K and V, each [capacity, kv_heads, head_dim].
 
     K is stored after the Q/K norm and RoPE, V as projected. append_layer
     writes at rows len.. without moving len; advance(m) moves it once per
     forward; truncate(keep) rewinds by a single store.
+
+    dtype "f32" (the workloads' cache) or "f16", the course's default cache
+    type ("A transformer from scratch", 12.4): appended rows are rounded to
+    IEEE half (nearest even) and read back exactly as f32.
     """
 
-    def __init__(self, n_layers: int, n_kv_heads: int, head_dim: int, capacity: int):
+    def __init__(self, n_layers: int, n_kv_heads: int, head_dim: int, capacity: int, dtype: str = "f32"):
+        if dtype not in ("f32", "f16"):
+            raise InvalidShape(f"KV cache dtype {dtype!r}")
         self.capacity = capacity
-        self.k = np.zeros((n_layers, capacity, n_kv_heads, head_dim), np.float32)
-        self.v = np.zeros((n_layers, capacity, n_kv_heads, head_dim), np.float32)
+        self.dtype = dtype
+        np_t = np.float32 if dtype == "f32" else np.float16
+        self.k = np.zeros((n_layers, capacity, n_kv_heads, head_dim), np_t)
+        self.v = np.zeros((n_layers, capacity, n_kv_heads, head_dim), np_t)
         self.len = 0
 
     def append_layer(self, layer: int, k_rows: np.ndarray, v_rows: np.ndarray) -> None:
         m = k_rows.shape[0]
         if self.len + m > self.capacity:
             raise KvCacheOverflow(f"len {self.len} + {m} > capacity {self.capacity}")
-        self.k[layer, self.len:self.len + m] = k_rows
-        self.v[layer, self.len:self.len + m] = v_rows
+        # numpy's f32 -> f16 conversion rounds to nearest even
+        self.k[layer, self.len:self.len + m] = np.asarray(k_rows, np.float32).astype(self.k.dtype)
+        self.v[layer, self.len:self.len + m] = np.asarray(v_rows, np.float32).astype(self.v.dtype)
 
     def advance(self, m: int) -> None:
         if self.len + m > self.capacity:
@@ -350,7 +359,7 @@ class KvCache:
         self.len = 0
 
     def layer_rows(self, layer: int, n: int):
-        return self.k[layer, :n], self.v[layer, :n]
+        return self.k[layer, :n].astype(np.float32), self.v[layer, :n].astype(np.float32)
 
 
 # ---------------------------------------------------------------------------
@@ -446,9 +455,9 @@ class OracleModel:
             del w
         return cls(shape, tensors, keep_f64=False, lazy=True)
 
-    def new_cache(self, capacity: int) -> KvCache:
+    def new_cache(self, capacity: int, dtype: str = "f32") -> KvCache:
         s = self.shape
-        return KvCache(s.n_layers, s.n_kv_heads, s.head_dim, capacity)
+        return KvCache(s.n_layers, s.n_kv_heads, s.head_dim, capacity, dtype)
 
     # -- blocks -------------------------------------------------------------
 

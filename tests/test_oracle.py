@@ -442,3 +442,53 @@ def test_lazy_block_storage_gives_identical_outputs():
     assert ia == ib
     for x, y in zip(la, lb):
         np.testing.assert_array_equal(np.asarray(x), np.asarray(y))
+
+
+def test_f16_kv_cache_rounds_to_nearest_even():
+    """The f16 cache mode ("A transformer from scratch", 12.4: the course's
+    default cache type) stores appended rows as IEEE half, nearest even:
+    1 + 2^-11 is a tie between 1 and 1 + 2^-10 and rounds to 1 (even);
+    1 + 3 * 2^-12 rounds up to 1 + 2^-10; 70000 overflows to inf; reads
+    return the stored halves exactly."""
+    c = orc.KvCache(1, 1, 4, 3, dtype="f16")
+    k = np.array([[[1 + 2.0 ** -11, 1 + 3 * 2.0 ** -12, 70000.0, -2.0 ** -25]]], np.float32)
+    v = np.array([[[0.1, -0.1, 65504.0, 3.0]]], np.float32)
+    c.append_layer(0, k, v)
+    c.advance(1)
+    kk, vv = c.layer_rows(0, 1)
+    np.testing.assert_array_equal(kk[0, 0], np.array([1.0, 1 + 2.0 ** -10, np.inf, -0.0], np.float32))
+    np.testing.assert_array_equal(vv[0, 0], np.float16(v[0, 0]).astype(np.float32))
+    assert kk.dtype == np.float32
+
+
+def test_f16_kv_single_position_attention_returns_rounded_v():
+    """Attention over one cached position returns V (12.3.5); in the f16
+    cache mode that is V rounded to half."""
+    c = orc.KvCache(1, 1, 8, 2, dtype="f16")
+    rng = np.random.default_rng(5)
+    k = rng.standard_normal((1, 1, 8)).astype(np.float32)
+    v = rng.standard_normal((1, 1, 8)).astype(np.float32)
+    c.append_layer(0, k, v)
+    kk, vv = c.layer_rows(0, 1)
+    q = rng.standard_normal((1, 1, 8)).astype(np.float32)
+    o = orc.attention(q, kk, vv, [0], 0.3, [0])
+    np.testing.assert_array_equal(o[0, 0], np.float16(v[0, 0]).astype(np.float32))
+
+
+def test_f16_kv_model_layer0_rows_are_rounded_f32_rows():
+    """Layer 0's K/V rows of a prefill depend only on the embedding, so in
+    the f16 mode they are exactly the f32 mode's rows rounded to half."""
+    from quantized_transformer_decode_gb300 import inputs
+    s = inputs.TINY
+    om = orc.OracleModel.from_f32(s, inputs.generate_weights(s, 0))
+    prompt = inputs.prompt_tokens(s, 0, 10)
+    c32, c16 = om.new_cache(12), om.new_cache(12, "f16")
+    om.forward(c32, prompt, 0)
+    om.forward(c16, prompt, 0)
+    k32, v32 = c32.layer_rows(0, 10)
+    k16, v16 = c16.layer_rows(0, 10)
+    np.testing.assert_array_equal(k16, k32.astype(np.float16).astype(np.float32))
+    np.testing.assert_array_equal(v16, v32.astype(np.float16).astype(np.float32))
+    g32, _ = om.generate_greedy(om.new_cache(20), prompt, 2)
+    g16, _ = om.generate_greedy(om.new_cache(20, "f16"), prompt, 2)
+    assert len(g16) == len(g32) == 3
