@@ -104,6 +104,12 @@ typedef struct qw3_config {
                                   data in the decode-step kernel gives up at
                                   its first miss (QW3_ERR_TIMEOUT) instead
                                   of after 1 s                                */
+#define QW3_FLAG_KV_F16 0x20     /* KV cache in IEEE half (the default cache
+                                  type of "A transformer from scratch",
+                                  12.4) instead of f32: half the cache bytes;
+                                  keys and values are rounded to nearest
+                                  even when appended. Batch-1 decode then
+                                  runs the per-kernel chain.                  */
 
 /* One decoder layer (minfer section 1). Q8_0 matrices [out][in]:
  *   attn_q [n_heads*head_dim][H], attn_k and attn_v [n_kv_heads*head_dim][H],

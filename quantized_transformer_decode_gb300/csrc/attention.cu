@@ -62,6 +62,46 @@ __device__ __forceinline__ void store_lane(float *dst, const float (&v)[HD / 32]
     }
 }
 
+// load_lane / store_lane for cache elements of type KT (f32 or IEEE half).
+template <int HD>
+__device__ __forceinline__ void load_lane_kv(const float *src, float (&v)[HD / 32], int lane) {
+    load_lane<HD>(src, v, lane);
+}
+
+template <int HD>
+__device__ __forceinline__ void load_lane_kv(const __half *src, float (&v)[HD / 32], int lane) {
+    constexpr int E = HD / 32;
+    if constexpr (E == 4) {
+        const uint2 t = *reinterpret_cast<const uint2 *>(src + lane * 4);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&t.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&t.y));
+        v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+    } else {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(src + lane * 2));
+        v[0] = a.x; v[1] = a.y;
+    }
+}
+
+template <int HD, typename KT>
+__device__ __forceinline__ void store_lane_kv(KT *dst, const float (&v)[HD / 32], int lane) {
+    constexpr int E = HD / 32;
+#pragma unroll
+    for (int e = 0; e < E; ++e) dst[lane * E + e] = kv_cvt<KT>(v[e]);
+}
+
+// Round a lane's values to the cache type and back (identity for f32).
+template <int HD, typename KT>
+__device__ __forceinline__ void round_lane_kv(float (&v)[HD / 32]) {
+#pragma unroll
+    for (int e = 0; e < HD / 32; ++e) v[e] = kv_f32(kv_cvt<KT>(v[e]));
+}
+
+// Positions per staged K/V tile: the tile buffers hold kTileP f32 rows;
+// half rows take half the bytes, so a tile holds twice the positions (kept
+// at kTileP for groups of 8, whose warps score 4 positions at a time).
+template <typename KT, int G>
+__host__ __device__ constexpr int tile_positions() { return (sizeof(KT) == 2 && G <= 4) ? 2 * kTileP : kTileP; }
+
 // Preloaded operands of one per-head norm + RoPE: the lane's norm weights
 // and (cos, sin) pairs (neither depends on the previous kernel).
 template <int HD>
@@ -97,9 +137,10 @@ __device__ __forceinline__ void norm_rope_pre(float (&v)[HD / 32], const NormRop
     }
 }
 
-template <int HD, int G>
+template <int HD, int G, typename KT>
 __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, int nsplit, int csize) {
     constexpr int E = HD / 32;
+    constexpr int TP = tile_positions<KT, G>();
     constexpr int PS = part_stride<HD>();
     constexpr int CM = attn_max_cluster(G);
     static_assert(kAttnWarps * G * PS <= kStages * kTileP * HD, "warp-merge rows must fit in the K tiles");
@@ -108,15 +149,17 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);                 // [kStages] K/V tiles
     uint64_t *rbar = bars + kStages;                                      // partials received (leader)
     int *flags = reinterpret_cast<int *>(smem + 64);
-    float *ktile = reinterpret_cast<float *>(smem + 128);               // [kStages][kTileP][HD]
-    float *vtile = ktile + kStages * kTileP * HD;                         // [kStages][kTileP][HD]
-    float *qn = vtile + kStages * kTileP * HD;                            // [G][HD]
+    float *ktile_f = reinterpret_cast<float *>(smem + 128);             // [kStages][kTileP][HD] f32 slots
+    float *vtile_f = ktile_f + kStages * kTileP * HD;                     // [kStages][kTileP][HD]
+    KT *ktile = reinterpret_cast<KT *>(ktile_f);                          // [kStages][TP][HD] cache rows
+    KT *vtile = reinterpret_cast<KT *>(vtile_f);
+    float *qn = vtile_f + kStages * kTileP * HD;                          // [G][HD]
     float *knew = qn + G * HD;                                            // [HD]
     float *vnew = knew + HD;                                              // [HD]
     // once the tiles are consumed: the warp-merge rows in the K tiles, the
     // split partials pushed to the leader in the V tiles
-    float *mrg = ktile;                                                   // [kAttnWarps][G][PS]
-    float *recv = vtile;                                                  // [CM][G][PS] (leader)
+    float *mrg = ktile_f;                                                 // [kAttnWarps][G][PS]
+    float *recv = vtile_f;                                                // [CM][G][PS] (leader)
     float *wts = vnew + HD;                                               // [G][CM] merge weights (leader)
     float *pbuf = wts + G * CM;                                           // [kAttnWarps][32] probabilities
     float *cbuf = pbuf + kAttnWarps * 32;                                 // [kAttnWarps][8] rescale factors
@@ -142,10 +185,11 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
     const int end = min(ctx, start + chunk);
     const bool has_new = (start <= p) && (p < end);
     const int n_cached = max(0, min(end, p) - start);
-    const int ntiles = (n_cached + kTileP - 1) / kTileP;
+    const int ntiles = (n_cached + TP - 1) / TP;
 
-    const float *kbase = a.kv + static_cast<size_t>(seq) * a.seq_stride + static_cast<size_t>(g) * a.head_stride;
-    const float *vbase = kbase + a.kvsel_stride;
+    KT *kbase = static_cast<KT *>(a.kv) + static_cast<size_t>(seq) * a.seq_stride +
+                static_cast<size_t>(g) * a.head_stride;
+    KT *vbase = kbase + a.kvsel_stride;
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) mbar_init(&bars[i], 1);
@@ -160,12 +204,12 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
     const uint64_t pol = policy_evict_first();
     if (tid == 0) {
         for (int t = 0; t < ntiles && t < kStages; ++t) {
-            const int rows = min(kTileP, n_cached - t * kTileP);
-            const uint32_t bytes = static_cast<uint32_t>(rows * HD * 4);
-            const size_t off = static_cast<size_t>(start + t * kTileP) * HD;
+            const int rows = min(TP, n_cached - t * TP);
+            const uint32_t bytes = static_cast<uint32_t>(rows * HD * sizeof(KT));
+            const size_t off = static_cast<size_t>(start + t * TP) * HD;
             mbar_arrive_expect_tx(&bars[t], 2 * bytes);
-            bulk_g2s(ktile + t * kTileP * HD, kbase + off, bytes, &bars[t], pol);
-            bulk_g2s(vtile + t * kTileP * HD, vbase + off, bytes, &bars[t], pol);
+            bulk_g2s(ktile + t * TP * HD, kbase + off, bytes, &bars[t], pol);
+            bulk_g2s(vtile + t * TP * HD, vbase + off, bytes, &bars[t], pol);
         }
         // the leader expects every peer's partial rows (acc, m, l per head)
         if (r == 0) mbar_arrive_expect_tx(rbar, static_cast<uint32_t>((C - 1) * G * (HD * 4 + 8)));
@@ -189,12 +233,14 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
         } else if (has_new && t == G) {
             load_lane<HD>(qkv_b + a.nh * HD + g * HD, v, lane);
             norm_rope_pre<HD>(v, nr, a.eps, lane);
+            round_lane_kv<HD, KT>(v);   // the new position is scored from its cached value
             store_lane<HD>(knew, v, lane);
-            store_lane<HD>(const_cast<float *>(kbase) + static_cast<size_t>(p) * HD, v, lane);
+            store_lane_kv<HD>(kbase + static_cast<size_t>(p) * HD, v, lane);
         } else if (has_new && t == G + 1) {
             load_lane<HD>(qkv_b + (a.nh + a.nkv) * HD + g * HD, v, lane);
+            round_lane_kv<HD, KT>(v);
             store_lane<HD>(vnew, v, lane);
-            store_lane<HD>(const_cast<float *>(vbase) + static_cast<size_t>(p) * HD, v, lane);
+            store_lane_kv<HD>(vbase + static_cast<size_t>(p) * HD, v, lane);
         }
     }
     __syncthreads();
@@ -225,14 +271,14 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
     const int k_own = lane & (V - 1);
     const int t_own = k_own / NP, j_own = k_own % NP;
     float m_own = -INFINITY, l_own = 0.0f;
-    auto consume = [&](const float *krows, const float *vrows, int n) {
+    auto consume = [&](const auto *krows, const auto *vrows, int n) {
         float sc[V];
         {
             float kv_[NP][E];
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
                 if (j < n) {
-                    load_lane<HD>(krows + j * HD, kv_[j], lane);
+                    load_lane_kv<HD>(krows + j * HD, kv_[j], lane);
                 } else {
 #pragma unroll
                     for (int e = 0; e < E; ++e) kv_[j][e] = 0.0f;
@@ -292,7 +338,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
         for (int j = 0; j < NP; ++j) {
             if (j < n) {
                 float vv[E];
-                load_lane<HD>(vrows + j * HD, vv, lane);
+                load_lane_kv<HD>(vrows + j * HD, vv, lane);
 #pragma unroll
                 for (int t = 0; t < G; ++t) {
                     const float pj = pb[t * NP + j];
@@ -306,7 +352,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
 
     // WPT warps share a tile (NP positions each); TPI tiles are consumed per
     // round, the next ones already in flight in the remaining stages.
-    constexpr int WPT = kTileP / NP;
+    constexpr int WPT = TP / NP;
     constexpr int TPI = kAttnWarps / WPT;
     static_assert(TPI >= 1 && TPI < kStages, "a stage stays in flight while a round is consumed");
     for (int t0 = 0; t0 < ntiles; t0 += TPI) {
@@ -317,10 +363,10 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
                 flags[0] = 1;
                 flags[1] = t0;
             } else {
-                const int rows = min(kTileP, n_cached - t * kTileP);
+                const int rows = min(TP, n_cached - t * TP);
                 const int j0 = (warp % WPT) * NP;
                 if (j0 < rows)
-                    consume(ktile + (si * kTileP + j0) * HD, vtile + (si * kTileP + j0) * HD, min(NP, rows - j0));
+                    consume(ktile + (si * TP + j0) * HD, vtile + (si * TP + j0) * HD, min(NP, rows - j0));
             }
         }
         __syncthreads();
@@ -328,12 +374,12 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
         if (tid == 0) {
             for (int tt = t0 + kStages; tt < t0 + kStages + TPI && tt < ntiles; ++tt) {
                 const int si = tt % kStages;
-                const int rows = min(kTileP, n_cached - tt * kTileP);
-                const uint32_t bytes = static_cast<uint32_t>(rows * HD * 4);
-                const size_t off = static_cast<size_t>(start + tt * kTileP) * HD;
+                const int rows = min(TP, n_cached - tt * TP);
+                const uint32_t bytes = static_cast<uint32_t>(rows * HD * sizeof(KT));
+                const size_t off = static_cast<size_t>(start + tt * TP) * HD;
                 mbar_arrive_expect_tx(&bars[si], 2 * bytes);
-                bulk_g2s(ktile + si * kTileP * HD, kbase + off, bytes, &bars[si], pol);
-                bulk_g2s(vtile + si * kTileP * HD, vbase + off, bytes, &bars[si], pol);
+                bulk_g2s(ktile + si * TP * HD, kbase + off, bytes, &bars[si], pol);
+                bulk_g2s(vtile + si * TP * HD, vbase + off, bytes, &bars[si], pol);
             }
         }
         __syncthreads();
@@ -504,15 +550,22 @@ size_t attn_decode_smem(int HD, int G) {
     return 128 + floats * 4;
 }
 
-template <int HD, int G>
-cudaError_t configure_attn_t() {
-    cudaError_t e = cudaFuncSetAttribute(k_attn_decode<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int HD, int G, typename KT>
+cudaError_t configure_attn_kt() {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_decode<HD, G, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(attn_decode_smem(HD, G)));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_attn_decode<HD, G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(k_attn_decode<HD, G, KT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_attn_decode<HD, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    return cudaFuncSetAttribute(k_attn_decode<HD, G, KT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                 cudaSharedmemCarveoutMaxShared);
+}
+
+template <int HD, int G>
+cudaError_t configure_attn_t() {
+    const cudaError_t e = configure_attn_kt<HD, G, float>();
+    if (e != cudaSuccess) return e;
+    return configure_attn_kt<HD, G, __half>();
 }
 
 // Largest cluster (splits per kv head) of at most attn_max_cluster(G) CTAs
@@ -534,7 +587,7 @@ int max_cluster_t(int units) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k_attn_decode<HD, G>, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, k_attn_decode<HD, G, float>, &cfg) != cudaSuccess) {
             (void)cudaGetLastError();
             n = 0;
         }
@@ -561,7 +614,8 @@ cudaError_t launch_attn_t(const AttnDecodeArgs &a, int B, int nsplit, int csize,
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, k_attn_decode<HD, G>, a, nsplit, csize);
+    if (a.kv16) return cudaLaunchKernelEx(&cfg, k_attn_decode<HD, G, __half>, a, nsplit, csize);
+    return cudaLaunchKernelEx(&cfg, k_attn_decode<HD, G, float>, a, nsplit, csize);
 }
 
 // ------------------------------------------------------------- prefill
@@ -570,9 +624,17 @@ cudaError_t launch_attn_t(const AttnDecodeArgs &a, int B, int nsplit, int csize,
 // appended just before). CTA = (64-query tile, query head); warp w owns 8
 // query rows; for each 32-key tile lane j scores key j, then lanes own
 // head_dim slices for the P.V product. f32 throughout.
-template <int HD>
+__device__ __forceinline__ float4 ld4_kv(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 ld4_kv(const __half *p) {
+    const uint2 t = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&t.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&t.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <int HD, typename KT>
 __global__ void __launch_bounds__(256) k_attn_prefill(const float *__restrict__ qkv, int M, int qkv_stride,
-                                                      const float *__restrict__ kv_k, const float *__restrict__ kv_v,
+                                                      const KT *__restrict__ kv_k, const KT *__restrict__ kv_v,
                                                       size_t head_stride, int pos0, int nh, int group, float scale,
                                                       float *__restrict__ out) {
     constexpr int E = HD / 32;
@@ -587,8 +649,8 @@ __global__ void __launch_bounds__(256) k_attn_prefill(const float *__restrict__ 
     const int g = h / group;
     const int q0 = tile * 64;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const float *kb = kv_k + static_cast<size_t>(g) * head_stride;
-    const float *vb = kv_v + static_cast<size_t>(g) * head_stride;
+    const KT *kb = kv_k + static_cast<size_t>(g) * head_stride;
+    const KT *vb = kv_v + static_cast<size_t>(g) * head_stride;
 
     for (int i = tid; i < 64 * HD / 4; i += 256) {
         const int r = (i * 4) / HD, c = (i * 4) % HD;
@@ -612,8 +674,8 @@ __global__ void __launch_bounds__(256) k_attn_prefill(const float *__restrict__ 
             const int r = (i * 4) / HD, c = (i * 4) % HD;
             float4 kv4 = make_float4(0.f, 0.f, 0.f, 0.f), vv4 = kv4;
             if (t0 + r < nkeys) {
-                kv4 = *reinterpret_cast<const float4 *>(kb + static_cast<size_t>(t0 + r) * HD + c);
-                vv4 = *reinterpret_cast<const float4 *>(vb + static_cast<size_t>(t0 + r) * HD + c);
+                kv4 = ld4_kv(kb + static_cast<size_t>(t0 + r) * HD + c);
+                vv4 = ld4_kv(vb + static_cast<size_t>(t0 + r) * HD + c);
             }
             *reinterpret_cast<float4 *>(Ks + r * KP + c) = kv4;
             *reinterpret_cast<float4 *>(Vs + r * HD + c) = vv4;
@@ -683,15 +745,26 @@ size_t prefill_smem() {
     return static_cast<size_t>(64 * HD + 32 * (HD + 4) + 32 * HD + 8 * 8 * 32) * 4;
 }
 
-template <int HD>
-cudaError_t launch_prefill_t(const float *qkv, int M, int qkv_stride, const float *kv_k, const float *kv_v,
+template <int HD, typename KT>
+cudaError_t launch_prefill_t(const float *qkv, int M, int qkv_stride, const KT *kv_k, const KT *kv_v,
                              size_t head_stride, int pos0, int nh, int group, float scale, float *out,
                              cudaStream_t s) {
     const size_t smem = prefill_smem<HD>();
     dim3 grid((M + 63) / 64, nh);
-    k_attn_prefill<HD><<<grid, 256, smem, s>>>(qkv, M, qkv_stride, kv_k, kv_v, head_stride, pos0, nh, group,
-                                               scale, out);
+    k_attn_prefill<HD, KT><<<grid, 256, smem, s>>>(qkv, M, qkv_stride, kv_k, kv_v, head_stride, pos0, nh, group,
+                                                   scale, out);
     return cudaGetLastError();
+}
+
+template <typename KT>
+cudaError_t launch_prefill_kt(const float *qkv, int M, int qkv_stride, const KT *kk, size_t kvsel_stride,
+                              size_t head_stride, int pos0, int nh, int nkv, int hd, float scale, float *out,
+                              cudaStream_t s) {
+    const KT *vv = kk + kvsel_stride;
+    const int group = nh / nkv;
+    if (hd == 128) return launch_prefill_t<128, KT>(qkv, M, qkv_stride, kk, vv, head_stride, pos0, nh, group, scale, out, s);
+    if (hd == 64) return launch_prefill_t<64, KT>(qkv, M, qkv_stride, kk, vv, head_stride, pos0, nh, group, scale, out, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -728,9 +801,13 @@ cudaError_t configure_attention() {
     QW3_CFG((configure_attn_t<64, 2>()));
     QW3_CFG((configure_attn_t<64, 4>()));
     QW3_CFG((configure_attn_t<64, 8>()));
-    QW3_CFG(cudaFuncSetAttribute(k_attn_prefill<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    QW3_CFG(cudaFuncSetAttribute(k_attn_prefill<128, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(prefill_smem<128>())));
-    QW3_CFG(cudaFuncSetAttribute(k_attn_prefill<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    QW3_CFG(cudaFuncSetAttribute(k_attn_prefill<64, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(prefill_smem<64>())));
+    QW3_CFG(cudaFuncSetAttribute(k_attn_prefill<128, __half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(prefill_smem<128>())));
+    QW3_CFG(cudaFuncSetAttribute(k_attn_prefill<64, __half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(prefill_smem<64>())));
 #undef QW3_CFG
     return cudaSuccess;
@@ -761,15 +838,14 @@ cudaError_t launch_attn_decode(const AttnDecodeArgs &a, int B, int nsplit, int c
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_attn_prefill(const float *qkv, int M, int qkv_stride, const float *kv, size_t layer_off,
-                                size_t seq_off, size_t kvsel_stride, size_t head_stride, int pos0, int nh,
-                                int nkv, int hd, float scale, float *out, cudaStream_t s) {
-    const float *kk = kv + layer_off + seq_off;
-    const float *vv = kk + kvsel_stride;
-    const int group = nh / nkv;
-    if (hd == 128) return launch_prefill_t<128>(qkv, M, qkv_stride, kk, vv, head_stride, pos0, nh, group, scale, out, s);
-    if (hd == 64) return launch_prefill_t<64>(qkv, M, qkv_stride, kk, vv, head_stride, pos0, nh, group, scale, out, s);
-    return cudaErrorInvalidValue;
+cudaError_t launch_attn_prefill(const float *qkv, int M, int qkv_stride, const void *kv_seq, size_t kvsel_stride,
+                                size_t head_stride, int pos0, int nh, int nkv, int hd, float scale, float *out,
+                                bool kv16, cudaStream_t s) {
+    if (kv16)
+        return launch_prefill_kt(qkv, M, qkv_stride, static_cast<const __half *>(kv_seq), kvsel_stride, head_stride,
+                                 pos0, nh, nkv, hd, scale, out, s);
+    return launch_prefill_kt(qkv, M, qkv_stride, static_cast<const float *>(kv_seq), kvsel_stride, head_stride, pos0,
+                             nh, nkv, hd, scale, out, s);
 }
 
 }  // namespace qw3

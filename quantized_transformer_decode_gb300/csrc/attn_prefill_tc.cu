@@ -78,8 +78,8 @@ __device__ __forceinline__ void split8_hl(const float (&v)[8], uint4 &hi, uint4 
 
 // Pack keys [0, ntiles * 64) of every kv head: thread = (head, tile, part, row,
 // 8-column group). Keys at or past ctx are zero.
-template <int HD>
-__global__ void k_pack_kv(const float *__restrict__ kc, const float *__restrict__ vc, size_t head_stride, int nkv,
+template <int HD, typename KT>
+__global__ void k_pack_kv(const KT *__restrict__ kc, const KT *__restrict__ vc, size_t head_stride, int nkv,
                           int ctx, int ntiles, uint8_t *__restrict__ dst) {
     using Z = PaSizes<HD>;
     constexpr int kItems = kKT * (HD / 8);   // K: rows x 8-dim groups (= V^T: HD rows x 8-key groups)
@@ -97,9 +97,9 @@ __global__ void k_pack_kv(const float *__restrict__ kc, const float *__restrict_
         // K: row = key, columns = dims
         const int r = item / (HD / 8), d0 = (item % (HD / 8)) * 8;
         const int key = tile * kKT + r;
-        const float *src = kc + static_cast<size_t>(g) * head_stride + static_cast<size_t>(key) * HD + d0;
+        const KT *src = kc + static_cast<size_t>(g) * head_stride + static_cast<size_t>(key) * HD + d0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = key < ctx ? src[j] : 0.0f;
+        for (int j = 0; j < 8; ++j) v[j] = key < ctx ? kv_f32(src[j]) : 0.0f;
         split8_hl(v, hi, lo);
         const int s = d0 / 64, kk = d0 % 64;
         uint8_t *base = t + s * 2 * (kKT * 128);
@@ -108,11 +108,11 @@ __global__ void k_pack_kv(const float *__restrict__ kc, const float *__restrict_
     } else {
         // V^T: row = dim, columns = keys
         const int d = item / (kKT / 8), k0 = (item % (kKT / 8)) * 8;
-        const float *src = vc + static_cast<size_t>(g) * head_stride;
+        const KT *src = vc + static_cast<size_t>(g) * head_stride;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int key = tile * kKT + k0 + j;
-            v[j] = key < ctx ? src[static_cast<size_t>(key) * HD + d] : 0.0f;
+            v[j] = key < ctx ? kv_f32(src[static_cast<size_t>(key) * HD + d]) : 0.0f;
         }
         split8_hl(v, hi, lo);
         uint8_t *base = t + Z::kk;
@@ -391,16 +391,16 @@ __global__ void __launch_bounds__(kPaThreads, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
 }
 
-template <int HD>
-cudaError_t launch_pa_t(const float *qkv, int M, int qkv_stride, const float *kc, const float *vc,
+template <int HD, typename KT>
+cudaError_t launch_pa_t(const float *qkv, int M, int qkv_stride, const KT *kc, const KT *vc,
                         size_t head_stride, int pos0, int nh, int nkv, float scale, float *out, uint8_t *kvpack,
                         int32_t *status, cudaStream_t s) {
     using Z = PaSizes<HD>;
     const int ctx = pos0 + M;
     const int ntiles = (ctx + kKT - 1) / kKT;
     const int64_t items = static_cast<int64_t>(nkv) * ntiles * 2 * kKT * (HD / 8);
-    k_pack_kv<HD><<<static_cast<unsigned>((items + 255) / 256), 256, 0, s>>>(kc, vc, head_stride, nkv, ctx, ntiles,
-                                                                              kvpack);
+    k_pack_kv<HD, KT><<<static_cast<unsigned>((items + 255) / 256), 256, 0, s>>>(kc, vc, head_stride, nkv, ctx,
+                                                                                  ntiles, kvpack);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const dim3 grid((M + kQT - 1) / kQT, nh);
@@ -426,16 +426,28 @@ cudaError_t configure_attn_prefill_tc() {
     return e;
 }
 
-cudaError_t launch_attn_prefill_tc(const float *qkv, int M, int qkv_stride, const float *kv, size_t layer_off,
-                                   size_t seq_off, size_t kvsel_stride, size_t head_stride, int pos0, int nh, int nkv,
-                                   int hd, float scale, float *out, uint8_t *kvpack, int32_t *status, cudaStream_t s) {
-    const float *kc = kv + layer_off + seq_off;
-    const float *vc = kc + kvsel_stride;
-    if (hd == 128) return launch_pa_t<128>(qkv, M, qkv_stride, kc, vc, head_stride, pos0, nh, nkv, scale, out, kvpack,
-                                           status, s);
-    if (hd == 64) return launch_pa_t<64>(qkv, M, qkv_stride, kc, vc, head_stride, pos0, nh, nkv, scale, out, kvpack,
-                                         status, s);
+template <typename KT>
+static cudaError_t launch_pa_kt(const float *qkv, int M, int qkv_stride, const KT *kc, size_t kvsel_stride,
+                         size_t head_stride, int pos0, int nh, int nkv, int hd, float scale, float *out,
+                         uint8_t *kvpack, int32_t *status, cudaStream_t s) {
+    const KT *vc = kc + kvsel_stride;
+    if (hd == 128)
+        return launch_pa_t<128, KT>(qkv, M, qkv_stride, kc, vc, head_stride, pos0, nh, nkv, scale, out, kvpack,
+                                    status, s);
+    if (hd == 64)
+        return launch_pa_t<64, KT>(qkv, M, qkv_stride, kc, vc, head_stride, pos0, nh, nkv, scale, out, kvpack,
+                                   status, s);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_prefill_tc(const float *qkv, int M, int qkv_stride, const void *kv_seq, size_t kvsel_stride,
+                                   size_t head_stride, int pos0, int nh, int nkv, int hd, float scale, float *out,
+                                   uint8_t *kvpack, int32_t *status, bool kv16, cudaStream_t s) {
+    if (kv16)
+        return launch_pa_kt(qkv, M, qkv_stride, static_cast<const __half *>(kv_seq), kvsel_stride, head_stride,
+                            pos0, nh, nkv, hd, scale, out, kvpack, status, s);
+    return launch_pa_kt(qkv, M, qkv_stride, static_cast<const float *>(kv_seq), kvsel_stride, head_stride, pos0, nh,
+                        nkv, hd, scale, out, kvpack, status, s);
 }
 
 }  // namespace qw3

@@ -471,8 +471,7 @@ __device__ __forceinline__ int slice_chunks(const Slice &s) {
 template <int LC>
 __device__ __forceinline__ void gemv_tasks(const Slice sl, const Ring ring, uint32_t &n, const uint8_t *planes,
                                         const float *scales, float *red, const WaitCtx w, int warp, int lane,
-                                        unsigned long long *tr, unsigned long long *dd = nullptr) {
-    if (dd) dd[0] = clock64();
+                                        unsigned long long *tr) {
     constexpr int kSeg = 32 * LC;
     const int nseg = sl.kt / kSeg;
     const int ntile = sl.ng * sl.ntk;
@@ -487,10 +486,8 @@ __device__ __forceinline__ void gemv_tasks(const Slice sl, const Ring ring, uint
     }
 #pragma unroll 1
     for (int c = 0; c < nch; ++c) {
-        if (dd && c == 0) dd[1] = clock64();
         const uint8_t *slot = ring_wait(ring, n, w);
         if (tr && c == 0) tr[1] = clock64();
-        if (dd && c == 0) dd[2] = clock64();
         const int tile_end = min(ntile, (c + 1) * sl.tpc);
 #pragma unroll 1
         for (; task < ntask && tile < tile_end; task += kCW) {
@@ -502,10 +499,8 @@ __device__ __forceinline__ void gemv_tasks(const Slice sl, const Ring ring, uint
 #pragma unroll
             for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
             dot_rows8<LC>(tp, sl.kt, colt, kti * sl.kt + colt, planes, scales, acc);
-            if (dd && c == 0) dd[3] = clock64() + static_cast<long long>(acc[0] * 0.0f);
             const float t = reduce8(acc, lane);
             if ((lane & 3) == 0) red[task * 8 + red8_row(lane)] = t;
-            if (dd && c == 0) dd[4] = clock64();
             seg += kCW;
             while (seg >= nseg) {
                 seg -= nseg;
@@ -513,11 +508,9 @@ __device__ __forceinline__ void gemv_tasks(const Slice sl, const Ring ring, uint
             }
         }
         ring_release(ring, n, lane);
-        if (dd && c == 0) dd[5] = clock64();
         ++n;
     }
     if (tr) tr[2] = clock64();
-    if (dd) dd[6] = clock64();
 }
 
 // Sum of the task partials of local row t of the slice (fixed order).
@@ -873,8 +866,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
     auto rec1 = [&](int l, int k) {
         if (ctr1 && l == 1) ctr1[k] = globaltimer_ns();
     };
-    unsigned long long *dbg = (P.trace && tid == 0 && c == NCTA - 1) ? P.trace + 2 * (nph * 4 + 64) + static_cast<size_t>(NCTA) * 16 : nullptr;
-#define DBG(l_, i_) do { if (dbg && (l_) == 1) dbg[i_] = clock64(); } while (0)
     rec(0, 0);
 
     if (tid == 0) {
@@ -1033,30 +1024,19 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
         // ---- P5: act = silu(W_gate h) * (W_up h), h = RMSNorm(x)
         {
             const Slice sl = slice_at(sls[2], l, P.lstride);
-            DBG(l, 0);
             if (sl.ng > 0 && tid < kSub) wait_count(ctr_at(P, tid), gate((2u * l + 1u) * nX[tid], nX[tid]), wc);
-            DBG(l, 1);
             csync();
-            DBG(l, 2);
             if (sl.ng > 0)
                 stage_planes<LC>(P.xb, step_tag(epoch, l, 4), wc, nullptr, 0, P.H, at_layer(P.L0.ffn_norm, l, P.lstride), planes, scales, ssw, tid);
-            DBG(l, 3);
             csync();
-            DBG(l, 4);
             rec(ph + 5, 0);
             if (warp == kCW - 1 && sl.ng > 0) {
                 const float r = norm_scale(ssw, P.H, P.eps);
                 if (lane == 0) *rsc = r;
             }
             rec1(l, 9);
-            gemv_tasks<LC>(sl, ring, n, planes, scales, red, wc, warp, lane, trace ? trace + (ph + 5) * 4 : nullptr,
-                           (dbg && l == 1) ? dbg + 5 : nullptr);
-            DBG(l, 12);
+            gemv_tasks<LC>(sl, ring, n, planes, scales, red, wc, warp, lane, trace ? trace + (ph + 5) * 4 : nullptr);
             csync();
-            DBG(l, 13);
-            bool wrote = false;
-            for (int pass = 0; pass < ((P.trace && l == 1) ? 2 : 1); ++pass) {
-            if (pass == 1) DBG(l, 16);
             if (sl.ng > 0) {
                 const float r = *rsc;
                 for (int t = 2 * tid; t < sl.ng * 8; t += 2 * kCT) {
@@ -1065,16 +1045,10 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
                         const float gt = row_sum<LC>(sl, red, t) * r;
                         const float up = row_sum<LC>(sl, red, t + 1) * r;
                         ll_st(P.actb, row / 2, __fdividef(gt, 1.0f + __expf(-gt)) * up, step_tag(epoch, l, 5));
-                        wrote = true;
                     }
                 }
             }
-            if (pass == 1) DBG(l, 17);
-            }
-            (void)wrote;
-            DBG(l, 14);
             arrive(ctr_at(P, 16 + xsub), sl.ng > 0, tid);
-            DBG(l, 15);
             rec(ph + 5, 1);
             rec1(l, 10);
         }

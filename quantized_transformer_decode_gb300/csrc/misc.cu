@@ -56,14 +56,14 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *__restrict__ 
 
 // One warp per (row, head task): q heads normalised and rotated in place,
 // k heads normalised, rotated and written to the cache, v heads copied.
-template <int HD>
+template <int HD, typename KT>
 __global__ void __launch_bounds__(128) k_qk_rope_append(float *__restrict__ qkv, int M, int qkv_stride,
                                                         const float *__restrict__ q_norm,
                                                         const float *__restrict__ k_norm, float eps,
                                                         const float2 *__restrict__ rope,
                                                         const int32_t *__restrict__ row_seq, int seq0,
                                                         const int32_t *__restrict__ row_pos, int pos0,
-                                                        float *__restrict__ kv_layer, size_t seq_stride,
+                                                        KT *__restrict__ kv_layer, size_t seq_stride,
                                                         size_t kvsel_stride, size_t head_stride, int nh,
                                                         int nkv) {
     constexpr int E = HD / 32;
@@ -95,17 +95,17 @@ __global__ void __launch_bounds__(128) k_qk_rope_append(float *__restrict__ qkv,
             v[e] = first ? (v[e] * cs.x - o * cs.y) : (o * cs.y + v[e] * cs.x);
         }
     }
-    float *dst;
     if (task < nh) {
-        dst = src;
+#pragma unroll
+        for (int e = 0; e < E; ++e) src[lane * E + e] = v[e];
     } else {
         const int kvsel = task < nh + nkv ? 0 : 1;
         const int g = task - nh - kvsel * nkv;
-        dst = kv_layer + static_cast<size_t>(seq) * seq_stride + kvsel * kvsel_stride +
-              static_cast<size_t>(g) * head_stride + static_cast<size_t>(pos) * HD;
-    }
+        KT *dst = kv_layer + static_cast<size_t>(seq) * seq_stride + kvsel * kvsel_stride +
+                  static_cast<size_t>(g) * head_stride + static_cast<size_t>(pos) * HD;
 #pragma unroll
-    for (int e = 0; e < E; ++e) dst[lane * E + e] = v[e];
+        for (int e = 0; e < E; ++e) dst[lane * E + e] = kv_cvt<KT>(v[e]);
+    }
 }
 
 __global__ void k_argmax_finalize(unsigned long long *__restrict__ key, int B, const DecodeIO *io,
@@ -128,7 +128,8 @@ __global__ void k_argmax_finalize(unsigned long long *__restrict__ key, int B, c
     if (threadIdx.x == 0 && step_ctr) *step_ctr = step + 1;
 }
 
-__global__ void k_copy_kv_rows(const float *__restrict__ base, size_t kvsel_stride, size_t head_stride, int pos0,
+template <typename KT>
+__global__ void k_copy_kv_rows(const KT *__restrict__ base, size_t kvsel_stride, size_t head_stride, int pos0,
                                int n, int nkv, int hd, float *__restrict__ k_out, float *__restrict__ v_out) {
     const size_t total = static_cast<size_t>(n) * nkv * hd;
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
@@ -137,8 +138,8 @@ __global__ void k_copy_kv_rows(const float *__restrict__ base, size_t kvsel_stri
         const int g = static_cast<int>((i / hd) % nkv);
         const int r = static_cast<int>(i / (static_cast<size_t>(hd) * nkv));
         const size_t src = static_cast<size_t>(g) * head_stride + static_cast<size_t>(pos0 + r) * hd + d;
-        k_out[i] = base[src];
-        v_out[i] = base[kvsel_stride + src];
+        k_out[i] = kv_f32(base[src]);
+        v_out[i] = kv_f32(base[kvsel_stride + src]);
     }
 }
 
@@ -169,23 +170,36 @@ cudaError_t launch_rmsnorm_rows(const float *x, int M, int K, const float *w, fl
     return cudaGetLastError();
 }
 
-cudaError_t launch_qk_rope_append(float *qkv, int M, int qkv_stride, const float *q_norm, const float *k_norm,
-                                  float eps, const float2 *rope, const int32_t *row_seq, int seq0,
-                                  const int32_t *row_pos, int pos0, float *kv_layer, size_t seq_stride,
-                                  size_t kvsel_stride, size_t head_stride, int nh, int nkv, int hd, cudaStream_t s) {
-    if (M <= 0) return cudaSuccess;
+template <typename KT>
+cudaError_t qk_rope_append_t(float *qkv, int M, int qkv_stride, const float *q_norm, const float *k_norm, float eps,
+                             const float2 *rope, const int32_t *row_seq, int seq0, const int32_t *row_pos, int pos0,
+                             KT *kv_layer, size_t seq_stride, size_t kvsel_stride, size_t head_stride, int nh, int nkv,
+                             int hd, cudaStream_t s) {
     const dim3 grid(M, (nh + 2 * nkv + 3) / 4);
     if (hd == 128)
-        k_qk_rope_append<128><<<grid, 128, 0, s>>>(qkv, M, qkv_stride, q_norm, k_norm, eps, rope, row_seq, seq0,
-                                                   row_pos, pos0, kv_layer, seq_stride, kvsel_stride, head_stride,
-                                                   nh, nkv);
+        k_qk_rope_append<128, KT><<<grid, 128, 0, s>>>(qkv, M, qkv_stride, q_norm, k_norm, eps, rope, row_seq, seq0,
+                                                       row_pos, pos0, kv_layer, seq_stride, kvsel_stride, head_stride,
+                                                       nh, nkv);
     else if (hd == 64)
-        k_qk_rope_append<64><<<grid, 128, 0, s>>>(qkv, M, qkv_stride, q_norm, k_norm, eps, rope, row_seq, seq0,
-                                                  row_pos, pos0, kv_layer, seq_stride, kvsel_stride, head_stride,
-                                                  nh, nkv);
+        k_qk_rope_append<64, KT><<<grid, 128, 0, s>>>(qkv, M, qkv_stride, q_norm, k_norm, eps, rope, row_seq, seq0,
+                                                      row_pos, pos0, kv_layer, seq_stride, kvsel_stride, head_stride,
+                                                      nh, nkv);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();
+}
+
+cudaError_t launch_qk_rope_append(float *qkv, int M, int qkv_stride, const float *q_norm, const float *k_norm,
+                                  float eps, const float2 *rope, const int32_t *row_seq, int seq0,
+                                  const int32_t *row_pos, int pos0, void *kv_layer, size_t seq_stride,
+                                  size_t kvsel_stride, size_t head_stride, int nh, int nkv, int hd, bool kv16,
+                                  cudaStream_t s) {
+    if (M <= 0) return cudaSuccess;
+    if (kv16)
+        return qk_rope_append_t(qkv, M, qkv_stride, q_norm, k_norm, eps, rope, row_seq, seq0, row_pos, pos0,
+                                static_cast<__half *>(kv_layer), seq_stride, kvsel_stride, head_stride, nh, nkv, hd, s);
+    return qk_rope_append_t(qkv, M, qkv_stride, q_norm, k_norm, eps, rope, row_seq, seq0, row_pos, pos0,
+                            static_cast<float *>(kv_layer), seq_stride, kvsel_stride, head_stride, nh, nkv, hd, s);
 }
 
 cudaError_t launch_argmax_finalize(unsigned long long *key, int B, const DecodeIO *io, int32_t *next_token,
@@ -194,12 +208,17 @@ cudaError_t launch_argmax_finalize(unsigned long long *key, int B, const DecodeI
     return cudaGetLastError();
 }
 
-cudaError_t launch_copy_kv_rows(const float *kv_layer_seq, size_t kvsel_stride, size_t head_stride, int pos0, int n,
-                                int nkv, int hd, float *k_out, float *v_out, cudaStream_t s) {
+cudaError_t launch_copy_kv_rows(const void *kv_layer_seq, size_t kvsel_stride, size_t head_stride, int pos0, int n,
+                                int nkv, int hd, float *k_out, float *v_out, bool kv16, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
     const size_t total = static_cast<size_t>(n) * nkv * hd;
     const unsigned grid = static_cast<unsigned>(std::min<size_t>((total + 255) / 256, 4096));
-    k_copy_kv_rows<<<grid, 256, 0, s>>>(kv_layer_seq, kvsel_stride, head_stride, pos0, n, nkv, hd, k_out, v_out);
+    if (kv16)
+        k_copy_kv_rows<<<grid, 256, 0, s>>>(static_cast<const __half *>(kv_layer_seq), kvsel_stride, head_stride, pos0,
+                                            n, nkv, hd, k_out, v_out);
+    else
+        k_copy_kv_rows<<<grid, 256, 0, s>>>(static_cast<const float *>(kv_layer_seq), kvsel_stride, head_stride, pos0,
+                                            n, nkv, hd, k_out, v_out);
     return cudaGetLastError();
 }
 

@@ -109,7 +109,8 @@ struct qw3_model {
     float *out_norm = nullptr;
     float2 *rope = nullptr;
 
-    float *kv = nullptr;
+    void *kv = nullptr;    // f32, or half when kv16
+    bool kv16 = false;
     size_t head_stride = 0, kvsel_stride = 0, seq_stride = 0, layer_stride = 0;
     std::vector<int32_t> seq_len;
 
@@ -142,6 +143,14 @@ struct qw3_model {
     StepParams sp{};
     int step_trace_words = 0;
 };
+
+namespace {
+// Address of (layer, seq)'s block of the KV cache.
+void *kv_at(const qw3_model *m, int layer, int seq) {
+    const size_t e = static_cast<size_t>(layer) * m->layer_stride + static_cast<size_t>(seq) * m->seq_stride;
+    return static_cast<uint8_t *>(m->kv) + e * (m->kv16 ? 2 : 4);
+}
+}  // namespace
 
 namespace {
 
@@ -332,7 +341,7 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
         }
         AttnDecodeArgs at{};
         at.qkv = m->qkv; at.qkv_stride = m->qkv_w; at.q_norm = L.q_norm; at.k_norm = L.k_norm; at.eps = c.rms_eps;
-        at.rope = m->rope; at.kv = m->kv + static_cast<size_t>(l) * m->layer_stride;
+        at.rope = m->rope; at.kv = kv_at(m, l, 0); at.kv16 = m->kv16;
         at.seq_stride = m->seq_stride; at.kvsel_stride = m->kvsel_stride; at.head_stride = m->head_stride;
         at.seq_ids = m->d_seq; at.pos = m->d_pos; at.nh = nh; at.nkv = nkv; at.hd = hd;
         at.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(hd)));
@@ -447,7 +456,7 @@ int setup_tensor_core_gemm(qw3_model *m) {
 // covered; the per-kernel path then serves batch 1 too.
 int setup_step(qw3_model *m) {
     const qw3_config &c = m->cfg;
-    if ((c.flags & QW3_FLAG_PER_KERNEL) || !step_supported(c)) return QW3_OK;
+    if ((c.flags & QW3_FLAG_PER_KERNEL) || m->kv16 || !step_supported(c)) return QW3_OK;
     // The step kernel wins where a layer is latency-bound (a few hundred KB
     // of weights per SM); past that a layer is bandwidth-bound and the
     // per-kernel chain, with two streaming CTAs per SM, moves it faster
@@ -493,7 +502,7 @@ int setup_step(qw3_model *m) {
     M_TRY(m, cudaMemcpyAsync(dl, m->layers.data(), sizeof(LayerDev) * c.n_layers, cudaMemcpyHostToDevice, m->stream));
     P.layers = dl;
     P.rope = m->rope;
-    P.kv = m->kv;
+    P.kv = static_cast<float *>(m->kv);
     P.seq_stride = m->seq_stride;
     P.kvsel_stride = m->kvsel_stride;
     P.head_stride = m->head_stride;
@@ -598,6 +607,7 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
 
     qw3_model *m = new qw3_model();
     m->cfg = *cfg;
+    m->kv16 = (cfg->flags & QW3_FLAG_KV_F16) != 0;
     auto bail = [&](int rc) {
         if (m->stream) cudaStreamSynchronize(m->stream);
         const std::string msg = m->err;
@@ -708,7 +718,7 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
     m->seq_stride = 2 * m->kvsel_stride;
     m->layer_stride = m->seq_stride * c.max_seqs;
     {
-        const size_t bytes = m->layer_stride * c.n_layers * sizeof(float);
+        const size_t bytes = m->layer_stride * c.n_layers * (m->kv16 ? 2 : 4);
         if (cudaError_t e = model_alloc(m, reinterpret_cast<void **>(&m->kv), bytes); e != cudaSuccess)
             return bail(cuda_err(m, e, "KV cache"));
     }
@@ -801,19 +811,19 @@ int qw3_prefill(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n,
         M_TRY(m, launch_embed(tokens_dev + off, M, m->embd, m->px, false, s));
         for (int l = 0; l < c.n_layers; ++l) {
             const LayerDev &L = m->layers[l];
-            float *kvl = m->kv + static_cast<size_t>(l) * m->layer_stride;
+            void *kvl = kv_at(m, l, 0);
             M_TRY(m, launch_rmsnorm_rows(m->px, M, H, L.attn_norm, c.rms_eps, m->ph, s));
             M_TRY(m, launch_gemm(m->ph, M, H, L.qkv, m->pqkv, GEMV_STORE, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
             M_TRY(m, launch_qk_rope_append(m->pqkv, M, m->qkv_w, L.q_norm, L.k_norm, c.rms_eps, m->rope, nullptr, seq,
                                            nullptr, pos0, kvl, m->seq_stride, m->kvsel_stride, m->head_stride, nh,
-                                           nkv, hd, s));
+                                           nkv, hd, m->kv16, s));
             if (m->kvpack && M >= kAttnPrefillTcMinRows) {
-                M_TRY(m, launch_attn_prefill_tc(m->pqkv, M, m->qkv_w, kvl, 0, static_cast<size_t>(seq) * m->seq_stride,
-                                                m->kvsel_stride, m->head_stride, pos0, nh, nkv, hd, scale, m->po,
-                                                m->kvpack, m->d_status, s));
+                M_TRY(m, launch_attn_prefill_tc(m->pqkv, M, m->qkv_w, kv_at(m, l, seq), m->kvsel_stride,
+                                                m->head_stride, pos0, nh, nkv, hd, scale, m->po, m->kvpack,
+                                                m->d_status, m->kv16, s));
             } else {
-                M_TRY(m, launch_attn_prefill(m->pqkv, M, m->qkv_w, kvl, 0, static_cast<size_t>(seq) * m->seq_stride,
-                                             m->kvsel_stride, m->head_stride, pos0, nh, nkv, hd, scale, m->po, s));
+                M_TRY(m, launch_attn_prefill(m->pqkv, M, m->qkv_w, kv_at(m, l, seq), m->kvsel_stride, m->head_stride,
+                                             pos0, nh, nkv, hd, scale, m->po, m->kv16, s));
             }
             M_TRY(m, launch_gemm(m->po, M, qw, L.o, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
             M_TRY(m, launch_rmsnorm_rows(m->px, M, H, L.ffn_norm, c.rms_eps, m->ph, s));
@@ -937,9 +947,8 @@ int qw3_debug_read_kv(qw3_model *m, int32_t layer, int32_t seq, int32_t pos0, in
     if (layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 || static_cast<int64_t>(pos0) + n > c.max_seq_len ||
         !k_out_dev || !v_out_dev || misaligned(k_out_dev, 4) || misaligned(v_out_dev, 4))
         return fail(m, QW3_ERR_INVALID_ARG, "bad KV read range");
-    const float *base = m->kv + static_cast<size_t>(layer) * m->layer_stride + static_cast<size_t>(seq) * m->seq_stride;
-    M_TRY(m, launch_copy_kv_rows(base, m->kvsel_stride, m->head_stride, pos0, n, c.n_kv_heads, c.head_dim, k_out_dev,
-                                 v_out_dev, m->stream));
+    M_TRY(m, launch_copy_kv_rows(kv_at(m, layer, seq), m->kvsel_stride, m->head_stride, pos0, n, c.n_kv_heads,
+                                 c.head_dim, k_out_dev, v_out_dev, m->kv16, m->stream));
     return QW3_OK;
 }
 

@@ -106,8 +106,9 @@ struct AttnDecodeArgs {
     const float *q_norm, *k_norm;
     float eps;
     const float2 *rope;   // [max_seq_len][hd/2] (cos, sin)
-    float *kv;            // this layer's cache: [seq][K|V][kv_head][capacity][head_dim]
-    size_t seq_stride, kvsel_stride, head_stride;  // floats
+    void *kv;             // this layer's cache: [seq][K|V][kv_head][capacity][head_dim]
+    int kv16;             // 1: IEEE half elements, 0: f32
+    size_t seq_stride, kvsel_stride, head_stride;  // elements
     const int32_t *seq_ids;  // [B]
     const int32_t *pos;      // [B] position of the new token
     int nh, nkv, hd;
@@ -186,29 +187,31 @@ cudaError_t launch_pack_w(const QMat &W, uint8_t *dst, cudaStream_t s);
 cudaError_t launch_gemm_tc(const float *A, int M, int K, const QMat &W, float *C, int mode,
                            unsigned long long *argmax_key, const DecodeIO *io, int32_t *status, uint8_t *apack,
                            cudaStream_t s, const GemmSplitK *sk = nullptr);
+// KV cache pointers below are the byte address of the layer's (or the
+// sequence's) first element; element strides are in elements; kv16 selects
+// IEEE half elements instead of f32.
 cudaError_t launch_qk_rope_append(float *qkv, int M, int qkv_stride, const float *q_norm,
                                   const float *k_norm, float eps, const float2 *rope,
                                   const int32_t *row_seq, int seq0, const int32_t *row_pos, int pos0,
-                                  float *kv_layer, size_t seq_stride, size_t kvsel_stride,
-                                  size_t head_stride, int nh, int nkv, int hd, cudaStream_t s);
-cudaError_t launch_attn_prefill(const float *qkv, int M, int qkv_stride, const float *kv,
-                                size_t layer_off, size_t seq_off, size_t kvsel_stride,
-                                size_t head_stride, int pos0, int nh, int nkv, int hd,
-                                float scale, float *out, cudaStream_t s);
+                                  void *kv_layer, size_t seq_stride, size_t kvsel_stride,
+                                  size_t head_stride, int nh, int nkv, int hd, bool kv16, cudaStream_t s);
+cudaError_t launch_attn_prefill(const float *qkv, int M, int qkv_stride, const void *kv_seq,
+                                size_t kvsel_stride, size_t head_stride, int pos0, int nh, int nkv, int hd,
+                                float scale, float *out, bool kv16, cudaStream_t s);
 // Causal prefill attention on tensor cores (attn_prefill_tc.cu): packs the
 // sequence's K/V of the layer into kvpack (attn_prefill_tc_pack_bytes) and
 // runs one CTA per (128-query tile, head); for chunks of >= 128 rows.
 constexpr int kAttnPrefillTcMinRows = 128;
 size_t attn_prefill_tc_pack_bytes(int hd, int nkv, int max_seq_len);
 cudaError_t configure_attn_prefill_tc();
-cudaError_t launch_attn_prefill_tc(const float *qkv, int M, int qkv_stride, const float *kv, size_t layer_off,
-                                   size_t seq_off, size_t kvsel_stride, size_t head_stride, int pos0, int nh, int nkv,
-                                   int hd, float scale, float *out, uint8_t *kvpack, int32_t *status, cudaStream_t s);
+cudaError_t launch_attn_prefill_tc(const float *qkv, int M, int qkv_stride, const void *kv_seq, size_t kvsel_stride,
+                                   size_t head_stride, int pos0, int nh, int nkv, int hd, float scale, float *out,
+                                   uint8_t *kvpack, int32_t *status, bool kv16, cudaStream_t s);
 cudaError_t launch_argmax_finalize(unsigned long long *key, int B, const DecodeIO *io,
                                    int32_t *next_token, int32_t *step_ctr, int32_t *pos_inc,
                                    int32_t *status, cudaStream_t s);
-cudaError_t launch_copy_kv_rows(const float *kv_layer_seq, size_t kvsel_stride, size_t head_stride,
-                                int pos0, int n, int nkv, int hd, float *k_out, float *v_out,
+cudaError_t launch_copy_kv_rows(const void *kv_layer_seq, size_t kvsel_stride, size_t head_stride,
+                                int pos0, int n, int nkv, int hd, float *k_out, float *v_out, bool kv16,
                                 cudaStream_t s);
 
 }  // namespace qw3
@@ -353,6 +356,16 @@ __device__ __forceinline__ float dsmem_ld(uint32_t addr) {
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---- KV cache element (f32, or IEEE half for a QW3_FLAG_KV_F16 model)
+__device__ __forceinline__ float kv_f32(float v) { return v; }
+__device__ __forceinline__ float kv_f32(__half v) { return __half2float(v); }
+template <typename KT>
+__device__ __forceinline__ KT kv_cvt(float v);
+template <>
+__device__ __forceinline__ float kv_cvt<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __half kv_cvt<__half>(float v) { return __float2half_rn(v); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -33,6 +33,7 @@ QW3_FLAG_NO_PDL = 0x2
 QW3_FLAG_TRACE = 0x4
 QW3_FLAG_PER_KERNEL = 0x8
 QW3_FLAG_TEST_NO_WAIT = 0x10
+QW3_FLAG_KV_F16 = 0x20
 
 # Every entry point of include/qw3.h, in declaration order.
 EXPORTS = (

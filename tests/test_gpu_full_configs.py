@@ -12,7 +12,7 @@ import pytest
 
 from oracle import qw3_oracle as orc
 from quantized_transformer_decode_gb300 import inputs
-from parity import assert_logits_close, cuda_ints
+from parity import assert_argmax, assert_ids_prefix, assert_logits_close, cuda_ints
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -103,16 +103,16 @@ def test_8b_geometry_two_layers(torch):
     with Qw3Model.from_f32(shape, inputs.iter_weights(shape, seed), max_seq_len=P + steps + 1, max_prefill=64) as gm:
         lg, am = gm.prefill(0, cuda_ints(prompt))
         assert_logits_close(_np(lg), logits[0], "8B-geometry prefill")
-        assert int(_np(am)[0]) == ids[0]
+        assert_argmax(int(_np(am)[0]), ids[0], logits[0], "8B-geometry prefill")
         for s in range(steps):
             lg, am = gm.decode(cuda_ints([ids[s]]), [P + s])
             assert_logits_close(_np(lg)[0], logits[s + 1], f"8B-geometry step {s + 1}")
-            assert int(_np(am)[0]) == ids[s + 1]
+            assert_argmax(int(_np(am)[0]), ids[s + 1], logits[s + 1], f"8B-geometry step {s + 1}")
         gm.reset(0)
         _, am = gm.prefill(0, cuda_ints(prompt), want_logits=False)
         out = gm.generate_greedy(am, steps)
         gm.sync()
-        assert [int(_np(am)[0])] + [int(v) for v in _np(out)[:, 0]] == ids
+        assert_ids_prefix([int(_np(am)[0])] + [int(v) for v in _np(out)[:, 0]], ids, logits)
 
 
 def test_8b_full_size_properties(torch):

@@ -2,7 +2,8 @@
 512 seeded tokens, then greedy decode at batch 1 in the launch configuration
 the benchmark times (captured graph, qw3_generate_greedy).
 
-Free-running greedy ids must equal the oracle's for 64 steps; logits are
+Free-running greedy ids must equal the oracle's for 64 steps (up to the first
+near tie of the oracle's own rows, the rule stated in parity.py); logits are
 checked under teacher forcing on the prefill row and every step.
 """
 import os
@@ -12,7 +13,7 @@ import pytest
 
 from oracle import qw3_oracle as orc
 from quantized_transformer_decode_gb300 import inputs
-from parity import assert_logits_close, cuda_ints
+from parity import assert_argmax, assert_ids_prefix, assert_logits_close, cuda_ints
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -44,8 +45,8 @@ def test_greedy_ids_bit_exact(pair):
     out = gm.generate_greedy(am, w.decode_steps)   # the full 256-step run the benchmark times
     gm.sync()
     got = [int(am.cpu()[0])] + [int(v) for v in out.cpu().numpy()[:, 0]]
-    first_bad = next((i for i in range(len(ids)) if got[i] != ids[i]), None)
-    assert first_bad is None, f"first divergence at id {first_bad}: {got[first_bad]} vs {ids[first_bad]}"
+    w_, _, _, _, _, logits = pair
+    assert_ids_prefix(got[:len(ids)], ids, logits, "0.6B greedy ids")
     assert gm.seq_len(0) == w.prompt_len + w.decode_steps
 
 
@@ -57,7 +58,7 @@ def test_teacher_forced_logits(pair):
     for s in range(STEPS):
         lg, am = gm.decode(cuda_ints([ids[s]]), [w.prompt_len + s])
         worst.append(assert_logits_close(lg.cpu().numpy()[0], logits[s + 1], f"step {s + 1}"))
-        assert int(am.cpu()[0]) == ids[s + 1]
+        assert_argmax(int(am.cpu()[0]), ids[s + 1], logits[s + 1], f"step {s + 1}")
     gm.sync()
     ma = max(x[0] for x in worst)
     rel = max(x[1] for x in worst)

@@ -11,7 +11,7 @@ import pytest
 
 from oracle import qw3_oracle as orc
 from quantized_transformer_decode_gb300 import inputs
-from parity import assert_logits_close, build_pair, cuda_ints
+from parity import assert_argmax, assert_ids_prefix, assert_logits_close, build_pair, cuda_ints
 
 pytestmark = pytest.mark.gpu
 
@@ -45,11 +45,11 @@ def run_greedy_case(torch, shape, seed, prompt_len, steps, flags=0, max_prefill=
         # teacher-forced: feed the oracle's ids, compare every row
         lg, am = gm.prefill(0, cuda_ints(prompt))
         assert_logits_close(_np(lg), ologits[0], "prefill last row")
-        assert int(_np(am)[0]) == ids[0]
+        assert_argmax(int(_np(am)[0]), ids[0], ologits[0], "prefill argmax")
         for s in range(steps):
             lg, am = gm.decode(cuda_ints([ids[s]]), [prompt_len + s])
             assert_logits_close(_np(lg)[0], ologits[s + 1], f"decode step {s + 1}")
-            assert int(_np(am)[0]) == ids[s + 1], f"argmax at step {s + 1}"
+            assert_argmax(int(_np(am)[0]), ids[s + 1], ologits[s + 1], f"argmax at step {s + 1}")
         gm.sync()
         # free-running on a fresh sequence state: ids bit-exact
         gm.reset(0)
@@ -57,7 +57,7 @@ def run_greedy_case(torch, shape, seed, prompt_len, steps, flags=0, max_prefill=
         out = gm.generate_greedy(am, steps)
         gm.sync()
         got = [int(_np(am)[0])] + [int(v) for v in _np(out)[:, 0]]
-        assert got == ids
+        assert_ids_prefix(got, ids, ologits)
         assert gm.seq_len(0) == prompt_len + steps
         return om, gm, ids
     except Exception:
@@ -90,35 +90,26 @@ def test_long_capacity_split_over_clusters(torch, prompt_len):
     """A model built for 4096+ positions decodes batch 1 with each kv head's
     context split over several clusters whose partials merge in global
     memory; against the oracle at short and medium contexts (many splits
-    hold no position at 70). Teacher-forced logits on every step; argmax
-    ids bit-exact except where the oracle's own top-2 margin is below 1e-4
-    (at 600 tokens step 6 has two logits 1.7e-5 apart: either is the
-    greedy token at f32 precision), and free-running ids up to that step."""
+    hold no position at 70). Teacher-forced logits on every step; ids
+    under the near-tie rule (at 600 tokens step 6 has two logits 1.7e-5
+    apart: either is the greedy token at f32 precision)."""
     shape, seed, steps = MID, 7, 8
     om, gm = build_pair(shape, seed, max_seq_len=4200, max_prefill=256, flags=PER_KERNEL)
     try:
         prompt = inputs.prompt_tokens(shape, seed, prompt_len)
         ids, ologits = om.generate_greedy(om.new_cache(prompt_len + steps + 1), prompt, steps)
-        tie_free = steps + 1
-        for s, lg in enumerate(ologits):
-            top2 = np.sort(lg)[-2:]
-            if top2[1] - top2[0] < 1e-4:
-                tie_free = min(tie_free, s)
         lg, am = gm.prefill(0, cuda_ints(prompt))
         assert_logits_close(_np(lg), ologits[0], "prefill last row")
-        assert int(_np(am)[0]) == ids[0]
+        assert_argmax(int(_np(am)[0]), ids[0], ologits[0], "prefill argmax")
         for s in range(steps):
             lg, am = gm.decode(cuda_ints([ids[s]]), [prompt_len + s])
-            want = ologits[s + 1]
-            assert_logits_close(_np(lg)[0], want, f"decode step {s + 1}")
-            got = int(_np(am)[0])
-            assert got == ids[s + 1] or want[ids[s + 1]] - want[got] < 1e-4, f"argmax at step {s + 1}"
+            assert_logits_close(_np(lg)[0], ologits[s + 1], f"decode step {s + 1}")
+            assert_argmax(int(_np(am)[0]), ids[s + 1], ologits[s + 1], f"argmax at step {s + 1}")
         gm.reset(0)
         _, am = gm.prefill(0, cuda_ints(prompt), want_logits=False)
         out = gm.generate_greedy(am, steps)
         gm.sync()
-        got = [int(_np(am)[0])] + [int(v) for v in _np(out)[:, 0]]
-        assert got[:tie_free] == ids[:tie_free]
+        assert_ids_prefix([int(_np(am)[0])] + [int(v) for v in _np(out)[:, 0]], ids, ologits)
     finally:
         gm.close()
 
@@ -230,7 +221,7 @@ def test_batched_decode_matches_per_sequence_oracle(torch, B):
             for b in range(B):
                 o = om.forward(caches[b][0], [toks[b]], pos[b])
                 assert_logits_close(lg[b], o, f"B={B} seq {b} step {step}")
-                assert int(am[b]) == orc.argmax_lowest(o)
+                assert_argmax(int(am[b]), orc.argmax_lowest(o), o, f"B={B} seq {b} step {step}")
                 toks[b] = int(am[b])
                 pos[b] += 1
         gm.sync()
@@ -245,18 +236,18 @@ def test_batched_generate_greedy(torch):
     B, steps = 3, 8
     om, gm = build_pair(shape, 0, max_seqs=B, max_seq_len=64, max_prefill=32)
     try:
-        firsts, want = [], []
+        firsts, want, rows = [], [], []
         for b in range(B):
             pre = inputs.batch_prefix_tokens(shape, 0, b, 9 + b)
-            ids, _ = om.generate_greedy(om.new_cache(64), pre, steps)
+            ids, lg = om.generate_greedy(om.new_cache(64), pre, steps)
             want.append(ids)
+            rows.append(lg)
             _, am = gm.prefill(b, cuda_ints(pre), want_logits=False)
             firsts.append(int(_np(am)[0]))
-        assert firsts == [w[0] for w in want]
         out = _np(gm.generate_greedy(cuda_ints(firsts), steps))
         gm.sync()
         for b in range(B):
-            assert [int(v) for v in out[:, b]] == want[b][1:]
+            assert_ids_prefix([firsts[b]] + [int(v) for v in out[:, b]], want[b], rows[b], f"sequence {b}")
     finally:
         gm.close()
 
@@ -270,7 +261,7 @@ def test_chunked_prefill_equals_single_pass(torch):
     lg, am = gm.prefill(0, cuda_ints(prompt))
     o = om.forward(om.new_cache(128), prompt, 0)
     assert_logits_close(_np(lg), o, "chunked prefill")
-    assert int(_np(am)[0]) == orc.argmax_lowest(o)
+    assert_argmax(int(_np(am)[0]), orc.argmax_lowest(o), o, "chunked prefill")
     gm.close()
 
 
