@@ -156,6 +156,16 @@ QW3_API int qw3_destroy(qw3_model *m);
 QW3_API int qw3_prefill(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n,
                 float *last_logits_dev, int32_t *argmax_dev);
 
+/* All-logits forward ("A transformer from scratch", 12.3.7 and 12.5: the
+ * step that returns logits for every appended row, the shape a speculative
+ * verify needs): append n tokens to sequence `seq` exactly as qw3_prefill
+ * does and return every appended row's logits in logits_dev (f32 [n][V],
+ * required) and, when argmax_dev (int32 [n]) is not NULL, each row's greedy
+ * argmax (lowest index among equal maxima). Row i is the prediction after
+ * token i. Errors as qw3_prefill; nothing is appended on an error. */
+QW3_API int qw3_forward_all_logits(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n,
+                                   float *logits_dev, int32_t *argmax_dev);
+
 /* One decode step for B sequences at once (course 12.5, batch decode: one
  * pass over the weights, RoPE positions, KV appends and attention per
  * sequence). seqs_host: int32 [B] distinct slot ids, NULL means 0..B-1.

@@ -3,6 +3,7 @@
 // 12.3.4, 12.4), the argmax finish of the batched path (12.6) and a KV
 // read-back for diagnostics.
 #include <algorithm>
+#include <climits>
 
 #include "qw3_internal.cuh"
 
@@ -108,6 +109,57 @@ __global__ void __launch_bounds__(128) k_qk_rope_append(float *__restrict__ qkv,
     }
 }
 
+// One CTA per row: each thread keeps the first maximum of its strided
+// columns, then (value, index) pairs reduce to the largest value, lowest
+// index on ties.
+__global__ void __launch_bounds__(512) k_argmax_rows(const float *__restrict__ logits, int V,
+                                                     int32_t *__restrict__ out, int32_t *status) {
+    __shared__ float sv[16];
+    __shared__ int si[16];
+    const float *row = logits + static_cast<size_t>(blockIdx.x) * V;
+    float best = -INFINITY;
+    int bi = INT_MAX;
+    bool nan = false;
+    for (int i = threadIdx.x; i < V; i += blockDim.x) {
+        const float v = row[i];
+        if (v != v) nan = true;
+        else if (v > best || bi == INT_MAX) {
+            best = v;
+            bi = i;
+        }
+    }
+    if (nan) record_status(status, QW3_ERR_NONFINITE);
+    auto better = [](float v, int i, float bv, int bj) { return v > bv || (v == bv && i < bj); };
+    for (int o = 16; o > 0; o >>= 1) {
+        const float v = __shfl_xor_sync(0xffffffffu, best, o);
+        const int i = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(v, i, best, bi)) {
+            best = v;
+            bi = i;
+        }
+    }
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (lane == 0) {
+        sv[warp] = best;
+        si[warp] = bi;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x / 32;
+        best = lane < nw ? sv[lane] : -INFINITY;
+        bi = lane < nw ? si[lane] : INT_MAX;
+        for (int o = 16; o > 0; o >>= 1) {
+            const float v = __shfl_xor_sync(0xffffffffu, best, o);
+            const int i = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (better(v, i, best, bi)) {
+                best = v;
+                bi = i;
+            }
+        }
+        if (lane == 0) out[blockIdx.x] = bi;
+    }
+}
+
 __global__ void k_argmax_finalize(unsigned long long *__restrict__ key, int B, const DecodeIO *io,
                                   int32_t *next_token, int32_t *step_ctr, int32_t *pos_inc, int32_t *status) {
     const int step = step_ctr ? *step_ctr : 0;
@@ -200,6 +252,12 @@ cudaError_t launch_qk_rope_append(float *qkv, int M, int qkv_stride, const float
                                 static_cast<__half *>(kv_layer), seq_stride, kvsel_stride, head_stride, nh, nkv, hd, s);
     return qk_rope_append_t(qkv, M, qkv_stride, q_norm, k_norm, eps, rope, row_seq, seq0, row_pos, pos0,
                             static_cast<float *>(kv_layer), seq_stride, kvsel_stride, head_stride, nh, nkv, hd, s);
+}
+
+cudaError_t launch_argmax_rows(const float *logits, int M, int V, int32_t *out, int32_t *status, cudaStream_t s) {
+    if (M < 1 || V < 1) return cudaErrorInvalidValue;
+    k_argmax_rows<<<M, 512, 0, s>>>(logits, V, out, status);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_argmax_finalize(unsigned long long *key, int B, const DecodeIO *io, int32_t *next_token,

@@ -790,12 +790,18 @@ int qw3_destroy(qw3_model *m) {
     return QW3_OK;
 }
 
-int qw3_prefill(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n, float *last_logits_dev,
-                int32_t *argmax_dev) {
+namespace {
+
+// Append n rows of sequence seq (max_prefill rows per pass through the
+// layers). Outputs: the last row's logits and argmax (nullable), or, when
+// all_logits is given, every row's logits [n][V] and argmax [n] (nullable).
+int forward_rows(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n, float *last_logits_dev,
+                 int32_t *argmax_dev, float *all_logits, int32_t *all_argmax) {
     if (check_model(m)) return QW3_ERR_INVALID_ARG;
     if (int rc = check_seq(m, seq)) return rc;
-    if (!tokens_dev || n < 1) return fail(m, QW3_ERR_INVALID_ARG, "prefill needs n >= 1 tokens");
-    if (misaligned(tokens_dev, 4) || misaligned(last_logits_dev, 4) || misaligned(argmax_dev, 4))
+    if (!tokens_dev || n < 1) return fail(m, QW3_ERR_INVALID_ARG, "a forward needs n >= 1 tokens");
+    if (misaligned(tokens_dev, 4) || misaligned(last_logits_dev, 4) || misaligned(argmax_dev, 4) ||
+        misaligned(all_logits, 4) || misaligned(all_argmax, 4))
         return fail(m, QW3_ERR_INVALID_ARG, "device buffers must be 4-byte aligned");
     const qw3_config &c = m->cfg;
     const int len = m->seq_len[seq];
@@ -830,7 +836,14 @@ int qw3_prefill(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n,
             M_TRY(m, launch_gemm(m->ph, M, H, L.gu, m->pact, GEMV_SWIGLU, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
             M_TRY(m, launch_gemm(m->pact, M, I, L.down, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
         }
-        if (off + M == n && (last_logits_dev || argmax_dev)) {
+        if (all_logits) {
+            // final norm of every row, the lm_head over all of them, each row's argmax
+            float *lg = all_logits + static_cast<size_t>(off) * c.vocab;
+            M_TRY(m, launch_rmsnorm_rows(m->px, M, H, m->out_norm, c.rms_eps, m->ph, s));
+            M_TRY(m, launch_gemm(m->ph, M, H, m->out, lg, GEMV_STORE, nullptr, nullptr, s, m->d_status, m->apack,
+                                 &m->gsk));
+            if (all_argmax) M_TRY(m, launch_argmax_rows(lg, M, c.vocab, all_argmax + off, m->d_status, s));
+        } else if (off + M == n && (last_logits_dev || argmax_dev)) {
             GemvArgs a{};
             a.W = m->out; a.N = c.vocab; a.K = H; a.B = 1;
             a.x = m->px + static_cast<size_t>(M - 1) * H; a.norm_w = m->out_norm; a.eps = c.rms_eps;
@@ -841,6 +854,20 @@ int qw3_prefill(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n,
     }
     m->seq_len[seq] = len + n;
     return QW3_OK;
+}
+
+}  // namespace
+
+int qw3_prefill(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n, float *last_logits_dev,
+                int32_t *argmax_dev) {
+    return forward_rows(m, seq, tokens_dev, n, last_logits_dev, argmax_dev, nullptr, nullptr);
+}
+
+int qw3_forward_all_logits(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n, float *logits_dev,
+                           int32_t *argmax_dev) {
+    if (check_model(m)) return QW3_ERR_INVALID_ARG;
+    if (!logits_dev) return fail(m, QW3_ERR_INVALID_ARG, "all-logits forward needs a logits buffer");
+    return forward_rows(m, seq, tokens_dev, n, nullptr, nullptr, logits_dev, argmax_dev);
 }
 
 int qw3_decode(qw3_model *m, int32_t B, const int32_t *seqs_host, const int32_t *tokens_dev, const int32_t *pos_host,

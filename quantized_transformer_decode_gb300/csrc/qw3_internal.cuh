@@ -207,6 +207,9 @@ cudaError_t configure_attn_prefill_tc();
 cudaError_t launch_attn_prefill_tc(const float *qkv, int M, int qkv_stride, const void *kv_seq, size_t kvsel_stride,
                                    size_t head_stride, int pos0, int nh, int nkv, int hd, float scale, float *out,
                                    uint8_t *kvpack, int32_t *status, bool kv16, cudaStream_t s);
+// Greedy argmax of each of M logits rows [M][V] (lowest index among equal
+// maxima); a NaN records QW3_ERR_NONFINITE.
+cudaError_t launch_argmax_rows(const float *logits, int M, int V, int32_t *out, int32_t *status, cudaStream_t s);
 cudaError_t launch_argmax_finalize(unsigned long long *key, int B, const DecodeIO *io,
                                    int32_t *next_token, int32_t *step_ctr, int32_t *pos_inc,
                                    int32_t *status, cudaStream_t s);

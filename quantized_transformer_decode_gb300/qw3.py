@@ -37,7 +37,7 @@ QW3_FLAG_KV_F16 = 0x20
 
 # Every entry point of include/qw3.h, in declaration order.
 EXPORTS = (
-    "qw3_create", "qw3_destroy", "qw3_prefill", "qw3_decode", "qw3_generate_greedy",
+    "qw3_create", "qw3_destroy", "qw3_prefill", "qw3_forward_all_logits", "qw3_decode", "qw3_generate_greedy",
     "qw3_reset", "qw3_truncate", "qw3_seq_len", "qw3_debug_read_kv", "qw3_debug_read_trace",
     "qw3_decode_plan", "qw3_sync", "qw3_stream", "qw3_status_string", "qw3_last_error",
     "qw3_q8_0_quantize", "qw3_q8_0_dequantize", "qw3_q8_0_gemv", "qw3_q8_0_gemv_splitk_noalloc",
@@ -95,6 +95,7 @@ def lib() -> ctypes.CDLL:
         "qw3_create": (ctypes.c_int, [ctypes.POINTER(Qw3Config), ctypes.POINTER(Qw3Weights), _P, ctypes.POINTER(_P)]),
         "qw3_destroy": (ctypes.c_int, [_P]),
         "qw3_prefill": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _P]),
+        "qw3_forward_all_logits": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _P]),
         "qw3_decode": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P]),
         "qw3_generate_greedy": (ctypes.c_int, [_P, _I32, _P, _I32, _P, _P]),
         "qw3_reset": (ctypes.c_int, [_P, _I32]),
@@ -149,6 +150,10 @@ def qw3_destroy(h: int) -> None:
 
 def qw3_prefill(h: int, seq: int, tokens_ptr: int, n: int, last_logits_ptr: int = 0, argmax_ptr: int = 0) -> None:
     _check(lib().qw3_prefill(h, seq, tokens_ptr, n, last_logits_ptr or None, argmax_ptr or None), h)
+
+
+def qw3_forward_all_logits(h: int, seq: int, tokens_ptr: int, n: int, logits_ptr: int, argmax_ptr: int = 0) -> None:
+    _check(lib().qw3_forward_all_logits(h, seq, tokens_ptr, n, logits_ptr or None, argmax_ptr or None), h)
 
 
 def qw3_decode(h: int, B: int, seqs: Optional[Sequence[int]], tokens_ptr: int, pos: Sequence[int],
@@ -353,6 +358,18 @@ class Qw3Model:
         with _Ordered(self):
             qw3_prefill(self.h, seq, tokens.data_ptr(), tokens.numel(),
                         logits.data_ptr() if logits is not None else 0, am.data_ptr())
+        return logits, am
+
+    def forward_all_logits(self, seq: int, tokens):
+        """Append tokens (CUDA int32 tensor [n]) to sequence seq; return
+        (logits [n, vocab], argmax int32 [n]) of every appended row."""
+        torch = _torch()
+        tokens = tokens.to(torch.int32).contiguous()
+        n = tokens.numel()
+        logits = torch.empty((n, self.shape.vocab), dtype=torch.float32, device=tokens.device)
+        am = torch.empty(n, dtype=torch.int32, device=tokens.device)
+        with _Ordered(self):
+            qw3_forward_all_logits(self.h, seq, tokens.data_ptr(), n, logits.data_ptr(), am.data_ptr())
         return logits, am
 
     def decode(self, tokens, pos: Sequence[int], seqs: Optional[Sequence[int]] = None, want_logits: bool = True):

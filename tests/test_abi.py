@@ -123,6 +123,8 @@ def test_model_calls_reject_null_model(L):
     assert L.qw3_seq_len(None, 0, ctypes.byref(n)) == 1
     assert L.qw3_reset(None, 0) == 1
     assert L.qw3_decode(None, 1, None, 16, None, None, None) == 1
+    assert L.qw3_prefill(None, 0, 16, 1, None, None) == 1
+    assert L.qw3_forward_all_logits(None, 0, 16, 1, 16, None) == 1
     assert L.qw3_destroy(None) == 0
     assert L.qw3_stream(None) is None
 

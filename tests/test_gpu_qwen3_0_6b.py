@@ -76,3 +76,20 @@ def test_kv_rows_sampled(pair):
         k, v = gm.read_kv(layer, 0, 0, w.prompt_len)
         assert_logits_close(k.cpu().numpy(), c.k[layer], f"K layer {layer}", max_abs=2e-3, rel_l2=1e-4)
         assert_logits_close(v.cpu().numpy(), c.v[layer], f"V layer {layer}", max_abs=2e-3, rel_l2=1e-4)
+
+
+def test_verify_block_all_logits(pair):
+    """The speculative-verify shape at full size: after the prompt, one
+    all-logits forward over the first 8 greedy ids gives the oracle's 8
+    teacher-forced decode rows (cached == uncached: one multi-row step and
+    8 single-row steps compute the same rows)."""
+    w, _, gm, prompt, ids, logits = pair
+    k = min(8, STEPS)
+    gm.reset(0)
+    gm.prefill(0, cuda_ints(prompt), want_logits=False)
+    lg, am = gm.forward_all_logits(0, cuda_ints(ids[:k]))
+    lg, am = lg.cpu().numpy(), am.cpu().numpy()
+    for i in range(k):
+        assert_logits_close(lg[i], logits[i + 1], f"verify row {i}")
+        assert_argmax(int(am[i]), ids[i + 1], logits[i + 1], f"verify row {i}")
+    assert gm.seq_len(0) == w.prompt_len + k
