@@ -279,8 +279,10 @@ class QLinear:
             raise InvalidShape(f"in-dimension {cols} is not a multiple of {QK8_0}")
         self.rows, self.cols = rows, cols
         self.lazy = lazy
+        # the wire blocks themselves, [rows][cols/32 blocks] (the q8act path
+        # reads codes and scales)
+        self.blocks = np.asarray(blocks, dtype=np.uint8).reshape(rows, (cols // QK8_0) * Q8_0_BYTES)
         if lazy:
-            self.blocks = np.asarray(blocks, dtype=np.uint8).reshape(rows, (cols // QK8_0) * Q8_0_BYTES)
             self.w = None
         else:
             w32 = matrix_from_blocks(blocks, rows, cols)
@@ -302,6 +304,40 @@ class QLinear:
             r1 = min(self.rows, r0 + step)
             wc = self._rows32(r0, r1).astype(np.float64)
             out[:, r0:r1] = (x64 @ wc.T).astype(np.float32)
+        return out
+
+    def q8act(self, x: np.ndarray) -> np.ndarray:
+        """The pages' quantized matmul ("Model files and quantization", 11.9,
+        dotBlocks): each f32 input row is encoded to Q8_0 blocks by the 11.7
+        encoder; each (weight block, activation block) pair contributes the
+        i32 dot of their codes times w.d * a.d, evaluated in f32 as the page's
+        dotBlocks writes it ((w.d * a.d) * f32(acc)); the per-block results of
+        a row sum in f64. f32 out.
+
+        Reading of the pages: dotBlocks fixes the per-block arithmetic; the
+        sum over a row's blocks is not shown, and is done in f64 like every
+        other reduction here.
+        """
+        x32 = np.asarray(x, np.float32)
+        if x32.ndim != 2 or x32.shape[1] != self.cols:
+            raise InvalidShape(f"q8act input {x32.shape} for a [{self.rows}, {self.cols}] weight")
+        M, nb = x32.shape[0], self.cols // QK8_0
+        _, qa, da16 = q8_0_quantize_parts(x32.reshape(-1))
+        qa = qa.reshape(M, nb, QK8_0).astype(np.float64)         # codes, exact in f64
+        da = da16.astype(np.float32).reshape(M, nb)
+        out = np.empty((M, self.rows), dtype=np.float32)
+        step = 8192
+        for r0 in range(0, self.rows, step):
+            r1 = min(self.rows, r0 + step)
+            wd16, wq = q8_0_unpack(self.blocks[r0:r1].reshape(-1), (r1 - r0) * self.cols)
+            wd = wd16.astype(np.float32).reshape(r1 - r0, nb)
+            wq = wq.reshape(r1 - r0, nb, QK8_0).astype(np.float64)
+            acc_sum = np.zeros((M, r1 - r0), dtype=np.float64)
+            for b in range(nb):
+                acc = qa[:, b, :] @ wq[:, b, :].T                    # integer dots (|acc| < 2^19: exact)
+                scale = (wd[None, :, b] * da[:, b, None]).astype(np.float32)   # w.d * a.d in f32
+                acc_sum += (scale * acc.astype(np.float32)).astype(np.float32)
+            out[:, r0:r1] = acc_sum.astype(np.float32)
         return out
 
     def row(self, r: np.ndarray) -> np.ndarray:
@@ -431,6 +467,21 @@ class OracleModel:
         self.output_norm = norm("output_norm", s.hidden)
         # tied lm_head: no output.weight means the embedding table is reused
         self.output = self.tok_embd if s.tied else lin("output", s.vocab, s.hidden)
+        self.act = "f32"
+
+    def set_activations(self, kind: str) -> "OracleModel":
+        """How the linear layers take their inputs: "f32" (the workloads'
+        path, f64 dots over f32 activations) or "q8_0" (the pages' CPU path,
+        "Model files and quantization" 11.9: activations re-quantized to Q8_0
+        per row per call, integer block dots; QLinear.q8act). The embedding
+        gather is a dequantising row lookup either way."""
+        if kind not in ("f32", "q8_0"):
+            raise InvalidShape(f"activation kind {kind!r}")
+        self.act = kind
+        return self
+
+    def _lin(self, W: QLinear, x: np.ndarray) -> np.ndarray:
+        return W.q8act(x) if self.act == "q8_0" else W(x)
 
     @classmethod
     def from_f32(cls, shape, weights: dict, keep_f64: bool | None = None) -> "OracleModel":
@@ -465,20 +516,20 @@ class OracleModel:
         s = self.shape
         M = x.shape[0]
         h = rms_norm(x, lw.attn_norm, s.rms_eps)
-        q = lw.wq(h).reshape(M, s.n_heads, s.head_dim)
-        k = lw.wk(h).reshape(M, s.n_kv_heads, s.head_dim)
-        v = lw.wv(h).reshape(M, s.n_kv_heads, s.head_dim)
+        q = self._lin(lw.wq, h).reshape(M, s.n_heads, s.head_dim)
+        k = self._lin(lw.wk, h).reshape(M, s.n_kv_heads, s.head_dim)
+        v = self._lin(lw.wv, h).reshape(M, s.n_kv_heads, s.head_dim)
         q = rope_neox(rms_norm(q, lw.q_norm, s.rms_eps), positions, s.rope_theta)
         k = rope_neox(rms_norm(k, lw.k_norm, s.rms_eps), positions, s.rope_theta)
         cache.append_layer(li, k, v)
         kk, vv = cache.layer_rows(li, cache.len + M)
         o = attention(q, kk, vv, positions, 1.0 / math.sqrt(s.head_dim), self.kv_head_for_head)
-        return add_f32(x, lw.wo(o.reshape(M, s.q_width)))
+        return add_f32(x, self._lin(lw.wo, o.reshape(M, s.q_width)))
 
     def _ffn_block(self, lw: _Layer, x):
         s = self.shape
         h2 = rms_norm(x, lw.ffn_norm, s.rms_eps)
-        return add_f32(x, lw.wd(swiglu(lw.wg(h2), lw.wu(h2))))
+        return add_f32(x, self._lin(lw.wd, swiglu(self._lin(lw.wg, h2), self._lin(lw.wu, h2))))
 
     # -- entry points -------------------------------------------------------
 
@@ -509,8 +560,8 @@ class OracleModel:
         cache.advance(M)
         xf = rms_norm(x, self.output_norm, s.rms_eps)
         if all_logits:
-            return self.output(xf)
-        return self.output(xf[-1:])[0]
+            return self._lin(self.output, xf)
+        return self._lin(self.output, xf[-1:])[0]
 
     def generate_greedy(self, cache: KvCache, prompt, n_steps: int):
         """Prefill the prompt, then n_steps greedy decode steps (12.6).

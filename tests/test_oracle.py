@@ -492,3 +492,89 @@ def test_f16_kv_model_layer0_rows_are_rounded_f32_rows():
     g32, _ = om.generate_greedy(om.new_cache(20), prompt, 2)
     g16, _ = om.generate_greedy(om.new_cache(20, "f16"), prompt, 2)
     assert len(g16) == len(g32) == 3
+
+
+# ---- q8act: dynamic Q8_0 activations ("Model files and quantization", 11.9)
+
+def _qlinear(w32):
+    w32 = np.asarray(w32, np.float32)
+    return orc.QLinear(orc.q8_0_quantize(w32), w32.shape[0], w32.shape[1], keep_f64=True)
+
+
+def test_q8act_hand_worked_block():
+    """One weight block with d_w = 0.5 (codes 127, -1, 2, 0, ...) against
+    activations whose amax is 127, so d_a = 1 and the codes are the values
+    rounded half away from zero: 127, 1.5 -> 2, -2.5 -> -3, 0.5 -> 1.
+    The integer dot is 127*127 - 1*2 + 2*(-3) + 0*1 = 16121; times
+    d_w * d_a = 0.5 gives 8060.5. The f32-activation path would give
+    0.5 * (16129 - 1.5 - 5) = 8061.25."""
+    w = np.zeros((1, 32), np.float32)
+    w[0, :3] = [63.5, -0.5, 1.0]
+    x = np.zeros((1, 32), np.float32)
+    x[0, :5] = [127.0, 1.5, -2.5, 0.5, -0.49]
+    L = _qlinear(w)
+    assert float(L.q8act(x)[0, 0]) == 8060.5
+    assert float(L(x)[0, 0]) == 8061.25
+
+
+def test_q8act_equals_f32_path_on_representable_activations():
+    """Activations already of the form d * q with amax = 127 d and d a power
+    of two quantise to themselves, so the integer path computes the same
+    sum as the f32-activation path (up to the f32 rounding of each block's
+    (w.d * a.d) * acc product)."""
+    rng = np.random.default_rng(5)
+    w = rng.standard_normal((24, 96)).astype(np.float32)
+    q = rng.integers(-127, 128, size=(3, 96)).astype(np.float32)
+    q[:, ::32] = 127.0                                    # every block reaches amax = 127 d
+    x = (q * np.float32(2.0 ** -3)).astype(np.float32)
+    L = _qlinear(w)
+    wq = orc.matrix_from_blocks(L.blocks.reshape(-1), 24, 96).astype(np.float64)
+    # each block's product rounds once in f32 (half an ulp of its magnitude),
+    # the sum is exact otherwise: bound by 2^-23 * sum |w| |x|
+    tol = 2.0 ** -23 * (np.abs(x).astype(np.float64) @ np.abs(wq).T) + 1e-7
+    assert np.all(np.abs(L.q8act(x).astype(np.float64) - L(x).astype(np.float64)) <= tol)
+
+
+def test_q8act_error_within_the_activation_rounding_bound():
+    """Per element |x - d16 q| <= d / 2 + 127 |d - d16| <= 0.5625 d (the f16
+    scale is within 2^-11 of d), so per output row
+    |q8act - f32 path| <= sum over blocks of 0.5625 d_a * sum |w| of the block
+    (plus f32 rounding)."""
+    rng = np.random.default_rng(6)
+    w = rng.standard_normal((16, 128)).astype(np.float32)
+    x = (rng.standard_normal((4, 128)) * rng.uniform(0.1, 10.0, size=(4, 1))).astype(np.float32)
+    L = _qlinear(w)
+    wq = orc.matrix_from_blocks(L.blocks.reshape(-1), 16, 128).astype(np.float64)
+    d = np.abs(x).reshape(4, 4, 32).max(axis=2) / 127.0                       # [M, blocks]
+    absw = np.abs(wq).reshape(16, 4, 32).sum(axis=2)                           # [rows, blocks]
+    bound = 0.5625 * d @ absw.T                                                # [M, rows]
+    err = np.abs(L.q8act(x).astype(np.float64) - L(x).astype(np.float64))
+    assert np.all(err <= bound + 1e-5 * np.abs(L(x)) + 1e-6)
+    assert err.max() > 0          # it is a different path
+
+
+def test_q8act_power_of_two_scaling_and_zero():
+    """Scaling the activations by 4 scales d_a by 4 exactly and leaves the
+    codes alone, so the result scales by 4 exactly; a zero row gives zero."""
+    rng = np.random.default_rng(7)
+    L = _qlinear(rng.standard_normal((8, 64)))
+    x = rng.standard_normal((2, 64)).astype(np.float32)
+    np.testing.assert_array_equal(L.q8act(4.0 * x), 4.0 * L.q8act(x))
+    assert not L.q8act(np.zeros((1, 64), np.float32)).any()
+
+
+def test_q8act_model_mode_changes_only_the_linears():
+    """The model in q8_0 activation mode: its logits stay within the
+    activation-rounding noise of the f32 mode (relative L2 a few 1e-3 on the
+    tiny model) but are not equal to them; set_activations rejects unknown
+    kinds."""
+    shape = inputs.TINY
+    om = orc.OracleModel.from_f32(shape, inputs.generate_weights(shape, 0))
+    prompt = inputs.prompt_tokens(shape, 0, 12)
+    a = om.forward(om.new_cache(16), prompt, 0)
+    om.set_activations("q8_0")
+    b = om.forward(om.new_cache(16), prompt, 0)
+    rel = np.linalg.norm(a - b) / np.linalg.norm(a)
+    assert 0 < rel < 5e-2
+    with pytest.raises(orc.InvalidShape):
+        om.set_activations("q4")
