@@ -110,6 +110,12 @@ typedef struct qw3_config {
                                   keys and values are rounded to nearest
                                   even when appended. Batch-1 decode then
                                   runs the per-kernel chain.                  */
+#define QW3_FLAG_ACT_Q8 0x40     /* every linear layer takes its input rows
+                                  re-quantized to Q8_0 per 32-block on the
+                                  fly ("Model files and quantization", 11.9:
+                                  dynamic activations, integer block dots)
+                                  instead of f32. Batch-1 decode then runs
+                                  the per-kernel chain.                       */
 
 /* One decoder layer (minfer section 1). Q8_0 matrices [out][in]:
  *   attn_q [n_heads*head_dim][H], attn_k and attn_v [n_kv_heads*head_dim][H],
@@ -249,9 +255,22 @@ QW3_API int qw3_q8_0_dequantize(const void *blocks_dev, int64_t n, float *y_dev,
 
 /* y[b][r] = sum_k W[r][k] * x[b][k] for a raw Q8_0 matrix W [rows][cols/32]
  * (GGUF layout), x f32 [B][cols], y f32 [B][rows]; f32 accumulation.
- * 1 <= B <= 8, cols % 32 == 0. */
+ * 1 <= B <= 8, cols % 32 == 0. When cols % 256 == 0 and W and x are 16-byte
+ * aligned (every row then starts 16-byte aligned) each row streams with
+ * 128-bit loads; otherwise a slower path with 2-byte loads runs. */
 QW3_API int qw3_q8_0_gemv(const void *W_dev, int32_t rows, int32_t cols,
                   const float *x_dev, int32_t B, float *y_dev, void *stream);
+
+/* The pages' quantized matmul ("Model files and quantization", 11.9, the
+ * dotBlocks step): each row x[b] is first encoded to Q8_0 per 32-block by
+ * the 11.7 encoder (d = amax/127, codes rounded half away from zero, d kept
+ * as f16), then y[b][r] = sum over blocks of (d_w * d_x) * (i32 dot of the
+ * 32 weight and activation codes), f32. A block of x holding NaN or inf
+ * makes the rows it touches NaN. Arguments as qw3_q8_0_gemv; cols % 256 == 0,
+ * B * cols <= 49152, W and x 16-byte aligned (QW3_ERR_SHAPE /
+ * QW3_ERR_INVALID_ARG otherwise). Asynchronous on `stream`. */
+QW3_API int qw3_q8_0_gemv_q8act(const void *W_dev, int32_t rows, int32_t cols,
+                        const float *x_dev, int32_t B, float *y_dev, void *stream);
 
 /* ---- no-allocation variant ------------------------------------------- */
 

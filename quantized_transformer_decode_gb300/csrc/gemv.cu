@@ -328,9 +328,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
 #pragma unroll
                 for (int i = 0; i < kMaxXLoads; ++i) {
                     const int k = (tid + i * kConsumers) * 4;
-                    if (i < nld && k < K) {
-                        float4 u = v[i];
-                        if (a.norm_w) {
+                    if (i < nld) {   // uniform: every lane of the warp takes part in the round trip
+                        const bool act = k < K;
+                        float4 u = act ? v[i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        if (a.norm_w && act) {
                             const float4 w = (i < kNormPre && npre) ? nw[i & (kNormPre - 1)]
                                                                     : *reinterpret_cast<const float4 *>(a.norm_w + k);
                             u.x = u.x * scale * w.x;
@@ -338,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
                             u.z = u.z * scale * w.z;
                             u.w = u.w * scale * w.w;
                         }
-                        *reinterpret_cast<float4 *>(xd + (k >> 5) * 36 + (k & 31)) = u;
+                        if (a.act_q8) u = q8_0_roundtrip4(u);
+                        if (act) *reinterpret_cast<float4 *>(xd + (k >> 5) * 36 + (k & 31)) = u;
                     }
                 }
             } else {
@@ -359,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv(GemvArgs a, GemvPlan p) {
                             u.z = u.z * scale * w.z;
                             u.w = u.w * scale * w.w;
                         }
+                        if (a.act_q8) u = q8_0_roundtrip4(u);
                         float amax = fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w)));
                         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
                         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));

@@ -254,6 +254,23 @@ cudaError_t launch_qk_rope_append(float *qkv, int M, int qkv_stride, const float
                             static_cast<float *>(kv_layer), seq_stride, kvsel_stride, head_stride, nh, nkv, hd, s);
 }
 
+namespace {
+__global__ void __launch_bounds__(256) k_q8act_rows(float4 *__restrict__ x, int64_t n4) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const bool act = i < n4;
+    const float4 u = act ? x[i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    const float4 r = q8_0_roundtrip4(u);   // every lane of the warp takes part
+    if (act) x[i] = r;
+}
+}  // namespace
+
+cudaError_t launch_q8act_rows(float *x, int M, int K, cudaStream_t s) {
+    if (M < 1 || K % 32) return cudaErrorInvalidValue;
+    const int64_t n4 = static_cast<int64_t>(M) * K / 4;
+    k_q8act_rows<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, s>>>(reinterpret_cast<float4 *>(x), n4);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_argmax_rows(const float *logits, int M, int V, int32_t *out, int32_t *status, cudaStream_t s) {
     if (M < 1 || V < 1) return cudaErrorInvalidValue;
     k_argmax_rows<<<M, 512, 0, s>>>(logits, V, out, status);

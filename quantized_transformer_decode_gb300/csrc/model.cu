@@ -111,6 +111,7 @@ struct qw3_model {
 
     void *kv = nullptr;    // f32, or half when kv16
     bool kv16 = false;
+    bool act_q8 = false;   // linear inputs through a Q8_0 round trip
     size_t head_stride = 0, kvsel_stride = 0, seq_stride = 0, layer_stride = 0;
     std::vector<int32_t> seq_len;
 
@@ -149,6 +150,16 @@ namespace {
 void *kv_at(const qw3_model *m, int layer, int seq) {
     const size_t e = static_cast<size_t>(layer) * m->layer_stride + static_cast<size_t>(seq) * m->seq_stride;
     return static_cast<uint8_t *>(m->kv) + e * (m->kv16 ? 2 : 4);
+}
+
+// A linear layer through the GEMM; in the q8_0 activation mode its input
+// rows (a scratch buffer no later step reads) first take their Q8_0 round
+// trip.
+cudaError_t lin_gemm(qw3_model *m, float *A, int M, int K, const QMat &W, float *C, GemvMode mode,
+                     unsigned long long *argmax_key, const DecodeIO *io, cudaStream_t s) {
+    if (m->act_q8)
+        if (cudaError_t e = launch_q8act_rows(A, M, K, s); e != cudaSuccess) return e;
+    return launch_gemm(A, M, K, W, C, mode, argmax_key, io, s, m->d_status, m->apack, &m->gsk);
 }
 }  // namespace
 
@@ -331,13 +342,14 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
         const LayerDev &L = m->layers[l];
         if (gv) {
             GemvArgs a{};
+            a.act_q8 = m->act_q8;
             a.W = L.qkv; a.N = L.qkv.rows; a.K = H; a.B = B;
             a.x = m->x; a.norm_w = L.attn_norm; a.eps = c.rms_eps; a.y = m->qkv; a.status = m->d_status;
             a.trace = tr();
             M_TRY(m, launch_gemv(a, GEMV_STORE, pdl, s));
         } else {
             M_TRY(m, launch_rmsnorm_rows(m->x, B, H, L.attn_norm, c.rms_eps, m->h, s));
-            M_TRY(m, launch_gemm(m->h, B, H, L.qkv, m->qkv, GEMV_STORE, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
+            M_TRY(m, lin_gemm(m, m->h, B, H, L.qkv, m->qkv, GEMV_STORE, nullptr, nullptr, s));
         }
         AttnDecodeArgs at{};
         at.qkv = m->qkv; at.qkv_stride = m->qkv_w; at.q_norm = L.q_norm; at.k_norm = L.k_norm; at.eps = c.rms_eps;
@@ -350,29 +362,33 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
         M_TRY(m, launch_attn_decode(at, B, nsplit, csize, pdl && gv, s));
         if (gv) {
             GemvArgs a{};
+            a.act_q8 = m->act_q8;
             a.W = L.o; a.N = H; a.K = qw; a.B = B; a.x = m->o; a.norm_w = nullptr;
             a.eps = c.rms_eps; a.y = m->x; a.status = m->d_status;
             a.trace = tr();
             M_TRY(m, launch_gemv(a, GEMV_RESID, pdl, s));
             GemvArgs g{};
+            g.act_q8 = m->act_q8;
             g.W = L.gu; g.N = 2 * I; g.K = H; g.B = B; g.x = m->x; g.norm_w = L.ffn_norm;
             g.eps = c.rms_eps; g.y = m->act; g.status = m->d_status;
             g.trace = tr();
             M_TRY(m, launch_gemv(g, GEMV_SWIGLU, pdl, s));
             GemvArgs dn{};
+            dn.act_q8 = m->act_q8;
             dn.W = L.down; dn.N = H; dn.K = I; dn.B = B; dn.x = m->act; dn.norm_w = nullptr;
             dn.eps = c.rms_eps; dn.y = m->x; dn.status = m->d_status;
             dn.trace = tr();
             M_TRY(m, launch_gemv(dn, GEMV_RESID, pdl, s));
         } else {
-            M_TRY(m, launch_gemm(m->o, B, qw, L.o, m->x, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
+            M_TRY(m, lin_gemm(m, m->o, B, qw, L.o, m->x, GEMV_RESID, nullptr, nullptr, s));
             M_TRY(m, launch_rmsnorm_rows(m->x, B, H, L.ffn_norm, c.rms_eps, m->h, s));
-            M_TRY(m, launch_gemm(m->h, B, H, L.gu, m->act, GEMV_SWIGLU, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
-            M_TRY(m, launch_gemm(m->act, B, I, L.down, m->x, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
+            M_TRY(m, lin_gemm(m, m->h, B, H, L.gu, m->act, GEMV_SWIGLU, nullptr, nullptr, s));
+            M_TRY(m, lin_gemm(m, m->act, B, I, L.down, m->x, GEMV_RESID, nullptr, nullptr, s));
         }
     }
     if (gv) {
         GemvArgs a{};
+            a.act_q8 = m->act_q8;
         a.W = m->out; a.N = c.vocab; a.K = H; a.B = B; a.x = m->x; a.norm_w = m->out_norm;
         a.eps = c.rms_eps; a.y = nullptr; a.argmax_key = m->argmax_key; a.done_counter = m->done_counter;
         a.io = m->d_io; a.next_token = m->d_tok; a.step_ctr = m->d_step; a.pos_inc = m->d_pos;
@@ -381,7 +397,7 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
         M_TRY(m, launch_gemv(a, GEMV_ARGMAX, pdl, s));
     } else {
         M_TRY(m, launch_rmsnorm_rows(m->x, B, H, m->out_norm, c.rms_eps, m->h, s));
-        M_TRY(m, launch_gemm(m->h, B, H, m->out, nullptr, GEMV_ARGMAX, m->argmax_key, m->d_io, s, m->d_status, m->apack, &m->gsk));
+        M_TRY(m, lin_gemm(m, m->h, B, H, m->out, nullptr, GEMV_ARGMAX, m->argmax_key, m->d_io, s));
         M_TRY(m, launch_argmax_finalize(m->argmax_key, B, m->d_io, m->d_tok, m->d_step, m->d_pos, m->d_status, s));
     }
     return QW3_OK;
@@ -456,7 +472,7 @@ int setup_tensor_core_gemm(qw3_model *m) {
 // covered; the per-kernel path then serves batch 1 too.
 int setup_step(qw3_model *m) {
     const qw3_config &c = m->cfg;
-    if ((c.flags & QW3_FLAG_PER_KERNEL) || m->kv16 || !step_supported(c)) return QW3_OK;
+    if ((c.flags & QW3_FLAG_PER_KERNEL) || m->kv16 || m->act_q8 || !step_supported(c)) return QW3_OK;
     // The step kernel wins where a layer is latency-bound (a few hundred KB
     // of weights per SM); past that a layer is bandwidth-bound and the
     // per-kernel chain, with two streaming CTAs per SM, moves it faster
@@ -608,6 +624,7 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
     qw3_model *m = new qw3_model();
     m->cfg = *cfg;
     m->kv16 = (cfg->flags & QW3_FLAG_KV_F16) != 0;
+    m->act_q8 = (cfg->flags & QW3_FLAG_ACT_Q8) != 0;
     auto bail = [&](int rc) {
         if (m->stream) cudaStreamSynchronize(m->stream);
         const std::string msg = m->err;
@@ -819,7 +836,7 @@ int forward_rows(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n
             const LayerDev &L = m->layers[l];
             void *kvl = kv_at(m, l, 0);
             M_TRY(m, launch_rmsnorm_rows(m->px, M, H, L.attn_norm, c.rms_eps, m->ph, s));
-            M_TRY(m, launch_gemm(m->ph, M, H, L.qkv, m->pqkv, GEMV_STORE, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
+            M_TRY(m, lin_gemm(m, m->ph, M, H, L.qkv, m->pqkv, GEMV_STORE, nullptr, nullptr, s));
             M_TRY(m, launch_qk_rope_append(m->pqkv, M, m->qkv_w, L.q_norm, L.k_norm, c.rms_eps, m->rope, nullptr, seq,
                                            nullptr, pos0, kvl, m->seq_stride, m->kvsel_stride, m->head_stride, nh,
                                            nkv, hd, m->kv16, s));
@@ -831,20 +848,20 @@ int forward_rows(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n
                 M_TRY(m, launch_attn_prefill(m->pqkv, M, m->qkv_w, kv_at(m, l, seq), m->kvsel_stride, m->head_stride,
                                              pos0, nh, nkv, hd, scale, m->po, m->kv16, s));
             }
-            M_TRY(m, launch_gemm(m->po, M, qw, L.o, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
+            M_TRY(m, lin_gemm(m, m->po, M, qw, L.o, m->px, GEMV_RESID, nullptr, nullptr, s));
             M_TRY(m, launch_rmsnorm_rows(m->px, M, H, L.ffn_norm, c.rms_eps, m->ph, s));
-            M_TRY(m, launch_gemm(m->ph, M, H, L.gu, m->pact, GEMV_SWIGLU, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
-            M_TRY(m, launch_gemm(m->pact, M, I, L.down, m->px, GEMV_RESID, nullptr, nullptr, s, m->d_status, m->apack, &m->gsk));
+            M_TRY(m, lin_gemm(m, m->ph, M, H, L.gu, m->pact, GEMV_SWIGLU, nullptr, nullptr, s));
+            M_TRY(m, lin_gemm(m, m->pact, M, I, L.down, m->px, GEMV_RESID, nullptr, nullptr, s));
         }
         if (all_logits) {
             // final norm of every row, the lm_head over all of them, each row's argmax
             float *lg = all_logits + static_cast<size_t>(off) * c.vocab;
             M_TRY(m, launch_rmsnorm_rows(m->px, M, H, m->out_norm, c.rms_eps, m->ph, s));
-            M_TRY(m, launch_gemm(m->ph, M, H, m->out, lg, GEMV_STORE, nullptr, nullptr, s, m->d_status, m->apack,
-                                 &m->gsk));
+            M_TRY(m, lin_gemm(m, m->ph, M, H, m->out, lg, GEMV_STORE, nullptr, nullptr, s));
             if (all_argmax) M_TRY(m, launch_argmax_rows(lg, M, c.vocab, all_argmax + off, m->d_status, s));
         } else if (off + M == n && (last_logits_dev || argmax_dev)) {
             GemvArgs a{};
+            a.act_q8 = m->act_q8;
             a.W = m->out; a.N = c.vocab; a.K = H; a.B = 1;
             a.x = m->px + static_cast<size_t>(M - 1) * H; a.norm_w = m->out_norm; a.eps = c.rms_eps;
             a.y = last_logits_dev; a.argmax_key = m->argmax_key; a.done_counter = m->done_counter; a.io = nullptr;
@@ -1048,7 +1065,21 @@ int qw3_q8_0_gemv(const void *W_dev, int32_t rows, int32_t cols, const float *x_
     if (misaligned(W_dev, 2) || misaligned(x_dev, 4) || misaligned(y_dev, 4))
         return fail(nullptr, QW3_ERR_INVALID_ARG, "W must be 2-byte, x and y 4-byte aligned");
     if (rows == 0) return QW3_OK;
-    QW3_CUDA_TRY(launch_gemv_raw(static_cast<const uint8_t *>(W_dev), rows, cols, x_dev, B, y_dev,
+    QW3_CUDA_TRY(launch_gemv_raw(static_cast<const uint8_t *>(W_dev), rows, cols, x_dev, B, y_dev, false,
+                                 static_cast<cudaStream_t>(stream)));
+    return QW3_OK;
+}
+
+int qw3_q8_0_gemv_q8act(const void *W_dev, int32_t rows, int32_t cols, const float *x_dev, int32_t B, float *y_dev,
+                        void *stream) {
+    if (!W_dev || !x_dev || !y_dev || rows < 0 || cols < 0 || B < 1 || B > 8)
+        return fail(nullptr, QW3_ERR_INVALID_ARG, "bad gemv arguments");
+    if (cols % 256) return fail(nullptr, QW3_ERR_SHAPE, "cols must be a multiple of 256");
+    if (static_cast<int64_t>(B) * cols > 49152) return fail(nullptr, QW3_ERR_SHAPE, "B * cols must be <= 49152");
+    if (misaligned(W_dev, 16) || misaligned(x_dev, 16) || misaligned(y_dev, 4))
+        return fail(nullptr, QW3_ERR_INVALID_ARG, "W and x must be 16-byte, y 4-byte aligned");
+    if (rows == 0) return QW3_OK;
+    QW3_CUDA_TRY(launch_gemv_raw(static_cast<const uint8_t *>(W_dev), rows, cols, x_dev, B, y_dev, true,
                                  static_cast<cudaStream_t>(stream)));
     return QW3_OK;
 }

@@ -98,6 +98,7 @@ struct GemvArgs {
     int32_t *pos_inc;                // nullable [B]: +1 by the last CTA
     int32_t *status;                 // device status word
     unsigned long long *trace;       // nullable: 2 records of 8 u64 (first, last CTA)
+    int act_q8;                      // 1: the (normalised) input rows go through a Q8_0 round trip
 };
 
 struct AttnDecodeArgs {
@@ -147,7 +148,10 @@ cudaError_t launch_quantize(const float *x, int64_t nblocks, uint8_t *out, int32
 cudaError_t launch_dequantize(const uint8_t *blocks, int64_t nblocks, float *y, cudaStream_t s);
 cudaError_t launch_repack(const uint8_t *raw, int rows, int cols, const QMat &dst,
                           int dst_row0, int dst_row_stride, cudaStream_t s);
-cudaError_t launch_gemv_raw(const uint8_t *W, int rows, int cols, const float *x, int B, float *y,
+// Raw GGUF Q8_0 GEMV (the boundary entries): y[b][r] = sum_k W[r][k] x[b][k];
+// q8act: x re-quantized to Q8_0 per 32-block, integer block dots (needs
+// cols % 256 == 0 and 16-byte aligned W and x).
+cudaError_t launch_gemv_raw(const uint8_t *W, int rows, int cols, const float *x, int B, float *y, bool q8act,
                             cudaStream_t s);
 
 cudaError_t launch_gemv(const GemvArgs &a, int mode, bool pdl, cudaStream_t s);
@@ -207,6 +211,9 @@ cudaError_t configure_attn_prefill_tc();
 cudaError_t launch_attn_prefill_tc(const float *qkv, int M, int qkv_stride, const void *kv_seq, size_t kvsel_stride,
                                    size_t head_stride, int pos0, int nh, int nkv, int hd, float scale, float *out,
                                    uint8_t *kvpack, int32_t *status, bool kv16, cudaStream_t s);
+// In-place Q8_0 round trip (q8_0_roundtrip4) of M rows of K values (K a
+// multiple of 32): the input of a linear layer in the q8_0 activation mode.
+cudaError_t launch_q8act_rows(float *x, int M, int K, cudaStream_t s);
 // Greedy argmax of each of M logits rows [M][V] (lowest index among equal
 // maxima); a NaN records QW3_ERR_NONFINITE.
 cudaError_t launch_argmax_rows(const float *logits, int M, int V, int32_t *out, int32_t *status, cudaStream_t s);
@@ -473,6 +480,30 @@ __device__ __forceinline__ void digit_planes4(const float (&v)[4], float inv_s, 
 __device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
     return (static_cast<uint32_t>(a) & 0xffu) | ((static_cast<uint32_t>(b) & 0xffu) << 8) |
            ((static_cast<uint32_t>(c) & 0xffu) << 16) | ((static_cast<uint32_t>(d) & 0xffu) << 24);
+}
+
+// Q8_0 round trip of activations ("Model files and quantization": the 11.7
+// encoder applied per row per call, 11.9): 8 consecutive lanes hold one
+// 32-value block, 4 values each; every value becomes f32(f16(d)) * q, the
+// value the integer block dot multiplies (d = amax / 127, q = the encoder's
+// code). A dot over these values is the pages' sum of d_w * d_a * i32 dots up
+// to f32 rounding. All 32 lanes of the warp call it; a NaN stays NaN and an
+// infinity turns its block into NaN.
+__device__ __forceinline__ float4 q8_0_roundtrip4(float4 u) {
+    float amax = fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float inv = (d == 0.0f) ? 0.0f : __fdiv_rn(1.0f, d);
+    const float dq = __half2float(__float2half_rn(d));
+    auto rt = [&](float v) {
+        if (isnan(v)) return v;
+        const float p = __fmul_rn(v, inv);
+        const float q = isnan(p) ? 0.0f : fminf(fmaxf(roundf(p), -127.0f), 127.0f);
+        return dq * q;
+    };
+    return make_float4(rt(u.x), rt(u.y), rt(u.z), rt(u.w));
 }
 
 // sum over 16 codes w of q * (h + m / 254 + l / 254^2), planes P[0..2]

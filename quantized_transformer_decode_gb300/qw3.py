@@ -34,13 +34,14 @@ QW3_FLAG_TRACE = 0x4
 QW3_FLAG_PER_KERNEL = 0x8
 QW3_FLAG_TEST_NO_WAIT = 0x10
 QW3_FLAG_KV_F16 = 0x20
+QW3_FLAG_ACT_Q8 = 0x40
 
 # Every entry point of include/qw3.h, in declaration order.
 EXPORTS = (
     "qw3_create", "qw3_destroy", "qw3_prefill", "qw3_forward_all_logits", "qw3_decode", "qw3_generate_greedy",
     "qw3_reset", "qw3_truncate", "qw3_seq_len", "qw3_debug_read_kv", "qw3_debug_read_trace",
     "qw3_decode_plan", "qw3_sync", "qw3_stream", "qw3_status_string", "qw3_last_error",
-    "qw3_q8_0_quantize", "qw3_q8_0_dequantize", "qw3_q8_0_gemv", "qw3_q8_0_gemv_splitk_noalloc",
+    "qw3_q8_0_quantize", "qw3_q8_0_dequantize", "qw3_q8_0_gemv", "qw3_q8_0_gemv_q8act", "qw3_q8_0_gemv_splitk_noalloc",
 )
 
 
@@ -111,6 +112,7 @@ def lib() -> ctypes.CDLL:
         "qw3_q8_0_quantize": (ctypes.c_int, [_P, _I64, _P, _P, _P]),
         "qw3_q8_0_dequantize": (ctypes.c_int, [_P, _I64, _P, _P]),
         "qw3_q8_0_gemv": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P]),
+        "qw3_q8_0_gemv_q8act": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P]),
         "qw3_q8_0_gemv_splitk_noalloc": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P]),
     }
     for name, (res, args) in sig.items():
@@ -227,6 +229,10 @@ def qw3_q8_0_gemv(W_ptr: int, rows: int, cols: int, x_ptr: int, B: int, y_ptr: i
     _check(lib().qw3_q8_0_gemv(W_ptr, rows, cols, x_ptr, B, y_ptr, stream or None))
 
 
+def qw3_q8_0_gemv_q8act(W_ptr: int, rows: int, cols: int, x_ptr: int, B: int, y_ptr: int, stream: int = 0) -> None:
+    _check(lib().qw3_q8_0_gemv_q8act(W_ptr, rows, cols, x_ptr, B, y_ptr, stream or None))
+
+
 def qw3_q8_0_gemv_splitk_noalloc(W_ptr: int, rows: int, cols: int, x_ptr: int, B: int, y_ptr: int,
                                  stream: int = 0) -> None:
     _check(lib().qw3_q8_0_gemv_splitk_noalloc(W_ptr, rows, cols, x_ptr, B, y_ptr, stream or None))
@@ -268,6 +274,16 @@ def q8_0_gemv(W, rows: int, cols: int, x):
     B = x.shape[0] if x.dim() == 2 else 1
     y = torch.empty((B, rows), dtype=torch.float32, device=x.device)
     qw3_q8_0_gemv(W.data_ptr(), rows, cols, x.data_ptr(), B, y.data_ptr(), _stream_ptr())
+    return y
+
+
+def q8_0_gemv_q8act(W, rows: int, cols: int, x):
+    """y = W . Q8_0(x) row by row (qw3_q8_0_gemv_q8act)."""
+    torch = _torch()
+    x = x.contiguous()
+    B = x.shape[0] if x.dim() == 2 else 1
+    y = torch.empty((B, rows), dtype=torch.float32, device=x.device)
+    qw3_q8_0_gemv_q8act(W.data_ptr(), rows, cols, x.data_ptr(), B, y.data_ptr(), _stream_ptr())
     return y
 
 

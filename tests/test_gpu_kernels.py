@@ -141,3 +141,28 @@ def test_raw_gemv_one_hot_returns_a_column(torch):
         x[0, k] = 1.0
         y = qw3.q8_0_gemv(torch.from_numpy(blocks).cuda(), rows, cols, torch.from_numpy(x).cuda()).cpu().numpy()
         np.testing.assert_array_equal(y[0], w[:, k])
+
+
+def test_raw_gemv_unaligned_input_takes_the_general_path(torch):
+    """x 4 bytes off a 16-byte boundary: the 2-byte-load path, same result
+    bound as the 128-bit streaming path."""
+    from quantized_transformer_decode_gb300 import qw3
+    rows, cols = 129, 1024
+    rng = np.random.default_rng(17)
+    blocks = orc.q8_0_quantize(rng.standard_normal((rows, cols), dtype=np.float32) * np.float32(0.02))
+    w = orc.matrix_from_blocks(blocks, rows, cols)
+    x = rng.standard_normal((1, cols), dtype=np.float32)
+    xd = torch.zeros(cols + 1, dtype=torch.float32, device="cuda")
+    xd[1:] = torch.from_numpy(x[0]).cuda()
+    y = torch.empty((1, rows), dtype=torch.float32, device="cuda")
+    Wd = torch.from_numpy(blocks).cuda()
+    qw3.qw3_q8_0_gemv(Wd.data_ptr(), rows, cols, xd.data_ptr() + 4, 1, y.data_ptr())
+    want = x.astype(np.float64) @ w.astype(np.float64).T
+    err = np.abs(_np_cpu(y) - want)
+    assert np.all(err <= _gemv_bound(w, x))
+
+
+def _np_cpu(t):
+    import torch as _t
+    _t.cuda.synchronize()
+    return t.cpu().numpy()
