@@ -231,6 +231,56 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_positions: Sequence
     return out.astype(np.float32)
 
 
+def q8_scores(q: np.ndarray, kq: np.ndarray, kd: np.ndarray, kv_head_for_head: Sequence[int]) -> np.ndarray:
+    """Raw attention scores of one query row over a q8_0 K cache ("The LLM
+    stack", 13.4: the query row is quantised once per head to q8_0 and the
+    scores are q8 x q8 dots straight on the cached K blocks).
+
+    q [nh, d] f32 (after the Q norm and RoPE); kq [T, nkv, d] int8 codes and
+    kd [T, nkv, d/32] f16 scales of the cached keys. Each head's query is
+    encoded by the 11.7 encoder; a (key block, query block) pair contributes
+    (k.d * q.d) * f32(i32 dot) in f32, the dotBlocks form of "Model files and
+    quantization", 11.9; the blocks of a row sum in f64. Returns [nh, T] f64,
+    before the 1/sqrt(d) scale.
+    """
+    q32 = np.asarray(q, np.float32)
+    nh, d = q32.shape
+    T = kq.shape[0]
+    nb = d // QK8_0
+    _, qa, qd16 = q8_0_quantize_parts(q32.reshape(-1))
+    qa = qa.reshape(nh, nb, QK8_0).astype(np.float64)
+    qd = qd16.astype(np.float32).reshape(nh, nb)
+    out = np.zeros((nh, T), dtype=np.float64)
+    for h in range(nh):
+        g = kv_head_for_head[h]
+        codes = kq[:, g, :].reshape(T, nb, QK8_0).astype(np.float64)
+        scales = kd[:, g, :].astype(np.float32)
+        for b in range(nb):
+            acc = codes[:, b, :] @ qa[h, b]                                   # exact integer dots
+            term = (scales[:, b] * qd[h, b]).astype(np.float32) * acc.astype(np.float32)
+            out[h] += term.astype(np.float32)
+    return out
+
+
+def attention_q8_decode(q: np.ndarray, cache, layer: int, n: int, scale: float,
+                        kv_head_for_head: Sequence[int]) -> np.ndarray:
+    """Decode attention of one new row over a q8_0 cache holding n rows
+    (13.4's integer score path): q8_scores, the 1/sqrt(d) scale and a
+    max-subtracted softmax in f64, then the weighted sum of the dequantised
+    V rows. Returns [1, nh, d] f32."""
+    s = q8_scores(np.asarray(q, np.float32)[0], cache.kq[layer, :n], cache.kd[layer, :n], kv_head_for_head)
+    s = s * float(scale)
+    s -= np.max(s, axis=1, keepdims=True)
+    p = np.exp(s)
+    p /= np.sum(p, axis=1, keepdims=True)
+    v64 = cache.v[layer, :n].astype(np.float64)                                # [n, nkv, d]
+    nh, d = p.shape[0], v64.shape[2]
+    out = np.empty((1, nh, d), dtype=np.float64)
+    for h in range(nh):
+        out[0, h] = p[h] @ v64[:, kv_head_for_head[h], :]
+    return out.astype(np.float32)
+
+
 def silu(z: np.ndarray) -> np.ndarray:
     """silu(z) = z * sigmoid(z) = z / (1 + e^-z), f64 (12.3.6)."""
     z64 = np.asarray(z, dtype=np.float64)
@@ -361,23 +411,49 @@ class KvCache:
 
     dtype "f32" (the workloads' cache) or "f16", the course's default cache
     type ("A transformer from scratch", 12.4): appended rows are rounded to
-    IEEE half (nearest even) and read back exactly as f32.
+    IEEE half (nearest even) and read back exactly as f32; or "q8_0" ("The
+    LLM stack", 13.4; 12.4): each (position, kv head) row is stored as
+    head_dim/32 Q8_0 blocks by the 11.7 encoder (codes in kq/vq, f16 scales
+    in kd/vd; k and v hold the dequantised rows f32(d) * q that every reader
+    sees). head_dim must be a multiple of 32.
     """
 
     def __init__(self, n_layers: int, n_kv_heads: int, head_dim: int, capacity: int, dtype: str = "f32"):
-        if dtype not in ("f32", "f16"):
+        if dtype not in ("f32", "f16", "q8_0"):
             raise InvalidShape(f"KV cache dtype {dtype!r}")
+        if dtype == "q8_0" and head_dim % QK8_0:
+            raise InvalidShape(f"a q8_0 KV cache needs head_dim % {QK8_0} == 0, got {head_dim}")
         self.capacity = capacity
         self.dtype = dtype
-        np_t = np.float32 if dtype == "f32" else np.float16
+        np_t = np.float16 if dtype == "f16" else np.float32
         self.k = np.zeros((n_layers, capacity, n_kv_heads, head_dim), np_t)
         self.v = np.zeros((n_layers, capacity, n_kv_heads, head_dim), np_t)
+        if dtype == "q8_0":
+            nb = head_dim // QK8_0
+            self.kq = np.zeros((n_layers, capacity, n_kv_heads, head_dim), np.int8)
+            self.vq = np.zeros((n_layers, capacity, n_kv_heads, head_dim), np.int8)
+            self.kd = np.zeros((n_layers, capacity, n_kv_heads, nb), np.float16)
+            self.vd = np.zeros((n_layers, capacity, n_kv_heads, nb), np.float16)
         self.len = 0
+
+    def _store_q8(self, codes, scales, deq, layer: int, rows: np.ndarray) -> None:
+        m, nkv, d = rows.shape
+        _, q, d16 = q8_0_quantize_parts(np.asarray(rows, np.float32).reshape(-1))
+        q = q.reshape(m, nkv, d)
+        d16 = d16.reshape(m, nkv, d // QK8_0)
+        codes[layer, self.len:self.len + m] = q
+        scales[layer, self.len:self.len + m] = d16
+        deq[layer, self.len:self.len + m] = (np.repeat(d16.astype(np.float32), QK8_0, axis=2)
+                                             * q.astype(np.float32)).astype(np.float32)
 
     def append_layer(self, layer: int, k_rows: np.ndarray, v_rows: np.ndarray) -> None:
         m = k_rows.shape[0]
         if self.len + m > self.capacity:
             raise KvCacheOverflow(f"len {self.len} + {m} > capacity {self.capacity}")
+        if self.dtype == "q8_0":
+            self._store_q8(self.kq, self.kd, self.k, layer, k_rows)
+            self._store_q8(self.vq, self.vd, self.v, layer, v_rows)
+            return
         # numpy's f32 -> f16 conversion rounds to nearest even
         self.k[layer, self.len:self.len + m] = np.asarray(k_rows, np.float32).astype(self.k.dtype)
         self.v[layer, self.len:self.len + m] = np.asarray(v_rows, np.float32).astype(self.v.dtype)
@@ -522,8 +598,14 @@ class OracleModel:
         q = rope_neox(rms_norm(q, lw.q_norm, s.rms_eps), positions, s.rope_theta)
         k = rope_neox(rms_norm(k, lw.k_norm, s.rms_eps), positions, s.rope_theta)
         cache.append_layer(li, k, v)
-        kk, vv = cache.layer_rows(li, cache.len + M)
-        o = attention(q, kk, vv, positions, 1.0 / math.sqrt(s.head_dim), self.kv_head_for_head)
+        scale = 1.0 / math.sqrt(s.head_dim)
+        if cache.dtype == "q8_0" and M == 1:
+            # one new row: the integer score path (13.4); a multi-row step
+            # (prefill, verify) reads the dequantised rows instead
+            o = attention_q8_decode(q, cache, li, cache.len + 1, scale, self.kv_head_for_head)
+        else:
+            kk, vv = cache.layer_rows(li, cache.len + M)
+            o = attention(q, kk, vv, positions, scale, self.kv_head_for_head)
         return add_f32(x, self._lin(lw.wo, o.reshape(M, s.q_width)))
 
     def _ffn_block(self, lw: _Layer, x):

@@ -578,3 +578,89 @@ def test_q8act_model_mode_changes_only_the_linears():
     assert 0 < rel < 5e-2
     with pytest.raises(orc.InvalidShape):
         om.set_activations("q4")
+
+
+# ---- q8_0 KV cache ("The LLM stack", 13.4; "A transformer from scratch", 12.4)
+
+def test_q8_kv_rows_are_the_codec_round_trip_per_position_and_head():
+    rng = np.random.default_rng(21)
+    c = orc.KvCache(1, 2, 64, 8, "q8_0")
+    k = rng.standard_normal((3, 2, 64)).astype(np.float32)
+    v = (rng.standard_normal((3, 2, 64)) * 5).astype(np.float32)
+    c.append_layer(0, k, v)
+    c.advance(3)
+    kk, vv = c.layer_rows(0, 3)
+    for t in range(3):
+        for g in range(2):
+            for rows, src in ((kk, k), (vv, v)):
+                blocks = orc.q8_0_quantize(src[t, g])
+                np.testing.assert_array_equal(rows[t, g], orc.q8_0_dequantize(blocks, 64))
+    d16, q = orc.q8_0_unpack(orc.q8_0_quantize(k[1, 0]), 64)
+    np.testing.assert_array_equal(c.kq[0, 1, 0], q.reshape(-1))
+    np.testing.assert_array_equal(c.kd[0, 1, 0], d16)
+    with pytest.raises(orc.InvalidShape):
+        orc.KvCache(1, 1, 48, 4, "q8_0")          # head_dim not a multiple of 32
+
+
+def test_q8_scores_hand_worked_integer_dot():
+    """Query [127, 0.5, 0, ...] encodes to codes [127, 1] with d = 1 (half
+    away from zero); key [127, 127, 0, ...] to [127, 127] with d = 1. The
+    integer score is 127*127 + 1*127 = 16256; the f32 dot would be
+    127*127 + 0.5*127 = 16192.5."""
+    c = orc.KvCache(1, 1, 32, 2, "q8_0")
+    k = np.zeros((1, 1, 32), np.float32)
+    k[0, 0, :2] = [127.0, 127.0]
+    c.append_layer(0, k, k)
+    q = np.zeros((1, 32), np.float32)
+    q[0, :2] = [127.0, 0.5]
+    s = orc.q8_scores(q, c.kq[0, :1], c.kd[0, :1], [0])
+    assert s.shape == (1, 1) and s[0, 0] == 16256.0
+
+
+def test_q8_decode_attention_one_position_and_two_key_sigmoid():
+    """One cached position returns its dequantised V; two keys whose codes
+    and scales are exact (d = 1/127 · 127) give the two-key softmax
+    sigmoid(scale * (s1 - s2)) on exactly representable V rows."""
+    c = orc.KvCache(1, 1, 32, 4, "q8_0")
+    rng = np.random.default_rng(3)
+    v1 = rng.standard_normal((1, 1, 32)).astype(np.float32)
+    k1 = rng.standard_normal((1, 1, 32)).astype(np.float32)
+    c.append_layer(0, k1, v1)
+    q = rng.standard_normal((1, 1, 32)).astype(np.float32)
+    o = orc.attention_q8_decode(q, c, 0, 1, 0.125, [0])
+    np.testing.assert_array_equal(o[0, 0], c.v[0, 0, 0])
+    # two keys, integer-valued with amax 127 (d = 1): scores are exact integers
+    c2 = orc.KvCache(1, 1, 32, 4, "q8_0")
+    ka = np.zeros((2, 1, 32), np.float32)
+    ka[0, 0, 0], ka[0, 0, 1] = 127.0, 3.0
+    ka[1, 0, 0], ka[1, 0, 1] = 127.0, -5.0
+    va = np.zeros((2, 1, 32), np.float32)
+    va[0, 0, 0], va[1, 0, 0] = 127.0, -127.0
+    c2.append_layer(0, ka, va)
+    qa = np.zeros((1, 1, 32), np.float32)
+    qa[0, 0, 0], qa[0, 0, 1] = 1.0, 127.0                 # codes [1, 127], d = 1
+    # s1 = 127 + 381 = 508, s2 = 127 - 635 = -508
+    scale = 1.0 / 256.0
+    o2 = orc.attention_q8_decode(qa, c2, 0, 2, scale, [0])
+    p1 = 1.0 / (1.0 + math.exp(-scale * (508.0 + 508.0)))
+    assert abs(float(o2[0, 0, 0]) - (p1 * 127.0 - (1 - p1) * 127.0)) < 1e-4
+
+
+def test_q8_kv_model_stays_within_its_noise_and_prefill_reads_dequantised_rows():
+    """The q8_0 cache changes logits by its quantisation noise only (tiny
+    model), and a one-token decode after a prompt differs from the last row
+    of the longer prompt (integer scores against dequantised f32 scores)
+    while both stay close."""
+    shape = inputs.TINY
+    om = orc.OracleModel.from_f32(shape, inputs.generate_weights(shape, 0))
+    prompt = inputs.prompt_tokens(shape, 0, 12)
+    a = om.forward(om.new_cache(16), prompt, 0)
+    b = om.forward(om.new_cache(16, "q8_0"), prompt, 0)
+    rel = np.linalg.norm(a - b) / np.linalg.norm(a)
+    assert 0 < rel < 5e-2
+    c = om.new_cache(16, "q8_0")
+    om.forward(c, prompt[:-1], 0)
+    dec = om.forward(c, prompt[-1:], 11)
+    pre = om.forward(om.new_cache(16, "q8_0"), prompt, 0)
+    assert not np.array_equal(dec, pre)
+    assert np.linalg.norm(dec - pre) / np.linalg.norm(pre) < 5e-2
