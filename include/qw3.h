@@ -110,6 +110,16 @@ typedef struct qw3_config {
                                   keys and values are rounded to nearest
                                   even when appended. Batch-1 decode then
                                   runs the per-kernel chain.                  */
+#define QW3_FLAG_KV_Q8  0x80     /* KV cache as q8_0 rows ("The LLM stack",
+                                  13.4): each (position, kv head) row is
+                                  head_dim/32 Q8_0 blocks (11.7 encoder) at
+                                  34 bytes per 32 values. A decode step
+                                  quantises the query once per head and scores
+                                  with the integer block dots (to f32
+                                  rounding); prefill and the all-logits
+                                  forward read the dequantised rows. Not with
+                                  QW3_FLAG_KV_F16. Batch-1 decode runs the
+                                  per-kernel chain.                           */
 #define QW3_FLAG_ACT_Q8 0x40     /* every linear layer takes its input rows
                                   re-quantized to Q8_0 per 32-block on the
                                   fly ("Model files and quantization", 11.9:

@@ -82,25 +82,69 @@ __device__ __forceinline__ void load_lane_kv(const __half *src, float (&v)[HD / 
     }
 }
 
+// A q8_0 row: the lane's E values from their block's codes and f16 scale.
+template <int HD>
+__device__ __forceinline__ void load_lane_kv(const kvq8 *src, float (&v)[HD / 32], int lane) {
+    constexpr int E = HD / 32, L = 32 / E;
+    const uint8_t *blk = &src->b + (lane / L) * 34;
+    const float sc = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(blk)));
+    const uint16_t *cp = reinterpret_cast<const uint16_t *>(blk + 2 + (lane % L) * E);   // 2-byte aligned
+#pragma unroll
+    for (int h = 0; h < E / 2; ++h) {
+        const uint16_t w = cp[h];
+        v[2 * h] = sc * static_cast<float>(static_cast<int8_t>(w & 0xff));
+        v[2 * h + 1] = sc * static_cast<float>(static_cast<int8_t>(w >> 8));
+    }
+}
+
 template <int HD, typename KT>
 __device__ __forceinline__ void store_lane_kv(KT *dst, const float (&v)[HD / 32], int lane) {
     constexpr int E = HD / 32;
+    if constexpr (kv_is_q8<KT>::value) {
+        q8_store_lanes<HD>(dst, v, lane);   // every lane of the warp takes part
+    } else {
 #pragma unroll
-    for (int e = 0; e < E; ++e) dst[lane * E + e] = kv_cvt<KT>(v[e]);
+        for (int e = 0; e < E; ++e) dst[lane * E + e] = kv_cvt<KT>(v[e]);
+    }
 }
 
-// Round a lane's values to the cache type and back (identity for f32).
+// Round a lane's values to the cache type and back (identity for f32): the
+// value a reader of the cache sees. For q8_0 every lane of the warp calls it.
 template <int HD, typename KT>
 __device__ __forceinline__ void round_lane_kv(float (&v)[HD / 32]) {
+    if constexpr (kv_is_q8<KT>::value) {
+        int q[HD / 32];
+        __half dh;
+        q8_encode_lanes<HD>(v, q, dh);
+        const float sc = __half2float(dh);
 #pragma unroll
-    for (int e = 0; e < HD / 32; ++e) v[e] = kv_f32(kv_cvt<KT>(v[e]));
+        for (int e = 0; e < HD / 32; ++e) v[e] = sc * static_cast<float>(q[e]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < HD / 32; ++e) v[e] = kv_f32(kv_cvt<KT>(v[e]));
+    }
+}
+
+// Row j of a run of cached rows (rows are kv_row<KT, HD>() elements apart).
+template <int HD, typename T>
+__device__ __forceinline__ const T *kv_rowp(const T *rows, int j) {
+    return rows + static_cast<size_t>(j) * kv_row<T, HD>();
 }
 
 // Positions per staged K/V tile: the tile buffers hold kTileP f32 rows;
-// half rows take half the bytes, so a tile holds twice the positions (kept
-// at kTileP for groups of 8, whose warps score 4 positions at a time).
+// half and q8_0 rows take at most half the bytes, so a tile holds twice the
+// positions (kept at kTileP for groups of 8, whose warps score 4 positions at
+// a time).
 template <typename KT, int G>
-__host__ __device__ constexpr int tile_positions() { return (sizeof(KT) == 2 && G <= 4) ? 2 * kTileP : kTileP; }
+__host__ __device__ constexpr int tile_positions() { return (sizeof(KT) <= 2 && G <= 4) ? 2 * kTileP : kTileP; }
+
+// Bytes of one bulk copy of `rows` cached rows, rounded up to the 16 bytes a
+// bulk copy moves (a q8_0 row is 34 * HD / 32 bytes; the cache allocation
+// carries the padding the last rows may need).
+template <typename KT, int HD>
+__device__ __forceinline__ uint32_t kv_copy_bytes(int rows) {
+    return static_cast<uint32_t>((static_cast<size_t>(rows) * kv_row<KT, HD>() * sizeof(KT) + 15) / 16 * 16);
+}
 
 // Preloaded operands of one per-head norm + RoPE: the lane's norm weights
 // and (cos, sin) pairs (neither depends on the previous kernel).
@@ -141,6 +185,8 @@ template <int HD, int G, typename KT>
 __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, int nsplit, int csize) {
     constexpr int E = HD / 32;
     constexpr int TP = tile_positions<KT, G>();
+    constexpr int RW = kv_row<KT, HD>();   // cache elements per row
+    static_assert((TP * RW * sizeof(KT) + 15) / 16 * 16 <= kTileP * HD * 4, "a K/V tile fits its slot");
     constexpr int PS = part_stride<HD>();
     constexpr int CM = attn_max_cluster(G);
     static_assert(kAttnWarps * G * PS <= kStages * kTileP * HD, "warp-merge rows must fit in the K tiles");
@@ -180,7 +226,11 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
     const int seq = a.seq_ids[b];
     const int p = a.pos[b];
     const int ctx = p + 1;
-    const int chunk = (ctx + nsplit - 1) / nsplit;
+    // a bulk copy starts 16-byte aligned: f32 and half rows always do; a
+    // q8_0 row is 68 or 136 bytes, so a split starts at a multiple of 4
+    // positions (4 * 68 = 17 * 16)
+    constexpr int kStartAlign = kv_is_q8<KT>::value ? 4 : 1;
+    const int chunk = ((ctx + nsplit - 1) / nsplit + kStartAlign - 1) / kStartAlign * kStartAlign;
     const int start = s * chunk;
     const int end = min(ctx, start + chunk);
     const bool has_new = (start <= p) && (p < end);
@@ -205,11 +255,11 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
     if (tid == 0) {
         for (int t = 0; t < ntiles && t < kStages; ++t) {
             const int rows = min(TP, n_cached - t * TP);
-            const uint32_t bytes = static_cast<uint32_t>(rows * HD * sizeof(KT));
-            const size_t off = static_cast<size_t>(start + t * TP) * HD;
+            const uint32_t bytes = kv_copy_bytes<KT, HD>(rows);
+            const size_t off = static_cast<size_t>(start + t * TP) * RW;
             mbar_arrive_expect_tx(&bars[t], 2 * bytes);
-            bulk_g2s(ktile + t * TP * HD, kbase + off, bytes, &bars[t], pol);
-            bulk_g2s(vtile + t * TP * HD, vbase + off, bytes, &bars[t], pol);
+            bulk_g2s(ktile + t * TP * RW, kbase + off, bytes, &bars[t], pol);
+            bulk_g2s(vtile + t * TP * RW, vbase + off, bytes, &bars[t], pol);
         }
         // the leader expects every peer's partial rows (acc, m, l per head)
         if (r == 0) mbar_arrive_expect_tx(rbar, static_cast<uint32_t>((C - 1) * G * (HD * 4 + 8)));
@@ -229,18 +279,22 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
         if (t < G) {
             load_lane<HD>(qkv_b + (g * G + t) * HD, v, lane);
             norm_rope_pre<HD>(v, nr, a.eps, lane);
+            // q8_0 cache: the query row goes through Q8_0 once per head, so
+            // each f32 score below is (k.d * q.d) * the integer dot of the
+            // codes, to f32 rounding ("The LLM stack", 13.4)
+            if constexpr (kv_is_q8<KT>::value) round_lane_kv<HD, KT>(v);
             store_lane<HD>(qn + t * HD, v, lane);
         } else if (has_new && t == G) {
             load_lane<HD>(qkv_b + a.nh * HD + g * HD, v, lane);
             norm_rope_pre<HD>(v, nr, a.eps, lane);
             round_lane_kv<HD, KT>(v);   // the new position is scored from its cached value
             store_lane<HD>(knew, v, lane);
-            store_lane_kv<HD>(kbase + static_cast<size_t>(p) * HD, v, lane);
+            store_lane_kv<HD>(kbase + static_cast<size_t>(p) * RW, v, lane);
         } else if (has_new && t == G + 1) {
             load_lane<HD>(qkv_b + (a.nh + a.nkv) * HD + g * HD, v, lane);
             round_lane_kv<HD, KT>(v);
             store_lane<HD>(vnew, v, lane);
-            store_lane_kv<HD>(vbase + static_cast<size_t>(p) * HD, v, lane);
+            store_lane_kv<HD>(vbase + static_cast<size_t>(p) * RW, v, lane);
         }
     }
     __syncthreads();
@@ -278,7 +332,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
                 if (j < n) {
-                    load_lane_kv<HD>(krows + j * HD, kv_[j], lane);
+                    load_lane_kv<HD>(kv_rowp<HD>(krows, j), kv_[j], lane);
                 } else {
 #pragma unroll
                     for (int e = 0; e < E; ++e) kv_[j][e] = 0.0f;
@@ -338,7 +392,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
         for (int j = 0; j < NP; ++j) {
             if (j < n) {
                 float vv[E];
-                load_lane_kv<HD>(vrows + j * HD, vv, lane);
+                load_lane_kv<HD>(kv_rowp<HD>(vrows, j), vv, lane);
 #pragma unroll
                 for (int t = 0; t < G; ++t) {
                     const float pj = pb[t * NP + j];
@@ -366,7 +420,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
                 const int rows = min(TP, n_cached - t * TP);
                 const int j0 = (warp % WPT) * NP;
                 if (j0 < rows)
-                    consume(ktile + (si * TP + j0) * HD, vtile + (si * TP + j0) * HD, min(NP, rows - j0));
+                    consume(ktile + (si * TP + j0) * RW, vtile + (si * TP + j0) * RW, min(NP, rows - j0));
             }
         }
         __syncthreads();
@@ -375,11 +429,11 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn_decode(AttnDecodeArgs a, 
             for (int tt = t0 + kStages; tt < t0 + kStages + TPI && tt < ntiles; ++tt) {
                 const int si = tt % kStages;
                 const int rows = min(TP, n_cached - tt * TP);
-                const uint32_t bytes = static_cast<uint32_t>(rows * HD * sizeof(KT));
-                const size_t off = static_cast<size_t>(start + tt * TP) * HD;
+                const uint32_t bytes = kv_copy_bytes<KT, HD>(rows);
+                const size_t off = static_cast<size_t>(start + tt * TP) * RW;
                 mbar_arrive_expect_tx(&bars[si], 2 * bytes);
-                bulk_g2s(ktile + si * TP * HD, kbase + off, bytes, &bars[si], pol);
-                bulk_g2s(vtile + si * TP * HD, vbase + off, bytes, &bars[si], pol);
+                bulk_g2s(ktile + si * TP * RW, kbase + off, bytes, &bars[si], pol);
+                bulk_g2s(vtile + si * TP * RW, vbase + off, bytes, &bars[si], pol);
             }
         }
         __syncthreads();
@@ -563,9 +617,10 @@ cudaError_t configure_attn_kt() {
 
 template <int HD, int G>
 cudaError_t configure_attn_t() {
-    const cudaError_t e = configure_attn_kt<HD, G, float>();
-    if (e != cudaSuccess) return e;
-    return configure_attn_kt<HD, G, __half>();
+    cudaError_t e = configure_attn_kt<HD, G, float>();
+    if (e == cudaSuccess) e = configure_attn_kt<HD, G, __half>();
+    if (e == cudaSuccess) e = configure_attn_kt<HD, G, kvq8>();
+    return e;
 }
 
 // Largest cluster (splits per kv head) of at most attn_max_cluster(G) CTAs
@@ -614,7 +669,8 @@ cudaError_t launch_attn_t(const AttnDecodeArgs &a, int B, int nsplit, int csize,
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    if (a.kv16) return cudaLaunchKernelEx(&cfg, k_attn_decode<HD, G, __half>, a, nsplit, csize);
+    if (a.kvtype == KV_F16) return cudaLaunchKernelEx(&cfg, k_attn_decode<HD, G, __half>, a, nsplit, csize);
+    if (a.kvtype == KV_Q8) return cudaLaunchKernelEx(&cfg, k_attn_decode<HD, G, kvq8>, a, nsplit, csize);
     return cudaLaunchKernelEx(&cfg, k_attn_decode<HD, G, float>, a, nsplit, csize);
 }
 
@@ -624,7 +680,23 @@ cudaError_t launch_attn_t(const AttnDecodeArgs &a, int B, int nsplit, int csize,
 // appended just before). CTA = (64-query tile, query head); warp w owns 8
 // query rows; for each 32-key tile lane j scores key j, then lanes own
 // head_dim slices for the P.V product. f32 throughout.
-__device__ __forceinline__ float4 ld4_kv(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+// Values c..c+3 (c % 4 == 0) of a cached row.
+template <int HD>
+__device__ __forceinline__ float4 ld4_row(const float *row, int c) { return *reinterpret_cast<const float4 *>(row + c); }
+__device__ __forceinline__ float4 ld4_kv(const __half *p);
+template <int HD>
+__device__ __forceinline__ float4 ld4_row(const __half *row, int c) { return ld4_kv(row + c); }
+template <int HD>
+__device__ __forceinline__ float4 ld4_row(const kvq8 *row, int c) {
+    const uint8_t *blk = &row->b + (c >> 5) * 34;
+    const float sc = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(blk)));
+    const uint16_t *cp = reinterpret_cast<const uint16_t *>(blk + 2 + (c & 31));   // 2-byte aligned
+    const uint16_t a = cp[0], b = cp[1];
+    return make_float4(sc * static_cast<float>(static_cast<int8_t>(a & 0xff)),
+                       sc * static_cast<float>(static_cast<int8_t>(a >> 8)),
+                       sc * static_cast<float>(static_cast<int8_t>(b & 0xff)),
+                       sc * static_cast<float>(static_cast<int8_t>(b >> 8)));
+}
 __device__ __forceinline__ float4 ld4_kv(const __half *p) {
     const uint2 t = *reinterpret_cast<const uint2 *>(p);
     const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&t.x));
@@ -674,8 +746,8 @@ __global__ void __launch_bounds__(256) k_attn_prefill(const float *__restrict__ 
             const int r = (i * 4) / HD, c = (i * 4) % HD;
             float4 kv4 = make_float4(0.f, 0.f, 0.f, 0.f), vv4 = kv4;
             if (t0 + r < nkeys) {
-                kv4 = ld4_kv(kb + static_cast<size_t>(t0 + r) * HD + c);
-                vv4 = ld4_kv(vb + static_cast<size_t>(t0 + r) * HD + c);
+                kv4 = ld4_row<HD>(kv_rowp<HD>(kb, t0 + r), c);
+                vv4 = ld4_row<HD>(kv_rowp<HD>(vb, t0 + r), c);
             }
             *reinterpret_cast<float4 *>(Ks + r * KP + c) = kv4;
             *reinterpret_cast<float4 *>(Vs + r * HD + c) = vv4;
@@ -809,6 +881,10 @@ cudaError_t configure_attention() {
                                  static_cast<int>(prefill_smem<128>())));
     QW3_CFG(cudaFuncSetAttribute(k_attn_prefill<64, __half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(prefill_smem<64>())));
+    QW3_CFG(cudaFuncSetAttribute(k_attn_prefill<128, kvq8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(prefill_smem<128>())));
+    QW3_CFG(cudaFuncSetAttribute(k_attn_prefill<64, kvq8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(prefill_smem<64>())));
 #undef QW3_CFG
     return cudaSuccess;
 }
@@ -840,9 +916,12 @@ cudaError_t launch_attn_decode(const AttnDecodeArgs &a, int B, int nsplit, int c
 
 cudaError_t launch_attn_prefill(const float *qkv, int M, int qkv_stride, const void *kv_seq, size_t kvsel_stride,
                                 size_t head_stride, int pos0, int nh, int nkv, int hd, float scale, float *out,
-                                bool kv16, cudaStream_t s) {
-    if (kv16)
+                                int kvtype, cudaStream_t s) {
+    if (kvtype == KV_F16)
         return launch_prefill_kt(qkv, M, qkv_stride, static_cast<const __half *>(kv_seq), kvsel_stride, head_stride,
+                                 pos0, nh, nkv, hd, scale, out, s);
+    if (kvtype == KV_Q8)
+        return launch_prefill_kt(qkv, M, qkv_stride, static_cast<const kvq8 *>(kv_seq), kvsel_stride, head_stride,
                                  pos0, nh, nkv, hd, scale, out, s);
     return launch_prefill_kt(qkv, M, qkv_stride, static_cast<const float *>(kv_seq), kvsel_stride, head_stride, pos0,
                              nh, nkv, hd, scale, out, s);

@@ -97,9 +97,9 @@ __global__ void k_pack_kv(const KT *__restrict__ kc, const KT *__restrict__ vc, 
         // K: row = key, columns = dims
         const int r = item / (HD / 8), d0 = (item % (HD / 8)) * 8;
         const int key = tile * kKT + r;
-        const KT *src = kc + static_cast<size_t>(g) * head_stride + static_cast<size_t>(key) * HD + d0;
+        const KT *row = kc + static_cast<size_t>(g) * head_stride + static_cast<size_t>(key) * kv_row<KT, HD>();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = key < ctx ? kv_f32(src[j]) : 0.0f;
+        for (int j = 0; j < 8; ++j) v[j] = key < ctx ? kv_elem<HD>(row, d0 + j) : 0.0f;
         split8_hl(v, hi, lo);
         const int s = d0 / 64, kk = d0 % 64;
         uint8_t *base = t + s * 2 * (kKT * 128);
@@ -112,7 +112,7 @@ __global__ void k_pack_kv(const KT *__restrict__ kc, const KT *__restrict__ vc, 
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int key = tile * kKT + k0 + j;
-            v[j] = key < ctx ? kv_f32(src[static_cast<size_t>(key) * HD + d]) : 0.0f;
+            v[j] = key < ctx ? kv_elem<HD>(src + static_cast<size_t>(key) * kv_row<KT, HD>(), d) : 0.0f;
         }
         split8_hl(v, hi, lo);
         uint8_t *base = t + Z::kk;
@@ -442,8 +442,11 @@ static cudaError_t launch_pa_kt(const float *qkv, int M, int qkv_stride, const K
 
 cudaError_t launch_attn_prefill_tc(const float *qkv, int M, int qkv_stride, const void *kv_seq, size_t kvsel_stride,
                                    size_t head_stride, int pos0, int nh, int nkv, int hd, float scale, float *out,
-                                   uint8_t *kvpack, int32_t *status, bool kv16, cudaStream_t s) {
-    if (kv16)
+                                   uint8_t *kvpack, int32_t *status, int kvtype, cudaStream_t s) {
+    if (kvtype == KV_Q8)
+        return launch_pa_kt(qkv, M, qkv_stride, static_cast<const kvq8 *>(kv_seq), kvsel_stride, head_stride,
+                            pos0, nh, nkv, hd, scale, out, kvpack, status, s);
+    if (kvtype == KV_F16)
         return launch_pa_kt(qkv, M, qkv_stride, static_cast<const __half *>(kv_seq), kvsel_stride, head_stride,
                             pos0, nh, nkv, hd, scale, out, kvpack, status, s);
     return launch_pa_kt(qkv, M, qkv_stride, static_cast<const float *>(kv_seq), kvsel_stride, head_stride, pos0, nh,

@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(128) k_qk_rope_append(float *__restrict__ qkv,
     const int seq = row_seq ? row_seq[row] : seq0;
     const int pos = row_pos ? row_pos[row] : pos0 + row;
     float *src = qkv + static_cast<size_t>(row) * qkv_stride + task * HD;
+    constexpr int RW = kv_row<KT, HD>();
     float v[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) v[e] = src[lane * E + e];
@@ -103,9 +104,13 @@ __global__ void __launch_bounds__(128) k_qk_rope_append(float *__restrict__ qkv,
         const int kvsel = task < nh + nkv ? 0 : 1;
         const int g = task - nh - kvsel * nkv;
         KT *dst = kv_layer + static_cast<size_t>(seq) * seq_stride + kvsel * kvsel_stride +
-                  static_cast<size_t>(g) * head_stride + static_cast<size_t>(pos) * HD;
+                  static_cast<size_t>(g) * head_stride + static_cast<size_t>(pos) * RW;
+        if constexpr (kv_is_q8<KT>::value) {
+            q8_store_lanes<HD>(dst, v, lane);   // the whole warp runs this task
+        } else {
 #pragma unroll
-        for (int e = 0; e < E; ++e) dst[lane * E + e] = kv_cvt<KT>(v[e]);
+            for (int e = 0; e < E; ++e) dst[lane * E + e] = kv_cvt<KT>(v[e]);
+        }
     }
 }
 
@@ -189,9 +194,10 @@ __global__ void k_copy_kv_rows(const KT *__restrict__ base, size_t kvsel_stride,
         const int d = static_cast<int>(i % hd);
         const int g = static_cast<int>((i / hd) % nkv);
         const int r = static_cast<int>(i / (static_cast<size_t>(hd) * nkv));
-        const size_t src = static_cast<size_t>(g) * head_stride + static_cast<size_t>(pos0 + r) * hd + d;
-        k_out[i] = kv_f32(base[src]);
-        v_out[i] = kv_f32(base[kvsel_stride + src]);
+        const size_t row = static_cast<size_t>(g) * head_stride +
+                           static_cast<size_t>(pos0 + r) * (kv_is_q8<KT>::value ? hd / 32 * 34 : hd);
+        k_out[i] = kv_elem<0>(base + row, d);
+        v_out[i] = kv_elem<0>(base + kvsel_stride + row, d);
     }
 }
 
@@ -244,10 +250,13 @@ cudaError_t qk_rope_append_t(float *qkv, int M, int qkv_stride, const float *q_n
 cudaError_t launch_qk_rope_append(float *qkv, int M, int qkv_stride, const float *q_norm, const float *k_norm,
                                   float eps, const float2 *rope, const int32_t *row_seq, int seq0,
                                   const int32_t *row_pos, int pos0, void *kv_layer, size_t seq_stride,
-                                  size_t kvsel_stride, size_t head_stride, int nh, int nkv, int hd, bool kv16,
+                                  size_t kvsel_stride, size_t head_stride, int nh, int nkv, int hd, int kvtype,
                                   cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
-    if (kv16)
+    if (kvtype == KV_Q8)
+        return qk_rope_append_t(qkv, M, qkv_stride, q_norm, k_norm, eps, rope, row_seq, seq0, row_pos, pos0,
+                                static_cast<kvq8 *>(kv_layer), seq_stride, kvsel_stride, head_stride, nh, nkv, hd, s);
+    if (kvtype == KV_F16)
         return qk_rope_append_t(qkv, M, qkv_stride, q_norm, k_norm, eps, rope, row_seq, seq0, row_pos, pos0,
                                 static_cast<__half *>(kv_layer), seq_stride, kvsel_stride, head_stride, nh, nkv, hd, s);
     return qk_rope_append_t(qkv, M, qkv_stride, q_norm, k_norm, eps, rope, row_seq, seq0, row_pos, pos0,
@@ -284,11 +293,14 @@ cudaError_t launch_argmax_finalize(unsigned long long *key, int B, const DecodeI
 }
 
 cudaError_t launch_copy_kv_rows(const void *kv_layer_seq, size_t kvsel_stride, size_t head_stride, int pos0, int n,
-                                int nkv, int hd, float *k_out, float *v_out, bool kv16, cudaStream_t s) {
+                                int nkv, int hd, float *k_out, float *v_out, int kvtype, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
     const size_t total = static_cast<size_t>(n) * nkv * hd;
     const unsigned grid = static_cast<unsigned>(std::min<size_t>((total + 255) / 256, 4096));
-    if (kv16)
+    if (kvtype == KV_Q8)
+        k_copy_kv_rows<<<grid, 256, 0, s>>>(static_cast<const kvq8 *>(kv_layer_seq), kvsel_stride, head_stride, pos0,
+                                            n, nkv, hd, k_out, v_out);
+    else if (kvtype == KV_F16)
         k_copy_kv_rows<<<grid, 256, 0, s>>>(static_cast<const __half *>(kv_layer_seq), kvsel_stride, head_stride, pos0,
                                             n, nkv, hd, k_out, v_out);
     else

@@ -109,8 +109,8 @@ struct qw3_model {
     float *out_norm = nullptr;
     float2 *rope = nullptr;
 
-    void *kv = nullptr;    // f32, or half when kv16
-    bool kv16 = false;
+    void *kv = nullptr;    // f32, IEEE half or q8_0 rows (kvtype)
+    int kvtype = KV_F32;
     bool act_q8 = false;   // linear inputs through a Q8_0 round trip
     size_t head_stride = 0, kvsel_stride = 0, seq_stride = 0, layer_stride = 0;
     std::vector<int32_t> seq_len;
@@ -149,7 +149,7 @@ namespace {
 // Address of (layer, seq)'s block of the KV cache.
 void *kv_at(const qw3_model *m, int layer, int seq) {
     const size_t e = static_cast<size_t>(layer) * m->layer_stride + static_cast<size_t>(seq) * m->seq_stride;
-    return static_cast<uint8_t *>(m->kv) + e * (m->kv16 ? 2 : 4);
+    return static_cast<uint8_t *>(m->kv) + e * kv_unit_bytes(m->kvtype);
 }
 
 // A linear layer through the GEMM; in the q8_0 activation mode its input
@@ -291,6 +291,7 @@ int validate_config(const qw3_config *c, std::string &why) {
         return bad("max_seqs, max_seq_len and max_prefill must be positive");
     if (!(c->rms_eps >= 0.0f) || !(c->rope_theta > 0.0f)) return bad("rms_eps must be >= 0 and rope_theta > 0");
     if (c->hidden > 16384 || c->intermediate > 65536) return bad("hidden or intermediate too large");
+    if ((c->flags & QW3_FLAG_KV_F16) && (c->flags & QW3_FLAG_KV_Q8)) return bad("one KV cache type at most");
     return QW3_OK;
 }
 
@@ -353,7 +354,7 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
         }
         AttnDecodeArgs at{};
         at.qkv = m->qkv; at.qkv_stride = m->qkv_w; at.q_norm = L.q_norm; at.k_norm = L.k_norm; at.eps = c.rms_eps;
-        at.rope = m->rope; at.kv = kv_at(m, l, 0); at.kv16 = m->kv16;
+        at.rope = m->rope; at.kv = kv_at(m, l, 0); at.kvtype = m->kvtype;
         at.seq_stride = m->seq_stride; at.kvsel_stride = m->kvsel_stride; at.head_stride = m->head_stride;
         at.seq_ids = m->d_seq; at.pos = m->d_pos; at.nh = nh; at.nkv = nkv; at.hd = hd;
         at.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(hd)));
@@ -472,7 +473,7 @@ int setup_tensor_core_gemm(qw3_model *m) {
 // covered; the per-kernel path then serves batch 1 too.
 int setup_step(qw3_model *m) {
     const qw3_config &c = m->cfg;
-    if ((c.flags & QW3_FLAG_PER_KERNEL) || m->kv16 || m->act_q8 || !step_supported(c)) return QW3_OK;
+    if ((c.flags & QW3_FLAG_PER_KERNEL) || m->kvtype != KV_F32 || m->act_q8 || !step_supported(c)) return QW3_OK;
     // The step kernel wins where a layer is latency-bound (a few hundred KB
     // of weights per SM); past that a layer is bandwidth-bound and the
     // per-kernel chain, with two streaming CTAs per SM, moves it faster
@@ -623,7 +624,7 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
 
     qw3_model *m = new qw3_model();
     m->cfg = *cfg;
-    m->kv16 = (cfg->flags & QW3_FLAG_KV_F16) != 0;
+    m->kvtype = (cfg->flags & QW3_FLAG_KV_Q8) ? KV_Q8 : ((cfg->flags & QW3_FLAG_KV_F16) ? KV_F16 : KV_F32);
     m->act_q8 = (cfg->flags & QW3_FLAG_ACT_Q8) != 0;
     auto bail = [&](int rc) {
         if (m->stream) cudaStreamSynchronize(m->stream);
@@ -729,13 +730,19 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
         if (cudaError_t e = cudaStreamSynchronize(m->stream); e != cudaSuccess) return bail(cuda_err(m, e, "sync"));
     }
 
-    // ---- KV cache: [layer][seq][K|V][kv_head][capacity][head_dim] f32
-    m->head_stride = static_cast<size_t>(c.max_seq_len) * hd;
+    // ---- KV cache: [layer][seq][K|V][kv_head][capacity][row] of f32 or
+    // half values, or of q8_0 rows (hd/32 blocks of 34 bytes; the capacity
+    // rounded up to 32 positions so every head and every 32-position tile
+    // starts 16-byte aligned, and 64 bytes of tail for the last bulk copy's
+    // rounding to 16 bytes)
+    const size_t cap = m->kvtype == KV_Q8 ? (static_cast<size_t>(c.max_seq_len) + 31) / 32 * 32
+                                          : static_cast<size_t>(c.max_seq_len);
+    m->head_stride = cap * kv_row_units(m->kvtype, hd);
     m->kvsel_stride = m->head_stride * nkv;
     m->seq_stride = 2 * m->kvsel_stride;
     m->layer_stride = m->seq_stride * c.max_seqs;
     {
-        const size_t bytes = m->layer_stride * c.n_layers * (m->kv16 ? 2 : 4);
+        const size_t bytes = m->layer_stride * c.n_layers * kv_unit_bytes(m->kvtype) + 64;
         if (cudaError_t e = model_alloc(m, reinterpret_cast<void **>(&m->kv), bytes); e != cudaSuccess)
             return bail(cuda_err(m, e, "KV cache"));
     }
@@ -839,14 +846,14 @@ int forward_rows(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n
             M_TRY(m, lin_gemm(m, m->ph, M, H, L.qkv, m->pqkv, GEMV_STORE, nullptr, nullptr, s));
             M_TRY(m, launch_qk_rope_append(m->pqkv, M, m->qkv_w, L.q_norm, L.k_norm, c.rms_eps, m->rope, nullptr, seq,
                                            nullptr, pos0, kvl, m->seq_stride, m->kvsel_stride, m->head_stride, nh,
-                                           nkv, hd, m->kv16, s));
+                                           nkv, hd, m->kvtype, s));
             if (m->kvpack && M >= kAttnPrefillTcMinRows) {
                 M_TRY(m, launch_attn_prefill_tc(m->pqkv, M, m->qkv_w, kv_at(m, l, seq), m->kvsel_stride,
                                                 m->head_stride, pos0, nh, nkv, hd, scale, m->po, m->kvpack,
-                                                m->d_status, m->kv16, s));
+                                                m->d_status, m->kvtype, s));
             } else {
                 M_TRY(m, launch_attn_prefill(m->pqkv, M, m->qkv_w, kv_at(m, l, seq), m->kvsel_stride, m->head_stride,
-                                             pos0, nh, nkv, hd, scale, m->po, m->kv16, s));
+                                             pos0, nh, nkv, hd, scale, m->po, m->kvtype, s));
             }
             M_TRY(m, lin_gemm(m, m->po, M, qw, L.o, m->px, GEMV_RESID, nullptr, nullptr, s));
             M_TRY(m, launch_rmsnorm_rows(m->px, M, H, L.ffn_norm, c.rms_eps, m->ph, s));
@@ -992,7 +999,7 @@ int qw3_debug_read_kv(qw3_model *m, int32_t layer, int32_t seq, int32_t pos0, in
         !k_out_dev || !v_out_dev || misaligned(k_out_dev, 4) || misaligned(v_out_dev, 4))
         return fail(m, QW3_ERR_INVALID_ARG, "bad KV read range");
     M_TRY(m, launch_copy_kv_rows(kv_at(m, layer, seq), m->kvsel_stride, m->head_stride, pos0, n, c.n_kv_heads,
-                                 c.head_dim, k_out_dev, v_out_dev, m->kv16, m->stream));
+                                 c.head_dim, k_out_dev, v_out_dev, m->kvtype, m->stream));
     return QW3_OK;
 }
 

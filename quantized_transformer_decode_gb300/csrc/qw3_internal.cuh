@@ -108,8 +108,8 @@ struct AttnDecodeArgs {
     float eps;
     const float2 *rope;   // [max_seq_len][hd/2] (cos, sin)
     void *kv;             // this layer's cache: [seq][K|V][kv_head][capacity][head_dim]
-    int kv16;             // 1: IEEE half elements, 0: f32
-    size_t seq_stride, kvsel_stride, head_stride;  // elements
+    int kvtype;           // KvType: f32, IEEE half or q8_0 rows
+    size_t seq_stride, kvsel_stride, head_stride;  // cache elements (bytes for q8_0)
     const int32_t *seq_ids;  // [B]
     const int32_t *pos;      // [B] position of the new token
     int nh, nkv, hd;
@@ -192,16 +192,16 @@ cudaError_t launch_gemm_tc(const float *A, int M, int K, const QMat &W, float *C
                            unsigned long long *argmax_key, const DecodeIO *io, int32_t *status, uint8_t *apack,
                            cudaStream_t s, const GemmSplitK *sk = nullptr);
 // KV cache pointers below are the byte address of the layer's (or the
-// sequence's) first element; element strides are in elements; kv16 selects
-// IEEE half elements instead of f32.
+// sequence's) first element; strides are in cache elements (bytes for a
+// q8_0 cache); kvtype (KvType) selects f32, IEEE half or q8_0 rows.
 cudaError_t launch_qk_rope_append(float *qkv, int M, int qkv_stride, const float *q_norm,
                                   const float *k_norm, float eps, const float2 *rope,
                                   const int32_t *row_seq, int seq0, const int32_t *row_pos, int pos0,
                                   void *kv_layer, size_t seq_stride, size_t kvsel_stride,
-                                  size_t head_stride, int nh, int nkv, int hd, bool kv16, cudaStream_t s);
+                                  size_t head_stride, int nh, int nkv, int hd, int kvtype, cudaStream_t s);
 cudaError_t launch_attn_prefill(const float *qkv, int M, int qkv_stride, const void *kv_seq,
                                 size_t kvsel_stride, size_t head_stride, int pos0, int nh, int nkv, int hd,
-                                float scale, float *out, bool kv16, cudaStream_t s);
+                                float scale, float *out, int kvtype, cudaStream_t s);
 // Causal prefill attention on tensor cores (attn_prefill_tc.cu): packs the
 // sequence's K/V of the layer into kvpack (attn_prefill_tc_pack_bytes) and
 // runs one CTA per (128-query tile, head); for chunks of >= 128 rows.
@@ -210,7 +210,7 @@ size_t attn_prefill_tc_pack_bytes(int hd, int nkv, int max_seq_len);
 cudaError_t configure_attn_prefill_tc();
 cudaError_t launch_attn_prefill_tc(const float *qkv, int M, int qkv_stride, const void *kv_seq, size_t kvsel_stride,
                                    size_t head_stride, int pos0, int nh, int nkv, int hd, float scale, float *out,
-                                   uint8_t *kvpack, int32_t *status, bool kv16, cudaStream_t s);
+                                   uint8_t *kvpack, int32_t *status, int kvtype, cudaStream_t s);
 // In-place Q8_0 round trip (q8_0_roundtrip4) of M rows of K values (K a
 // multiple of 32): the input of a linear layer in the q8_0 activation mode.
 cudaError_t launch_q8act_rows(float *x, int M, int K, cudaStream_t s);
@@ -221,7 +221,7 @@ cudaError_t launch_argmax_finalize(unsigned long long *key, int B, const DecodeI
                                    int32_t *next_token, int32_t *step_ctr, int32_t *pos_inc,
                                    int32_t *status, cudaStream_t s);
 cudaError_t launch_copy_kv_rows(const void *kv_layer_seq, size_t kvsel_stride, size_t head_stride,
-                                int pos0, int n, int nkv, int hd, float *k_out, float *v_out, bool kv16,
+                                int pos0, int n, int nkv, int hd, float *k_out, float *v_out, int kvtype,
                                 cudaStream_t s);
 
 }  // namespace qw3
@@ -376,6 +376,80 @@ template <>
 __device__ __forceinline__ float kv_cvt<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ __half kv_cvt<__half>(float v) { return __float2half_rn(v); }
+
+// ---- q8_0 KV cache ("The LLM stack", 13.4; "A transformer from scratch",
+// 12.4): a cached (position, kv head) row of head_dim values is head_dim/32
+// Q8_0 blocks (f16 scale, 32 int8 codes: 34 bytes), so a q8_0 cache is
+// addressed in bytes and a row is kv_row<kvq8, HD>() of them.
+struct kvq8 {
+    uint8_t b;
+};
+enum KvType : int { KV_F32 = 0, KV_F16 = 1, KV_Q8 = 2 };
+template <typename KT>
+struct kv_is_q8 {
+    static constexpr bool value = false;
+};
+template <>
+struct kv_is_q8<kvq8> {
+    static constexpr bool value = true;
+};
+// Elements of type KT in one cached row of head_dim HD.
+template <typename KT, int HD>
+__host__ __device__ constexpr int kv_row() { return kv_is_q8<KT>::value ? HD / 32 * 34 : HD; }
+inline size_t kv_row_units(int kvtype, int hd) { return kvtype == KV_Q8 ? static_cast<size_t>(hd) / 32 * 34 : hd; }
+inline size_t kv_unit_bytes(int kvtype) { return kvtype == KV_F32 ? 4 : (kvtype == KV_F16 ? 2 : 1); }
+
+// Value d of a cached row (any element type).
+template <int HD>
+__device__ __forceinline__ float kv_elem(const float *row, int d) { return row[d]; }
+template <int HD>
+__device__ __forceinline__ float kv_elem(const __half *row, int d) { return __half2float(row[d]); }
+template <int HD>
+__device__ __forceinline__ float kv_elem(const kvq8 *row, int d) {
+    const uint8_t *blk = &row->b + (d >> 5) * 34;
+    const float sc = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(blk)));
+    return sc * static_cast<float>(static_cast<int8_t>(blk[2 + (d & 31)]));
+}
+
+// Q8_0 encoding of a row spread over a warp, lane holding values
+// [lane * E, lane * E + E) (E = HD / 32): 32 / E consecutive lanes hold one
+// 32-value block. The 11.7 encoder: d = amax / 127, inv = d ? 1 / d : 0,
+// q = clamp(round(v * inv), +-127), halves away from zero, d kept as f16.
+// All 32 lanes call it.
+template <int HD>
+__device__ __forceinline__ void q8_encode_lanes(const float (&v)[HD / 32], int (&q)[HD / 32], __half &dh) {
+    constexpr int E = HD / 32, L = 32 / E;
+    float amax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(v[e]));
+#pragma unroll
+    for (int o = 1; o < L; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float inv = (d == 0.0f) ? 0.0f : __fdiv_rn(1.0f, d);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const float p = __fmul_rn(v[e], inv);
+        q[e] = isnan(p) ? 0 : static_cast<int>(fminf(fmaxf(roundf(p), -127.0f), 127.0f));
+    }
+    dh = __float2half_rn(d);
+}
+
+// Store a warp's row (lane layout as q8_encode_lanes) as Q8_0 blocks at row:
+// the first lane of each block writes its f16 scale, every lane its codes
+// (2-byte stores: a block's codes start 2 bytes into it). All 32 lanes call it.
+template <int HD>
+__device__ __forceinline__ void q8_store_lanes(kvq8 *row, const float (&v)[HD / 32], int lane) {
+    constexpr int E = HD / 32, L = 32 / E;
+    int q[E];
+    __half dh;
+    q8_encode_lanes<HD>(v, q, dh);
+    uint8_t *blk = &row->b + (lane / L) * 34;
+    if (lane % L == 0) *reinterpret_cast<uint16_t *>(blk) = __half_as_ushort(dh);
+    uint16_t *cp = reinterpret_cast<uint16_t *>(blk + 2 + (lane % L) * E);
+#pragma unroll
+    for (int h = 0; h < E / 2; ++h)
+        cp[h] = static_cast<uint16_t>((q[2 * h] & 0xff) | ((q[2 * h + 1] & 0xff) << 8));
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

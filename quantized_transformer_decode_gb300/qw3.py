@@ -35,6 +35,7 @@ QW3_FLAG_PER_KERNEL = 0x8
 QW3_FLAG_TEST_NO_WAIT = 0x10
 QW3_FLAG_KV_F16 = 0x20
 QW3_FLAG_ACT_Q8 = 0x40
+QW3_FLAG_KV_Q8 = 0x80
 
 # Every entry point of include/qw3.h, in declaration order.
 EXPORTS = (
