@@ -148,6 +148,120 @@ def q8_0_dequantize(blocks: np.ndarray, n: int) -> np.ndarray:
     return (d[:, None] * q.astype(np.float32)).astype(np.float32).reshape(-1)
 
 
+# ---------------------------------------------------------------------------
+# Q4_K codec -- "Model files and quantization", section 11.8
+# ---------------------------------------------------------------------------
+
+QK_K = 256          # values per Q4_K super-block
+Q4_K_BYTES = 144    # f16 d, f16 dmin, 12 bytes of packed 6-bit scales/mins, 128 bytes of 4-bit codes
+
+
+def q4k_pack_scales(sc: np.ndarray, m: np.ndarray) -> np.ndarray:
+    """Eight 6-bit sub-scales and eight 6-bit sub-mins per super-block into
+    the 12 bytes of the GGUF block (its published byte layout): bytes 0-3
+    hold sub-scales 0-3 in their low six bits, bytes 4-7 sub-mins 0-3; the
+    low nibbles of bytes 8-11 hold the low four bits of sub-scales 4-7, their
+    high nibbles those of sub-mins 4-7; the top two bits of sub-scales 4-7
+    sit in the top two bits of bytes 0-3, those of sub-mins 4-7 in bytes 4-7.
+    sc, m: [nb, 8] integers in [0, 63]."""
+    sc = sc.astype(np.uint16)
+    m = m.astype(np.uint16)
+    out = np.zeros((sc.shape[0], 12), np.uint16)
+    out[:, 0:4] = sc[:, 0:4] | ((sc[:, 4:8] >> 4) << 6)
+    out[:, 4:8] = m[:, 0:4] | ((m[:, 4:8] >> 4) << 6)
+    out[:, 8:12] = (sc[:, 4:8] & 0xF) | ((m[:, 4:8] & 0xF) << 4)
+    return out.astype(np.uint8)
+
+
+def q4k_unpack_scales(scales: np.ndarray):
+    """The inverse of the packing above: scales [nb, 12] bytes -> (sc, m),
+    each [nb, 8] in [0, 63]."""
+    b = scales.astype(np.uint16)
+    sc = np.empty((b.shape[0], 8), np.uint16)
+    m = np.empty((b.shape[0], 8), np.uint16)
+    sc[:, 0:4] = b[:, 0:4] & 63
+    m[:, 0:4] = b[:, 4:8] & 63
+    sc[:, 4:8] = (b[:, 8:12] & 0xF) | ((b[:, 0:4] >> 6) << 4)
+    m[:, 4:8] = (b[:, 8:12] >> 4) | ((b[:, 4:8] >> 6) << 4)
+    return sc, m
+
+
+def q4_k_quantize(x: np.ndarray) -> np.ndarray:
+    """Encode f32 values in super-blocks of 256 to Q4_K wire bytes.
+
+    The pages fix the block (f16 d and dmin, eight 6-bit sub-scales and
+    sub-mins, 4-bit codes; x ~ d*sc*q - dmin*m per 32-value sub-block) but
+    give no encoding algorithm; this is the plainest one, in f32:
+    per sub-block lo = min(0, min x), S = (max x - lo) / 15, O = -lo; d =
+    max S / 63 and dmin = max O / 63, stored as f16 (nearest even); sc =
+    round(S / d16), m = round(O / dmin16), clamped to [0, 63] (0 when the
+    stored scale is 0); per value q = round((x + dmin16*m) / (d16*sc)),
+    clamped to [0, 15] (0 when d16*sc is 0). Rounding halves away from zero.
+    Non-finite input is an error.
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    if x.size % QK_K:
+        raise InvalidShape(f"length {x.size} is not a multiple of {QK_K}")
+    if not np.all(np.isfinite(x)):
+        raise NonFiniteValue("Q4_K encoder input holds NaN or inf")
+    nb = x.size // QK_K
+    v = x.reshape(nb, 8, 32)
+    lo = np.minimum(np.float32(0.0), v.min(axis=2)).astype(np.float32)
+    S = ((v.max(axis=2) - lo).astype(np.float32) / np.float32(15.0)).astype(np.float32)
+    O = (np.float32(0.0) - lo).astype(np.float32)            # +0, never -0, for an all-positive sub-block
+    d = (S.max(axis=1) / np.float32(63.0)).astype(np.float32)
+    dm = (O.max(axis=1) / np.float32(63.0)).astype(np.float32)
+    with np.errstate(over="ignore"):
+        d16 = d.astype(np.float16)
+        dm16 = dm.astype(np.float16)
+    d32 = d16.astype(np.float32)
+    dm32 = dm16.astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        sc = np.where(d32[:, None] > 0, np.clip(_round_half_away((S / d32[:, None]).astype(np.float32)), 0, 63), 0)
+        m = np.where(dm32[:, None] > 0, np.clip(_round_half_away((O / dm32[:, None]).astype(np.float32)), 0, 63), 0)
+    Se = (d32[:, None] * sc.astype(np.float32)).astype(np.float32)            # exact
+    Oe = (dm32[:, None] * m.astype(np.float32)).astype(np.float32)            # exact
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = ((v + Oe[:, :, None]).astype(np.float32) / Se[:, :, None]).astype(np.float32)
+        q = np.where(Se[:, :, None] > 0, np.clip(_round_half_away(np.nan_to_num(t)), 0, 15), 0).astype(np.uint8)
+    q = q.reshape(nb, 4, 2, 32)                       # chunk c holds sub-blocks 2c (low nibble), 2c+1 (high)
+    qs = (q[:, :, 0, :] | (q[:, :, 1, :] << 4)).reshape(nb, 128)
+    out = np.empty((nb, Q4_K_BYTES), np.uint8)
+    out[:, 0:2] = d16.astype("<f2").view(np.uint8).reshape(nb, 2)
+    out[:, 2:4] = dm16.astype("<f2").view(np.uint8).reshape(nb, 2)
+    out[:, 4:16] = q4k_pack_scales(sc.astype(np.uint16), m.astype(np.uint16))
+    out[:, 16:] = qs
+    return out.reshape(-1)
+
+
+def q4_k_unpack(blocks: np.ndarray, n: int):
+    """Wire bytes -> (d16 [nb], dmin16 [nb], sc [nb, 8], m [nb, 8], q [nb, 256] in value order)."""
+    if n % QK_K:
+        raise InvalidShape(f"length {n} is not a multiple of {QK_K}")
+    nb = n // QK_K
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1)
+    if b.size != nb * Q4_K_BYTES:
+        raise InvalidShape(f"{b.size} bytes do not hold {nb} Q4_K blocks")
+    b = b.reshape(nb, Q4_K_BYTES)
+    d16 = np.ascontiguousarray(b[:, 0:2]).view("<f2").reshape(nb)
+    dm16 = np.ascontiguousarray(b[:, 2:4]).view("<f2").reshape(nb)
+    sc, m = q4k_unpack_scales(b[:, 4:16])
+    qs = b[:, 16:].reshape(nb, 4, 32)
+    q = np.stack([qs & 0xF, qs >> 4], axis=2).reshape(nb, 256)    # [chunk][low 32 | high 32]
+    return d16, dm16, sc, m, q
+
+
+def q4_k_dequantize(blocks: np.ndarray, n: int) -> np.ndarray:
+    """Decode: per 32-value sub-block j, x = (d * sc_j) * q - (dmin * m_j),
+    in f32 (the two products are exact; the difference rounds once)."""
+    d16, dm16, sc, m, q = q4_k_unpack(blocks, n)
+    nb = d16.size
+    d1 = (d16.astype(np.float32)[:, None] * sc.astype(np.float32)).astype(np.float32)     # [nb, 8]
+    m1 = (dm16.astype(np.float32)[:, None] * m.astype(np.float32)).astype(np.float32)
+    qv = q.reshape(nb, 8, 32).astype(np.float32)
+    return ((d1[:, :, None] * qv).astype(np.float32) - m1[:, :, None]).astype(np.float32).reshape(-1)
+
+
 def matrix_from_blocks(blocks: np.ndarray, rows: int, cols: int) -> np.ndarray:
     """Dequantise a Q8_0 matrix stored [rows][cols/32 blocks] to f32 [rows, cols]."""
     return q8_0_dequantize(blocks, rows * cols).reshape(rows, cols)
@@ -324,23 +438,33 @@ class QLinear:
     give identical results.
     """
 
-    def __init__(self, blocks: np.ndarray, rows: int, cols: int, keep_f64: bool, lazy: bool = False):
-        if cols % QK8_0:
-            raise InvalidShape(f"in-dimension {cols} is not a multiple of {QK8_0}")
+    def __init__(self, blocks: np.ndarray, rows: int, cols: int, keep_f64: bool, lazy: bool = False,
+                 wtype: str = "q8_0"):
+        if wtype not in ("q8_0", "q4_k"):
+            raise InvalidShape(f"weight type {wtype!r}")
+        qk, nbytes = (QK8_0, Q8_0_BYTES) if wtype == "q8_0" else (QK_K, Q4_K_BYTES)
+        if cols % qk:
+            raise InvalidShape(f"in-dimension {cols} is not a multiple of {qk}")
         self.rows, self.cols = rows, cols
         self.lazy = lazy
-        # the wire blocks themselves, [rows][cols/32 blocks] (the q8act path
-        # reads codes and scales)
-        self.blocks = np.asarray(blocks, dtype=np.uint8).reshape(rows, (cols // QK8_0) * Q8_0_BYTES)
+        self.wtype = wtype
+        # the wire blocks themselves, [rows][blocks of the row] (the q8act
+        # path reads codes and scales)
+        self.blocks = np.asarray(blocks, dtype=np.uint8).reshape(rows, (cols // qk) * nbytes)
         if lazy:
             self.w = None
         else:
-            w32 = matrix_from_blocks(blocks, rows, cols)
+            w32 = self._decode(self.blocks.reshape(-1), rows)
             self.w = w32.astype(np.float64) if keep_f64 else w32
+
+    def _decode(self, blocks: np.ndarray, rows: int) -> np.ndarray:
+        if self.wtype == "q4_k":
+            return q4_k_dequantize(blocks, rows * self.cols).reshape(rows, self.cols)
+        return matrix_from_blocks(blocks, rows, self.cols)
 
     def _rows32(self, r0: int, r1: int) -> np.ndarray:
         if self.lazy:
-            return matrix_from_blocks(self.blocks[r0:r1].reshape(-1), r1 - r0, self.cols)
+            return self._decode(self.blocks[r0:r1].reshape(-1), r1 - r0)
         return self.w[r0:r1]
 
     def __call__(self, x: np.ndarray) -> np.ndarray:
@@ -368,6 +492,8 @@ class QLinear:
         sum over a row's blocks is not shown, and is done in f64 like every
         other reduction here.
         """
+        if self.wtype != "q8_0":
+            raise InvalidShape("the q8_0-activation path takes Q8_0 weights")
         x32 = np.asarray(x, np.float32)
         if x32.ndim != 2 or x32.shape[1] != self.cols:
             raise InvalidShape(f"q8act input {x32.shape} for a [{self.rows}, {self.cols}] weight")
@@ -503,7 +629,8 @@ class OracleModel:
 
     F64_BUDGET_BYTES = 12 << 30
 
-    def __init__(self, shape, tensors: dict, keep_f64: bool | None = None, lazy: bool = False):
+    def __init__(self, shape, tensors: dict, keep_f64: bool | None = None, lazy: bool = False,
+                 wtype: str = "q8_0"):
         s = shape
         self.shape = s
         if s.head_dim % 2:
@@ -515,7 +642,7 @@ class OracleModel:
             keep_f64 = n_params * 8 <= self.F64_BUDGET_BYTES
 
         def lin(name, rows, cols):
-            return QLinear(tensors[name], rows, cols, keep_f64, lazy)
+            return QLinear(tensors[name], rows, cols, keep_f64, lazy, wtype)
 
         def norm(name, n):
             w = np.asarray(tensors[name], np.float32)
@@ -560,14 +687,16 @@ class OracleModel:
         return W.q8act(x) if self.act == "q8_0" else W(x)
 
     @classmethod
-    def from_f32(cls, shape, weights: dict, keep_f64: bool | None = None) -> "OracleModel":
-        """Quantise f32 linear weights with this module's Q8_0 encoder."""
+    def from_f32(cls, shape, weights: dict, keep_f64: bool | None = None, wtype: str = "q8_0") -> "OracleModel":
+        """Quantise f32 linear weights (the embedding included) with this
+        module's Q8_0 or Q4_K encoder."""
         from quantized_transformer_decode_gb300.inputs import tensor_specs
+        enc = q8_0_quantize if wtype == "q8_0" else q4_k_quantize
         tensors = {}
         for name, kind, _ in tensor_specs(shape):
             w = weights[name]
-            tensors[name] = q8_0_quantize(w) if kind == "linear" else np.asarray(w, np.float32)
-        return cls(shape, tensors, keep_f64)
+            tensors[name] = enc(w) if kind == "linear" else np.asarray(w, np.float32)
+        return cls(shape, tensors, keep_f64, wtype=wtype)
 
     @classmethod
     def from_f32_stream(cls, shape, named_weights) -> "OracleModel":

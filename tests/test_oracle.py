@@ -664,3 +664,94 @@ def test_q8_kv_model_stays_within_its_noise_and_prefill_reads_dequantised_rows()
     pre = om.forward(om.new_cache(16, "q8_0"), prompt, 0)
     assert not np.array_equal(dec, pre)
     assert np.linalg.norm(dec - pre) / np.linalg.norm(pre) < 5e-2
+
+
+# ---- Q4_K ("Model files and quantization", 11.8: super-block of 256, f16 d
+# and dmin, eight 6-bit sub-scales and sub-mins packed in 12 bytes, 4-bit
+# codes; x = d*sc*q - dmin*m)
+
+def _q4k_hand_block():
+    """One block built byte by byte: d = 1 (f16 0x3c00), dmin = 0.5 (0x3800),
+    sub-scales 1, 2, 3, 4, 5, 6, 7, 63 and sub-mins 0, 1, 2, 3, 4, 5, 6, 63
+    packed by hand into the 12 scale bytes (bytes 0-3: scales 0-3, top two
+    bits of scales 4-7; bytes 4-7: mins 0-3, top two bits of mins 4-7;
+    bytes 8-11: low nibbles of scales 4-7 | low nibbles of mins 4-7 << 4),
+    every code equal to its value index mod 16 (byte 32c + l of the codes
+    holds value 64c + l in its low nibble and 64c + 32 + l in its high one)."""
+    b = np.zeros(144, np.uint8)
+    b[0:2] = [0x00, 0x3C]
+    b[2:4] = [0x00, 0x38]
+    b[4:16] = [1, 2, 3, 196, 0, 1, 2, 195, 69, 86, 103, 255]
+    for c in range(4):
+        for l in range(32):
+            b[16 + 32 * c + l] = (l % 16) * 17
+    return b
+
+
+def test_q4_k_hand_built_block_decodes_to_hand_computed_values():
+    x = orc.q4_k_dequantize(_q4k_hand_block(), 256)
+    # value index: sub-block j = i // 32, code i % 16; x = sc_j * q - 0.5 * m_j
+    assert x[0] == 0.0                        # j 0: 1*0 - 0
+    assert x[33] == 1.5                       # j 1: 2*1 - 0.5*1
+    assert x[95] == 3 * 15 - 0.5 * 2          # j 2
+    assert x[130] == 5 * 2 - 0.5 * 4          # j 4: scale and min from the split bytes
+    assert x[191] == 6 * 15 - 0.5 * 5         # j 5
+    assert x[255] == 63 * 15 - 0.5 * 63       # j 7: both six-bit fields at their maximum
+
+
+def test_q4_k_encoder_picks_the_nearest_grid_point():
+    """Each value decodes to the point of its sub-block's grid
+    d16*sc*q - dmin16*m (q in 0..15) nearest to it (ties either way)."""
+    x = inputs.uniform_block_values(31, 256 * 16, -0.3, 0.5)
+    b = orc.q4_k_quantize(x)
+    y = orc.q4_k_dequantize(b, x.size)
+    d16, dm16, sc, m, _ = orc.q4_k_unpack(b, x.size)
+    grid = ((d16.astype(np.float32)[:, None] * sc.astype(np.float32))[:, :, None] * np.arange(16, dtype=np.float32)
+            - (dm16.astype(np.float32)[:, None] * m.astype(np.float32))[:, :, None]).astype(np.float32)  # [nb, 8, 16]
+    xv = x.reshape(-1, 8, 32)
+    best = np.min(np.abs(xv[..., None] - grid[:, :, None, :]), axis=-1)
+    got = np.abs(xv - y.reshape(-1, 8, 32))
+    assert np.all(got <= best + 1e-7)
+
+
+def test_q4_k_round_trip_bound_and_zero_block():
+    """With the encoder's grid the error is at most half a step (d16*sc / 2)
+    for values inside [-dmin16*m, 15*d16*sc - dmin16*m] and the zero block is
+    all zero bytes."""
+    x = (np.random.default_rng(8).standard_normal(256 * 8) * 0.02).astype(np.float32)
+    b = orc.q4_k_quantize(x)
+    y = orc.q4_k_dequantize(b, x.size)
+    d16, dm16, sc, m, _ = orc.q4_k_unpack(b, x.size)
+    step = (d16.astype(np.float32)[:, None] * sc.astype(np.float32))            # [nb, 8]
+    off = (dm16.astype(np.float32)[:, None] * m.astype(np.float32))
+    xv, yv = x.reshape(-1, 8, 32), y.reshape(-1, 8, 32)
+    inside = (xv >= -off[..., None]) & (xv <= 15 * step[..., None] - off[..., None])
+    err = np.abs(xv - yv)
+    assert np.all(err[inside] <= (step[..., None] / 2 + 1e-7).repeat(32, axis=2)[inside])
+    assert np.mean(inside) > 0.9
+    assert not orc.q4_k_quantize(np.zeros(256, np.float32)).any()
+    with pytest.raises(orc.NonFiniteValue):
+        orc.q4_k_quantize(np.full(256, np.inf, np.float32))
+
+
+def test_q4_k_scale_packing_round_trips_every_six_bit_pair():
+    sc = np.arange(64 * 8, dtype=np.uint16).reshape(64, 8) % 64
+    m = (np.arange(64 * 8, dtype=np.uint16).reshape(64, 8) * 7 + 3) % 64
+    s2, m2 = orc.q4k_unpack_scales(orc.q4k_pack_scales(sc, m))
+    np.testing.assert_array_equal(s2, sc)
+    np.testing.assert_array_equal(m2, m)
+
+
+def test_q4_k_linear_one_hot_and_model_mode():
+    rng = np.random.default_rng(12)
+    w = (rng.standard_normal((9, 512)) * 0.05).astype(np.float32)
+    L = orc.QLinear(orc.q4_k_quantize(w), 9, 512, keep_f64=True, wtype="q4_k")
+    deq = orc.q4_k_dequantize(orc.q4_k_quantize(w), w.size).reshape(9, 512)
+    for k in (0, 255, 256, 511):
+        x = np.zeros((1, 512), np.float32)
+        x[0, k] = 1.0
+        np.testing.assert_array_equal(L(x)[0], deq[:, k])
+    shape = inputs.TINY
+    om = orc.OracleModel.from_f32(shape, inputs.generate_weights(shape, 0), wtype="q4_k")
+    lg = om.forward(om.new_cache(8), inputs.prompt_tokens(shape, 0, 4), 0)
+    assert lg.shape == (shape.vocab,) and np.all(np.isfinite(lg))
