@@ -120,6 +120,16 @@ typedef struct qw3_config {
                                   forward read the dequantised rows. Not with
                                   QW3_FLAG_KV_F16. Batch-1 decode runs the
                                   per-kernel chain.                           */
+#define QW3_FLAG_WEIGHTS_Q4_K 0x100 /* every linear weight (the embedding and
+                                  output included) is given as Q4_K blocks
+                                  ("Model files and quantization", 11.8:
+                                  144 bytes per 256 values, GGUF layout)
+                                  instead of Q8_0; hidden, intermediate and
+                                  n_heads*head_dim must be multiples of 256.
+                                  Decode of up to 8 rows streams the Q4_K
+                                  rows; prefill and larger batches run the
+                                  tensor-core GEMMs on tiles packed from
+                                  them. Not with QW3_FLAG_ACT_Q8.             */
 #define QW3_FLAG_ACT_Q8 0x40     /* every linear layer takes its input rows
                                   re-quantized to Q8_0 per 32-block on the
                                   fly ("Model files and quantization", 11.9:
@@ -281,6 +291,31 @@ QW3_API int qw3_q8_0_gemv(const void *W_dev, int32_t rows, int32_t cols,
  * QW3_ERR_INVALID_ARG otherwise). Asynchronous on `stream`. */
 QW3_API int qw3_q8_0_gemv_q8act(const void *W_dev, int32_t rows, int32_t cols,
                         const float *x_dev, int32_t B, float *y_dev, void *stream);
+
+/* ---- Q4_K ("Model files and quantization", 11.8) ------------------------
+ * Block: 256 values in 144 bytes: f16 d, f16 dmin, 12 bytes packing eight
+ * 6-bit sub-scales sc_j and eight 6-bit sub-mins m_j (GGUF layout), 128
+ * bytes of 4-bit codes; value i of sub-block j = i/32 is
+ * (d*sc_j)*q - dmin*m_j in f32. */
+
+/* Encode n values (n % 256 == 0) to Q4_K. The pages give no encoding
+ * algorithm; this one: per 32-value sub-block lo = min(0, min x),
+ * S = (max x - lo)/15, O = -lo; d = max S/63, dmin = max O/63 as f16; sub-
+ * scales, sub-mins (0..63) and codes (0..15) rounded half away from zero.
+ * A block holding NaN or inf is written as zero bytes and, if status_dev is
+ * not NULL, *status_dev = QW3_ERR_NONFINITE. x and blocks 16-byte aligned. */
+QW3_API int qw3_q4_k_quantize(const float *x_dev, int64_t n, void *blocks_dev,
+                      int32_t *status_dev, void *stream);
+
+/* Decode n values (n % 256 == 0) of Q4_K blocks to f32. */
+QW3_API int qw3_q4_k_dequantize(const void *blocks_dev, int64_t n, float *y_dev, void *stream);
+
+/* y[b][r] = sum_k W[r][k] * x[b][k] for a raw Q4_K matrix W [rows][cols/256]
+ * (GGUF layout), x f32 [B][cols], y f32 [B][rows]; f32 accumulation (a
+ * sub-block adds d1 * sum(q x) - m1 * sum(x)). 1 <= B <= 8, cols % 256 == 0,
+ * B * cols <= 49152; W and x 16-byte aligned. Asynchronous on `stream`. */
+QW3_API int qw3_q4_k_gemv(const void *W_dev, int32_t rows, int32_t cols,
+                  const float *x_dev, int32_t B, float *y_dev, void *stream);
 
 /* ---- no-allocation variant ------------------------------------------- */
 

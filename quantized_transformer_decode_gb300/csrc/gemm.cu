@@ -252,6 +252,30 @@ __global__ void k_pack_w(const QMat W, int N, int K, uint8_t *__restrict__ dst) 
     *reinterpret_cast<uint4 *>(t + TC_OPERAND + core_off(r % TC_BM, k % TC_BK)) = lo;
 }
 
+// One thread per (row, 8-column group): weights of a raw Q4_K matrix (rows of
+// K / 256 blocks of 144 bytes), decoded exactly in f32 then split.
+__global__ void k_pack_w_q4k(const uint8_t *__restrict__ W, int N, int K, uint8_t *__restrict__ dst) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int groups = K / 8;
+    const int rows = (N + TC_BM - 1) / TC_BM * TC_BM;
+    if (i >= static_cast<int64_t>(rows) * groups) return;
+    const int r = static_cast<int>(i / groups), k = static_cast<int>(i % groups) * 8;
+    float v[8];
+    if (r < N) {
+        const uint8_t *blk = W + (static_cast<size_t>(r) * (K / 256) + k / 256) * 144;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = q4k_value(blk, (k % 256) + j);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+    }
+    uint4 hi, lo;
+    split8(v, hi, lo);
+    uint8_t *t = dst + ut_tile(r / TC_BM, k / TC_BK, K / TC_BK);
+    *reinterpret_cast<uint4 *>(t + core_off(r % TC_BM, k % TC_BK)) = hi;
+    *reinterpret_cast<uint4 *>(t + TC_OPERAND + core_off(r % TC_BM, k % TC_BK)) = lo;
+}
+
 // One thread per (row, 8-column group) of an f32 activation matrix.
 __global__ void k_pack_act(const float *__restrict__ A, int M, int K, uint8_t *__restrict__ dst) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -552,13 +576,21 @@ size_t ut_bytes(int rows, int K) {
 }
 
 bool gemm_tc_supported(int M, int K, const QMat &W) {
-    return W.ut != nullptr && M >= kGemmTcMinRows && K % TC_BK == 0 && W.cols == K;
+    // a matrix held only as tensor-core tiles (Q4_K models) takes every M
+    return W.ut != nullptr && (M >= kGemmTcMinRows || W.base == nullptr) && K % TC_BK == 0 && W.cols == K;
 }
 
 cudaError_t launch_pack_w(const QMat &W, uint8_t *dst, cudaStream_t s) {
     const int rows = (W.rows + TC_BM - 1) / TC_BM * TC_BM;
     const int64_t n = static_cast<int64_t>(rows) * (W.cols / 8);
     k_pack_w<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(W, W.rows, W.cols, dst);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_w_q4k(const uint8_t *W, int N, int K, uint8_t *dst, cudaStream_t s) {
+    const int rows = (N + TC_BM - 1) / TC_BM * TC_BM;
+    const int64_t n = static_cast<int64_t>(rows) * (K / 8);
+    k_pack_w_q4k<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(W, N, K, dst);
     return cudaGetLastError();
 }
 

@@ -67,6 +67,7 @@ cudaError_t configure_all() {
         if (e == cudaSuccess) e = configure_misc();
         if (e == cudaSuccess) e = configure_step();
         if (e == cudaSuccess) e = configure_gemm_tc();
+        if (e == cudaSuccess) e = configure_q4k();
         if (e == cudaSuccess) e = configure_attn_prefill_tc();
         g_cfg_err = e;
     });
@@ -112,6 +113,8 @@ struct qw3_model {
     void *kv = nullptr;    // f32, IEEE half or q8_0 rows (kvtype)
     int kvtype = KV_F32;
     bool act_q8 = false;   // linear inputs through a Q8_0 round trip
+    bool q4k = false;      // Q4_K weights: raw rows per matrix (QMat::q4), tensor-core tiles, no Q8_0 tiles
+    uint8_t *emb4 = nullptr, *out4 = nullptr;
     size_t head_stride = 0, kvsel_stride = 0, seq_stride = 0, layer_stride = 0;
     std::vector<int32_t> seq_len;
 
@@ -292,6 +295,11 @@ int validate_config(const qw3_config *c, std::string &why) {
     if (!(c->rms_eps >= 0.0f) || !(c->rope_theta > 0.0f)) return bad("rms_eps must be >= 0 and rope_theta > 0");
     if (c->hidden > 16384 || c->intermediate > 65536) return bad("hidden or intermediate too large");
     if ((c->flags & QW3_FLAG_KV_F16) && (c->flags & QW3_FLAG_KV_Q8)) return bad("one KV cache type at most");
+    if (c->flags & QW3_FLAG_WEIGHTS_Q4_K) {
+        if (c->hidden % 256 || c->intermediate % 256 || (c->n_heads * c->head_dim) % 256)
+            return bad("Q4_K weights need hidden, intermediate and n_heads*head_dim multiples of 256");
+        if (c->flags & QW3_FLAG_ACT_Q8) return bad("the Q8_0 activation mode takes Q8_0 weights");
+    }
     return QW3_OK;
 }
 
@@ -313,7 +321,47 @@ constexpr int kAttnLongClusters = 4;
 
 bool use_gemv(const qw3_config &c, int B) {
     const int kmax = std::max(c.hidden, std::max(c.intermediate, c.n_heads * c.head_dim));
+    if (c.flags & QW3_FLAG_WEIGHTS_Q4_K) return q4k_gemv_fits(B, kmax);
     return B <= 4 && B * kmax <= kGemvMaxBK;
+}
+
+// Attention arguments of layer l for the decode step.
+AttnDecodeArgs attn_args(qw3_model *m, int l) {
+    const qw3_config &c = m->cfg;
+    const LayerDev &L = m->layers[l];
+    AttnDecodeArgs at{};
+    at.qkv = m->qkv; at.qkv_stride = m->qkv_w; at.q_norm = L.q_norm; at.k_norm = L.k_norm; at.eps = c.rms_eps;
+    at.rope = m->rope; at.kv = kv_at(m, l, 0); at.kvtype = m->kvtype;
+    at.seq_stride = m->seq_stride; at.kvsel_stride = m->kvsel_stride; at.head_stride = m->head_stride;
+    at.seq_ids = m->d_seq; at.pos = m->d_pos; at.nh = c.n_heads; at.nkv = c.n_kv_heads; at.hd = c.head_dim;
+    at.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(c.head_dim)));
+    at.out = m->o; at.status = m->d_status; at.cpart = m->attn_cpart; at.ccnt = m->attn_ccnt;
+    return at;
+}
+
+// One decode step of a Q4_K model for B rows the Q4_K GEMV takes: every
+// projection streams the raw Q4_K rows (norms fused as prologues, SwiGLU over
+// the interleaved gate/up pairs), the lm_head keeps packed argmax keys that
+// k_argmax_finalize turns into tokens.
+int enqueue_decode_q4k(qw3_model *m, int B, int nsplit, int csize, cudaStream_t s) {
+    const qw3_config &c = m->cfg;
+    const int H = c.hidden, I = c.intermediate, qw = c.n_heads * c.head_dim;
+    const float eps = c.rms_eps;
+    M_TRY(m, launch_embed_q4k(m->d_tok, B, m->emb4, H, c.vocab, m->x, s));
+    for (int l = 0; l < c.n_layers; ++l) {
+        const LayerDev &L = m->layers[l];
+        M_TRY(m, launch_gemv_q4k(L.qkv.q4, m->qkv_w, H, B, m->x, L.attn_norm, eps, m->qkv, GEMV_STORE, nullptr,
+                                 nullptr, s));
+        M_TRY(m, launch_attn_decode(attn_args(m, l), B, nsplit, csize, false, s));
+        M_TRY(m, launch_gemv_q4k(L.o.q4, H, qw, B, m->o, nullptr, eps, m->x, GEMV_RESID, nullptr, nullptr, s));
+        M_TRY(m, launch_gemv_q4k(L.gu.q4, 2 * I, H, B, m->x, L.ffn_norm, eps, m->act, GEMV_SWIGLU, nullptr, nullptr,
+                                 s));
+        M_TRY(m, launch_gemv_q4k(L.down.q4, H, I, B, m->act, nullptr, eps, m->x, GEMV_RESID, nullptr, nullptr, s));
+    }
+    M_TRY(m, launch_gemv_q4k(m->out4, c.vocab, H, B, m->x, m->out_norm, eps, nullptr, GEMV_ARGMAX, m->d_io,
+                             m->argmax_key, s));
+    M_TRY(m, launch_argmax_finalize(m->argmax_key, B, m->d_io, m->d_tok, m->d_step, m->d_pos, m->d_status, s));
+    return QW3_OK;
 }
 
 // Enqueue one decode step for B rows on stream s: inputs d_tok/d_seq/d_pos,
@@ -332,13 +380,15 @@ int enqueue_decode(qw3_model *m, int B, cudaStream_t s) {
         nsplit = csize * kAttnLongClusters;
     }
     const bool gv = use_gemv(c, B);
+    if (m->q4k && gv) return enqueue_decode_q4k(m, B, nsplit, csize, s);
     int kidx = 0;
     auto tr = [&]() -> unsigned long long * {
         if (!m->trace) return nullptr;
         const int i = kidx++;
         return i < m->trace_kernels ? m->trace + static_cast<size_t>(i) * 2 * kTraceWords : nullptr;
     };
-    M_TRY(m, launch_embed(m->d_tok, B, m->embd, m->x, pdl && gv, s, tr()));
+    if (m->q4k) M_TRY(m, launch_embed_q4k(m->d_tok, B, m->emb4, H, c.vocab, m->x, s));
+    else M_TRY(m, launch_embed(m->d_tok, B, m->embd, m->x, pdl && gv, s, tr()));
     for (int l = 0; l < c.n_layers; ++l) {
         const LayerDev &L = m->layers[l];
         if (gv) {
@@ -434,15 +484,17 @@ int run_decode_step(qw3_model *m, int B) {
 // copy as bf16 hi/lo tensor-core tiles, 4 bytes per weight.
 int setup_tensor_core_gemm(qw3_model *m) {
     const qw3_config &c = m->cfg;
-    const bool prefill_tc = c.max_prefill >= kGemmTcMinRows;
-    const bool batch_tc = c.max_seqs >= kGemmTcMinRows;
+    // a Q4_K model's prefill and batches past the GEMV's rows run here at any size
+    const bool prefill_tc = c.max_prefill >= kGemmTcMinRows || m->q4k;
+    const bool batch_tc = c.max_seqs >= kGemmTcMinRows || m->q4k;
     if (!prefill_tc && !batch_tc) return QW3_OK;
     const int H = c.hidden, qw = c.n_heads * c.head_dim, I = c.intermediate;
     if (H % 64 || qw % 64 || I % 64) return QW3_OK;
     auto pack = [&](QMat &q) -> int {
         uint8_t *p = nullptr;
         M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&p), ut_bytes(q.rows, q.cols)));
-        M_TRY(m, launch_pack_w(q, p, m->stream));
+        if (q.q4) M_TRY(m, launch_pack_w_q4k(q.q4, q.rows, q.cols, p, m->stream));
+        else M_TRY(m, launch_pack_w(q, p, m->stream));
         q.ut = p;
         return QW3_OK;
     };
@@ -473,7 +525,8 @@ int setup_tensor_core_gemm(qw3_model *m) {
 // covered; the per-kernel path then serves batch 1 too.
 int setup_step(qw3_model *m) {
     const qw3_config &c = m->cfg;
-    if ((c.flags & QW3_FLAG_PER_KERNEL) || m->kvtype != KV_F32 || m->act_q8 || !step_supported(c)) return QW3_OK;
+    if ((c.flags & QW3_FLAG_PER_KERNEL) || m->kvtype != KV_F32 || m->act_q8 || m->q4k || !step_supported(c))
+        return QW3_OK;
     // The step kernel wins where a layer is latency-bound (a few hundred KB
     // of weights per SM); past that a layer is bandwidth-bound and the
     // per-kernel chain, with two streaming CTAs per SM, moves it faster
@@ -626,6 +679,7 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
     m->cfg = *cfg;
     m->kvtype = (cfg->flags & QW3_FLAG_KV_Q8) ? KV_Q8 : ((cfg->flags & QW3_FLAG_KV_F16) ? KV_F16 : KV_F32);
     m->act_q8 = (cfg->flags & QW3_FLAG_ACT_Q8) != 0;
+    m->q4k = (cfg->flags & QW3_FLAG_WEIGHTS_Q4_K) != 0;
     auto bail = [&](int rc) {
         if (m->stream) cudaStreamSynchronize(m->stream);
         const std::string msg = m->err;
@@ -649,10 +703,12 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
     m->qkv_w = (nh + 2 * nkv) * hd;
     const int qw = nh * hd;
 
-    // ---- weights: one arena, zero-filled so padding rows are zero
-    size_t wbytes = qmat_bytes(V, H) + (c.tied_lm_head ? 0 : qmat_bytes(V, H));
+    // ---- weights: one arena, zero-filled so padding rows are zero (Q4_K
+    // models keep only the norms there; their matrices are raw rows)
+    const int qm = m->q4k ? 0 : 1;
+    size_t wbytes = qm * (qmat_bytes(V, H) + (c.tied_lm_head ? 0 : qmat_bytes(V, H)));
     wbytes += static_cast<size_t>(c.n_layers) *
-              (qmat_bytes(m->qkv_w, H) + qmat_bytes(H, qw) + qmat_bytes(2 * I, H) + qmat_bytes(H, I) +
+              (qm * (qmat_bytes(m->qkv_w, H) + qmat_bytes(H, qw) + qmat_bytes(2 * I, H) + qmat_bytes(H, I)) +
                align_up(static_cast<size_t>(2 * H + 2 * hd) * 4, 256) + 4 * 256);
     wbytes += align_up(static_cast<size_t>(H) * 4, 256);
     uint8_t *arena = nullptr;
@@ -663,7 +719,22 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
     uint8_t *cur = arena;
     const bool on_dev = w->on_device != 0;
     uint8_t *staging = nullptr;
-    if (!on_dev) {
+    // Q4_K: a device buffer of `rows` raw rows per matrix, filled by plain copies
+    auto q4mat = [&](QMat &q, int rows, int cols) -> uint8_t * {
+        q = qmat_shape(rows, cols);
+        uint8_t *p = nullptr;
+        if (model_alloc(m, reinterpret_cast<void **>(&p), static_cast<size_t>(rows) * q4k_row_bytes(cols)) != cudaSuccess)
+            return nullptr;
+        q.q4 = p;
+        return p;
+    };
+    auto q4copy = [&](uint8_t *dst, size_t dpitch, const void *src, int rows, int cols) -> int {
+        const size_t rb = q4k_row_bytes(cols);
+        if (!src) return fail(m, QW3_ERR_INVALID_ARG, "a weight pointer is NULL");
+        M_TRY(m, cudaMemcpy2DAsync(dst, dpitch, src, rb, rb, rows, cudaMemcpyDefault, m->stream));
+        return QW3_OK;
+    };
+    if (!on_dev && !m->q4k) {
         size_t biggest = static_cast<size_t>(V) * H;
         biggest = std::max(biggest, static_cast<size_t>(qw) * H);
         biggest = std::max(biggest, static_cast<size_t>(I) * H);
@@ -671,29 +742,58 @@ int qw3_create(const qw3_config *cfg, const qw3_weights *w, void *cuda_stream, q
         if (cudaError_t e = model_alloc(m, reinterpret_cast<void **>(&staging), biggest); e != cudaSuccess)
             return bail(cuda_err(m, e, "staging"));
     }
-    qmat_place(m->embd, cur, V, H);
-    if (int rc = repack_into(m, m->embd, w->token_embd, V, H, 0, 1, on_dev, staging)) return bail(rc);
-    if (c.tied_lm_head) {
-        m->out = m->embd;
+    if (m->q4k) {
+        const size_t rbH = q4k_row_bytes(H);
+        if (!(m->emb4 = q4mat(m->embd, V, H))) return bail(fail(m, QW3_ERR_OOM, "Q4_K embedding"));
+        if (int rc = q4copy(m->emb4, rbH, w->token_embd, V, H)) return bail(rc);
+        if (c.tied_lm_head) {
+            m->out = m->embd;
+            m->out4 = m->emb4;
+        } else {
+            if (!(m->out4 = q4mat(m->out, V, H))) return bail(fail(m, QW3_ERR_OOM, "Q4_K output"));
+            if (int rc = q4copy(m->out4, rbH, w->output, V, H)) return bail(rc);
+        }
     } else {
-        qmat_place(m->out, cur, V, H);
-        if (int rc = repack_into(m, m->out, w->output, V, H, 0, 1, on_dev, staging)) return bail(rc);
+        qmat_place(m->embd, cur, V, H);
+        if (int rc = repack_into(m, m->embd, w->token_embd, V, H, 0, 1, on_dev, staging)) return bail(rc);
+        if (c.tied_lm_head) {
+            m->out = m->embd;
+        } else {
+            qmat_place(m->out, cur, V, H);
+            if (int rc = repack_into(m, m->out, w->output, V, H, 0, 1, on_dev, staging)) return bail(rc);
+        }
     }
     m->layers.resize(c.n_layers);
     for (int l = 0; l < c.n_layers; ++l) {
         const qw3_layer_weights &lw = w->layers[l];
         LayerDev &L = m->layers[l];
-        qmat_place(L.qkv, cur, m->qkv_w, H);
-        qmat_place(L.o, cur, H, qw);
-        qmat_place(L.gu, cur, 2 * I, H);
-        qmat_place(L.down, cur, H, I);
-        int rc = repack_into(m, L.qkv, lw.attn_q, qw, H, 0, 1, on_dev, staging);
-        if (!rc) rc = repack_into(m, L.qkv, lw.attn_k, nkv * hd, H, qw, 1, on_dev, staging);
-        if (!rc) rc = repack_into(m, L.qkv, lw.attn_v, nkv * hd, H, qw + nkv * hd, 1, on_dev, staging);
-        if (!rc) rc = repack_into(m, L.o, lw.attn_output, H, qw, 0, 1, on_dev, staging);
-        if (!rc) rc = repack_into(m, L.gu, lw.ffn_gate, I, H, 0, 2, on_dev, staging);
-        if (!rc) rc = repack_into(m, L.gu, lw.ffn_up, I, H, 1, 2, on_dev, staging);
-        if (!rc) rc = repack_into(m, L.down, lw.ffn_down, H, I, 0, 1, on_dev, staging);
+        int rc = QW3_OK;
+        if (m->q4k) {
+            // the Q8_0 layout's row order: [q; k; v], gate/up interleaved
+            const size_t rbH = q4k_row_bytes(H);
+            uint8_t *pq = q4mat(L.qkv, m->qkv_w, H), *po = q4mat(L.o, H, qw);
+            uint8_t *pg = q4mat(L.gu, 2 * I, H), *pd = q4mat(L.down, H, I);
+            if (!pq || !po || !pg || !pd) return bail(fail(m, QW3_ERR_OOM, "Q4_K layer weights"));
+            rc = q4copy(pq, rbH, lw.attn_q, qw, H);
+            if (!rc) rc = q4copy(pq + static_cast<size_t>(qw) * rbH, rbH, lw.attn_k, nkv * hd, H);
+            if (!rc) rc = q4copy(pq + static_cast<size_t>(qw + nkv * hd) * rbH, rbH, lw.attn_v, nkv * hd, H);
+            if (!rc) rc = q4copy(po, q4k_row_bytes(qw), lw.attn_output, H, qw);
+            if (!rc) rc = q4copy(pg, 2 * rbH, lw.ffn_gate, I, H);
+            if (!rc) rc = q4copy(pg + rbH, 2 * rbH, lw.ffn_up, I, H);
+            if (!rc) rc = q4copy(pd, q4k_row_bytes(I), lw.ffn_down, H, I);
+        } else {
+            qmat_place(L.qkv, cur, m->qkv_w, H);
+            qmat_place(L.o, cur, H, qw);
+            qmat_place(L.gu, cur, 2 * I, H);
+            qmat_place(L.down, cur, H, I);
+            rc = repack_into(m, L.qkv, lw.attn_q, qw, H, 0, 1, on_dev, staging);
+            if (!rc) rc = repack_into(m, L.qkv, lw.attn_k, nkv * hd, H, qw, 1, on_dev, staging);
+            if (!rc) rc = repack_into(m, L.qkv, lw.attn_v, nkv * hd, H, qw + nkv * hd, 1, on_dev, staging);
+            if (!rc) rc = repack_into(m, L.o, lw.attn_output, H, qw, 0, 1, on_dev, staging);
+            if (!rc) rc = repack_into(m, L.gu, lw.ffn_gate, I, H, 0, 2, on_dev, staging);
+            if (!rc) rc = repack_into(m, L.gu, lw.ffn_up, I, H, 1, 2, on_dev, staging);
+            if (!rc) rc = repack_into(m, L.down, lw.ffn_down, H, I, 0, 1, on_dev, staging);
+        }
         if (rc) return bail(rc);
         float *nb = reinterpret_cast<float *>(cur);
         L.attn_norm = nb;
@@ -838,7 +938,8 @@ int forward_rows(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n
     for (int off = 0; off < n; off += c.max_prefill) {
         const int M = std::min(c.max_prefill, n - off);
         const int pos0 = len + off;
-        M_TRY(m, launch_embed(tokens_dev + off, M, m->embd, m->px, false, s));
+        if (m->q4k) M_TRY(m, launch_embed_q4k(tokens_dev + off, M, m->emb4, H, c.vocab, m->px, s));
+        else M_TRY(m, launch_embed(tokens_dev + off, M, m->embd, m->px, false, s));
         for (int l = 0; l < c.n_layers; ++l) {
             const LayerDev &L = m->layers[l];
             void *kvl = kv_at(m, l, 0);
@@ -866,6 +967,10 @@ int forward_rows(qw3_model *m, int32_t seq, const int32_t *tokens_dev, int32_t n
             M_TRY(m, launch_rmsnorm_rows(m->px, M, H, m->out_norm, c.rms_eps, m->ph, s));
             M_TRY(m, lin_gemm(m, m->ph, M, H, m->out, lg, GEMV_STORE, nullptr, nullptr, s));
             if (all_argmax) M_TRY(m, launch_argmax_rows(lg, M, c.vocab, all_argmax + off, m->d_status, s));
+        } else if (off + M == n && (last_logits_dev || argmax_dev) && m->q4k) {
+            M_TRY(m, launch_gemv_q4k(m->out4, c.vocab, H, 1, m->px + static_cast<size_t>(M - 1) * H, m->out_norm,
+                                     c.rms_eps, last_logits_dev, GEMV_ARGMAX, nullptr, m->argmax_key, s));
+            M_TRY(m, launch_argmax_finalize(m->argmax_key, 1, nullptr, argmax_dev, nullptr, nullptr, m->d_status, s));
         } else if (off + M == n && (last_logits_dev || argmax_dev)) {
             GemvArgs a{};
             a.act_q8 = m->act_q8;
@@ -1028,7 +1133,8 @@ int qw3_decode_plan(const qw3_model *m, int32_t B, int32_t *persistent, int32_t 
         return QW3_OK;
     }
     *persistent = 0;
-    *launches_per_step = use_gemv(c, B) ? 2 + 5 * c.n_layers : 4 + 7 * c.n_layers;
+    *launches_per_step = use_gemv(c, B) ? ((c.flags & QW3_FLAG_WEIGHTS_Q4_K) ? 3 : 2) + 5 * c.n_layers
+                                        : 4 + 7 * c.n_layers;
     return QW3_OK;
 }
 
@@ -1061,6 +1167,40 @@ int qw3_q8_0_dequantize(const void *blocks_dev, int64_t n, float *y_dev, void *s
         return fail(nullptr, QW3_ERR_INVALID_ARG, "blocks must be 2-byte, y 4-byte aligned");
     QW3_CUDA_TRY(launch_dequantize(static_cast<const uint8_t *>(blocks_dev), n / 32, y_dev,
                                    static_cast<cudaStream_t>(stream)));
+    return QW3_OK;
+}
+
+int qw3_q4_k_quantize(const float *x_dev, int64_t n, void *blocks_dev, int32_t *status_dev, void *stream) {
+    if (n < 0 || (n > 0 && (!x_dev || !blocks_dev))) return fail(nullptr, QW3_ERR_INVALID_ARG, "bad quantize arguments");
+    if (n % 256) return fail(nullptr, QW3_ERR_SHAPE, "n must be a multiple of 256");
+    if (misaligned(x_dev, 16) || misaligned(blocks_dev, 16) || misaligned(status_dev, 4))
+        return fail(nullptr, QW3_ERR_INVALID_ARG, "x and blocks must be 16-byte aligned");
+    QW3_CUDA_TRY(launch_q4k_quantize(x_dev, n / 256, static_cast<uint8_t *>(blocks_dev), status_dev,
+                                     static_cast<cudaStream_t>(stream)));
+    return QW3_OK;
+}
+
+int qw3_q4_k_dequantize(const void *blocks_dev, int64_t n, float *y_dev, void *stream) {
+    if (n < 0 || (n > 0 && (!y_dev || !blocks_dev))) return fail(nullptr, QW3_ERR_INVALID_ARG, "bad dequantize arguments");
+    if (n % 256) return fail(nullptr, QW3_ERR_SHAPE, "n must be a multiple of 256");
+    if (misaligned(blocks_dev, 2) || misaligned(y_dev, 4))
+        return fail(nullptr, QW3_ERR_INVALID_ARG, "blocks must be 2-byte, y 4-byte aligned");
+    QW3_CUDA_TRY(launch_q4k_dequantize(static_cast<const uint8_t *>(blocks_dev), n / 256, y_dev,
+                                       static_cast<cudaStream_t>(stream)));
+    return QW3_OK;
+}
+
+int qw3_q4_k_gemv(const void *W_dev, int32_t rows, int32_t cols, const float *x_dev, int32_t B, float *y_dev,
+                  void *stream) {
+    if (!W_dev || !x_dev || !y_dev || rows < 0 || cols < 0 || B < 1 || B > 8)
+        return fail(nullptr, QW3_ERR_INVALID_ARG, "bad gemv arguments");
+    if (cols % 256 || !q4k_gemv_fits(B, cols)) return fail(nullptr, QW3_ERR_SHAPE, "cols % 256 and B * cols <= 49152");
+    if (misaligned(W_dev, 16) || misaligned(x_dev, 16) || misaligned(y_dev, 4))
+        return fail(nullptr, QW3_ERR_INVALID_ARG, "W and x must be 16-byte, y 4-byte aligned");
+    if (rows == 0) return QW3_OK;
+    QW3_CUDA_TRY(configure_all());   // the kernel's shared-memory limit
+    QW3_CUDA_TRY(launch_gemv_q4k(static_cast<const uint8_t *>(W_dev), rows, cols, B, x_dev, nullptr, 0.0f, y_dev,
+                                 GEMV_STORE, nullptr, nullptr, static_cast<cudaStream_t>(stream)));
     return QW3_OK;
 }
 

@@ -30,6 +30,7 @@ struct QMat {
     int kt = 0;           // tile width: divides cols, multiple of 32
     int ktile_major = 0;  // 0: row-group-major, 1: k-tile-major
     uint8_t *ut = nullptr;  // nullable: the same weights as bf16 hi/lo tensor-core tiles
+    const uint8_t *q4 = nullptr;  // Q4_K models: the raw rows (base is then null)
 };
 
 constexpr int kRowAlign = 16;
@@ -188,6 +189,22 @@ bool gemm_tc_supported(int M, int K, const QMat &W);
 size_t ut_bytes(int rows, int K);   // bytes of a matrix packed into bf16 hi/lo UMMA tiles
 cudaError_t configure_gemm_tc();
 cudaError_t launch_pack_w(const QMat &W, uint8_t *dst, cudaStream_t s);
+// The same tiles from a raw Q4_K matrix [N][K / 256 blocks].
+cudaError_t launch_pack_w_q4k(const uint8_t *W, int N, int K, uint8_t *dst, cudaStream_t s);
+
+// ---- Q4_K weights (q4k.cu; "Model files and quantization", 11.8)
+size_t q4k_row_bytes(int cols);                 // cols / 256 blocks of 144 bytes
+bool q4k_gemv_fits(int B, int K);               // B <= 8, K % 256 == 0, B * K <= 49152
+cudaError_t configure_q4k();
+cudaError_t launch_q4k_quantize(const float *x, int64_t nblocks, uint8_t *out, int32_t *status, cudaStream_t s);
+cudaError_t launch_q4k_dequantize(const uint8_t *blocks, int64_t nblocks, float *y, cudaStream_t s);
+cudaError_t launch_embed_q4k(const int32_t *tokens, int M, const uint8_t *E, int H, int vocab, float *x,
+                             cudaStream_t s);
+// y = W xn for B rows (xn = RMSNorm(x) * norm_w when norm_w is given); mode
+// GEMV_STORE / GEMV_RESID / GEMV_SWIGLU (row pairs) / GEMV_ARGMAX (y nullable
+// or io->logits; packed keys max'ed into key[B]).
+cudaError_t launch_gemv_q4k(const uint8_t *W, int N, int K, int B, const float *x, const float *norm_w, float eps,
+                            float *y, int mode, const DecodeIO *io, unsigned long long *key, cudaStream_t s);
 cudaError_t launch_gemm_tc(const float *A, int M, int K, const QMat &W, float *C, int mode,
                            unsigned long long *argmax_key, const DecodeIO *io, int32_t *status, uint8_t *apack,
                            cudaStream_t s, const GemmSplitK *sk = nullptr);
@@ -410,6 +427,36 @@ __device__ __forceinline__ float kv_elem(const kvq8 *row, int d) {
     const float sc = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(blk)));
     return sc * static_cast<float>(static_cast<int8_t>(blk[2 + (d & 31)]));
 }
+
+// ---- Q4_K block decode ("Model files and quantization", 11.8; layout in q4k.cu)
+__device__ __forceinline__ float q4k_half(const uint8_t *p) {
+    return __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(p)));
+}
+
+// (d * sc_j, dmin * m_j) of sub-block j of a block.
+__device__ __forceinline__ void q4k_sub(const uint8_t *blk, int j, float &d1, float &m1) {
+    const uint8_t *s = blk + 4;
+    int sc, m;
+    if (j < 4) {
+        sc = s[j] & 63;
+        m = s[j + 4] & 63;
+    } else {
+        sc = (s[j + 4] & 0xF) | ((s[j - 4] >> 6) << 4);
+        m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+    }
+    d1 = q4k_half(blk) * static_cast<float>(sc);
+    m1 = q4k_half(blk + 2) * static_cast<float>(m);
+}
+
+// Value t (0..255) of a block.
+__device__ __forceinline__ float q4k_value(const uint8_t *blk, int t) {
+    float d1, m1;
+    q4k_sub(blk, t >> 5, d1, m1);
+    const uint8_t byte = blk[16 + 32 * (t >> 6) + (t & 31)];
+    const int q = ((t >> 5) & 1) ? (byte >> 4) : (byte & 0xF);
+    return fmaf(d1, static_cast<float>(q), -m1);
+}
+
 
 // Q8_0 encoding of a row spread over a warp, lane holding values
 // [lane * E, lane * E + E) (E = HD / 32): 32 / E consecutive lanes hold one

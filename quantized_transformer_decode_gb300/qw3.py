@@ -36,13 +36,15 @@ QW3_FLAG_TEST_NO_WAIT = 0x10
 QW3_FLAG_KV_F16 = 0x20
 QW3_FLAG_ACT_Q8 = 0x40
 QW3_FLAG_KV_Q8 = 0x80
+QW3_FLAG_WEIGHTS_Q4_K = 0x100
 
 # Every entry point of include/qw3.h, in declaration order.
 EXPORTS = (
     "qw3_create", "qw3_destroy", "qw3_prefill", "qw3_forward_all_logits", "qw3_decode", "qw3_generate_greedy",
     "qw3_reset", "qw3_truncate", "qw3_seq_len", "qw3_debug_read_kv", "qw3_debug_read_trace",
     "qw3_decode_plan", "qw3_sync", "qw3_stream", "qw3_status_string", "qw3_last_error",
-    "qw3_q8_0_quantize", "qw3_q8_0_dequantize", "qw3_q8_0_gemv", "qw3_q8_0_gemv_q8act", "qw3_q8_0_gemv_splitk_noalloc",
+    "qw3_q8_0_quantize", "qw3_q8_0_dequantize", "qw3_q8_0_gemv", "qw3_q8_0_gemv_q8act",
+    "qw3_q4_k_quantize", "qw3_q4_k_dequantize", "qw3_q4_k_gemv", "qw3_q8_0_gemv_splitk_noalloc",
 )
 
 
@@ -114,6 +116,9 @@ def lib() -> ctypes.CDLL:
         "qw3_q8_0_dequantize": (ctypes.c_int, [_P, _I64, _P, _P]),
         "qw3_q8_0_gemv": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P]),
         "qw3_q8_0_gemv_q8act": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P]),
+        "qw3_q4_k_quantize": (ctypes.c_int, [_P, _I64, _P, _P, _P]),
+        "qw3_q4_k_dequantize": (ctypes.c_int, [_P, _I64, _P, _P]),
+        "qw3_q4_k_gemv": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P]),
         "qw3_q8_0_gemv_splitk_noalloc": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P]),
     }
     for name, (res, args) in sig.items():
@@ -234,6 +239,18 @@ def qw3_q8_0_gemv_q8act(W_ptr: int, rows: int, cols: int, x_ptr: int, B: int, y_
     _check(lib().qw3_q8_0_gemv_q8act(W_ptr, rows, cols, x_ptr, B, y_ptr, stream or None))
 
 
+def qw3_q4_k_quantize(x_ptr: int, n: int, blocks_ptr: int, status_ptr: int = 0, stream: int = 0) -> None:
+    _check(lib().qw3_q4_k_quantize(x_ptr, n, blocks_ptr, status_ptr or None, stream or None))
+
+
+def qw3_q4_k_dequantize(blocks_ptr: int, n: int, y_ptr: int, stream: int = 0) -> None:
+    _check(lib().qw3_q4_k_dequantize(blocks_ptr, n, y_ptr, stream or None))
+
+
+def qw3_q4_k_gemv(W_ptr: int, rows: int, cols: int, x_ptr: int, B: int, y_ptr: int, stream: int = 0) -> None:
+    _check(lib().qw3_q4_k_gemv(W_ptr, rows, cols, x_ptr, B, y_ptr, stream or None))
+
+
 def qw3_q8_0_gemv_splitk_noalloc(W_ptr: int, rows: int, cols: int, x_ptr: int, B: int, y_ptr: int,
                                  stream: int = 0) -> None:
     _check(lib().qw3_q8_0_gemv_splitk_noalloc(W_ptr, rows, cols, x_ptr, B, y_ptr, stream or None))
@@ -285,6 +302,32 @@ def q8_0_gemv_q8act(W, rows: int, cols: int, x):
     B = x.shape[0] if x.dim() == 2 else 1
     y = torch.empty((B, rows), dtype=torch.float32, device=x.device)
     qw3_q8_0_gemv_q8act(W.data_ptr(), rows, cols, x.data_ptr(), B, y.data_ptr(), _stream_ptr())
+    return y
+
+
+def q4_k_quantize(x, status=None):
+    """f32 CUDA tensor (numel % 256 == 0) -> uint8 Q4_K wire bytes."""
+    torch = _torch()
+    x = x.contiguous()
+    out = torch.empty(x.numel() // 256 * 144, dtype=torch.uint8, device=x.device)
+    qw3_q4_k_quantize(x.data_ptr(), x.numel(), out.data_ptr(), status.data_ptr() if status is not None else 0,
+                      _stream_ptr())
+    return out
+
+
+def q4_k_dequantize(blocks, n: int):
+    torch = _torch()
+    y = torch.empty(n, dtype=torch.float32, device=blocks.device)
+    qw3_q4_k_dequantize(blocks.data_ptr(), n, y.data_ptr(), _stream_ptr())
+    return y
+
+
+def q4_k_gemv(W, rows: int, cols: int, x):
+    torch = _torch()
+    x = x.contiguous()
+    B = x.shape[0] if x.dim() == 2 else 1
+    y = torch.empty((B, rows), dtype=torch.float32, device=x.device)
+    qw3_q4_k_gemv(W.data_ptr(), rows, cols, x.data_ptr(), B, y.data_ptr(), _stream_ptr())
     return y
 
 
@@ -342,13 +385,15 @@ class Qw3Model:
     @classmethod
     def from_f32(cls, shape, weights: Iterable, device: str = "cuda", **kw) -> "Qw3Model":
         """weights: iterable of (name, kind, f32 numpy array) in any order;
-        linear tensors are quantised on the device with qw3_q8_0_quantize."""
+        linear tensors are quantised on the device with qw3_q8_0_quantize, or
+        qw3_q4_k_quantize when flags hold QW3_FLAG_WEIGHTS_Q4_K."""
         torch = _torch()
         tensors = {}
         status = torch.zeros(1, dtype=torch.int32, device=device)
+        enc = q4_k_quantize if kw.get("flags", 0) & QW3_FLAG_WEIGHTS_Q4_K else q8_0_quantize
         for name, kind, arr in weights:
             t = torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32)).to(device)
-            tensors[name] = q8_0_quantize(t.reshape(-1), status) if kind == "linear" else t
+            tensors[name] = enc(t.reshape(-1), status) if kind == "linear" else t
             del t
         if int(status.item()) != 0:
             raise Qw3Error(int(status.item()), "non-finite weight values")
