@@ -50,11 +50,13 @@ def q8_0_bytes(rows: int, cols: int) -> int:
     return rows * (cols // 32) * 34
 
 
-def weight_bytes_per_step(s: inputs.Qwen3Shape) -> int:
-    """Q8_0 bytes every decode step streams: all layer linears plus lm_head."""
+def weight_bytes_per_step(s: inputs.Qwen3Shape, wtype: str = "q8_0") -> int:
+    """Weight bytes every decode step streams (all layer linears plus the
+    lm_head): Q8_0 34 bytes per 32 weights, Q4_K 144 per 256."""
     layer = (q8_0_bytes(s.q_width + 2 * s.kv_width, s.hidden) + q8_0_bytes(s.hidden, s.q_width)
              + q8_0_bytes(2 * s.intermediate, s.hidden) + q8_0_bytes(s.hidden, s.intermediate))
-    return s.n_layers * layer + q8_0_bytes(s.vocab, s.hidden)
+    total = s.n_layers * layer + q8_0_bytes(s.vocab, s.hidden)
+    return total if wtype == "q8_0" else total // 34 * 32 // 256 * 144
 
 
 def kv_bytes_per_position(s: inputs.Qwen3Shape) -> int:
@@ -67,10 +69,11 @@ def kv_bytes_per_position(s: inputs.Qwen3Shape) -> int:
 KV_SCALE = {"f32": 1.0, "f16": 0.5, "q8_0": 34.0 / 128.0}
 
 
-def decode_bytes(s: inputs.Qwen3Shape, B: int, positions: list[list[int]], kv: str = "f32") -> int:
+def decode_bytes(s: inputs.Qwen3Shape, B: int, positions: list[list[int]], kv: str = "f32",
+                 wtype: str = "q8_0") -> int:
     """Algorithmic bytes of the decode steps: positions[step][b] is the
     position of the new token of sequence b; it attends over pos+1 rows."""
-    w = weight_bytes_per_step(s) * len(positions)
+    w = weight_bytes_per_step(s, wtype) * len(positions)
     kvb = sum((p + 1) for step in positions for p in step) * kv_bytes_per_position(s) * KV_SCALE[kv]
     return int(w + kvb)
 
@@ -327,14 +330,15 @@ def run_reference(a, w: inputs.Workload):
     return 0
 
 
-def workload_config(w: inputs.Workload, steps: int, kv: str = "f32") -> dict:
+def workload_config(w: inputs.Workload, steps: int, kv: str = "f32", wtype: str = "q8_0") -> dict:
     s = w.shape
     cfg = {"workload": f"{w.name}: Qwen3 dense, vocab {s.vocab}, hidden {s.hidden}, {s.n_layers} layers, "
                        f"{s.n_heads}/{s.n_kv_heads} heads, head_dim {s.head_dim}, intermediate {s.intermediate}, "
                        f"{'tied' if s.tied else 'untied'} lm_head, seed {w.seed}; "
                        f"prefill {w.prompt_len} tokens untimed, then greedy decode at B={w.batch}",
            "batch": w.batch, "prompt_len": w.prompt_len, "timed_positions": [w.prompt_len, w.prompt_len + steps - 1],
-           "weights": f"Q8_0, {weight_bytes_per_step(s) / 1e6:.1f} MB streamed per step", "kv_cache": kv,
+           "weights": f"{wtype.upper()}, {weight_bytes_per_step(s, wtype) / 1e6:.1f} MB streamed per step",
+           "kv_cache": kv,
            "l2": ("inputs larger than L2 (the Q8_0 weights streamed every step exceed the 129 MB L2)"
                   if weight_bytes_per_step(s) > 129e6 else
                   "inputs smaller than L2: the weights stay L2-resident between steps (a small test case)")}
@@ -418,10 +422,11 @@ def time_decode(torch, qw3, model, w: inputs.Workload, K: int, W: int, runs: int
     return ms, out, first, clk
 
 
-def decode_roofline(w: inputs.Workload, K: int, ms_step: float, key: str, kv: str = "f32") -> dict:
+def decode_roofline(w: inputs.Workload, K: int, ms_step: float, key: str, kv: str = "f32",
+                    wtype: str = "q8_0") -> dict:
     s, B, P = w.shape, w.batch, w.prompt_len
     positions = [[P + i] * B for i in range(K)]
-    alg = decode_bytes(s, B, positions, kv) / K
+    alg = decode_bytes(s, B, positions, kv, wtype) / K
     hbm_peak, _, kind = peaks()
     achieved = alg / (ms_step / 1e3) / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
@@ -465,12 +470,14 @@ def step_phase_table(torch, qw3, w: inputs.Workload, dev, sm_mhz):
 
 
 def run_decode_line(a, torch, qw3, world, rank, local, dev, w: inputs.Workload, K: int, W: int, headline: bool,
-                    kv: str = "f32"):
+                    kv: str = "f32", wtype: str = "q8_0"):
     s, B, P = w.shape, w.batch, w.prompt_len
     runs = max(1, a.runs)
     cap = P + max(K, 1) + W + 2
     flags = qw3.QW3_FLAG_PER_KERNEL if a.per_kernel else 0
     flags |= {"f32": 0, "f16": qw3.QW3_FLAG_KV_F16, "q8_0": qw3.QW3_FLAG_KV_Q8}[kv]
+    if wtype == "q4_k":
+        flags |= qw3.QW3_FLAG_WEIGHTS_Q4_K
     model = _decode_model(qw3, w, cap, flags)
     persistent, launches_per_step = model.decode_plan(B)
     ms_runs, out, first, clk = time_decode(torch, qw3, model, w, K, W, runs, world, local, dev)
@@ -478,17 +485,18 @@ def run_decode_line(a, torch, qw3, world, rank, local, dev, w: inputs.Workload, 
     ms_max = aggregate_max(ms, world, dev)
     tokens_all = aggregate_sum(float(K * B), world, dev)
     value = tokens_all / (ms_max / 1e3)
-    roof = decode_roofline(w, K, ms / K, "k_step" if persistent else "decode_step", kv)
+    roof = decode_roofline(w, K, ms / K, "k_step" if persistent else "decode_step", kv, wtype)
     roof["kernel"] = ("k_step: one persistent launch per decode step (embedding, every layer's projections, "
                       "attention, FFN, lm_head and argmax)" if persistent else
                       "decode step (per-kernel path: Q8_0 GEMVs or GEMMs, attention, embedding, lm_head + argmax)")
     line = {
         "metric": (METRIC if headline and w.name == "qwen3-0.6b-decode" else
-                   f"{w.name} decode tok/s" + ("" if kv == "f32" else f" ({kv} KV cache)")),
+                   f"{w.name} decode tok/s" + ("" if kv == "f32" else f" ({kv} KV cache)")
+                   + ("" if wtype == "q8_0" else f" ({wtype} weights)")),
         "value": value, "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded random-init weights quantised to Q8_0, seeded prompt)",
-        "config": dict(workload_config(w, K, kv), parallelism="replicas" if world > 1 else "single GPU",
+        "dtype": "f32", "data": f"synthetic (seeded random-init weights quantised to {wtype.upper()}, seeded prompt)",
+        "config": dict(workload_config(w, K, kv, wtype), parallelism="replicas" if world > 1 else "single GPU",
                        timing=f"CUDA events on the model stream around one qw3_generate_greedy call of K steps; "
                               f"median of {runs} runs from the same cache state (ms per run: "
                               f"{', '.join(f'{x:.3f}' for x in ms_runs)})"),
@@ -641,6 +649,9 @@ def run_ours(a, w: inputs.Workload):
         for kv in ("f16", "q8_0"):
             extra[f"batch64_kv_{kv}"] = run_decode_line(a, torch, qw3, world, rank, local, dev, wb, wb.decode_steps,
                                                         W, headline=False, kv=kv)
+        # batch-1 decode of the 0.6B shape with Q4_K weights (4.5 bits per weight)
+        extra["decode_q4_k"] = run_decode_line(a, torch, qw3, world, rank, local, dev, w, K, W, headline=False,
+                                               wtype="q4_k")
         if rank == 0 and not a.no_cpu_baseline:
             for key, name in (("prefill4096", "qwen3-0.6b-prefill4096"), ("batch64", "qwen3-0.6b-batch64"),
                               ("qwen3_8b", "qwen3-8b")):

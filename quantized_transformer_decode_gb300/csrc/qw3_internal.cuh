@@ -204,7 +204,8 @@ cudaError_t launch_embed_q4k(const int32_t *tokens, int M, const uint8_t *E, int
 // GEMV_STORE / GEMV_RESID / GEMV_SWIGLU (row pairs) / GEMV_ARGMAX (y nullable
 // or io->logits; packed keys max'ed into key[B]).
 cudaError_t launch_gemv_q4k(const uint8_t *W, int N, int K, int B, const float *x, const float *norm_w, float eps,
-                            float *y, int mode, const DecodeIO *io, unsigned long long *key, cudaStream_t s);
+                            float *y, int mode, const DecodeIO *io, unsigned long long *key, bool pdl,
+                            cudaStream_t s);
 cudaError_t launch_gemm_tc(const float *A, int M, int K, const QMat &W, float *C, int mode,
                            unsigned long long *argmax_key, const DecodeIO *io, int32_t *status, uint8_t *apack,
                            cudaStream_t s, const GemmSplitK *sk = nullptr);
