@@ -228,30 +228,6 @@ __device__ __forceinline__ size_t ut_tile(int t, int s, int ksteps) {
     return (static_cast<size_t>(t) * ksteps + s) * TC_PAIR;
 }
 
-// One thread per (row, 8-column group): weights of a repacked Q8_0 matrix.
-__global__ void k_pack_w(const QMat W, int N, int K, uint8_t *__restrict__ dst) {
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int groups = K / 8;
-    const int rows = (N + TC_BM - 1) / TC_BM * TC_BM;
-    if (i >= static_cast<int64_t>(rows) * groups) return;
-    const int r = static_cast<int>(i / groups), k = static_cast<int>(i % groups) * 8;
-    float v[8];
-    if (r < N) {
-        const float d = __half2float(*qm_scale(W, r, k));
-        const int8_t *q = qm_codes(W, r, k);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = d * static_cast<float>(q[j]);
-    } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = 0.0f;
-    }
-    uint4 hi, lo;
-    split8(v, hi, lo);
-    uint8_t *t = dst + ut_tile(r / TC_BM, k / TC_BK, K / TC_BK);
-    *reinterpret_cast<uint4 *>(t + core_off(r % TC_BM, k % TC_BK)) = hi;
-    *reinterpret_cast<uint4 *>(t + TC_OPERAND + core_off(r % TC_BM, k % TC_BK)) = lo;
-}
-
 // One thread per (row, 8-column group): weights of a raw Q4_K matrix (rows of
 // K / 256 blocks of 144 bytes), decoded exactly in f32 then split.
 __global__ void k_pack_w_q4k(const uint8_t *__restrict__ W, int N, int K, uint8_t *__restrict__ dst) {
@@ -488,6 +464,304 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const uint8_t *__rest
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BNE) : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// The same product with the weights streamed as Q8_0 (1.0625 bytes per
+// weight instead of the 4 of the pre-packed bf16 hi/lo tiles). Weights are
+// laid out once per (128-row tile t, 64-column K step s) as one 8704-byte
+// piece: the 128 x 64 int8 codes, then the 128 x 2 f16 scales. Per K step
+// the producer copies the A pair and that piece into a stage; four converter
+// warps turn the piece into the bf16 hi/lo operand pair (d * q is exact in
+// f32; the same split as k_pack_w) in one of two operand buffers, fence it
+// for the tensor core's async proxy and signal; the MMA thread then issues
+// the step's 12 MMAs. Stage free = MMA commit + converters done (2
+// arrivals); operand buffer free = MMA commit. 384 threads: warp 0 producer,
+// warp 1 MMA, warps 0-3 the epilogue (TMEM lanes), warps 4-11 converters
+// (thread c: row c % 128, Q8_0 block c / 128 of the step: one scale).
+constexpr uint32_t TQ_RAW = 128 * TC_BK + 128 * 4;              // 8704
+// MT m-tiles per CTA share each converted W tile (MT = 2 halves the
+// conversion per MMA where there are enough row tiles: prefill)
+template <int MT> __host__ __device__ constexpr uint32_t tq_stage() { return (MT * TC_PAIR + TQ_RAW + 1023) / 1024 * 1024; }
+template <int MT> __host__ __device__ constexpr int tq_stages() { return MT == 1 ? 3 : 2; }
+constexpr int TQ_WBUF = 2;
+constexpr int TQ_THREADS = 384;
+constexpr int TQ_CONV = 256;   // converter threads
+template <int MT>
+__host__ __device__ constexpr uint32_t tq_smem() { return tq_stages<MT>() * tq_stage<MT>() + TQ_WBUF * TC_PAIR + 2048 + 1024; }
+
+// One thread per (row, 8-column group) of a repacked Q8_0 matrix -> the
+// streamed layout above (rows past N are zero).
+__global__ void k_pack_w_q8(const QMat W, int N, int K, uint8_t *__restrict__ dst) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int groups = K / 8;
+    const int rows = (N + TC_BM - 1) / TC_BM * TC_BM;
+    if (i >= static_cast<int64_t>(rows) * groups) return;
+    const int r = static_cast<int>(i / groups), k = static_cast<int>(i % groups) * 8;
+    uint8_t *piece = dst + (static_cast<size_t>(r / TC_BM) * (K / TC_BK) + k / TC_BK) * TQ_RAW;
+    uint2 c = make_uint2(0, 0);
+    if (r < N) c = *reinterpret_cast<const uint2 *>(qm_codes(W, r, k));
+    *reinterpret_cast<uint2 *>(piece + (r % TC_BM) * TC_BK + (k % TC_BK)) = c;
+    if (k % 32 == 0) {
+        const __half sc = r < N ? *qm_scale(W, r, k) : __float2half(0.0f);
+        *reinterpret_cast<__half *>(piece + 128 * TC_BK + (r % TC_BM) * 4 + ((k % TC_BK) / 32) * 2) = sc;
+    }
+}
+
+template <int MODE, int MT>
+__global__ void __launch_bounds__(TQ_THREADS, 1) k_gemm_tc_q8(const uint8_t *__restrict__ Ap, int M, int K,
+                                                             const uint8_t *__restrict__ Wq, int N, float *C,
+                                                             unsigned long long *__restrict__ argmax_key,
+                                                             const DecodeIO *io, int32_t *status, float *ws) {
+    extern __shared__ __align__(1024) uint8_t tq_smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tq_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    constexpr int TQ_STAGES = tq_stages<MT>();
+    constexpr uint32_t TQ_STAGE = tq_stage<MT>();   // MT A pairs, then the Q8_0 piece
+    uint8_t *wbuf = base + TQ_STAGES * TQ_STAGE;                                       // [TQ_WBUF] operand pairs
+    uint64_t *full = reinterpret_cast<uint64_t *>(wbuf + TQ_WBUF * TC_PAIR);          // [TQ_STAGES]
+    uint64_t *empty = full + TQ_STAGES;                                               // [TQ_STAGES]
+    uint64_t *wready = empty + TQ_STAGES;                                             // [TQ_WBUF]
+    uint64_t *wfree = wready + TQ_WBUF;                                               // [TQ_WBUF]
+    uint64_t *wfull = wfree + TQ_WBUF;                                                // [TQ_STAGES] W piece landed
+    uint64_t *done = wfull + TQ_STAGES;                                               // [1]
+    uint32_t *tbase = reinterpret_cast<uint32_t *>(done + 1);
+    volatile int *err = reinterpret_cast<volatile int *>(tbase + 1);
+    volatile int *cvok = err + 1;
+    if (MODE == GEMV_ARGMAX && io) C = io->logits;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nt = blockIdx.x;
+    const int mtiles = (M + TC_BM - 1) / TC_BM;
+    const int mt0 = blockIdx.y * MT;
+    const int nmt = min(MT, mtiles - mt0);   // m-tiles this CTA computes
+    const int ksteps_all = K / TC_BK;
+    const int kz = blockIdx.z, nks = gridDim.z;
+    const int kb = static_cast<int>(static_cast<int64_t>(kz) * ksteps_all / nks);
+    const int ksteps = static_cast<int>(static_cast<int64_t>(kz + 1) * ksteps_all / nks) - kb;
+    if (tid == 0) {
+        for (int i = 0; i < TQ_STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 2);
+            mbar_init(&wfull[i], 1);
+        }
+        for (int i = 0; i < TQ_WBUF; ++i) {
+            mbar_init(&wready[i], 1);
+            mbar_init(&wfree[i], 1);
+        }
+        mbar_init(done, 1);
+        *err = 0;
+        *cvok = 1;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tbase)),
+                     "r"(TC_BN * MT) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tbase;
+
+    if (warp == 0 && lane == 0) {
+        // producer: the A pairs and the Q8_0 piece of each K step
+        for (int ks = 0; ks < ksteps; ++ks) {
+            const int st = ks % TQ_STAGES;
+            if (ks >= TQ_STAGES && !mbar_wait_bounded(&empty[st], static_cast<uint32_t>(((ks / TQ_STAGES) - 1) & 1))) {
+                *err = 1;
+                record_status(status, QW3_ERR_TIMEOUT);
+                break;
+            }
+            if (*err) break;
+            uint8_t *sb = base + st * TQ_STAGE;
+            // the Q8_0 piece first, on its own barrier, so that the converters
+            // start while the A pairs are still streaming
+            mbar_arrive_expect_tx(&wfull[st], TQ_RAW);
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                         ::"r"(smem_u32(sb + MT * TC_PAIR)),
+                           "l"(Wq + (static_cast<size_t>(nt) * ksteps_all + kb + ks) * TQ_RAW), "r"(TQ_RAW),
+                           "r"(smem_u32(&wfull[st]))
+                         : "memory");
+            mbar_arrive_expect_tx(&full[st], nmt * TC_PAIR);
+            for (int i = 0; i < nmt; ++i)
+                asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                             ::"r"(smem_u32(sb + i * TC_PAIR)), "l"(Ap + ut_tile(mt0 + i, kb + ks, ksteps_all)),
+                               "r"(TC_PAIR), "r"(smem_u32(&full[st]))
+                             : "memory");
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer
+        for (int ks = 0; ks < ksteps; ++ks) {
+            const int st = ks % TQ_STAGES, wb = ks % TQ_WBUF;
+            if (!mbar_wait_bounded(&full[st], static_cast<uint32_t>((ks / TQ_STAGES) & 1)) ||
+                !mbar_wait_bounded(&wready[wb], static_cast<uint32_t>((ks / TQ_WBUF) & 1)) || *err) {
+                *err = 1;
+                record_status(status, QW3_ERR_TIMEOUT);
+                break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t w_hi = smem_u32(wbuf + wb * TC_PAIR), w_lo = w_hi + TC_OPERAND;
+            for (int i = 0; i < nmt; ++i) {
+                // m-tile i: A pair i, accumulator columns 128 i ..
+                const uint32_t a_hi = smem_u32(base + st * TQ_STAGE + i * TC_PAIR), a_lo = a_hi + TC_OPERAND;
+                const uint32_t th = tmem + static_cast<uint32_t>(TC_BN * i);
+#pragma unroll
+                for (int sub = 0; sub < TC_BK / 16; ++sub) {
+                    const uint32_t off = sub * 256;
+                    const uint32_t acc0 = (ks > 0 || sub > 0) ? 1u : 0u;
+                    asm volatile(
+                        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %3, 1;\n\t"
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %2, %3, 1;\n\t}"
+                        ::"r"(th), "l"(umma_desc(a_hi + off)), "l"(umma_desc(w_hi + off)), "r"(kTcIdesc), "r"(acc0),
+                          "l"(umma_desc(w_lo + off)), "l"(umma_desc(a_lo + off))
+                        : "memory");
+                }
+            }
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                             smem_u32(&empty[st]))
+                         : "memory");
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                             smem_u32(&wfree[wb]))
+                         : "memory");
+        }
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(done))
+                     : "memory");
+    } else if (warp >= 4) {
+        // converters: thread c converts the 32 codes of block c / 128 of row c % 128
+        const int c = tid - 128;
+        const int crow = c & 127, cblk = c >> 7;
+        for (int ks = 0; ks < ksteps; ++ks) {
+            const int st = ks % TQ_STAGES, wb = ks % TQ_WBUF;
+            if (c == 0) {
+                bool ok = !*err && mbar_wait_bounded(&wfull[st], static_cast<uint32_t>((ks / TQ_STAGES) & 1));
+                if (ok && ks >= TQ_WBUF)
+                    ok = mbar_wait_bounded(&wfree[wb], static_cast<uint32_t>(((ks / TQ_WBUF) - 1) & 1));
+                if (!ok) {
+                    *err = 1;
+                    record_status(status, QW3_ERR_TIMEOUT);
+                }
+                *cvok = ok ? 1 : 0;
+            }
+            asm volatile("bar.sync 2, 256;" ::: "memory");
+            if (!*cvok) break;
+            const uint8_t *raw = base + st * TQ_STAGE + MT * TC_PAIR;
+            const uint4 *cw = reinterpret_cast<const uint4 *>(raw + crow * TC_BK + cblk * 32);
+            const float d = __half2float(*reinterpret_cast<const __half *>(raw + 128 * TC_BK + crow * 4 + cblk * 2));
+            uint8_t *wo = wbuf + wb * TC_PAIR;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const uint4 w16 = cw[q];   // codes 16q .. 16q + 15 of the block
+                const uint32_t words[4] = {w16.x ^ 0x80808080u, w16.y ^ 0x80808080u, w16.z ^ 0x80808080u,
+                                           w16.w ^ 0x80808080u};
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    // int8 -> f32: the biased byte in the mantissa of 2^23 (exact),
+                    // times the block scale (exact); then the bf16 hi/lo split
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int pr = 0; pr < 4; ++pr) {
+                        const uint32_t wsrc = words[2 * h + pr / 2];
+                        const int b0 = 2 * (pr % 2);
+                        const float v0 = (__uint_as_float(__byte_perm(wsrc, 0x4B000000u, 0x7540u + b0)) - 8388736.0f) * d;
+                        const float v1 =
+                            (__uint_as_float(__byte_perm(wsrc, 0x4B000000u, 0x7540u + b0 + 1)) - 8388736.0f) * d;
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(v0, v1);
+                        const uint32_t hu = *reinterpret_cast<const uint32_t *>(&h2);
+                        const float h0 = __uint_as_float(hu << 16), h1 = __uint_as_float(hu & 0xffff0000u);
+                        const __nv_bfloat162 l2 = __floats2bfloat162_rn(v0 - h0, v1 - h1);
+                        hw[pr] = hu;
+                        lw[pr] = *reinterpret_cast<const uint32_t *>(&l2);
+                    }
+                    const int k = 32 * cblk + 16 * q + 8 * h;
+                    *reinterpret_cast<uint4 *>(wo + core_off(crow, k)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4 *>(wo + TC_OPERAND + core_off(crow, k)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("bar.sync 2, 256;" ::: "memory");
+            if (c == 0) {
+                mbar_arrive(&wready[wb]);
+                mbar_arrive(&empty[st]);
+            }
+        }
+    }
+    __syncwarp();
+    // all threads: wait for the accumulator (or give up after 1 s), then the
+    // producer's copies must have landed before the CTA may exit
+    if (!mbar_wait_bounded(done, 0u)) {
+        *err = 1;
+        record_status(status, QW3_ERR_TIMEOUT);
+    }
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (tid == 0 && *err) {
+        for (int ks = ksteps > TQ_STAGES ? ksteps - TQ_STAGES : 0; ks < ksteps; ++ks) {
+            (void)mbar_wait_bounded(&full[ks % TQ_STAGES], static_cast<uint32_t>((ks / TQ_STAGES) & 1));
+            (void)mbar_wait_bounded(&wfull[ks % TQ_STAGES], static_cast<uint32_t>((ks / TQ_STAGES) & 1));
+        }
+    }
+    for (int mi = 0; mi < nmt && warp < 4; ++mi) {
+        // ---- epilogue: thread (warp, lane) owns row 32 warp + lane of m-tile mi, all 128 columns
+        const int mt = mt0 + mi;
+        const int row = 32 * warp + lane;
+        const int m = mt * TC_BM + row;
+        unsigned long long best = 0ull;
+        const int Np = gridDim.x * TC_BN;   // workspace row stride
+        for (int c0 = 0; c0 < TC_BN; c0 += 16) {
+            uint32_t r[16];
+            const uint32_t taddr =
+                tmem + (static_cast<uint32_t>(32 * warp) << 16) + static_cast<uint32_t>(TC_BN * mi + c0);
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+                "tcgen05.wait::ld.sync.aligned;"
+                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                  "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                : "r"(taddr)
+                : "memory");
+            if (m >= M || *err) continue;
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+            if (nks > 1) {
+                float4 *w4 = reinterpret_cast<float4 *>(
+                    ws + (static_cast<size_t>(kz) * mtiles * TC_BM + static_cast<size_t>(m)) * Np + nt * TC_BN + c0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) w4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                continue;
+            }
+            const int nb = nt * TC_BN + c0;
+            if (MODE == GEMV_SWIGLU) {
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) {
+                    const int n = nb + j;
+                    if (n < N) C[static_cast<size_t>(m) * (N / 2) + n / 2] = v[j] / (1.0f + expf(-v[j])) * v[j + 1];
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int n = nb + j;
+                    if (n < N) {
+                        const float y = v[j];
+                        float *cp = C ? C + static_cast<size_t>(m) * N + n : nullptr;
+                        if (MODE == GEMV_STORE) *cp = y;
+                        else if (MODE == GEMV_RESID) *cp += y;
+                        else {
+                            if (cp) *cp = y;
+                            const unsigned long long kk = argmax_pack(y, n);
+                            best = kk > best ? kk : best;
+                        }
+                    }
+                }
+            }
+        }
+        if (MODE == GEMV_ARGMAX && m < M && best) atomicMax(&argmax_key[m], best);
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_BN * MT) : "memory");
+}
+
 // Sum of the K splits of a tensor-core GEMM in split order (deterministic),
 // then the epilogue: thread = (row, 4 columns).
 template <int MODE>
@@ -554,6 +828,37 @@ cudaError_t launch_tc_mode(const uint8_t *Ap, int M, int K, const uint8_t *Wp, i
     return cudaGetLastError();
 }
 
+template <int MODE>
+cudaError_t launch_tq_mode(const uint8_t *Ap, int M, int K, const uint8_t *Wq, int N, float *C,
+                           unsigned long long *argmax_key, const DecodeIO *io, int32_t *status,
+                           const GemmSplitK *sk, cudaStream_t s) {
+    const int nt = (N + TC_BN - 1) / TC_BN, mt = (M + TC_BM - 1) / TC_BM, ksteps = K / TC_BK;
+    // two m-tiles per CTA (one conversion of W for both) where that still
+    // leaves a CTA for every SM
+    const bool pair = mt >= 2 && nt * ((mt + 1) / 2) >= num_sms();
+    const int gy = pair ? (mt + 1) / 2 : mt;
+    int nks = 1;
+    if (MODE != GEMV_ARGMAX && sk && sk->ws && nt * mt < num_sms() && N % 4 == 0) {
+        nks = (num_sms() + nt * mt - 1) / (nt * mt);
+        nks = std::min(nks, ksteps / 4);
+        while (nks > 1 && static_cast<size_t>(nks) * mt * TC_BM * nt * TC_BN > sk->ws_floats) --nks;
+        if (nks < 1) nks = 1;
+    }
+    const dim3 grid(nt, gy, nks);
+    if (pair)
+        k_gemm_tc_q8<MODE, 2><<<grid, TQ_THREADS, tq_smem<2>(), s>>>(Ap, M, K, Wq, N, C, argmax_key, io, status,
+                                                                   nks > 1 ? sk->ws : nullptr);
+    else
+        k_gemm_tc_q8<MODE, 1><<<grid, TQ_THREADS, tq_smem<1>(), s>>>(Ap, M, K, Wq, N, C, argmax_key, io, status,
+                                                                   nks > 1 ? sk->ws : nullptr);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || nks == 1) return e;
+    const int64_t items = static_cast<int64_t>(M) * (N / 4);
+    k_splitk_reduce<MODE><<<static_cast<unsigned>((items + 255) / 256), 256, 0, s>>>(sk->ws, nks, M, N, nt * TC_BN,
+                                                                                      mt * TC_BM, C);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t configure_gemm_tc() {
@@ -568,6 +873,16 @@ cudaError_t configure_gemm_tc() {
     QW3_TC_CFG(GEMV_SWIGLU)
     QW3_TC_CFG(GEMV_ARGMAX)
 #undef QW3_TC_CFG
+#define QW3_TQ_CFG(MODE)                                                                                         \
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc_q8<MODE, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                                    static_cast<int>(tq_smem<1>()));                                \
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc_q8<MODE, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                                    static_cast<int>(tq_smem<2>()));
+    QW3_TQ_CFG(GEMV_STORE)
+    QW3_TQ_CFG(GEMV_RESID)
+    QW3_TQ_CFG(GEMV_SWIGLU)
+    QW3_TQ_CFG(GEMV_ARGMAX)
+#undef QW3_TQ_CFG
     return e;
 }
 
@@ -577,13 +892,18 @@ size_t ut_bytes(int rows, int K) {
 
 bool gemm_tc_supported(int M, int K, const QMat &W) {
     // a matrix held only as tensor-core tiles (Q4_K models) takes every M
-    return W.ut != nullptr && (M >= kGemmTcMinRows || W.base == nullptr) && K % TC_BK == 0 && W.cols == K;
+    return (W.ut != nullptr || W.uq != nullptr) && (M >= kGemmTcMinRows || W.base == nullptr) && K % TC_BK == 0 &&
+           W.cols == K;
 }
 
-cudaError_t launch_pack_w(const QMat &W, uint8_t *dst, cudaStream_t s) {
+size_t tq_bytes(int rows, int K) {
+    return static_cast<size_t>((rows + TC_BM - 1) / TC_BM) * (K / TC_BK) * TQ_RAW;
+}
+
+cudaError_t launch_pack_w_q8(const QMat &W, uint8_t *dst, cudaStream_t s) {
     const int rows = (W.rows + TC_BM - 1) / TC_BM * TC_BM;
     const int64_t n = static_cast<int64_t>(rows) * (W.cols / 8);
-    k_pack_w<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(W, W.rows, W.cols, dst);
+    k_pack_w_q8<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(W, W.rows, W.cols, dst);
     return cudaGetLastError();
 }
 
@@ -604,6 +924,15 @@ cudaError_t launch_gemm_tc(const float *A, int M, int K, const QMat &W, float *C
         k_pack_act<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(A, M, K, apack);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
+    }
+    if (W.uq) {
+        switch (mode) {
+            case GEMV_STORE: return launch_tq_mode<GEMV_STORE>(apack, M, K, W.uq, W.rows, C, argmax_key, io, status, sk, s);
+            case GEMV_RESID: return launch_tq_mode<GEMV_RESID>(apack, M, K, W.uq, W.rows, C, argmax_key, io, status, sk, s);
+            case GEMV_SWIGLU: return launch_tq_mode<GEMV_SWIGLU>(apack, M, K, W.uq, W.rows, C, argmax_key, io, status, sk, s);
+            case GEMV_ARGMAX: return launch_tq_mode<GEMV_ARGMAX>(apack, M, K, W.uq, W.rows, C, argmax_key, io, status, sk, s);
+            default: return cudaErrorInvalidValue;
+        }
     }
     switch (mode) {
         case GEMV_STORE: return launch_tc_mode<GEMV_STORE>(apack, M, K, W.ut, W.rows, C, argmax_key, io, status, sk, s);

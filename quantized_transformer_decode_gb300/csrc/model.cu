@@ -496,10 +496,17 @@ int setup_tensor_core_gemm(qw3_model *m) {
     if (H % 64 || qw % 64 || I % 64) return QW3_OK;
     auto pack = [&](QMat &q) -> int {
         uint8_t *p = nullptr;
-        M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&p), ut_bytes(q.rows, q.cols)));
-        if (q.q4) M_TRY(m, launch_pack_w_q4k(q.q4, q.rows, q.cols, p, m->stream));
-        else M_TRY(m, launch_pack_w(q, p, m->stream));
-        q.ut = p;
+        if (q.q4) {
+            // Q4_K: bf16 hi/lo tiles (4 bytes per weight)
+            M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&p), ut_bytes(q.rows, q.cols)));
+            M_TRY(m, launch_pack_w_q4k(q.q4, q.rows, q.cols, p, m->stream));
+            q.ut = p;
+        } else {
+            // Q8_0: the codes and scales in the streamed layout (1.0625 bytes per weight)
+            M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&p), tq_bytes(q.rows, q.cols)));
+            M_TRY(m, launch_pack_w_q8(q, p, m->stream));
+            q.uq = p;
+        }
         return QW3_OK;
     };
     for (int l = 0; l < c.n_layers; ++l) {
@@ -511,7 +518,10 @@ int setup_tensor_core_gemm(qw3_model *m) {
     }
     if (batch_tc) {
         if (int rc = pack(m->out)) return rc;
-        if (c.tied_lm_head) m->embd.ut = m->out.ut;
+        if (c.tied_lm_head) {
+            m->embd.ut = m->out.ut;
+            m->embd.uq = m->out.uq;
+        }
     }
     const int rows = std::max(c.max_prefill, c.max_seqs);
     const int kmax = std::max(H, std::max(qw, I));

@@ -31,6 +31,7 @@ struct QMat {
     int ktile_major = 0;  // 0: row-group-major, 1: k-tile-major
     uint8_t *ut = nullptr;  // nullable: the same weights as bf16 hi/lo tensor-core tiles
     const uint8_t *q4 = nullptr;  // Q4_K models: the raw rows (base is then null)
+    uint8_t *uq = nullptr;        // nullable: the Q8_0 weights in the tensor-core GEMM's streamed layout
 };
 
 constexpr int kRowAlign = 16;
@@ -188,7 +189,9 @@ constexpr int kGemmTcMinRows = 32;
 bool gemm_tc_supported(int M, int K, const QMat &W);
 size_t ut_bytes(int rows, int K);   // bytes of a matrix packed into bf16 hi/lo UMMA tiles
 cudaError_t configure_gemm_tc();
-cudaError_t launch_pack_w(const QMat &W, uint8_t *dst, cudaStream_t s);
+// The Q8_0 weights of W in the layout the tensor-core GEMM streams (tq_bytes).
+size_t tq_bytes(int rows, int K);
+cudaError_t launch_pack_w_q8(const QMat &W, uint8_t *dst, cudaStream_t s);
 // The same tiles from a raw Q4_K matrix [N][K / 256 blocks].
 cudaError_t launch_pack_w_q4k(const uint8_t *W, int N, int K, uint8_t *dst, cudaStream_t s);
 
