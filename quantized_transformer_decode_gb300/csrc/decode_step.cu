@@ -172,7 +172,11 @@ __device__ __forceinline__ void wait_split(const StepParams &P, int base, const 
 // After a phase's writes: the CTA synchronises, then one thread adds the
 // CTA's arrival (relaxed: the readers check every word's tag, so the counter
 // only has to say "probably published" and costs no fence). Called by all
-// consumer threads.
+// consumer threads. The GEMV phases and the attention units add theirs
+// earlier, as soon as their dot products are done and before their
+// epilogue writes the words: the readers' counter wait then overlaps that
+// epilogue, and their tag polls catch the words as they land (measured
+// 556 -> 536 us per 0.6B token).
 __device__ __forceinline__ void arrive(unsigned *ctr, bool wrote, int tid) {
     csync();
     if (tid == 0 && wrote) red_relaxed_add(ctr, 1u);
@@ -720,6 +724,7 @@ __device__ __forceinline__ void attention_phase(const StepParams &P, int l, int 
         }
     }
     csync();
+    if (tid == 0) red_relaxed_add(ctr_at(P, 24 + P.nkv + u.g), 1u);
     {
         // one (head, dim) output per consumer thread: max and weights over
         // the 16 warps' partials, independent loads and exps in flight
@@ -750,8 +755,8 @@ __device__ __forceinline__ void attention_phase(const StepParams &P, int l, int 
             }
         }
     }
-    // the scratch is the next phase's plane buffer: arrive() synchronises
-    arrive(ctr_at(P, 24 + P.nkv + u.g), true, tid);
+    // the scratch is the next phase's plane buffer
+    csync();
 }
 
 // P3: outputs [j GD / S, (j + 1) GD / S) of kv head g's G*HD attention
@@ -972,6 +977,9 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
             gemv_tasks<LC>(sl, ring, n, planes, scales, red, wc, warp, lane, trace ? trace + (ph + 1) * 4 : nullptr);
             csync();
             const int r0 = sl.row0, r1 = min(sl.row0 + 8 * sl.ng, P.qkv_w);
+            if (tid == 0 && sl.ng > 0)
+                for (int g = 0; g < P.nkv; ++g)
+                    if (rows_touch_group(r0, r1, g, G, HD, P.nh, P.nkv)) red_relaxed_add(ctr_at(P, 24 + g), 1u);
             if (sl.ng > 0) {
                 const float r = *rsc;
                 bool wrote = false;
@@ -982,9 +990,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
                 (void)wrote;
             }
             csync();
-            if (tid == 0 && sl.ng > 0)
-                for (int g = 0; g < P.nkv; ++g)
-                    if (rows_touch_group(r0, r1, g, G, HD, P.nh, P.nkv)) red_relaxed_add(ctr_at(P, 24 + g), 1u);
             rec(ph + 1, 1);
             rec1(l, 1);
         }
@@ -1009,6 +1014,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
             rec1(l, 7);
             gemv_tasks<LC>(sl, ring, n, planes, scales, red, wc, warp, lane, trace ? trace + (ph + 4) * 4 : nullptr);
             csync();
+            if (tid == 0 && sl.ng > 0) red_relaxed_add(ctr_at(P, xsub), 1u);
             bool wrote = false;
             for (int t = tid; t < sl.ng * 8; t += kCT) {
                 const float y = xown[t] + row_sum<LC>(sl, red, t);
@@ -1017,7 +1023,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
                 wrote = true;
             }
             (void)wrote;
-            arrive(ctr_at(P, xsub), sl.ng > 0, tid);
+            csync();
             rec(ph + 4, 1);
             rec1(l, 8);
         }
@@ -1037,6 +1043,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
             rec1(l, 9);
             gemv_tasks<LC>(sl, ring, n, planes, scales, red, wc, warp, lane, trace ? trace + (ph + 5) * 4 : nullptr);
             csync();
+            if (tid == 0 && sl.ng > 0) red_relaxed_add(ctr_at(P, 16 + xsub), 1u);
             if (sl.ng > 0) {
                 const float r = *rsc;
                 for (int t = 2 * tid; t < sl.ng * 8; t += 2 * kCT) {
@@ -1048,7 +1055,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
                     }
                 }
             }
-            arrive(ctr_at(P, 16 + xsub), sl.ng > 0, tid);
+            csync();
             rec(ph + 5, 1);
             rec1(l, 10);
         }
@@ -1064,6 +1071,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
             rec1(l, 11);
             gemv_tasks<LC>(sl, ring, n, planes, scales, red, wc, warp, lane, trace ? trace + (ph + 6) * 4 : nullptr);
             csync();
+            if (tid == 0 && sl.ng > 0) red_relaxed_add(ctr_at(P, xsub), 1u);
             bool wrote = false;
             for (int t = tid; t < sl.ng * 8; t += kCT) {
                 const float y = xown[t] + row_sum<LC>(sl, red, t);
@@ -1072,7 +1080,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) k_step(const __grid_constant_
                 wrote = true;
             }
             (void)wrote;
-            arrive(ctr_at(P, xsub), sl.ng > 0, tid);
+            csync();
             rec(ph + 6, 1);
             rec1(l, 12);
         }
