@@ -184,7 +184,9 @@ __device__ __forceinline__ void arrive(unsigned *ctr, bool wrote, int tid) {
 
 // Read N (2 or 4) tagged words at word index i of buf, re-reading until all
 // carry the tag (the arrival counters are relaxed: a word can trail its
-// counter by a little); v receives the values.
+// counter by a little); v receives the values. The re-reads do not sleep
+// between rounds: they run only in a hand-off's tail (measured faster than
+// a 32 ns back-off).
 template <int N>
 __device__ __forceinline__ void ll_read(const float *buf, int i, unsigned tag, float (&v)[N], const WaitCtx &w) {
     const unsigned long long *p = reinterpret_cast<const unsigned long long *>(buf) + i;
@@ -197,7 +199,6 @@ __device__ __forceinline__ void ll_read(const float *buf, int i, unsigned tag, f
     if (!ok) {
         const long long c0 = clock64();
         for (int it = 1;; ++it) {
-            __nanosleep(32);
             ll_ld2(p, u[0], u[1]);
             if constexpr (N == 4) ll_ld2(p + 2, u[2], u[3]);
             ok = true;
