@@ -345,6 +345,30 @@ QW3_API int qw3_q8_0_gemv_splitk_noalloc(const void *W_dev, int32_t rows, int32_
                                          const float *x_dev, int32_t B, float *y_dev,
                                          void *stream);
 
+/* ---- The dense contraction on the tensor cores ----------------------------
+ * The product prefill and large batches run ("A transformer from scratch",
+ * 12.3: every linear layer applies to all rows of a chunk at once), as one
+ * call: y[m][r] = sum_k W[r][k] * x[m][k] for raw Q8_0 W [rows][cols/32
+ * blocks] ("Model files and quantization", 11.6) and f32 x [M][cols], y f32
+ * [M][rows]. tcgen05 MMAs on fp16 hi/lo operand pairs, each row of W and of x
+ * first multiplied by its own power of two (largest magnitude into
+ * [2^14, 2^15)); f32 accumulation; results within f32 reassociation error of
+ * the exact product.
+ *
+ * Returns the workspace bytes qw3_q8_0_gemm needs for these sizes, or -1 if
+ * a size is negative or cols % 64 != 0. */
+QW3_API int64_t qw3_q8_0_gemm_workspace_bytes(int32_t rows, int32_t cols, int32_t M);
+
+/* W 2-byte aligned, x and the workspace 16-byte aligned, y 4-byte aligned;
+ * workspace_bytes at least qw3_q8_0_gemm_workspace_bytes(rows, cols, M)
+ * (QW3_ERR_INVALID_ARG otherwise; QW3_ERR_SHAPE if cols % 64 != 0). The
+ * caller owns every buffer; the workspace must not be used by another call
+ * until this one has completed on `stream`. rows == 0 or M == 0 is a no-op;
+ * cols == 0 writes zeros. Asynchronous on `stream`. */
+QW3_API int qw3_q8_0_gemm(const void *W_dev, int32_t rows, int32_t cols, const float *x_dev,
+                          int32_t M, float *y_dev, void *workspace_dev, int64_t workspace_bytes,
+                          void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -4,23 +4,33 @@
 // h to kv head h / (n_heads / n_kv_heads)).
 //
 // Flash-attention over 64-key tiles, one CTA per (128-query tile, query
-// head), f32 accuracy from bf16 operands: every operand x is split into
-// hi = bf16(x) and lo = bf16(x - hi), and each product is hi.hi + hi.lo +
-// lo.hi (three tcgen05.mma, f32 accumulation in TMEM), as in the GEMMs.
-//  * Per layer, k_pack_kv converts the cached K and V of the sequence into
-//    per-(kv head, 64-key tile) UMMA operand tiles (K as B of S = Q K^T,
-//    V transposed as B of O = P V), so attention CTAs fetch each tile with
-//    one bulk copy into a two-buffer ring.
+// head), f32 accuracy from fp16 operands as in the GEMMs: every operand x,
+// first multiplied by a power of two 2^t chosen per row, is split into
+// hi = fp16(x) and lo = fp16(x - hi), and each product is hi.hi + hi.lo +
+// lo.hi (three tcgen05.mma, f32 accumulation in TMEM); the results are
+// multiplied by the inverse powers (exact). The factors: one per query row
+// and one per key (S = Q K^T contracts over the head dimension), one per
+// (kv head, 8 dimensions) over all keys for V (O = P V contracts over keys,
+// so V's factor must not vary along them); P lies in [0, 2^8] and needs none.
+//  * Per layer, k_pack_k and k_pack_v convert the cached K and V of the
+//    sequence into per-(kv head, 64-key tile) UMMA operand tiles (K as B of
+//    S = Q K^T, V transposed as B of O = P V) with the keys' inverse factors
+//    beside them, so attention CTAs fetch each tile with one bulk copy (and
+//    its 64 factors with another) into a two-buffer ring.
 //  * The CTA packs its 128 query rows once; per key tile: S = Q K^T into 64
 //    TMEM columns; each thread owns one query row (its TMEM lane) and runs
-//    the online softmax on it without shuffles (in base 2); P (hi/lo) goes to shared
-//    memory; O (in TMEM) is rescaled only where the row's reference maximum
-//    moved (it trails the true maximum by at most 8 in base 2); then
-//    O += P V. The row's 1/l scaling is applied when O is read back.
+//    the online softmax on it without shuffles (in base 2); P (hi/lo) goes
+//    to shared memory; then P V accumulates into a partial O in TMEM. The
+//    tensor core's f32 accumulation truncates toward zero, so a long chain of
+//    MMAs into one accumulator loses a relative ~1.6e-8 per MMA; the partial
+//    therefore holds at most kPvChain tiles before the threads add it into
+//    the master O (CUDA-core f32, round to nearest). The row's reference
+//    maximum trails its true maximum by at most 8 (base 2) and moves rarely:
+//    where it moves, the row's partial and master are rescaled in place, and
+//    a promotion applies the tile's rescale: master = (master + partial) *
+//    corr. The row's 1/l scaling is applied when O is read back.
 //  * Every wait is bounded (1 s -> QW3_ERR_TIMEOUT, then the kernel drains
 //    and frees its tensor memory without waiting further).
-#include <cuda_bf16.h>
-
 #include "qw3_internal.cuh"
 
 namespace qw3 {
@@ -30,6 +40,7 @@ namespace {
 constexpr int kQT = 128;          // queries per CTA (TMEM lanes)
 constexpr int kKT = 64;           // keys per tile
 constexpr int kPaThreads = 128;
+constexpr int kPvChain = 4;       // key tiles per P V accumulation chain
 
 // Bytes of the packed operand tiles.
 template <int HD>
@@ -39,8 +50,26 @@ struct PaSizes {
     static constexpr uint32_t kv = 2 * (HD * 128);                // V^T tile: hi + lo, HD rows x 64 keys
     static constexpr uint32_t kkv = kk + kv;                      // one packed (K, V) tile
     static constexpr uint32_t kp = 2 * (kQT * 128);               // P: hi + lo, 128 rows x 64 keys
-    static constexpr uint32_t smem = kq + 2 * kkv + kp + 1024 + 256;
+    static constexpr uint32_t kinv = kKT * 4;                     // a tile's inverse key factors
+    static constexpr uint32_t smem = kq + 2 * kkv + kp + 2 * kinv + 1024 + 256;
 };
+
+// The pack buffer: nkv * ntiles (K, V^T) tiles, then the keys' inverse
+// factors [nkv][ntiles][64], then V's inverse factors [nkv][HD], then V's
+// maxima [nkv][HD / 8].
+template <int HD>
+__host__ __device__ inline float *pa_kinv(uint8_t *pack, int nkv, int ntiles) {
+    return reinterpret_cast<float *>(pack + static_cast<size_t>(nkv) * ntiles * PaSizes<HD>::kkv);
+}
+template <int HD>
+__host__ __device__ inline float *pa_vinv(uint8_t *pack, int nkv, int ntiles) {
+    return pa_kinv<HD>(pack, nkv, ntiles) + static_cast<size_t>(nkv) * ntiles * kKT;
+}
+// then the scratch of V's maxima [nkv][HD / 8]
+template <int HD>
+__host__ __device__ inline unsigned *pa_vmax(uint8_t *pack, int nkv, int ntiles) {
+    return reinterpret_cast<unsigned *>(pa_vinv<HD>(pack, nkv, ntiles) + static_cast<size_t>(nkv) * HD);
+}
 
 // Byte offset of element (row r, column k) in a K-major no-swizzle UMMA tile
 // of 64 columns: 8x8 core matrices (128 B), 8-row groups 1024 B apart.
@@ -53,72 +82,107 @@ __device__ __forceinline__ uint64_t pa_desc(uint32_t saddr) {
            (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46);
 }
 
-// kind::f16 instruction descriptor: f32 accumulate, bf16 A and B, K-major.
+// kind::f16 instruction descriptor: f32 accumulate (bit 4), fp16 A and B
+// (format fields 0), K-major.
 __host__ __device__ constexpr uint32_t pa_idesc(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (static_cast<uint32_t>(M >> 4) << 24);
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-__device__ __forceinline__ uint32_t bf16x2(float a, float b) {
-    const __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<const uint32_t *>(&p);
-}
-
-// hi/lo bf16 parts of 8 values as two uint4 (value j in halfword j).
-__device__ __forceinline__ void split8_hl(const float (&v)[8], uint4 &hi, uint4 &lo) {
-    float h[8], l[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        h[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
-        l[i] = v[i] - h[i];
-    }
-    hi = make_uint4(bf16x2(h[0], h[1]), bf16x2(h[2], h[3]), bf16x2(h[4], h[5]), bf16x2(h[6], h[7]));
-    lo = make_uint4(bf16x2(l[0], l[1]), bf16x2(l[2], l[3]), bf16x2(l[4], l[5]), bf16x2(l[6], l[7]));
-}
-
-// Pack keys [0, ntiles * 64) of every kv head: thread = (head, tile, part, row,
-// 8-column group). Keys at or past ctx are zero.
+// K tiles: HD / 8 threads per (kv head, key) of keys [0, ntiles * 64), 8
+// dimensions each: the key's largest magnitude (a shuffle over its threads)
+// sets its factor; the scaled row goes to the K part of its tile, the
+// inverse factor beside the tiles. Keys at or past ctx are zero.
 template <int HD, typename KT>
-__global__ void k_pack_kv(const KT *__restrict__ kc, const KT *__restrict__ vc, size_t head_stride, int nkv,
-                          int ctx, int ntiles, uint8_t *__restrict__ dst) {
+__global__ void k_pack_k(const KT *__restrict__ kc, size_t head_stride, int nkv, int ctx, int ntiles,
+                         uint8_t *__restrict__ dst) {
     using Z = PaSizes<HD>;
-    constexpr int kItems = kKT * (HD / 8);   // K: rows x 8-dim groups (= V^T: HD rows x 8-key groups)
+    constexpr int G = HD / 8;   // threads per key: aligned groups of 8 or 16 lanes
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t total = static_cast<int64_t>(nkv) * ntiles * 2 * kItems;
-    if (i >= total) return;
-    const int item = static_cast<int>(i % kItems);
-    const int part = static_cast<int>((i / kItems) % 2);
-    const int tile = static_cast<int>((i / (2 * kItems)) % ntiles);
-    const int g = static_cast<int>(i / (2 * static_cast<int64_t>(kItems) * ntiles));
-    uint8_t *t = dst + (static_cast<size_t>(g) * ntiles + tile) * Z::kkv;
+    const int64_t keys = static_cast<int64_t>(nkv) * ntiles * kKT;
+    const bool live = i < keys * G;   // the grid is whole warps: dead lanes still shuffle
+    const int64_t kid = live ? i / G : 0;
+    const int d0 = static_cast<int>(i % G) * 8;
+    const int key = static_cast<int>(kid % (static_cast<int64_t>(ntiles) * kKT));
+    const int g = static_cast<int>(kid / (static_cast<int64_t>(ntiles) * kKT));
+    const KT *row = kc + static_cast<size_t>(g) * head_stride + static_cast<size_t>(key) * kv_row<KT, HD>();
     float v[8];
-    uint4 hi, lo;
-    if (part == 0) {
-        // K: row = key, columns = dims
-        const int r = item / (HD / 8), d0 = (item % (HD / 8)) * 8;
-        const int key = tile * kKT + r;
-        const KT *row = kc + static_cast<size_t>(g) * head_stride + static_cast<size_t>(key) * kv_row<KT, HD>();
+    float amax = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = key < ctx ? kv_elem<HD>(row, d0 + j) : 0.0f;
-        split8_hl(v, hi, lo);
-        const int s = d0 / 64, kk = d0 % 64;
-        uint8_t *base = t + s * 2 * (kKT * 128);
-        *reinterpret_cast<uint4 *>(base + pa_core(r, kk)) = hi;
-        *reinterpret_cast<uint4 *>(base + kKT * 128 + pa_core(r, kk)) = lo;
-    } else {
-        // V^T: row = dim, columns = keys
-        const int d = item / (kKT / 8), k0 = (item % (kKT / 8)) * 8;
-        const KT *src = vc + static_cast<size_t>(g) * head_stride;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int key = tile * kKT + k0 + j;
-            v[j] = key < ctx ? kv_elem<HD>(src + static_cast<size_t>(key) * kv_row<KT, HD>(), d) : 0.0f;
-        }
-        split8_hl(v, hi, lo);
-        uint8_t *base = t + Z::kk;
-        *reinterpret_cast<uint4 *>(base + pa_core(d, k0)) = hi;
-        *reinterpret_cast<uint4 *>(base + HD * 128 + pa_core(d, k0)) = lo;
+    for (int j = 0; j < 8; ++j) {
+        v[j] = (live && key < ctx) ? kv_elem<HD>(row, d0 + j) : 0.0f;
+        amax = fmaxf(amax, fabsf(v[j]));
     }
+#pragma unroll
+    for (int o = 1; o < G; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (!live) return;
+    const int t = f16_row_exp(amax);
+    const float sr = pow2_f32(t);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] *= sr;
+    uint4 hi, lo;
+    split8_f16(v, hi, lo);
+    const int tile = key / kKT, r = key % kKT;
+    uint8_t *base = dst + (static_cast<size_t>(g) * ntiles + tile) * Z::kkv + (d0 / 64) * 2 * (kKT * 128);
+    *reinterpret_cast<uint4 *>(base + pa_core(r, d0 % 64)) = hi;
+    *reinterpret_cast<uint4 *>(base + kKT * 128 + pa_core(r, d0 % 64)) = lo;
+    if (d0 == 0) pa_kinv<HD>(dst, nkv, ntiles)[static_cast<size_t>(g) * ntiles * kKT + key] = pow2_f32(-t);
+}
+
+// The largest magnitude of each (kv head, 8 dimensions) of V over keys
+// [0, ctx), as the bits of a non-negative f32 (atomicMax on unsigned order;
+// vmax zeroed first): a CTA covers 256 keys of one head, thread = (key, 8
+// dimensions), reduced in shared memory before one atomic per group.
+template <int HD, typename KT>
+__global__ void __launch_bounds__(256) k_v_absmax(const KT *__restrict__ vc, size_t head_stride, int ctx,
+                                                  unsigned *__restrict__ vmax) {
+    constexpr int G = HD / 8, KPI = 256 / G;   // dimension groups; keys per pass of the CTA
+    __shared__ float red[256];
+    const int g = blockIdx.y, tid = threadIdx.x, dg = tid % G;
+    const KT *src = vc + static_cast<size_t>(g) * head_stride;
+    float amax = 0.0f;
+    const int k_end = min(ctx, (blockIdx.x + 1) * 256);
+    for (int key = blockIdx.x * 256 + tid / G; key < k_end; key += KPI) {
+        const KT *row = src + static_cast<size_t>(key) * kv_row<KT, HD>();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(kv_elem<HD>(row, dg * 8 + j)));
+    }
+    red[tid] = amax;
+    __syncthreads();
+    if (tid < G) {
+        for (int k = tid + G; k < 256; k += G) amax = fmaxf(amax, red[k]);
+        atomicMax(&vmax[g * G + tid], __float_as_uint(amax));
+    }
+}
+
+// V^T tiles: one thread per (kv head, tile, dimension, 8-key group); each
+// (kv head, 8 dimensions) scaled by the common factor of vmax. Keys at or
+// past ctx are zero.
+template <int HD, typename KT>
+__global__ void k_pack_v(const KT *__restrict__ vc, size_t head_stride, int nkv, int ctx, int ntiles,
+                         const unsigned *__restrict__ vmax, uint8_t *__restrict__ dst) {
+    using Z = PaSizes<HD>;
+    constexpr int kItems = HD * (kKT / 8);
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= static_cast<int64_t>(nkv) * ntiles * kItems) return;
+    const int item = static_cast<int>(i % kItems);
+    const int tile = static_cast<int>((i / kItems) % ntiles);
+    const int g = static_cast<int>(i / (static_cast<int64_t>(kItems) * ntiles));
+    const int d = item / (kKT / 8), k0 = (item % (kKT / 8)) * 8;
+    const int t = f16_row_exp(__uint_as_float(vmax[g * (HD / 8) + d / 8]));
+    const float sr = pow2_f32(t);
+    const KT *src = vc + static_cast<size_t>(g) * head_stride;
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int key = tile * kKT + k0 + j;
+        v[j] = key < ctx ? kv_elem<HD>(src + static_cast<size_t>(key) * kv_row<KT, HD>(), d) * sr : 0.0f;
+    }
+    uint4 hi, lo;
+    split8_f16(v, hi, lo);
+    uint8_t *base = dst + (static_cast<size_t>(g) * ntiles + tile) * Z::kkv + Z::kk;
+    *reinterpret_cast<uint4 *>(base + pa_core(d, k0)) = hi;
+    *reinterpret_cast<uint4 *>(base + HD * 128 + pa_core(d, k0)) = lo;
+    if (tile == 0 && k0 == 0) pa_vinv<HD>(dst, nkv, ntiles)[static_cast<size_t>(g) * HD + d] = pow2_f32(-t);
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
@@ -132,18 +196,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
         : "memory");
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-        ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-          "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-          "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-          "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-          "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-          "r"(__float_as_uint(v[15]))
-        : "memory");
 }
 
 // Three MMAs (hi.hi, hi.lo, lo.hi) over one 64-deep step: A at a_hi / a_lo,
@@ -166,6 +218,55 @@ __device__ __forceinline__ void mma3(uint32_t tmem, uint32_t a_hi, uint32_t a_lo
     }
 }
 
+// This thread's row of the master O (TMEM lanes of its warp): master =
+// ((has_master ? master : 0) + partial) * corr, over HD columns; the stores
+// complete before it returns. Warp-collective (has_master warp-uniform).
+template <int HD>
+__device__ __forceinline__ void promote_o(uint32_t master, uint32_t partial, bool has_master, float corr) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < HD; c0 += 8) {
+        uint32_t a[8], b[8];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%16];\n\t"
+            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%17];\n\t"
+            "tcgen05.wait::ld.sync.aligned;"
+            : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+              "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7])
+            : "r"(master + c0), "r"(partial + c0)
+            : "memory");
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float m = has_master ? __uint_as_float(a[j]) : 0.0f;
+            a[j] = __float_as_uint((m + __uint_as_float(b[j])) * corr);
+        }
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                     ::"r"(master + c0), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]),
+                       "r"(a[7])
+                     : "memory");
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// This thread's row of an O accumulator times corr, in place (warp-collective).
+template <int HD>
+__device__ __forceinline__ void rescale_o(uint32_t taddr, float corr) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < HD; c0 += 16) {
+        float t16[16];
+        tmem_ld16(taddr + static_cast<uint32_t>(c0), t16);
+        uint32_t u[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(t16[e] * corr);
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+            ::"r"(taddr + static_cast<uint32_t>(c0)), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]),
+              "r"(u[5]), "r"(u[6]), "r"(u[7]), "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]),
+              "r"(u[13]), "r"(u[14]), "r"(u[15])
+            : "memory");
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
@@ -175,7 +276,7 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 
 template <int HD>
 __global__ void __launch_bounds__(kPaThreads, 1)
-    k_attn_prefill_tc(const float *__restrict__ qkv, int M, int qkv_stride, const uint8_t *__restrict__ kvpack,
+    k_attn_prefill_tc(const float *__restrict__ qkv, int M, int qkv_stride, uint8_t *kvpack, int nkv,
                       int ntiles, int pos0, int group, float scale, float *__restrict__ out, int32_t *status) {
     using Z = PaSizes<HD>;
     extern __shared__ __align__(1024) uint8_t pa_smem[];
@@ -183,7 +284,8 @@ __global__ void __launch_bounds__(kPaThreads, 1)
     uint8_t *Qs = base;                    // [HD/64][hi|lo] 128 x 64 tiles
     uint8_t *KV0 = Qs + Z::kq;             // two packed (K, V^T) tiles
     uint8_t *Ps = KV0 + 2 * Z::kkv;        // [hi|lo] 128 x 64
-    uint64_t *bars = reinterpret_cast<uint64_t *>(Ps + Z::kp);   // kv_full[2], s_done, o_done
+    float *Kinv = reinterpret_cast<float *>(Ps + Z::kp);          // [2][64] the tiles' inverse key factors
+    uint64_t *bars = reinterpret_cast<uint64_t *>(Ps + Z::kp + 2 * Z::kinv);   // kv_full[2], s_done, o_done
     uint64_t *kv_full = bars, *s_done = bars + 2, *o_done = bars + 3;
     uint32_t *tbase = reinterpret_cast<uint32_t *>(bars + 4);
     volatile int *err = reinterpret_cast<volatile int *>(tbase + 1);
@@ -196,6 +298,20 @@ __global__ void __launch_bounds__(kPaThreads, 1)
     const int last_q = min(M - 1, qt * kQT + kQT - 1);
     const int ntl = min(ntiles, (pos0 + last_q) / kKT + 1);   // key tiles this CTA needs
     const uint8_t *kvg = kvpack + static_cast<size_t>(g) * ntiles * Z::kkv;
+    const float *kinvg = pa_kinv<HD>(kvpack, nkv, ntiles) + static_cast<size_t>(g) * ntiles * kKT;
+    const float *vinvg = pa_vinv<HD>(kvpack, nkv, ntiles) + static_cast<size_t>(g) * HD;
+    // thread 0: tile jt (its K/V^T pair and its key factors) into buffer b
+    auto fetch = [&](int jt, int b) {
+        mbar_arrive_expect_tx(&kv_full[b], Z::kkv + Z::kinv);
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(smem_u32(KV0 + b * Z::kkv)), "l"(kvg + static_cast<size_t>(jt) * Z::kkv), "r"(Z::kkv),
+                       "r"(smem_u32(&kv_full[b]))
+                     : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(smem_u32(Kinv + b * kKT)), "l"(kinvg + static_cast<size_t>(jt) * kKT), "r"(Z::kinv),
+                       "r"(smem_u32(&kv_full[b]))
+                     : "memory");
+    };
 
     if (tid == 0) {
         mbar_init(&kv_full[0], 1);
@@ -207,43 +323,51 @@ __global__ void __launch_bounds__(kPaThreads, 1)
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tbase)),
-                     "r"(256) : "memory");
+                     "r"(512) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tbase;
-    const uint32_t tS = tmem, tO = tmem + 128;              // S: 64 columns, O: HD columns
+    const uint32_t tS = tmem, tO = tmem + 128, tP = tmem + 256;   // S: 64 columns; master and partial O: HD
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
 
     int last_issued[2] = {-1, -1};   // thread 0: the last tile fetched into each buffer
     if (tid == 0) {
         for (int j = 0; j < 2 && j < ntl; ++j) {
             last_issued[j] = j;
-            mbar_arrive_expect_tx(&kv_full[j], Z::kkv);
-            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                         ::"r"(smem_u32(KV0 + j * Z::kkv)), "l"(kvg + static_cast<size_t>(j) * Z::kkv), "r"(Z::kkv),
-                           "r"(smem_u32(&kv_full[j]))
-                         : "memory");
+            fetch(j, j);
         }
     }
-    // ---- this thread's query row -> Q tiles (hi / lo)
+    // ---- this thread's query row -> Q tiles (hi / lo), scaled by its factor
+    float qinv = 1.0f;
     {
         const float *src = qkv + static_cast<size_t>(q) * qkv_stride + static_cast<size_t>(h) * HD;
+        float amax = 0.0f;
+        if (q < M)
+#pragma unroll 4
+            for (int d0 = 0; d0 < HD; d0 += 4) {
+                const float4 a = *reinterpret_cast<const float4 *>(src + d0);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+            }
+        const int t = f16_row_exp(amax);
+        const float sr = pow2_f32(t);
+        qinv = pow2_f32(-t);
 #pragma unroll
         for (int d0 = 0; d0 < HD; d0 += 8) {
             float v[8];
             if (q < M) {
                 const float4 a = *reinterpret_cast<const float4 *>(src + d0);
                 const float4 b = *reinterpret_cast<const float4 *>(src + d0 + 4);
-                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+                v[0] = a.x * sr; v[1] = a.y * sr; v[2] = a.z * sr; v[3] = a.w * sr;
+                v[4] = b.x * sr; v[5] = b.y * sr; v[6] = b.z * sr; v[7] = b.w * sr;
             } else {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) v[j] = 0.0f;
             }
             uint4 hi, lo;
-            split8_hl(v, hi, lo);
+            split8_f16(v, hi, lo);
             uint8_t *tq = Qs + (d0 / 64) * 2 * (kQT * 128);
             *reinterpret_cast<uint4 *>(tq + pa_core(row, d0 % 64)) = hi;
             *reinterpret_cast<uint4 *>(tq + kQT * 128 + pa_core(row, d0 % 64)) = lo;
@@ -257,6 +381,8 @@ __global__ void __launch_bounds__(kPaThreads, 1)
     // softmax in base 2: exp(x) = 2^(x log2 e), scores pre-scaled by log2 e
     const float scale2 = scale * 1.4426950408889634f;
     float m_run = -INFINITY, l_run = 0.0f;
+    int chain = 0;              // tiles in the partial O (CTA-uniform)
+    bool has_master = false;    // the master O holds promoted tiles
     for (int j = 0; j < ntl; ++j) {
         const int buf = j & 1;
         const uint8_t *KV = KV0 + buf * Z::kkv;
@@ -278,6 +404,10 @@ __global__ void __launch_bounds__(kPaThreads, 1)
         __syncwarp();
         if (!mbar_wait_bounded(s_done, static_cast<uint32_t>(j & 1))) *err = 1;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        // the tile's key factors (landed with the tile: its phase is complete)
+        if (!mbar_wait_bounded(&kv_full[buf], static_cast<uint32_t>((j >> 1) & 1))) *err = 1;
+        const float *kinv = Kinv + buf * kKT;
+        const float qs2 = qinv * scale2;   // exact: qinv is a power of two
         // ---- online softmax of this row over the tile's 64 keys
         float sv[kKT];
 #pragma unroll
@@ -291,7 +421,7 @@ __global__ void __launch_bounds__(kPaThreads, 1)
 #pragma unroll
         for (int c = 0; c < kKT; ++c) {
             const int key = j * kKT + c;
-            sv[c] = (key <= qpos) ? sv[c] * scale2 : -INFINITY;
+            sv[c] = (key <= qpos) ? sv[c] * kinv[c] * qs2 : -INFINITY;
             mx = fmaxf(mx, sv[c]);
         }
         // The reference maximum moves only when the tile's maximum exceeds it
@@ -307,7 +437,7 @@ __global__ void __launch_bounds__(kPaThreads, 1)
         }
         l_run = fmaf(l_run, corr, ps);
         m_run = m_new;
-        // ---- the previous O += P V must be complete before P and O change
+        // ---- the previous P V must be complete before P and O change
         if (j > 0) {
             if (!mbar_wait_bounded(o_done, static_cast<uint32_t>((j - 1) & 1))) *err = 1;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -315,24 +445,17 @@ __global__ void __launch_bounds__(kPaThreads, 1)
             if (tid == 0 && j + 1 < ntl && !*err) {
                 const int nb = (j + 1) & 1;
                 last_issued[nb] = j + 1;
-                mbar_arrive_expect_tx(&kv_full[nb], Z::kkv);
-                asm volatile(
-                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                    ::"r"(smem_u32(KV0 + nb * Z::kkv)), "l"(kvg + static_cast<size_t>(j + 1) * Z::kkv), "r"(Z::kkv),
-                      "r"(smem_u32(&kv_full[nb]))
-                    : "memory");
+                fetch(j + 1, nb);
             }
-            // rescale O where a row's maximum moved (warp-uniform skip)
-            if (__any_sync(0xffffffffu, corr != 1.0f)) {
-#pragma unroll
-                for (int c = 0; c < HD; c += 16) {
-                    float t16[16];
-                    tmem_ld16(tO + lane_off + static_cast<uint32_t>(c), t16);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) t16[e] *= corr;
-                    tmem_st16(tO + lane_off + static_cast<uint32_t>(c), t16);
-                }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            if (chain == kPvChain) {
+                // the partial is full: master = (master + partial) * corr
+                promote_o<HD>(tO + lane_off, tP + lane_off, has_master, corr);
+                has_master = true;
+                chain = 0;
+            } else if (__any_sync(0xffffffffu, corr != 1.0f)) {
+                // a row's maximum moved: rescale its partial (and master) in place
+                rescale_o<HD>(tP + lane_off, corr);
+                if (has_master) rescale_o<HD>(tO + lane_off, corr);
             }
         }
         // ---- P (hi / lo) of this row
@@ -340,23 +463,24 @@ __global__ void __launch_bounds__(kPaThreads, 1)
         for (int c = 0; c < kKT; c += 8) {
             const float v8[8] = {sv[c], sv[c + 1], sv[c + 2], sv[c + 3], sv[c + 4], sv[c + 5], sv[c + 6], sv[c + 7]};
             uint4 hi, lo;
-            split8_hl(v8, hi, lo);
+            split8_f16(v8, hi, lo);
             *reinterpret_cast<uint4 *>(Ps + pa_core(row, c)) = hi;
             *reinterpret_cast<uint4 *>(Ps + kQT * 128 + pa_core(row, c)) = lo;
         }
         fence_async_smem();
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncthreads();
-        // ---- O += P V_j
+        // ---- partial O += P V_j (a new chain after a promotion)
         if (tid == 0) {
             if (!*err) {
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t a = smem_u32(Ps);
                 const uint32_t b = smem_u32(KV + Z::kk);
-                mma3(tO, a, a + kQT * 128, b, b + HD * 128, kIdO, j == 0);
+                mma3(tP, a, a + kQT * 128, b, b + HD * 128, kIdO, chain == 0);
             }
             mma_commit(o_done);
         }
+        ++chain;
         __syncwarp();
     }
     // ---- O / l of this row to global memory
@@ -369,12 +493,21 @@ __global__ void __launch_bounds__(kPaThreads, 1)
 #pragma unroll
     for (int c = 0; c < HD; c += 16) {
         float t16[16];
-        tmem_ld16(tO + lane_off + static_cast<uint32_t>(c), t16);
+        tmem_ld16(tP + lane_off + static_cast<uint32_t>(c), t16);
+        if (has_master) {
+            float m16[16];
+            tmem_ld16(tO + lane_off + static_cast<uint32_t>(c), m16);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) t16[e] += m16[e];
+        }
         if (q < M && ntl > 0) {
 #pragma unroll
-            for (int e = 0; e < 16; e += 4)
+            for (int e = 0; e < 16; e += 4) {
+                const float4 vi = *reinterpret_cast<const float4 *>(vinvg + c + e);
                 *reinterpret_cast<float4 *>(dst + c + e) =
-                    make_float4(t16[e] * inv, t16[e + 1] * inv, t16[e + 2] * inv, t16[e + 3] * inv);
+                    make_float4((t16[e] * vi.x) * inv, (t16[e + 1] * vi.y) * inv, (t16[e + 2] * vi.z) * inv,
+                                (t16[e + 3] * vi.w) * inv);
+            }
         }
     }
     __syncthreads();
@@ -388,7 +521,7 @@ __global__ void __launch_bounds__(kPaThreads, 1)
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
 }
 
 template <int HD, typename KT>
@@ -398,14 +531,23 @@ cudaError_t launch_pa_t(const float *qkv, int M, int qkv_stride, const KT *kc, c
     using Z = PaSizes<HD>;
     const int ctx = pos0 + M;
     const int ntiles = (ctx + kKT - 1) / kKT;
-    const int64_t items = static_cast<int64_t>(nkv) * ntiles * 2 * kKT * (HD / 8);
-    k_pack_kv<HD, KT><<<static_cast<unsigned>((items + 255) / 256), 256, 0, s>>>(kc, vc, head_stride, nkv, ctx,
-                                                                                  ntiles, kvpack);
+    const int64_t kthreads = static_cast<int64_t>(nkv) * ntiles * kKT * (HD / 8);
+    k_pack_k<HD, KT><<<static_cast<unsigned>((kthreads + 255) / 256), 256, 0, s>>>(kc, head_stride, nkv, ctx,
+                                                                                    ntiles, kvpack);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    unsigned *vmax = pa_vmax<HD>(kvpack, nkv, ntiles);
+    if ((e = cudaMemsetAsync(vmax, 0, static_cast<size_t>(nkv) * (HD / 8) * sizeof(unsigned), s)) != cudaSuccess)
+        return e;
+    k_v_absmax<HD, KT><<<dim3((ctx + 255) / 256, nkv), 256, 0, s>>>(vc, head_stride, ctx, vmax);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t vitems = static_cast<int64_t>(nkv) * ntiles * HD * (kKT / 8);
+    k_pack_v<HD, KT><<<static_cast<unsigned>((vitems + 255) / 256), 256, 0, s>>>(vc, head_stride, nkv, ctx, ntiles,
+                                                                                  vmax, kvpack);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const dim3 grid((M + kQT - 1) / kQT, nh);
-    k_attn_prefill_tc<HD><<<grid, kPaThreads, Z::smem, s>>>(qkv, M, qkv_stride, kvpack, ntiles, pos0, nh / nkv,
-                                                            scale, out, status);
+    k_attn_prefill_tc<HD><<<grid, kPaThreads, Z::smem, s>>>(qkv, M, qkv_stride, kvpack, nkv, ntiles, pos0,
+                                                            nh / nkv, scale, out, status);
     return cudaGetLastError();
 }
 
@@ -414,7 +556,8 @@ cudaError_t launch_pa_t(const float *qkv, int M, int qkv_stride, const KT *kc, c
 size_t attn_prefill_tc_pack_bytes(int hd, int nkv, int max_seq_len) {
     const size_t ntiles = (static_cast<size_t>(max_seq_len) + kKT - 1) / kKT;
     const size_t tile = hd == 128 ? PaSizes<128>::kkv : PaSizes<64>::kkv;
-    return static_cast<size_t>(nkv) * ntiles * tile;
+    return static_cast<size_t>(nkv) * ntiles * (tile + kKT * 4) + static_cast<size_t>(nkv) * hd * 4 +
+           static_cast<size_t>(nkv) * (hd / 8) * 4;
 }
 
 cudaError_t configure_attn_prefill_tc() {

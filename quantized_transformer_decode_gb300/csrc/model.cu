@@ -485,7 +485,9 @@ int run_decode_step(qw3_model *m, int B) {
 
 // ---- tensor-core GEMM (prefill, batches from kGemmTcMinRows rows): every
 // layer matrix (and the lm_head when batches that large are possible) gets a
-// copy as bf16 hi/lo tensor-core tiles, 4 bytes per weight.
+// copy in the layout the tensor-core GEMM reads: Q8_0 pieces streamed as they
+// are (1.0625 bytes per weight), Q4_K decoded into fp16 hi/lo tiles (4 bytes
+// per weight); each with its power-of-two row factors.
 int setup_tensor_core_gemm(qw3_model *m) {
     const qw3_config &c = m->cfg;
     // a Q4_K model's prefill and batches past the GEMV's rows run here at any size
@@ -497,7 +499,7 @@ int setup_tensor_core_gemm(qw3_model *m) {
     auto pack = [&](QMat &q) -> int {
         uint8_t *p = nullptr;
         if (q.q4) {
-            // Q4_K: bf16 hi/lo tiles (4 bytes per weight)
+            // Q4_K: fp16 hi/lo tiles (4 bytes per weight) and row factors
             M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&p), ut_bytes(q.rows, q.cols)));
             M_TRY(m, launch_pack_w_q4k(q.q4, q.rows, q.cols, p, m->stream));
             q.ut = p;
@@ -525,7 +527,7 @@ int setup_tensor_core_gemm(qw3_model *m) {
     }
     const int rows = std::max(c.max_prefill, c.max_seqs);
     const int kmax = std::max(H, std::max(qw, I));
-    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&m->apack), ut_bytes(rows, kmax)));
+    M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&m->apack), apack_bytes(rows, kmax)));
     // split-K partials of products with few output tiles (batched decode, short prefill chunks)
     m->gsk.ws_floats = static_cast<size_t>(4) << 20;
     M_TRY(m, model_alloc(m, reinterpret_cast<void **>(&m->gsk.ws), m->gsk.ws_floats * 4));
@@ -1228,6 +1230,33 @@ int qw3_q8_0_gemv(const void *W_dev, int32_t rows, int32_t cols, const float *x_
     if (rows == 0) return QW3_OK;
     QW3_CUDA_TRY(launch_gemv_raw(static_cast<const uint8_t *>(W_dev), rows, cols, x_dev, B, y_dev, false,
                                  static_cast<cudaStream_t>(stream)));
+    return QW3_OK;
+}
+
+int64_t qw3_q8_0_gemm_workspace_bytes(int32_t rows, int32_t cols, int32_t M) {
+    if (rows < 0 || cols < 0 || M < 0 || cols % 64) return -1;
+    return static_cast<int64_t>(gemm_q8_raw_workspace_bytes(rows, cols, M));
+}
+
+int qw3_q8_0_gemm(const void *W_dev, int32_t rows, int32_t cols, const float *x_dev, int32_t M, float *y_dev,
+                  void *workspace_dev, int64_t workspace_bytes, void *stream) {
+    if (!W_dev || !x_dev || !y_dev || rows < 0 || cols < 0 || M < 0)
+        return fail(nullptr, QW3_ERR_INVALID_ARG, "bad gemm arguments");
+    if (cols % 64) return fail(nullptr, QW3_ERR_SHAPE, "cols must be a multiple of 64");
+    if (misaligned(W_dev, 2) || misaligned(x_dev, 16) || misaligned(y_dev, 4) || misaligned(workspace_dev, 16))
+        return fail(nullptr, QW3_ERR_INVALID_ARG, "W must be 2-byte, x and the workspace 16-byte, y 4-byte aligned");
+    if (rows == 0 || M == 0) return QW3_OK;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cols == 0) {
+        QW3_CUDA_TRY(cudaMemsetAsync(y_dev, 0, static_cast<size_t>(M) * rows * sizeof(float), s));
+        return QW3_OK;
+    }
+    if (!workspace_dev || workspace_bytes < 0 ||
+        static_cast<uint64_t>(workspace_bytes) < gemm_q8_raw_workspace_bytes(rows, cols, M))
+        return fail(nullptr, QW3_ERR_INVALID_ARG, "workspace too small");
+    QW3_CUDA_TRY(configure_all());
+    QW3_CUDA_TRY(launch_gemm_q8_raw(static_cast<const uint8_t *>(W_dev), rows, cols, x_dev, M, y_dev,
+                                    static_cast<uint8_t *>(workspace_dev), s));
     return QW3_OK;
 }
 

@@ -180,18 +180,28 @@ struct GemmSplitK {
 
 // Dense contraction C[M][N] = A[M][K] . W[N][K]^T with the GEMV epilogue
 // modes; tensor cores (tcgen05) from kGemmTcMinRows rows, CUDA cores below.
-// apack: scratch for the packed activations (ut_bytes(M, K)); nullptr keeps
-// the CUDA-core path. sk (nullable): lets small-M products split K.
+// apack: scratch for the packed activations (apack_bytes(M, K)); nullptr
+// keeps the CUDA-core path. sk (nullable): lets small-M products split K.
 cudaError_t launch_gemm(const float *A, int M, int K, const QMat &W, float *C, int mode,
                         unsigned long long *argmax_key, const DecodeIO *io, cudaStream_t s,
                         int32_t *status = nullptr, uint8_t *apack = nullptr, const GemmSplitK *sk = nullptr);
 constexpr int kGemmTcMinRows = 32;
 bool gemm_tc_supported(int M, int K, const QMat &W);
-size_t ut_bytes(int rows, int K);   // bytes of a matrix packed into bf16 hi/lo UMMA tiles
+// bytes of a weight matrix packed into fp16 hi/lo UMMA tiles plus its row factors
+size_t ut_bytes(int rows, int K);
+// bytes of the packed activations of a GEMM with up to `rows` rows and K columns
+size_t apack_bytes(int rows, int K);
 cudaError_t configure_gemm_tc();
-// The Q8_0 weights of W in the layout the tensor-core GEMM streams (tq_bytes).
+// The Q8_0 weights of W in the layout the tensor-core GEMM streams, plus the
+// row factors (tq_bytes).
 size_t tq_bytes(int rows, int K);
 cudaError_t launch_pack_w_q8(const QMat &W, uint8_t *dst, cudaStream_t s);
+// C[M][N] = A[M][K] . W[N][K]^T on the tensor cores from a raw Q8_0 matrix
+// (K % 64 == 0): the weights are packed into the streamed layout and A into
+// its operand tiles inside ws (gemm_q8_raw_workspace_bytes, 16-byte aligned).
+size_t gemm_q8_raw_workspace_bytes(int N, int K, int M);
+cudaError_t launch_gemm_q8_raw(const uint8_t *W, int N, int K, const float *A, int M, float *C, uint8_t *ws,
+                               cudaStream_t s);
 // The same tiles from a raw Q4_K matrix [N][K / 256 blocks].
 cudaError_t launch_pack_w_q4k(const uint8_t *W, int N, int K, uint8_t *dst, cudaStream_t s);
 
@@ -461,6 +471,37 @@ __device__ __forceinline__ float q4k_value(const uint8_t *blk, int t) {
     return fmaf(d1, static_cast<float>(q), -m1);
 }
 
+
+// ---- fp16 hi/lo operands of the tensor-core products
+// A row (of an activation matrix, a weight matrix, a query, a key) whose
+// largest magnitude is amax is multiplied by the power of two 2^t that brings
+// amax into [2^14, 2^15); each scaled value x then splits exactly enough into
+// fp16 parts hi = rn(x), lo = rn(x - hi) (22 significant bits, no overflow:
+// fp16 holds up to 65504), and the product's f32 result is multiplied by the
+// inverse powers afterwards (exact). t is clamped to [-100, 100] so that both
+// 2^t and 2^-t are normal f32; amax = 0 gives t = 0.
+__device__ __forceinline__ int f16_row_exp(float amax) {
+    if (!(amax > 0.0f)) return 0;
+    const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127;   // floor(log2 amax), normal amax
+    return max(-100, min(100, 14 - e));
+}
+__device__ __forceinline__ float pow2_f32(int t) { return __uint_as_float(static_cast<uint32_t>(127 + t) << 23); }
+
+// hi/lo fp16 parts of 8 (already scaled) values as two uint4, value j in
+// halfword j.
+__device__ __forceinline__ void split8_f16(const float (&v)[8], uint4 &hi, uint4 &lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 p = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+        const float2 pf = __half22float2(p);
+        const __half2 r = __floats2half2_rn(v[2 * i] - pf.x, v[2 * i + 1] - pf.y);
+        h[i] = *reinterpret_cast<const uint32_t *>(&p);
+        l[i] = *reinterpret_cast<const uint32_t *>(&r);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
 
 // Q8_0 encoding of a row spread over a warp, lane holding values
 // [lane * E, lane * E + E) (E = HD / 32): 32 / E consecutive lanes hold one

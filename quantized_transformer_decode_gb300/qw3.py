@@ -45,6 +45,7 @@ EXPORTS = (
     "qw3_decode_plan", "qw3_sync", "qw3_stream", "qw3_status_string", "qw3_last_error",
     "qw3_q8_0_quantize", "qw3_q8_0_dequantize", "qw3_q8_0_gemv", "qw3_q8_0_gemv_q8act",
     "qw3_q4_k_quantize", "qw3_q4_k_dequantize", "qw3_q4_k_gemv", "qw3_q8_0_gemv_splitk_noalloc",
+    "qw3_q8_0_gemm_workspace_bytes", "qw3_q8_0_gemm",
 )
 
 
@@ -120,6 +121,8 @@ def lib() -> ctypes.CDLL:
         "qw3_q4_k_dequantize": (ctypes.c_int, [_P, _I64, _P, _P]),
         "qw3_q4_k_gemv": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P]),
         "qw3_q8_0_gemv_splitk_noalloc": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P]),
+        "qw3_q8_0_gemm_workspace_bytes": (_I64, [_I32, _I32, _I32]),
+        "qw3_q8_0_gemm": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _I64, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -256,6 +259,15 @@ def qw3_q8_0_gemv_splitk_noalloc(W_ptr: int, rows: int, cols: int, x_ptr: int, B
     _check(lib().qw3_q8_0_gemv_splitk_noalloc(W_ptr, rows, cols, x_ptr, B, y_ptr, stream or None))
 
 
+def qw3_q8_0_gemm_workspace_bytes(rows: int, cols: int, M: int) -> int:
+    return int(lib().qw3_q8_0_gemm_workspace_bytes(rows, cols, M))
+
+
+def qw3_q8_0_gemm(W_ptr: int, rows: int, cols: int, x_ptr: int, M: int, y_ptr: int, ws_ptr: int, ws_bytes: int,
+                  stream: int = 0) -> None:
+    _check(lib().qw3_q8_0_gemm(W_ptr, rows, cols, x_ptr, M, y_ptr, ws_ptr or None, ws_bytes, stream or None))
+
+
 # ---------------------------------------------------------- torch wrapper
 
 def _torch():
@@ -292,6 +304,21 @@ def q8_0_gemv(W, rows: int, cols: int, x):
     B = x.shape[0] if x.dim() == 2 else 1
     y = torch.empty((B, rows), dtype=torch.float32, device=x.device)
     qw3_q8_0_gemv(W.data_ptr(), rows, cols, x.data_ptr(), B, y.data_ptr(), _stream_ptr())
+    return y
+
+
+def q8_0_gemm(W, rows: int, cols: int, x):
+    """y = x . W^T for raw Q8_0 W [rows][cols] and CUDA f32 x [M][cols] on the
+    tensor cores (qw3_q8_0_gemm), the workspace allocated here."""
+    torch = _torch()
+    x = x.contiguous()
+    M = x.shape[0]
+    y = torch.empty((M, rows), dtype=torch.float32, device=x.device)
+    nbytes = qw3_q8_0_gemm_workspace_bytes(rows, cols, M)
+    if nbytes < 0:
+        raise Qw3Error(QW3_ERR_SHAPE, "cols must be a multiple of 64")
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=x.device)
+    qw3_q8_0_gemm(W.data_ptr(), rows, cols, x.data_ptr(), M, y.data_ptr(), ws.data_ptr(), nbytes, _stream_ptr())
     return y
 
 

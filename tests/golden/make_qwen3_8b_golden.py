@@ -9,13 +9,14 @@ seeded input generators run here; nothing comes from the CUDA path.
 
 Output, tests/golden/qwen3_8b_greedy.npz:
   ids     int32 [65]: the prefill's argmax, then each step's argmax;
+  margins f32 [65]:   the oracle's top-2 logit gap of each of those rows;
   steps   int32 [R]:  which rows of the greedy run the stored logits are
                       (0 = the prefill's last row, s = decode step s);
   logits  f32 [R][V]: those rows (the row each id was taken from; the GPU
                       is fed the oracle's ids, so these are teacher-forced);
   prompt_len, n_steps, seed.
 
-Run (about half an hour on 8 host cores, ~12 GB of memory):
+Run (about two hours on 8 host cores, ~12 GB of memory):
     python tests/golden/make_qwen3_8b_golden.py
 """
 from __future__ import annotations
@@ -48,8 +49,10 @@ def main() -> int:
     ids, logits = om.generate_greedy(cache, prompt, n_steps)
     print(f"prefill + {n_steps} steps in {time.time() - t1:.0f} s", flush=True)
     rows = np.stack([np.asarray(logits[k], np.float32) for k in STORED_STEPS])
+    margins = np.asarray([np.diff(np.sort(np.asarray(lg, np.float64))[-2:])[0] for lg in logits], np.float32)
     out = os.path.join(HERE, "qwen3_8b_greedy.npz")
-    np.savez_compressed(out, ids=np.asarray(ids, np.int32), steps=np.asarray(STORED_STEPS, np.int32), logits=rows,
+    np.savez_compressed(out, ids=np.asarray(ids, np.int32), margins=margins,
+                        steps=np.asarray(STORED_STEPS, np.int32), logits=rows,
                         prompt_len=np.int32(P), n_steps=np.int32(n_steps), seed=np.int32(w.seed))
     print(f"wrote {out}: ids {ids[:8]}...", flush=True)
     return 0

@@ -4,8 +4,10 @@ workloads, through the C ABI, in the launch configuration the benchmark uses.
 Where the oracle cannot finish the full workload (it is a plain f64 numpy
 statement of the model), the check uses outputs it can compute one by one
 (sampled sequences of the batch, layer-0 K/V rows, which depend on their own
-token only) and properties that hold at any size (a decode step after a
-prefill equals the last row of the prefill that includes its token).
+token only), outputs it wrote once into tests/golden/ by a script that runs
+only the oracle (the batch-64 and 8B greedy runs), and properties that hold at
+any size (a decode step after a prefill equals the last row of the prefill
+that includes its token).
 """
 import os
 
@@ -137,25 +139,72 @@ def test_8b_geometry_two_layers(torch):
         assert_ids_prefix([int(_np(am)[0])] + [int(v) for v in _np(out)[:, 0]], ids, logits)
 
 
-def test_8b_full_size_properties(torch):
+@pytest.fixture(scope="module")
+def model_8b(torch):
+    """The Qwen3-8B-shape model at full size (36 layers, 8.7 GB of Q8_0
+    weights), room for two sequences of the 8192-token prompt plus 64 steps."""
+    from quantized_transformer_decode_gb300.qw3 import Qw3Model
+    w = inputs.WORKLOADS["qwen3-8b"]
+    gm = Qw3Model.from_f32(w.shape, inputs.iter_weights(w.shape, w.seed), max_seqs=2,
+                           max_seq_len=w.prompt_len + 66, max_prefill=4096)
+    yield gm
+    gm.close()
+
+
+def test_8b_greedy_against_stored_oracle(model_8b):
+    """Qwen3-8B shape, the 8192-token prompt, then 64 greedy steps at batch 1
+    through qw3_generate_greedy. tests/golden/make_qwen3_8b_golden.py wrote
+    the oracle's ids (prefill argmax, then each step's) with each row's top-2
+    margin, and its logits rows at steps 0, 1, 32 and 64. The ids must match
+    bit for bit up to the oracle's first near tie (parity.py); then, fed the
+    oracle's ids (teacher-forced), the stored rows must meet the bar."""
+    g = np.load(os.path.join(GOLDEN, "qwen3_8b_greedy.npz"))
+    w = inputs.WORKLOADS["qwen3-8b"]
+    s, P, N = w.shape, w.prompt_len, int(g["n_steps"])
+    assert int(g["prompt_len"]) == P and int(g["seed"]) == w.seed
+    ids = [int(v) for v in g["ids"]]
+    margins = g["margins"] if "margins" in g.files else np.full(N + 1, np.inf)     # absent: all strict
+    stored = {int(k): g["logits"][i] for i, k in enumerate(g["steps"])}
+    gm = model_8b
+    gm.reset(0)
+    gm.reset(1)
+    prompt = inputs.prompt_tokens(s, w.seed, P)
+    lg, am = gm.prefill(0, cuda_ints(prompt), want_logits=True)
+    assert_logits_close(_np(lg), stored[0], "8B prefill last row")
+    out = _np(gm.generate_greedy(am, N, seqs=[0]))
+    run = [int(_np(am)[0])] + [int(v) for v in out[:, 0]]
+    n = next((k for k in range(N + 1) if margins[k] < TIE_MARGIN), N + 1)
+    assert run[:n] == ids[:n], f"8B greedy ids differ before row {n}"
+    gm.truncate(0, P)
+    for k in range(N):
+        want = stored.get(k + 1)
+        lg, am = gm.decode(cuda_ints([ids[k]]), [P + k], seqs=[0], want_logits=want is not None)
+        if want is not None:
+            assert_logits_close(_np(lg)[0], want, f"8B step {k + 1}")
+            assert_argmax(int(_np(am)[0]), ids[k + 1], want, f"8B step {k + 1}")
+    gm.sync()
+
+
+def test_8b_full_size_properties(model_8b):
     """Qwen3-8B shape at full size (36 layers, 8.7 GB of Q8_0 weights, an
     8192-token prompt): layer-0 K/V rows at sampled positions against the
     oracle's layer 0 for those tokens, and the cached == uncached property
     (course 12.4): decoding token t after the 8192-token prefill gives the
     logits of the last row of an 8193-token prefill."""
-    from quantized_transformer_decode_gb300.qw3 import Qw3Model
     w = inputs.WORKLOADS["qwen3-8b"]
     s, P = w.shape, w.prompt_len
     prompt = inputs.prompt_tokens(s, w.seed, P + 1)
-    with Qw3Model.from_f32(s, inputs.iter_weights(s, w.seed), max_seqs=2, max_seq_len=P + 2, max_prefill=4096) as gm:
-        _, am = gm.prefill(0, cuda_ints(prompt[:P]), want_logits=False)
-        lg_dec, am_dec = gm.decode(cuda_ints(prompt[P:P + 1]), [P], seqs=[0])
-        lg_full, am_full = gm.prefill(1, cuda_ints(prompt))
-        gm.sync()
-        assert_logits_close(_np(lg_dec)[0], _np(lg_full), "decode after prefill vs longer prefill")
-        assert int(_np(am_dec)[0]) == int(_np(am_full)[0])
-        k, v = gm.read_kv(0, 0, 0, P)
-        k, v = _np(k), _np(v)
+    gm = model_8b
+    gm.reset(0)
+    gm.reset(1)
+    _, am = gm.prefill(0, cuda_ints(prompt[:P]), want_logits=False)
+    lg_dec, am_dec = gm.decode(cuda_ints(prompt[P:P + 1]), [P], seqs=[0])
+    lg_full, am_full = gm.prefill(1, cuda_ints(prompt))
+    gm.sync()
+    assert_logits_close(_np(lg_dec)[0], _np(lg_full), "decode after prefill vs longer prefill")
+    assert int(_np(am_dec)[0]) == int(_np(am_full)[0])
+    k, v = gm.read_kv(0, 0, 0, P)
+    k, v = _np(k), _np(v)
     # the oracle's layer 0 for single tokens at their own positions
     w0 = {}
     for name, kind, arr in inputs.iter_weights(s, w.seed):
