@@ -594,10 +594,12 @@ def run_prefill_line(a, torch, qw3, world, rank, local, dev, w: inputs.Workload,
                                  f"(ms: {', '.join(f'{x:.3f}' for x in ms_runs)})"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf_peak, "unit": "TFLOP/s",
                          "frac": achieved / tf_peak,
-                         "peak_source": f"{peak_kind} bf16 sustained (MEASURED_PEAKS.json bf16_tflops_sustained)",
+                         "peak_source": f"{peak_kind} bf16 sustained (MEASURED_PEAKS.json bf16_tflops_sustained; "
+                                        "the dense fp16 rate is nominally the bf16 rate)",
                          "note": "achieved counts the model's FLOPs (linear + causal attention + last-row lm_head); "
-                                 "the GEMMs and the causal attention run as three bf16 MMAs per product (hi/lo "
-                                 "split for f32 accuracy)",
+                                 "the GEMMs and the causal attention run as three fp16 MMAs per product (hi/lo "
+                                 "split of power-of-two-scaled rows, for f32 accuracy) in short accumulation "
+                                 "chains promoted into f32",
                          "algorithmic_flops_per_step": flops, "traffic": None},
             "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
             "gpu_launches": launches * runs,

@@ -5,18 +5,18 @@
 //
 // Flash-attention over 64-key tiles, one CTA per (128-query tile, query
 // head), f32 accuracy from fp16 operands as in the GEMMs: every operand x,
-// first multiplied by a power of two 2^t chosen per row, is split into
-// hi = fp16(x) and lo = fp16(x - hi), and each product is hi.hi + hi.lo +
-// lo.hi (three tcgen05.mma, f32 accumulation in TMEM); the results are
-// multiplied by the inverse powers (exact). The factors: one per query row
-// and one per key (S = Q K^T contracts over the head dimension), one per
-// (kv head, 8 dimensions) over all keys for V (O = P V contracts over keys,
-// so V's factor must not vary along them); P lies in [0, 2^8] and needs none.
-//  * Per layer, k_pack_k and k_pack_v convert the cached K and V of the
-//    sequence into per-(kv head, 64-key tile) UMMA operand tiles (K as B of
-//    S = Q K^T, V transposed as B of O = P V) with the keys' inverse factors
-//    beside them, so attention CTAs fetch each tile with one bulk copy (and
-//    its 64 factors with another) into a two-buffer ring.
+// first multiplied by a power of two 2^t, is split into hi = fp16(x) and
+// lo = fp16(x - hi), and each product is hi.hi + hi.lo + lo.hi (three
+// tcgen05.mma, f32 accumulation in TMEM); the results are multiplied by the
+// inverse powers (exact). The factors: one per query row and one per kv head
+// for K (from the largest magnitude over its keys: keys after the Q/K norm
+// have like magnitudes), one per (kv head, 8 dimensions) over all keys for V
+// (O = P V contracts over keys, so V's factor must not vary along them); P
+// lies in [0, 2^8] and needs none.
+//  * Per layer, k_kv_absmax, k_pack_k and k_pack_v convert the cached K and V
+//    of the sequence into per-(kv head, 64-key tile) UMMA operand tiles (K as
+//    B of S = Q K^T, V transposed as B of O = P V), so attention CTAs fetch
+//    each tile with one bulk copy into a two-buffer ring.
 //  * The CTA packs its 128 query rows once; per key tile: S = Q K^T into 64
 //    TMEM columns; each thread owns one query row (its TMEM lane) and runs
 //    the online softmax on it without shuffles (in base 2); P (hi/lo) goes
@@ -50,25 +50,23 @@ struct PaSizes {
     static constexpr uint32_t kv = 2 * (HD * 128);                // V^T tile: hi + lo, HD rows x 64 keys
     static constexpr uint32_t kkv = kk + kv;                      // one packed (K, V) tile
     static constexpr uint32_t kp = 2 * (kQT * 128);               // P: hi + lo, 128 rows x 64 keys
-    static constexpr uint32_t kinv = kKT * 4;                     // a tile's inverse key factors
-    static constexpr uint32_t smem = kq + 2 * kkv + kp + 2 * kinv + 1024 + 256;
+    static constexpr uint32_t smem = kq + 2 * kkv + kp + 1024 + 256;
 };
 
-// The pack buffer: nkv * ntiles (K, V^T) tiles, then the keys' inverse
-// factors [nkv][ntiles][64], then V's inverse factors [nkv][HD], then V's
-// maxima [nkv][HD / 8].
+// The pack buffer: nkv * ntiles (K, V^T) tiles, then V's inverse factors
+// [nkv][HD], then K's [nkv] (padded to 4), then the scratch of the maxima of
+// K and V [2][nkv][HD / 8].
 template <int HD>
-__host__ __device__ inline float *pa_kinv(uint8_t *pack, int nkv, int ntiles) {
+__host__ __device__ inline float *pa_vinv(uint8_t *pack, int nkv, int ntiles) {
     return reinterpret_cast<float *>(pack + static_cast<size_t>(nkv) * ntiles * PaSizes<HD>::kkv);
 }
 template <int HD>
-__host__ __device__ inline float *pa_vinv(uint8_t *pack, int nkv, int ntiles) {
-    return pa_kinv<HD>(pack, nkv, ntiles) + static_cast<size_t>(nkv) * ntiles * kKT;
+__host__ __device__ inline float *pa_kinv(uint8_t *pack, int nkv, int ntiles) {
+    return pa_vinv<HD>(pack, nkv, ntiles) + static_cast<size_t>(nkv) * HD;
 }
-// then the scratch of V's maxima [nkv][HD / 8]
 template <int HD>
-__host__ __device__ inline unsigned *pa_vmax(uint8_t *pack, int nkv, int ntiles) {
-    return reinterpret_cast<unsigned *>(pa_vinv<HD>(pack, nkv, ntiles) + static_cast<size_t>(nkv) * HD);
+__host__ __device__ inline unsigned *pa_kvmax(uint8_t *pack, int nkv, int ntiles) {
+    return reinterpret_cast<unsigned *>(pa_kinv<HD>(pack, nkv, ntiles) + (nkv + 3) / 4 * 4);
 }
 
 // Byte offset of element (row r, column k) in a K-major no-swizzle UMMA tile
@@ -88,78 +86,82 @@ __host__ __device__ constexpr uint32_t pa_idesc(int M, int N) {
     return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// K tiles: HD / 8 threads per (kv head, key) of keys [0, ntiles * 64), 8
-// dimensions each: the key's largest magnitude (a shuffle over its threads)
-// sets its factor; the scaled row goes to the K part of its tile, the
-// inverse factor beside the tiles. Keys at or past ctx are zero.
+// The largest magnitudes of K and of V per (kv head, 8 dimensions) over keys
+// [0, ctx), as the bits of non-negative f32 (atomicMax in unsigned order;
+// kvmax zeroed first; [0] K, [1] V): a CTA covers 256 keys of one head,
+// thread = (key, 8 dimensions), reduced in shared memory before one atomic
+// per group.
+template <int HD, typename KT>
+__global__ void __launch_bounds__(256) k_kv_absmax(const KT *__restrict__ kc, const KT *__restrict__ vc,
+                                                   size_t head_stride, int nkv, int ctx,
+                                                   unsigned *__restrict__ kvmax) {
+    constexpr int G = HD / 8, KPI = 256 / G;   // dimension groups; keys per pass of the CTA
+    __shared__ float red[2][256];
+    const int g = blockIdx.y, tid = threadIdx.x, dg = tid % G;
+    const KT *ksrc = kc + static_cast<size_t>(g) * head_stride;
+    const KT *vsrc = vc + static_cast<size_t>(g) * head_stride;
+    float km = 0.0f, vm = 0.0f;
+    const int k_end = min(ctx, (blockIdx.x + 1) * 256);
+    for (int key = blockIdx.x * 256 + tid / G; key < k_end; key += KPI) {
+        const size_t off = static_cast<size_t>(key) * kv_row<KT, HD>();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            km = fmaxf(km, fabsf(kv_elem<HD>(ksrc + off, dg * 8 + j)));
+            vm = fmaxf(vm, fabsf(kv_elem<HD>(vsrc + off, dg * 8 + j)));
+        }
+    }
+    red[0][tid] = km;
+    red[1][tid] = vm;
+    __syncthreads();
+    if (tid < G) {
+        for (int k = tid + G; k < 256; k += G) {
+            km = fmaxf(km, red[0][k]);
+            vm = fmaxf(vm, red[1][k]);
+        }
+        atomicMax(&kvmax[g * G + tid], __float_as_uint(km));
+        atomicMax(&kvmax[(nkv + g) * G + tid], __float_as_uint(vm));
+    }
+}
+
+// K tiles: one thread per (kv head, key, 8 dimensions) of keys
+// [0, ntiles * 64), every key of a head scaled by the head's factor (from
+// its largest magnitude over keys and dimensions: keys after the Q/K norm
+// have like magnitudes). Keys at or past ctx are zero.
 template <int HD, typename KT>
 __global__ void k_pack_k(const KT *__restrict__ kc, size_t head_stride, int nkv, int ctx, int ntiles,
-                         uint8_t *__restrict__ dst) {
+                         const unsigned *__restrict__ kvmax, uint8_t *__restrict__ dst) {
     using Z = PaSizes<HD>;
-    constexpr int G = HD / 8;   // threads per key: aligned groups of 8 or 16 lanes
+    constexpr int G = HD / 8;
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t keys = static_cast<int64_t>(nkv) * ntiles * kKT;
-    const bool live = i < keys * G;   // the grid is whole warps: dead lanes still shuffle
-    const int64_t kid = live ? i / G : 0;
+    if (i >= static_cast<int64_t>(nkv) * ntiles * kKT * G) return;
     const int d0 = static_cast<int>(i % G) * 8;
+    const int64_t kid = i / G;
     const int key = static_cast<int>(kid % (static_cast<int64_t>(ntiles) * kKT));
     const int g = static_cast<int>(kid / (static_cast<int64_t>(ntiles) * kKT));
-    const KT *row = kc + static_cast<size_t>(g) * head_stride + static_cast<size_t>(key) * kv_row<KT, HD>();
-    float v[8];
     float amax = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        v[j] = (live && key < ctx) ? kv_elem<HD>(row, d0 + j) : 0.0f;
-        amax = fmaxf(amax, fabsf(v[j]));
-    }
-#pragma unroll
-    for (int o = 1; o < G; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (!live) return;
+    for (int q = 0; q < G; ++q) amax = fmaxf(amax, __uint_as_float(kvmax[g * G + q]));
     const int t = f16_row_exp(amax);
     const float sr = pow2_f32(t);
+    const KT *row = kc + static_cast<size_t>(g) * head_stride + static_cast<size_t>(key) * kv_row<KT, HD>();
+    float v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] *= sr;
+    for (int j = 0; j < 8; ++j) v[j] = key < ctx ? kv_elem<HD>(row, d0 + j) * sr : 0.0f;
     uint4 hi, lo;
     split8_f16(v, hi, lo);
     const int tile = key / kKT, r = key % kKT;
     uint8_t *base = dst + (static_cast<size_t>(g) * ntiles + tile) * Z::kkv + (d0 / 64) * 2 * (kKT * 128);
     *reinterpret_cast<uint4 *>(base + pa_core(r, d0 % 64)) = hi;
     *reinterpret_cast<uint4 *>(base + kKT * 128 + pa_core(r, d0 % 64)) = lo;
-    if (d0 == 0) pa_kinv<HD>(dst, nkv, ntiles)[static_cast<size_t>(g) * ntiles * kKT + key] = pow2_f32(-t);
-}
-
-// The largest magnitude of each (kv head, 8 dimensions) of V over keys
-// [0, ctx), as the bits of a non-negative f32 (atomicMax on unsigned order;
-// vmax zeroed first): a CTA covers 256 keys of one head, thread = (key, 8
-// dimensions), reduced in shared memory before one atomic per group.
-template <int HD, typename KT>
-__global__ void __launch_bounds__(256) k_v_absmax(const KT *__restrict__ vc, size_t head_stride, int ctx,
-                                                  unsigned *__restrict__ vmax) {
-    constexpr int G = HD / 8, KPI = 256 / G;   // dimension groups; keys per pass of the CTA
-    __shared__ float red[256];
-    const int g = blockIdx.y, tid = threadIdx.x, dg = tid % G;
-    const KT *src = vc + static_cast<size_t>(g) * head_stride;
-    float amax = 0.0f;
-    const int k_end = min(ctx, (blockIdx.x + 1) * 256);
-    for (int key = blockIdx.x * 256 + tid / G; key < k_end; key += KPI) {
-        const KT *row = src + static_cast<size_t>(key) * kv_row<KT, HD>();
-#pragma unroll
-        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(kv_elem<HD>(row, dg * 8 + j)));
-    }
-    red[tid] = amax;
-    __syncthreads();
-    if (tid < G) {
-        for (int k = tid + G; k < 256; k += G) amax = fmaxf(amax, red[k]);
-        atomicMax(&vmax[g * G + tid], __float_as_uint(amax));
-    }
+    if (key == 0 && d0 == 0) pa_kinv<HD>(dst, nkv, ntiles)[g] = pow2_f32(-t);
 }
 
 // V^T tiles: one thread per (kv head, tile, dimension, 8-key group); each
-// (kv head, 8 dimensions) scaled by the common factor of vmax. Keys at or
-// past ctx are zero.
+// (kv head, 8 dimensions) scaled by the factor of its maximum over all keys.
+// Keys at or past ctx are zero.
 template <int HD, typename KT>
 __global__ void k_pack_v(const KT *__restrict__ vc, size_t head_stride, int nkv, int ctx, int ntiles,
-                         const unsigned *__restrict__ vmax, uint8_t *__restrict__ dst) {
+                         const unsigned *__restrict__ kvmax, uint8_t *__restrict__ dst) {
     using Z = PaSizes<HD>;
     constexpr int kItems = HD * (kKT / 8);
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -168,7 +170,7 @@ __global__ void k_pack_v(const KT *__restrict__ vc, size_t head_stride, int nkv,
     const int tile = static_cast<int>((i / kItems) % ntiles);
     const int g = static_cast<int>(i / (static_cast<int64_t>(kItems) * ntiles));
     const int d = item / (kKT / 8), k0 = (item % (kKT / 8)) * 8;
-    const int t = f16_row_exp(__uint_as_float(vmax[g * (HD / 8) + d / 8]));
+    const int t = f16_row_exp(__uint_as_float(kvmax[(nkv + g) * (HD / 8) + d / 8]));
     const float sr = pow2_f32(t);
     const KT *src = vc + static_cast<size_t>(g) * head_stride;
     float v[8];
@@ -198,6 +200,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// 32 columns of this warp's TMEM lanes into v[o .. o + 32) (one wait).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[kKT], int o) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[o + j] = __uint_as_float(r[j]);
+}
+
 // Three MMAs (hi.hi, hi.lo, lo.hi) over one 64-deep step: A at a_hi / a_lo,
 // B at b_hi / b_lo (each a K-major tile of 64 columns); accumulate unless
 // first.
@@ -224,25 +243,28 @@ __device__ __forceinline__ void mma3(uint32_t tmem, uint32_t a_hi, uint32_t a_lo
 template <int HD>
 __device__ __forceinline__ void promote_o(uint32_t master, uint32_t partial, bool has_master, float corr) {
 #pragma unroll 1
-    for (int c0 = 0; c0 < HD; c0 += 8) {
-        uint32_t a[8], b[8];
+    for (int c0 = 0; c0 < HD; c0 += 16) {
+        uint32_t a[16], b[16];
         asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%16];\n\t"
-            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%17];\n\t"
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
             "tcgen05.wait::ld.sync.aligned;"
             : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
-              "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7])
+              "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
+              "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]),
+              "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15])
             : "r"(master + c0), "r"(partial + c0)
             : "memory");
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 16; ++j) {
             const float m = has_master ? __uint_as_float(a[j]) : 0.0f;
             a[j] = __float_as_uint((m + __uint_as_float(b[j])) * corr);
         }
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-                     ::"r"(master + c0), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]),
-                       "r"(a[7])
-                     : "memory");
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+            ::"r"(master + c0), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]),
+              "r"(a[7]), "r"(a[8]), "r"(a[9]), "r"(a[10]), "r"(a[11]), "r"(a[12]), "r"(a[13]), "r"(a[14]), "r"(a[15])
+            : "memory");
     }
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -284,8 +306,7 @@ __global__ void __launch_bounds__(kPaThreads, 1)
     uint8_t *Qs = base;                    // [HD/64][hi|lo] 128 x 64 tiles
     uint8_t *KV0 = Qs + Z::kq;             // two packed (K, V^T) tiles
     uint8_t *Ps = KV0 + 2 * Z::kkv;        // [hi|lo] 128 x 64
-    float *Kinv = reinterpret_cast<float *>(Ps + Z::kp);          // [2][64] the tiles' inverse key factors
-    uint64_t *bars = reinterpret_cast<uint64_t *>(Ps + Z::kp + 2 * Z::kinv);   // kv_full[2], s_done, o_done
+    uint64_t *bars = reinterpret_cast<uint64_t *>(Ps + Z::kp);   // kv_full[2], s_done, o_done
     uint64_t *kv_full = bars, *s_done = bars + 2, *o_done = bars + 3;
     uint32_t *tbase = reinterpret_cast<uint32_t *>(bars + 4);
     volatile int *err = reinterpret_cast<volatile int *>(tbase + 1);
@@ -298,17 +319,13 @@ __global__ void __launch_bounds__(kPaThreads, 1)
     const int last_q = min(M - 1, qt * kQT + kQT - 1);
     const int ntl = min(ntiles, (pos0 + last_q) / kKT + 1);   // key tiles this CTA needs
     const uint8_t *kvg = kvpack + static_cast<size_t>(g) * ntiles * Z::kkv;
-    const float *kinvg = pa_kinv<HD>(kvpack, nkv, ntiles) + static_cast<size_t>(g) * ntiles * kKT;
+    const float kinv_g = pa_kinv<HD>(kvpack, nkv, ntiles)[g];
     const float *vinvg = pa_vinv<HD>(kvpack, nkv, ntiles) + static_cast<size_t>(g) * HD;
-    // thread 0: tile jt (its K/V^T pair and its key factors) into buffer b
+    // thread 0: the K/V^T pair of tile jt into buffer b
     auto fetch = [&](int jt, int b) {
-        mbar_arrive_expect_tx(&kv_full[b], Z::kkv + Z::kinv);
+        mbar_arrive_expect_tx(&kv_full[b], Z::kkv);
         asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                      ::"r"(smem_u32(KV0 + b * Z::kkv)), "l"(kvg + static_cast<size_t>(jt) * Z::kkv), "r"(Z::kkv),
-                       "r"(smem_u32(&kv_full[b]))
-                     : "memory");
-        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                     ::"r"(smem_u32(Kinv + b * kKT)), "l"(kinvg + static_cast<size_t>(jt) * kKT), "r"(Z::kinv),
                        "r"(smem_u32(&kv_full[b]))
                      : "memory");
     };
@@ -378,8 +395,10 @@ __global__ void __launch_bounds__(kPaThreads, 1)
     __syncthreads();
 
     constexpr uint32_t kIdS = pa_idesc(kQT, kKT), kIdO = pa_idesc(kQT, HD);
-    // softmax in base 2: exp(x) = 2^(x log2 e), scores pre-scaled by log2 e
+    // softmax in base 2: exp(x) = 2^(x log2 e), scores pre-scaled by log2 e;
+    // qs2 also undoes the row's and the head's operand factors (powers of two)
     const float scale2 = scale * 1.4426950408889634f;
+    const float qs2 = (qinv * kinv_g) * scale2;
     float m_run = -INFINITY, l_run = 0.0f;
     int chain = 0;              // tiles in the partial O (CTA-uniform)
     bool has_master = false;    // the master O holds promoted tiles
@@ -404,25 +423,24 @@ __global__ void __launch_bounds__(kPaThreads, 1)
         __syncwarp();
         if (!mbar_wait_bounded(s_done, static_cast<uint32_t>(j & 1))) *err = 1;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        // the tile's key factors (landed with the tile: its phase is complete)
-        if (!mbar_wait_bounded(&kv_full[buf], static_cast<uint32_t>((j >> 1) & 1))) *err = 1;
-        const float *kinv = Kinv + buf * kKT;
-        const float qs2 = qinv * scale2;   // exact: qinv is a power of two
         // ---- online softmax of this row over the tile's 64 keys
         float sv[kKT];
-#pragma unroll
-        for (int c = 0; c < kKT; c += 16) {
-            float t16[16];
-            tmem_ld16(tS + lane_off + static_cast<uint32_t>(c), t16);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) sv[c + e] = t16[e];
-        }
+        tmem_ld32(tS + lane_off, sv, 0);
+        tmem_ld32(tS + lane_off + 32u, sv, 32);
         float mx = -INFINITY;
+        if ((j + 1) * kKT - 1 > pos0 + qt * kQT) {
+            // a tile on the diagonal: keys past the row's position are masked
 #pragma unroll
-        for (int c = 0; c < kKT; ++c) {
-            const int key = j * kKT + c;
-            sv[c] = (key <= qpos) ? sv[c] * kinv[c] * qs2 : -INFINITY;
-            mx = fmaxf(mx, sv[c]);
+            for (int c = 0; c < kKT; ++c) {
+                sv[c] = (j * kKT + c <= qpos) ? sv[c] * qs2 : -INFINITY;
+                mx = fmaxf(mx, sv[c]);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < kKT; ++c) {
+                sv[c] *= qs2;
+                mx = fmaxf(mx, sv[c]);
+            }
         }
         // The reference maximum moves only when the tile's maximum exceeds it
         // by more than 8 (probabilities up to 2^8 are exact to represent and
@@ -531,19 +549,18 @@ cudaError_t launch_pa_t(const float *qkv, int M, int qkv_stride, const KT *kc, c
     using Z = PaSizes<HD>;
     const int ctx = pos0 + M;
     const int ntiles = (ctx + kKT - 1) / kKT;
+    unsigned *kvmax = pa_kvmax<HD>(kvpack, nkv, ntiles);
+    cudaError_t e = cudaMemsetAsync(kvmax, 0, static_cast<size_t>(2 * nkv) * (HD / 8) * sizeof(unsigned), s);
+    if (e != cudaSuccess) return e;
+    k_kv_absmax<HD, KT><<<dim3((ctx + 255) / 256, nkv), 256, 0, s>>>(kc, vc, head_stride, nkv, ctx, kvmax);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t kthreads = static_cast<int64_t>(nkv) * ntiles * kKT * (HD / 8);
     k_pack_k<HD, KT><<<static_cast<unsigned>((kthreads + 255) / 256), 256, 0, s>>>(kc, head_stride, nkv, ctx,
-                                                                                    ntiles, kvpack);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    unsigned *vmax = pa_vmax<HD>(kvpack, nkv, ntiles);
-    if ((e = cudaMemsetAsync(vmax, 0, static_cast<size_t>(nkv) * (HD / 8) * sizeof(unsigned), s)) != cudaSuccess)
-        return e;
-    k_v_absmax<HD, KT><<<dim3((ctx + 255) / 256, nkv), 256, 0, s>>>(vc, head_stride, ctx, vmax);
+                                                                                    ntiles, kvmax, kvpack);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t vitems = static_cast<int64_t>(nkv) * ntiles * HD * (kKT / 8);
     k_pack_v<HD, KT><<<static_cast<unsigned>((vitems + 255) / 256), 256, 0, s>>>(vc, head_stride, nkv, ctx, ntiles,
-                                                                                  vmax, kvpack);
+                                                                                  kvmax, kvpack);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const dim3 grid((M + kQT - 1) / kQT, nh);
     k_attn_prefill_tc<HD><<<grid, kPaThreads, Z::smem, s>>>(qkv, M, qkv_stride, kvpack, nkv, ntiles, pos0,
@@ -556,8 +573,8 @@ cudaError_t launch_pa_t(const float *qkv, int M, int qkv_stride, const KT *kc, c
 size_t attn_prefill_tc_pack_bytes(int hd, int nkv, int max_seq_len) {
     const size_t ntiles = (static_cast<size_t>(max_seq_len) + kKT - 1) / kKT;
     const size_t tile = hd == 128 ? PaSizes<128>::kkv : PaSizes<64>::kkv;
-    return static_cast<size_t>(nkv) * ntiles * (tile + kKT * 4) + static_cast<size_t>(nkv) * hd * 4 +
-           static_cast<size_t>(nkv) * (hd / 8) * 4;
+    return static_cast<size_t>(nkv) * ntiles * tile + static_cast<size_t>(nkv) * hd * 4 +
+           static_cast<size_t>(nkv + 3) / 4 * 16 + static_cast<size_t>(2 * nkv) * (hd / 8) * 4;
 }
 
 cudaError_t configure_attn_prefill_tc() {
