@@ -118,6 +118,30 @@ def test_codec_entries_check_sizes_first(L):
     assert L.qw3_q8_0_gemv(16, 0, 64, 16, 1, 16, None) == 0         # no rows: nothing to do
 
 
+def test_gemm_entry_checks_arguments_before_device_work(L):
+    """qw3_q8_0_gemm: sizes, alignment and the workspace are checked on the
+    host, so every case here returns before a CUDA call (pointers are never
+    dereferenced)."""
+    ws = L.qw3_q8_0_gemm_workspace_bytes
+    assert ws(128, 96, 4) == -1                                      # cols % 64
+    assert ws(-1, 64, 4) == -1 and ws(128, 64, -1) == -1
+    # pieces of 8704 bytes per (128-row tile, 64 columns) + 8 bytes of row
+    # factors per padded row, then the packed activations: 4 bytes per value
+    # of the padded rows + their inverse factors
+    assert ws(128, 64, 4) == 8704 + 128 * 8 + 128 * 64 * 4 + 128 * 4
+    assert ws(300, 1024, 130) == 3 * 16 * 8704 + 384 * 8 + 256 * 1024 * 4 + 256 * 4
+    g = L.qw3_q8_0_gemm
+    assert g(16, 8, 96, 16, 4, 16, 16, 1 << 20, None) == 2          # cols % 64
+    assert g(None, 8, 64, 16, 4, 16, 16, 1 << 20, None) == 1        # null W
+    assert g(17, 8, 64, 16, 4, 16, 16, 1 << 20, None) == 1          # W misaligned
+    assert g(16, 8, 64, 24, 4, 16, 16, 1 << 20, None) == 1          # x not 16-byte aligned
+    assert g(16, 8, 64, 16, 4, 16, 24, 1 << 20, None) == 1          # workspace misaligned
+    assert g(16, 8, 64, 16, 4, 16, 16, 100, None) == 1              # workspace too small
+    assert g(16, 8, 64, 16, 4, 16, None, 0, None) == 1              # no workspace
+    assert g(16, 0, 64, 16, 4, 16, None, 0, None) == 0              # no rows: nothing to do
+    assert g(16, 8, 64, 16, 0, 16, None, 0, None) == 0              # no activation rows
+
+
 def test_model_calls_reject_null_model(L):
     n = ctypes.c_int32()
     assert L.qw3_seq_len(None, 0, ctypes.byref(n)) == 1
