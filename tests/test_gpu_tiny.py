@@ -71,6 +71,22 @@ def test_tiny_greedy_and_logits(torch):
     gm.close()
 
 
+@pytest.mark.parametrize("flags", [0, 0x20, 0x80])
+def test_tiny_tensor_core_prefill_head_dim_64(torch, flags):
+    """head_dim 64 through the tensor-core prefill: a 300-token prompt in
+    one chunk takes the tcgen05 GEMMs and the tcgen05 causal attention (one
+    64-deep step per S product, 64-column O accumulators), with the f32,
+    f16 and q8_0 caches; then decode against the oracle (the f16 and q8_0
+    caches through the checks of their own test modules)."""
+    if flags:
+        from test_gpu_kv_f16 import _greedy_f16
+        from test_gpu_kv_q8 import _greedy_q8
+        (_greedy_f16 if flags == 0x20 else _greedy_q8)(inputs.TINY, 3, 300, 4, max_prefill=512)
+        return
+    _, gm, _ = run_greedy_case(torch, inputs.TINY, 3, 300, 4, max_prefill=512)
+    gm.close()
+
+
 PER_KERNEL = 0x8      # batch-1 decode through the per-kernel chain
 TEST_NO_WAIT = 0x10   # waits on other CTAs give up at their first miss
 
