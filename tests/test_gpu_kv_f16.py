@@ -140,7 +140,8 @@ def test_tiny_f16_cache_greedy_and_logits(torch):
 @pytest.mark.parametrize("prompt_len,max_prefill", [(40, 64), (300, 512)])
 def test_mid_f16_cache_greedy_and_logits(torch, prompt_len, max_prefill):
     """300 prompt rows in one chunk take the tensor-core prefill attention
-    (which packs the half cache into bf16 hi/lo pairs, exactly); 40 the SIMT
+    (which packs the half cache into fp16 hi/lo pairs of power-of-two-scaled
+    values); 40 the SIMT
     one. Decode at batch 1 runs the per-kernel chain in this mode."""
     _greedy_f16(MID, 3, prompt_len, 6, max_prefill=max_prefill)
 
