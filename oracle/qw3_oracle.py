@@ -20,13 +20,15 @@ Sources (page title, section):
   * "A transformer from scratch" (Fucina course ch. 12): sections 12.1 (config),
     12.3 (forward pass), 12.3.2 (RMSNorm), 12.3.3 (QKV), 12.3.4 (RoPE),
     12.3.5 (GQA, causal attention, scale), 12.3.6 (SwiGLU), 12.3.7 (residual,
-    final norm, last-row lm_head), 12.4 (KV cache and its contracts),
-    12.6 (greedy loop).
+    final norm, last-row lm_head; the all-rows form for verification),
+    12.4 (KV cache and its contracts, the f16 cache), 12.6 (greedy loop).
   * "Model files and quantization" (Fucina course ch. 11): section 11.7
-    (Q8_0 block, encoder, decoder, round-trip bound), 11.10 (finite-input
-    guard).
+    (Q8_0 block, encoder, decoder, round-trip bound), 11.8 (the Q4_K block
+    and its decode), 11.9 (the quantized matmul on Q8_0-encoded activations:
+    per-block integer dots times d_w * d_a), 11.10 (finite-input guard).
   * "The LLM stack (fucina_llm)" (Fucina reference section 13): 13.4 (KV cache
-    contract and its worked test), 13.6 (greedy argmax example).
+    contract and its worked test; the q8_0 cache with integer-score decode
+    attention), 13.6 (greedy argmax example).
   * minfer "Qwen3 Support Plan (dense)": section 1 (tensor inventory),
     section 2.1 (head_dim 128, scale 1/sqrt(128), full-head NeoX RoPE,
     theta 1e6), section 2.2 (per-head Q/K RMSNorm before RoPE).
