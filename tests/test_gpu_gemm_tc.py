@@ -45,10 +45,11 @@ def _gemm(torch, blocks, rows, cols, x):
 
 
 # (rows, cols, M): ragged row and column tiles; one K step; 16 K steps over
-# m-tile pairs (4096 x 1280 fills the GPU with two m-tiles per CTA); the
-# longest contraction of the 8B geometry
+# m-tile pairs (4096 x 1280 fills the GPU with two m-tiles per CTA; 6144 x
+# 896 has 7 row tiles, so the last CTA row holds one); the longest
+# contraction of the 8B geometry
 @pytest.mark.parametrize("rows,cols,M", [(1000, 1024, 300), (128, 64, 1), (257, 3072, 33), (4096, 1024, 1280),
-                                         (1024, 12288, 256), (77, 4096, 130)])
+                                         (6144, 1024, 896), (1024, 12288, 256), (77, 4096, 130)])
 def test_gemm_elementwise(torch, rows, cols, M):
     blocks, x, want, mag = _case(rows, cols, M, 0)
     y = _gemm(torch, blocks, rows, cols, x)
